@@ -1,0 +1,136 @@
+"""fp64 verify pass of a Qwen3-8B-shaped decoder stack (test infrastructure only).
+
+The pages fix the target's shape (36 layers, 8 key/value heads with grouped
+query attention, "Speculative Decoding Spends Arithmetic You May Not Have",
+"Why a better draft model can be a worse deal") and that all gamma+1 rows go
+through ONE forward pass (Algorithm 1).  The layer internals are this
+project's reading: pre-RMSNorm (eps 1e-6), RoPE (theta 1e6, rotate-half) on
+q and k, causal GQA attention over the cache, SwiGLU MLP, residual adds, a
+final RMSNorm and the LM head.
+
+bf16 rounding happens exactly where the CUDA path stores bf16 tensors, so the
+two chains are comparable; the logits are left unrounded (fp64).
+"""
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import ops
+from .bf16 import decode, round_to_bf16 as r16
+
+
+@dataclass
+class Dims:
+    d: int = 4096
+    Hq: int = 32
+    Hkv: int = 8
+    D: int = 128
+    I: int = 12288
+    V: int = 151936
+    layers: int = 36
+    eps: float = 1e-6
+    theta: float = 1e6
+
+
+@dataclass
+class LayerWeights:
+    """bf16 bit patterns (uint16); decoded per matrix on use."""
+    w_qkv: np.ndarray            # [(Hq + 2 Hkv) D, d]
+    w_o: np.ndarray              # [d, Hq D]
+    w_gu: np.ndarray             # [2 I, d]   gate rows then up rows
+    w_down: np.ndarray           # [d, I]
+    attn_norm: np.ndarray        # [d]
+    mlp_norm: np.ndarray         # [d]
+
+
+@dataclass
+class StackWeights:
+    layers: list = field(default_factory=list)
+    final_norm: np.ndarray | None = None
+    w_lm: np.ndarray | None = None   # [V, d]
+
+
+def layer_forward(x, lw: LayerWeights, dims: Dims, cu_rows, ctx_len, Kc, Vc):
+    """One decoder layer over the packed verify rows.
+
+    x [M, d] (bf16 values, fp64); Kc/Vc [B, Hkv, cap, D] this layer's cache.
+    Returns (x', Kc', Vc').
+    """
+    M = x.shape[0]
+    Hq, Hkv, D = dims.Hq, dims.Hkv, dims.D
+    pos = np.concatenate([ctx_len[b] + np.arange(cu_rows[b + 1] - cu_rows[b])
+                          for b in range(len(cu_rows) - 1)]) if M else np.zeros(0)
+    h = r16(ops.rmsnorm(x, decode(lw.attn_norm), dims.eps))
+    qkv = r16(ops.linear(h, decode(lw.w_qkv)))
+    q = qkv[:, :Hq * D].reshape(M, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(M, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(M, Hkv, D)
+    q = r16(ops.rope(q, pos, dims.theta))
+    k = r16(ops.rope(k, pos, dims.theta))
+    o, Kc, Vc = ops.verify_attention(q, k, v, cu_rows, Kc, Vc, ctx_len, 1.0 / np.sqrt(D))
+    o = r16(o)
+    x = r16(ops.linear(o.reshape(M, Hq * D), decode(lw.w_o), residual=x))
+    h = r16(ops.rmsnorm(x, decode(lw.mlp_norm), dims.eps))
+    gu = r16(ops.linear(h, decode(lw.w_gu)))
+    a = r16(ops.silu_mul(gu[:, :dims.I], gu[:, dims.I:]))
+    x = r16(ops.linear(a, decode(lw.w_down), residual=x))
+    return x, Kc, Vc
+
+
+def head_logits(x, sw: StackWeights, dims: Dims):
+    """Final RMSNorm and LM head: logits [M, V] in fp64 (unrounded)."""
+    h = r16(ops.rmsnorm(x, decode(sw.final_norm), dims.eps))
+    return ops.linear(h, decode(sw.w_lm))
+
+
+def verify_pass(x0, sw: StackWeights, dims: Dims, cu_rows, ctx_len, Kcaches, Vcaches,
+                n_layers: int | None = None):
+    """Run the stack once over all packed verify rows.
+
+    Returns (final hidden x [M, d], logits [M, V] or None if there is no LM
+    head, updated caches).
+    """
+    x = np.asarray(x0, dtype=np.float64)
+    Kc = list(Kcaches)
+    Vc = list(Vcaches)
+    L = len(sw.layers) if n_layers is None else n_layers
+    for li in range(L):
+        x, Kc[li], Vc[li] = layer_forward(x, sw.layers[li], dims, cu_rows, ctx_len, Kc[li], Vc[li])
+    logits = head_logits(x, sw, dims) if sw.w_lm is not None else None
+    return x, logits, Kc, Vc
+
+
+def decode_steps(x0, sw: StackWeights, dims: Dims, cu_rows, ctx_len, Kcaches, Vcaches):
+    """The same rows as gamma_b+1 sequential single-position decode steps.
+
+    Step j feeds row j of every sequence that has one, at context ctx_b + j,
+    with the cache written by steps 0..j-1.  Returns (x [M, d], logits or None,
+    caches) in the packed row order of ``verify_pass``.
+    """
+    x0 = np.asarray(x0, dtype=np.float64)
+    cu = np.asarray(cu_rows)
+    ctx = np.asarray(ctx_len)
+    B = len(cu) - 1
+    rows = cu[1:] - cu[:-1]
+    Kc = [np.array(k, dtype=np.float64, copy=True) for k in Kcaches]
+    Vc = [np.array(v, dtype=np.float64, copy=True) for v in Vcaches]
+    X = np.zeros_like(x0)
+    logits = None
+    for j in range(int(rows.max())):
+        seqs = np.nonzero(rows > j)[0]
+        idx = cu[seqs] + j
+        sub_cu = np.arange(len(seqs) + 1)
+        sub_ctx = ctx[seqs] + j
+        x = x0[idx]
+        sub_K = [k[seqs] for k in Kc]
+        sub_V = [v[seqs] for v in Vc]
+        x, lg, sub_K, sub_V = verify_pass(x, sw, dims, sub_cu, sub_ctx, sub_K, sub_V)
+        for li in range(len(Kc)):
+            Kc[li][seqs] = sub_K[li]
+            Vc[li][seqs] = sub_V[li]
+        X[idx] = x
+        if lg is not None:
+            if logits is None:
+                logits = np.zeros((x0.shape[0], lg.shape[1]))
+            logits[idx] = lg
+    return X, logits, Kc, Vc
