@@ -1,0 +1,207 @@
+/*
+ * spec_verify.h — C ABI of the GB300 (sm_103a) speculative-decoding verify library.
+ *
+ * The library runs the target model's side of one speculative-decoding round:
+ * the verify pass that scores all gamma+1 positions of B sequences in ONE
+ * forward pass (every weight byte read once for M = sum_b (gamma_b + 1) rows),
+ * and the rejection-sampling step that accepts a prefix of the drafts and
+ * emits a correction or bonus token.
+ *
+ * Sources (web pages describing the method):
+ *   [P1] "Speculative Decoding Spends Arithmetic You May Not Have" — section
+ *        "What one iteration actually does" (Algorithm 1) and "The speedup is
+ *        borrowed, and there is a lender".
+ *   [P3] "How Speculative Decoding Works (and When It Doesn't)" — "Prefill and
+ *        Decode", "How speculative decoding works", "Why the output doesn't
+ *        change".
+ *   [P5] "Speculative Decoding Is a Bet on How Predictable Your Traffic Is" —
+ *        "What it looks like in code" (score_parallel, sample_residual).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or copies host memory for them.
+ *   - spec_bf16 is a bf16 bit pattern; matrices are row-major with the given
+ *     leading dimension (elements).  bf16 matrices must start on a 16-byte
+ *     boundary and have a leading dimension that is a multiple of 8.
+ *   - Packed ragged rows: sequence b owns verify rows cu_rows[b] ..
+ *     cu_rows[b+1]-1 (gamma_b + 1 >= 1 rows).  Row 0 of a sequence is its last
+ *     committed token, rows 1..gamma_b are its drafts x_1..x_gamma.  Per-draft
+ *     arrays (Q, draft_tok) hold sum_b gamma_b rows; sequence b's start at
+ *     cu_rows[b] - b.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and may be captured in a CUDA graph.  Arguments are
+ *     checked on the host before anything is launched; on error nothing is
+ *     launched and a non-zero code is returned.  spec_last_error() gives the
+ *     message (per host thread).
+ *   - Workspace: ops with a *_workspace_bytes query need a caller-provided
+ *     device buffer of at least that size, zero-filled before its FIRST use.
+ *     Its first 64 KiB hold arrival counters that the kernels return to zero
+ *     themselves; scratch follows.  So one workspace, sized for the largest
+ *     call, can serve any sequence of calls on one stream without clearing.
+ *     Calls that may run concurrently must not share a workspace.
+ *   - Device-side waits (TMA/MMA pipelines) are bounded; a wait that runs out
+ *     sets a status word read by spec_device_status().
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+typedef uint16_t spec_bf16;
+typedef void* spec_stream;
+
+enum {
+  SPEC_OK = 0,
+  SPEC_EINVAL = 1,        /* bad argument (null pointer, size, alignment) */
+  SPEC_EUNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  SPEC_ECUDA = 3,         /* a CUDA runtime / driver call or launch failed */
+  SPEC_ETIMEOUT = 4       /* a bounded device wait ran out (spec_device_status) */
+};
+
+/* Message of the last failing call on this host thread ("" if none). */
+SPEC_API const char* spec_last_error(void);
+
+/* Library ABI version (increments on any signature change). */
+SPEC_API int spec_version(void);
+
+/* Tuning knobs (process-wide): "gemv_max_m" (0..4, default 4): largest M
+ * that takes the CUDA-core path of spec_verify_linear; "linear_splits" (0..64,
+ * default 0 = automatic): force the K split of the tensor-core path.  Changing
+ * a knob changes spec_linear_workspace_bytes.  Returns SPEC_EINVAL for an
+ * unknown name or value. */
+SPEC_API int spec_set_option(const char* name, int value);
+
+/* Synchronizes `stream`, then reads and clears the current device's status
+ * word (the first problem any kernel recorded since the last read).  Returns
+ * SPEC_OK; SPEC_ETIMEOUT when a bounded wait ran out; SPEC_EINVAL when a
+ * kernel met invalid device-side input (ragged arrays past max_rows or the
+ * cache capacity, draft tokens outside the vocabulary); or SPEC_ECUDA.
+ * *detail (may be NULL) gets the kernel's site code. */
+SPEC_API int spec_device_status(spec_stream stream, int* detail);
+
+/* ------------------------------------------------------------------------ */
+/* Verify linear: Y = X W^T (+ residual)                                     */
+/* ------------------------------------------------------------------------ */
+/* One weight read serves all M verify rows ([P1] "The speedup is borrowed";
+ * [P3] "Prefill and Decode": intensity ~ M FLOP/byte in bf16).
+ *   X        [M x K] bf16, leading dim ldx          (activations)
+ *   W        [N x K] bf16, leading dim ldw           (nn.Linear weight)
+ *   Y        [M x N] bf16, leading dim ldy           (output, fp32 accumulate)
+ *   residual [M x N] bf16, leading dim ldr, or NULL  (added before rounding;
+ *            may alias Y exactly: same pointer and leading dimension)
+ * Requires N >= 1, K % 8 == 0; M = 0 is a no-op.  M <= 4 runs on CUDA cores
+ * (a pure weight stream), larger M on tcgen05 tensor cores with TMA-staged
+ * 128 x 64 weight tiles.  Workspace: spec_linear_workspace_bytes (0 when no
+ * K split is needed; the pointer may then be NULL). */
+SPEC_API size_t spec_linear_workspace_bytes(int M, int N, int K);
+SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,
+                       const spec_bf16* W, int N, int ldw,
+                       spec_bf16* Y, int ldy,
+                       const spec_bf16* residual, int ldr,
+                       void* workspace, size_t workspace_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Verify attention (causal GQA over the KV cache + the new block)           */
+/* ------------------------------------------------------------------------ */
+/* Row j of sequence b sits at position ctx_len[b] + j and attends the
+ * ctx_len[b] committed keys plus new keys 0..j of its own block, which is
+ * what gamma_b + 1 sequential decode steps would see ([P1] Algorithm 1,
+ * parallel line; "the cache read serves every query position").  The new
+ * keys/values are written into the cache at positions ctx_len[b] ..
+ * ctx_len[b] + gamma_b (the caller advances ctx_len by n_acc + 1 afterwards;
+ * entries past that are overwritten next round).
+ *   Q       row r, query head h  at Q + r*ldq + h*D         (bf16, RoPE applied)
+ *   Knew    row r, kv head g     at Knew + r*ldkv + g*D      (bf16, RoPE applied)
+ *   Vnew    row r, kv head g     at Vnew + r*ldkv + g*D
+ *   Kcache, Vcache [B][Hkv][cap][D] bf16 (in/out)
+ *   cu_rows [B+1], ctx_len [B] int32 device arrays; max_rows >= max_b (gamma_b+1)
+ *   O       row r, query head h  at O + r*ldo + h*D          (bf16 out)
+ *   scale   softmax scale (1/sqrt(D) for the standard model)
+ * Query head h reads kv head h / (Hq / Hkv).  Requires D == 128,
+ * Hq % Hkv == 0, (Hq / Hkv) * max_rows <= 64, ctx_len[b] + gamma_b + 1 <= cap.
+ * The last two are checked on the device: a sequence that breaks them is
+ * skipped and the status word is set (spec_device_status).
+ * Workspace: spec_attention_workspace_bytes. */
+SPEC_API size_t spec_attention_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int D, int cap);
+SPEC_API int spec_verify_attention(const spec_bf16* Q, int ldq,
+                          const spec_bf16* Knew, const spec_bf16* Vnew, int ldkv,
+                          const int32_t* cu_rows, const int32_t* ctx_len, int B, int max_rows,
+                          spec_bf16* Kcache, spec_bf16* Vcache, int cap,
+                          int Hq, int Hkv, int D, float scale,
+                          spec_bf16* O, int ldo,
+                          void* workspace, size_t workspace_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* LM head + softmax: P = softmax((H W_lm^T) / T); T == 0 -> one-hot argmax  */
+/* ------------------------------------------------------------------------ */
+/* Produces p_1 .. p_{gamma+1} for every verify row from the same pass
+ * ([P1] Algorithm 1).  Greedy ties go to the lowest token index.
+ *   H   [M x K] bf16 (final-normed hidden states), W_lm [V x K] bf16
+ *   P   [M x V] fp32 out
+ * Requires V % 128 == 0, K % 8 == 0, temperature >= 0.
+ * Workspace: spec_lmhead_workspace_bytes. */
+SPEC_API size_t spec_lmhead_workspace_bytes(int M, int K, int V);
+SPEC_API int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                        float temperature, float* P,
+                        void* workspace, size_t workspace_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Rejection sampler (one CTA per sequence)                                  */
+/* ------------------------------------------------------------------------ */
+/* [P1] Algorithm 1 in order: accept x_i iff U_i * q_i(x_i) <= p_i(x_i)
+ * (exact product; q = 0 accepts), stop at the first rejection n; draw t from
+ * max(0, p_{n+1} - q_{n+1}) (falling back to p_{n+1} if that is all zero) when
+ * n < gamma, else from p_{gamma+1} (bonus).  t is the smallest token x with
+ * sum_{y<=x} w(y) > u * sum_y w(y), summed in fp64, u = U[row gamma_b].
+ *   P [M x V] fp32, Q [sum gamma x V] fp32, draft_tok [sum gamma] int32,
+ *   U [M] fp32 in (0,1): rows 0..gamma_b-1 = acceptance draws, row gamma_b =
+ *   the draw for t.
+ *   n_acc [B] out: accepted drafts n_b in 0..gamma_b
+ *   out_tok [M] out: sequence b emits out_tok[cu_rows[b] .. cu_rows[b]+n_b]
+ *                    (x_1..x_n, t); later slots are set to -1
+ *   near_tie [B] out: decisions with |u*q - p| < tie_eps plus a final pick
+ *                    whose CDF boundary is within tie_eps * sum(w) of u*sum(w)
+ * Requires V >= 1, draft tokens in [0, V) (an out-of-range token is clamped
+ * and flagged in the status word). */
+SPEC_API int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
+                       const float* U, const int32_t* cu_rows, int B, int V,
+                       float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                       spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Layer glue of the decoder stack (not on the pages)         */
+/* ------------------------------------------------------------------------ */
+/* Y = X / sqrt(mean(X^2) + eps) * w per row; X [M x N], w [N] bf16.
+ * Y may alias X.  Requires N % 8 == 0, N <= 16384. */
+SPEC_API int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, float eps,
+                 spec_bf16* Y, int ldy, spec_stream stream);
+
+/* In-place rotary embedding (rotate-half pairs (i, i + D/2), frequency
+ * theta^(-2i/D)) on Hq query heads at Q + r*ldq + h*D and Hkv key heads at
+ * K + r*ldk + g*D; row r of sequence b is at position ctx_len[b] + (r - cu_rows[b]).
+ * Requires D even, D <= 256. */
+SPEC_API int spec_rope(spec_bf16* Q, int ldq, int Hq, spec_bf16* K, int ldk, int Hkv, int D,
+              const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, float theta,
+              spec_stream stream);
+
+/* A[r, i] = silu(GU[r, i]) * GU[r, I + i] for i < I (gate columns then up
+ * columns).  Requires I % 8 == 0. */
+SPEC_API int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int lda,
+                  spec_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,273 @@
+"""Python binding of ``libspecverify.so`` — argument marshalling only.
+
+Every function here has the name of the C entry point it wraps.  It reads
+shapes, strides and device pointers off torch tensors, passes them through
+ctypes and raises :class:`SpecError` on a non-zero status.  All arithmetic
+of the verify round runs in the library's CUDA kernels; torch only provides
+device memory and the current stream.  If the library is missing the import
+fails loudly: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SPEC_OK, SPEC_EINVAL, SPEC_EUNSUPPORTED, SPEC_ECUDA, SPEC_ETIMEOUT = range(5)
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "spec_last_error": (ctypes.c_char_p, []),
+    "spec_version": (_i, []),
+    "spec_set_option": (_i, [ctypes.c_char_p, _i]),
+    "spec_device_status": (_i, [_vp, ctypes.POINTER(_i)]),
+    "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
+    "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
+    "spec_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "spec_verify_attention": (_i, [_vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp, _i,
+                                   _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
+    "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
+    "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
+    "spec_reject_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _vp, _vp, _vp, _vp]),
+    "spec_rmsnorm": (_i, [_vp, _i, _i, _i, _vp, _f, _vp, _i, _vp]),
+    "spec_rope": (_i, [_vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp]),
+    "spec_silu_mul": (_i, [_vp, _i, _i, _i, _vp, _i, _vp]),
+}
+EXPORTS = tuple(_SIGS)
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[spec code {code}] {msg}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library and declare every exported signature (no device work)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(the verify path has no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = load()
+
+
+def _check(rc: int) -> None:
+    if rc != SPEC_OK:
+        raise SpecError(rc, _lib.spec_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _rowmajor(t: torch.Tensor, name: str) -> int:
+    """Leading dimension of a 2-D tensor whose rows are contiguous."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with contiguous rows")
+    return t.stride(0)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA {dtype} tensor")
+
+
+# --------------------------------------------------------------------------- misc
+def spec_version() -> int:
+    return _lib.spec_version()
+
+
+def spec_set_option(name: str, value: int) -> None:
+    _check(_lib.spec_set_option(name.encode(), int(value)))
+
+
+def spec_device_status(stream=None) -> int:
+    """Synchronize and read/clear the device status word (raises on a timeout)."""
+    detail = ctypes.c_int(0)
+    _check(_lib.spec_device_status(_stream(stream), ctypes.byref(detail)))
+    return detail.value
+
+
+class Workspace:
+    """A zero-filled device buffer that grows on demand (plumbing for the kernels' scratch).
+
+    One Workspace can serve every call issued on one stream: the library keeps
+    its counters at zero between calls.
+    """
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = None
+        if nbytes:
+            self.ensure(nbytes)
+
+    def ensure(self, nbytes: int) -> "Workspace":
+        if nbytes and (self.buf is None or self.buf.numel() < nbytes):
+            self.buf = torch.zeros(int(nbytes), dtype=torch.uint8, device=self.device)
+        return self
+
+    def args(self):
+        if self.buf is None:
+            return None, 0
+        return ctypes.c_void_p(self.buf.data_ptr()), self.buf.numel()
+
+
+def _ws_args(ws: Workspace | None, need: int, device):
+    if need == 0:
+        return (ws.args() if ws is not None else (None, 0))
+    if ws is None:
+        ws = Workspace(device)
+    ws.ensure(need)
+    return ws.args()
+
+
+# --------------------------------------------------------------------------- verify linear
+def spec_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return _lib.spec_linear_workspace_bytes(M, N, K)
+
+
+def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None, stream=None):
+    """Y[M, N] = X[M, K] @ W[N, K]^T (+ residual), bf16 in/out, fp32 accumulate."""
+    _need(X, torch.bfloat16, "X"); _need(W, torch.bfloat16, "W")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("W must be [N, K]")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _need(Y, torch.bfloat16, "Y")
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual")
+    wp, wn = _ws_args(ws, spec_linear_workspace_bytes(M, N, K), X.device)
+    _check(_lib.spec_verify_linear(
+        _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
+        _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
+        wp, wn, _stream(stream)))
+    return Y
+
+
+# --------------------------------------------------------------------------- attention
+def spec_attention_workspace_bytes(B, max_rows, Hq, Hkv, D, cap) -> int:
+    return _lib.spec_attention_workspace_bytes(B, max_rows, Hq, Hkv, D, cap)
+
+
+def spec_verify_attention(Q, Knew, Vnew, cu_rows, ctx_len, Kcache, Vcache, max_rows: int,
+                          scale: float | None = None, O=None, ws: Workspace | None = None,
+                          stream=None):
+    """Causal GQA verify attention; appends Knew/Vnew to the cache at ctx_len.
+
+    Q [M, Hq*D] and Knew/Vnew [M, Hkv*D] are 2-D (possibly strided column
+    slices of a fused QKV output); Kcache/Vcache [B, Hkv, cap, D].
+    """
+    for t, n in ((Q, "Q"), (Knew, "Knew"), (Vnew, "Vnew"), (Kcache, "Kcache"), (Vcache, "Vcache")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_rows, torch.int32, "cu_rows"); _need(ctx_len, torch.int32, "ctx_len")
+    B, Hkv, cap, D = Kcache.shape
+    if not (Kcache.is_contiguous() and Vcache.is_contiguous() and Vcache.shape == Kcache.shape):
+        raise ValueError("Kcache/Vcache must be contiguous [B, Hkv, cap, D]")
+    M = Q.shape[0]
+    Hq = Q.shape[1] // D
+    ldkv = _rowmajor(Knew, "Knew")
+    if _rowmajor(Vnew, "Vnew") != ldkv:
+        raise ValueError("Knew and Vnew must share a leading dimension")
+    if O is None:
+        O = torch.empty((M, Hq * D), dtype=torch.bfloat16, device=Q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    wp, wn = _ws_args(ws, spec_attention_workspace_bytes(B, max_rows, Hq, Hkv, D, cap), Q.device)
+    _check(_lib.spec_verify_attention(
+        _p(Q), _rowmajor(Q, "Q"), _p(Knew), _p(Vnew), ldkv, _p(cu_rows), _p(ctx_len), B,
+        int(max_rows), _p(Kcache), _p(Vcache), cap, Hq, Hkv, D, float(scale), _p(O),
+        _rowmajor(O, "O"), wp, wn, _stream(stream)))
+    return O
+
+
+# --------------------------------------------------------------------------- LM head
+def spec_lmhead_workspace_bytes(M, K, V) -> int:
+    return _lib.spec_lmhead_workspace_bytes(M, K, V)
+
+
+def spec_lmhead_softmax(H, Wlm, temperature: float, P=None, ws: Workspace | None = None, stream=None):
+    """P[M, V] = softmax(H @ Wlm^T / T) in fp32; T == 0 gives one-hot argmax rows."""
+    _need(H, torch.bfloat16, "H"); _need(Wlm, torch.bfloat16, "Wlm")
+    M, K = H.shape
+    V = Wlm.shape[0]
+    if not (H.is_contiguous() and Wlm.is_contiguous()):
+        raise ValueError("H and Wlm must be contiguous")
+    if P is None:
+        P = torch.empty((M, V), dtype=torch.float32, device=H.device)
+    _need(P, torch.float32, "P")
+    wp, wn = _ws_args(ws, spec_lmhead_workspace_bytes(M, K, V), H.device)
+    _check(_lib.spec_lmhead_softmax(_p(H), M, K, _p(Wlm), V, float(temperature), _p(P), wp, wn,
+                                    _stream(stream)))
+    return P
+
+
+# --------------------------------------------------------------------------- sampler
+def spec_reject_sample(P, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5, out=None, stream=None):
+    """Returns (n_acc [B], out_tok [M], near_tie [B]) int32 device tensors."""
+    _need(P, torch.float32, "P"); _need(Q, torch.float32, "Q"); _need(U, torch.float32, "U")
+    _need(draft_tok, torch.int32, "draft_tok"); _need(cu_rows, torch.int32, "cu_rows")
+    M, V = P.shape
+    B = cu_rows.numel() - 1
+    if out is None:
+        dev = P.device
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(M, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    n_acc, out_tok, near = out
+    for t in (P, Q, U, draft_tok, cu_rows):
+        if not t.is_contiguous():
+            raise ValueError("sampler inputs must be contiguous")
+    _check(_lib.spec_reject_sample(_p(P), _p(Q), _p(draft_tok), _p(U), _p(cu_rows), B, V,
+                                   float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)))
+    return n_acc, out_tok, near
+
+
+# --------------------------------------------------------------------------- glue
+def spec_rmsnorm(X, w, eps: float = 1e-6, Y=None, stream=None):
+    _need(X, torch.bfloat16, "X"); _need(w, torch.bfloat16, "w")
+    M, N = X.shape
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _check(_lib.spec_rmsnorm(_p(X), M, N, _rowmajor(X, "X"), _p(w), float(eps), _p(Y),
+                             _rowmajor(Y, "Y"), _stream(stream)))
+    return Y
+
+
+def spec_rope(Q, K, cu_rows, ctx_len, D: int, theta: float = 1e6, stream=None):
+    """In-place RoPE on Q [M, Hq*D] and K [M, Hkv*D] (2-D, contiguous rows)."""
+    _need(Q, torch.bfloat16, "Q"); _need(K, torch.bfloat16, "K")
+    M = Q.shape[0]
+    B = cu_rows.numel() - 1
+    _check(_lib.spec_rope(_p(Q), _rowmajor(Q, "Q"), Q.shape[1] // D, _p(K), _rowmajor(K, "K"),
+                          K.shape[1] // D, D, _p(cu_rows), _p(ctx_len), B, M, float(theta),
+                          _stream(stream)))
+
+
+def spec_silu_mul(GU, A=None, stream=None):
+    """A[M, I] = silu(GU[:, :I]) * GU[:, I:2I]."""
+    _need(GU, torch.bfloat16, "GU")
+    M, two_i = GU.shape
+    inter = two_i // 2
+    if A is None:
+        A = torch.empty((M, inter), dtype=torch.bfloat16, device=GU.device)
+    _check(_lib.spec_silu_mul(_p(GU), M, inter, _rowmajor(GU, "GU"), _p(A), _rowmajor(A, "A"),
+                              _stream(stream)))
+    return A

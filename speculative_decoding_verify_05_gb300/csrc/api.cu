@@ -1,0 +1,497 @@
+// C ABI of the verify library: argument checks, launch planning (tile widths,
+// split-K, key chunks), TMA tensor-map encoding and dispatch to the kernels.
+// Nothing here allocates device memory; workspaces come from the caller.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/spec_verify.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace spec;
+
+// Library status word: a bounded device wait that runs out records its site here.
+__device__ unsigned g_spec_status;
+
+namespace {
+
+constexpr int kVersion = 1;
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+int ok() {
+  t_err.clear();
+  return SPEC_OK;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SPEC_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DevInfo {
+  int sms = 0;
+  unsigned* status = nullptr;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int dev_info(DevInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SPEC_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_spec_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<unsigned*>(p);
+  }
+  *out = &d;
+  return SPEC_OK;
+}
+
+// sm count for planning without touching the device (workspace queries may
+// run before any context exists): falls back to the GB300's 152.
+int plan_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev[dev].sms > 0) return g_dev[dev].sms;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      return n;
+  }
+  cudaGetLastError();
+  return 152;
+}
+
+// --------------------------------------------------------------------------- TMA
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(SPEC_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  return SPEC_OK;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, rank-1 entries)
+int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+  if (int rc = get_encoder()) return rc;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPEC_ECUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return SPEC_OK;
+}
+
+// --------------------------------------------------------------------------- workspace layout
+// Every workspace starts with a fixed counter region that kernels leave at
+// zero; scratch (fp32 partials, statistics) follows.  Because the counters
+// always sit at the same place, one zero-filled workspace can serve any
+// sequence of calls on one stream, whatever their shapes.
+constexpr size_t kCounterBytes = 64 * 1024;
+constexpr size_t kMaxCounters = kCounterBytes / 4;
+
+// --------------------------------------------------------------------------- linear plan
+int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
+int g_force_splits = 0;  // tunable: 0 = heuristic
+
+struct LinPlan {
+  bool gemv = false;
+  int BN = 16, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
+  int gemv_grid = 1, k_per_split = 0, groups = 0;
+  size_t counters_off = 0, partial_off = 0, bytes = 0;
+};
+
+int choose_splits(int tiles, int k_steps, int sms, int min_steps) {
+  if (g_force_splits > 0) return std::min(g_force_splits, std::max(1, k_steps));
+  if (tiles >= 2 * sms) return 1;
+  const int smax = std::max(1, std::min(32, k_steps / min_steps));
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= smax; ++s) {
+    const double units = double(tiles) * s / sms;
+    const double eff = units / std::ceil(units);
+    if (eff >= 0.9) return s;
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+  }
+  return best;
+}
+
+LinPlan plan_linear(int M, int N, int K, bool lmhead) {
+  LinPlan p;
+  const int sms = plan_sms();
+  p.k_tiles = (K + 63) / 64;
+  if (!lmhead && M <= g_gemv_max_m && M <= 4) {
+    p.gemv = true;
+    const int ks = gemv_k_slice(M);
+    p.k_per_split = ks;
+    p.splits = (K + ks - 1) / ks;
+    if ((size_t)(N + 3) / 4 > kMaxCounters) p.splits = 1;   // (only for N > 65536)
+    p.groups = (N + 3) / 4;
+    const long long items = (long long)p.groups * p.splits;
+    long long grid = (items + 7) / 8;
+    if (grid > (long long)sms * 8) grid = (long long)sms * 8;
+    p.gemv_grid = (int)std::max(1LL, grid);
+    p.counters_off = 0;
+    p.partial_off = kCounterBytes;
+    p.bytes = p.splits > 1 ? kCounterBytes + round_up(size_t(p.splits) * M * N * 4, 256) : 0;
+    return p;
+  }
+  p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
+  const int per = (M + p.tiles_m - 1) / p.tiles_m;
+  p.BN = std::max(16, (per + 15) / 16 * 16);
+  p.tiles_n = (N + 127) / 128;
+  const int tiles = p.tiles_m * p.tiles_n;
+  p.counters_off = 0;
+  p.partial_off = kCounterBytes;
+  if (lmhead) {
+    p.splits = 1;
+    p.bytes = kCounterBytes + round_up(size_t(M) * p.tiles_n * sizeof(float2), 256);
+    return p;
+  }
+  const int smem = linear_tc_smem_bytes(p.BN);
+  int cps = (228 * 1024) / (smem + 1024);
+  cps = std::max(1, std::min(cps, 512 / linear_tc_tmem_cols(p.BN)));
+  p.splits = choose_splits(tiles, p.k_tiles, sms, 4);
+  if ((size_t)tiles > kMaxCounters) p.splits = 1;
+  (void)cps;
+  p.bytes = p.splits > 1 ? kCounterBytes + round_up(size_t(tiles) * p.splits * p.BN * 128 * 4, 256) : 0;
+  return p;
+}
+
+// --------------------------------------------------------------------------- attention plan
+struct AttnPlan {
+  int chunk = 256, max_chunks = 1;
+  size_t counters_off = 0, partial_off = 0, bytes = 0;
+};
+
+AttnPlan plan_attention(int B, int Hkv, int cap) {
+  AttnPlan p;
+  const int sms = plan_sms();
+  const double keys = double(B) * Hkv * cap;
+  int chunk = 256;
+  while (chunk < 4096 && keys / (chunk * 2) >= 8.0 * sms) chunk *= 2;
+  p.chunk = chunk;
+  p.max_chunks = std::max(1, (cap + chunk - 1) / chunk);
+  p.counters_off = 0;
+  p.partial_off = kCounterBytes;
+  p.bytes = kCounterBytes + round_up(size_t(B) * Hkv * p.max_chunks * 64 * (128 + 2) * 4, 256);
+  return p;
+}
+
+}  // namespace
+
+// =========================================================================== C ABI
+extern "C" {
+
+const char* spec_last_error(void) { return t_err.c_str(); }
+int spec_version(void) { return kVersion; }
+
+int spec_set_option(const char* name, int value) {
+  if (!name) return fail(SPEC_EINVAL, "option name is NULL");
+  if (!strcmp(name, "gemv_max_m")) {
+    if (value < 0 || value > 4) return fail(SPEC_EINVAL, "gemv_max_m must be in [0, 4]");
+    g_gemv_max_m = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_splits")) {
+    if (value < 0 || value > 64) return fail(SPEC_EINVAL, "linear_splits must be in [0, 64]");
+    g_force_splits = value;
+    return ok();
+  }
+  return fail(SPEC_EINVAL, "unknown option '%s'", name);
+}
+
+int spec_device_status(spec_stream stream, int* detail) {
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (detail) *detail = (int)v;
+  if (v) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    if ((v & 0xF0u) == 0xF0u)
+      return fail(SPEC_EINVAL, "a kernel rejected device-side input (site 0x%x)", v);
+    return fail(SPEC_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", v);
+  }
+  return ok();
+}
+
+// --------------------------------------------------------------------------- linear
+size_t spec_linear_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return plan_linear(M, N, K, false).bytes;
+}
+
+int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                       int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
+                       void* workspace, size_t workspace_bytes, spec_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
+  if (M == 0) return ok();
+  if (!X || !W || !Y) return fail(SPEC_EINVAL, "X, W and Y must be non-NULL");
+  if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
+  if (ldx < K || ldw < K || ldy < N || (residual && ldr < N))
+    return fail(SPEC_EINVAL, "leading dimensions too small");
+  if (ldx % 8 || ldw % 8 || ldy % 8 || (residual && ldr % 8))
+    return fail(SPEC_EINVAL, "leading dimensions must be multiples of 8");
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (residual && !aligned16(residual)))
+    return fail(SPEC_EINVAL, "X, W, Y, residual must be 16-byte aligned");
+  if (residual && residual != Y) {
+    const char* y0 = reinterpret_cast<const char*>(Y);
+    const char* y1 = reinterpret_cast<const char*>(Y + (size_t)(M - 1) * ldy + N);
+    const char* r0 = reinterpret_cast<const char*>(residual);
+    const char* r1 = reinterpret_cast<const char*>(residual + (size_t)(M - 1) * ldr + N);
+    if (r0 < y1 && y0 < r1) return fail(SPEC_EINVAL, "residual overlaps Y without being Y");
+  }
+  if (residual == Y && ldr != ldy) return fail(SPEC_EINVAL, "residual aliases Y with another ldr");
+  LinPlan p = plan_linear(M, N, K, false);
+  if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes))
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (p.gemv) {
+    GemvArgs a;
+    a.X = X; a.ldx = ldx; a.W = W; a.ldw = ldw; a.Y = Y; a.ldy = ldy;
+    a.residual = residual; a.ldr = ldr; a.M = M; a.N = N; a.K = K;
+    a.splits = p.splits; a.k_per_split = p.k_per_split;
+    a.partial = p.splits > 1 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
+    a.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
+    cudaError_t e = launch_gemv(a, p.gemv_grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    return ok();
+  }
+  CUtensorMap tw, tx;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W")) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
+  }
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.splits = p.splits; a.tiles_m = p.tiles_m;
+  a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
+  a.partial = p.splits > 1 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
+  a.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
+  a.status = d->status;
+  dim3 grid(p.tiles_m, p.tiles_n, p.splits);
+  cudaError_t e = launch_linear_tc_bf16(p.BN, tw, tx, a, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
+  return ok();
+}
+
+// --------------------------------------------------------------------------- LM head
+size_t spec_lmhead_workspace_bytes(int M, int K, int V) {
+  if (M <= 0 || K <= 0 || V <= 0) return 0;
+  return plan_linear(M, V, K, true).bytes;
+}
+
+int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                        float temperature, float* P, void* workspace, size_t workspace_bytes,
+                        spec_stream stream) {
+  if (M < 0 || K <= 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d", M, K, V);
+  if (M == 0) return ok();
+  if (!H || !Wlm || !P) return fail(SPEC_EINVAL, "H, Wlm and P must be non-NULL");
+  if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
+  if (V % 4) return fail(SPEC_EINVAL, "V=%d must be a multiple of 4", V);
+  if (!(temperature >= 0.f) || std::isinf(temperature))
+    return fail(SPEC_EINVAL, "temperature must be finite and >= 0");
+  if (!aligned16(H) || !aligned16(Wlm) || !aligned16(P))
+    return fail(SPEC_EINVAL, "H, Wlm, P must be 16-byte aligned");
+  LinPlan p = plan_linear(M, V, K, true);
+  if (!workspace || workspace_bytes < p.bytes)
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tw, tx;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)V};
+    cuuint64_t str[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (int rc = encode_bf16(&tw, Wlm, 2, dims, str, box, "Wlm")) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    if (int rc = encode_bf16(&tx, H, 2, dims, str, box, "H")) return rc;
+  }
+  const bool greedy = temperature == 0.f;
+  LinearArgs a{};
+  a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.splits = 1; a.tiles_m = p.tiles_m;
+  a.status = d->status;
+  a.inv_temp = greedy ? 1.f : 1.f / temperature;
+  a.P = P;
+  a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
+  a.n_tiles = p.tiles_n;
+  dim3 grid(p.tiles_m, p.tiles_n, 1);
+  cudaError_t e = launch_linear_tc_lmhead(p.BN, greedy, tw, tx, a, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
+  e = launch_lmhead_normalize(P, a.stats, M, V, p.tiles_n, greedy, s);
+  if (e != cudaSuccess) return cuda_fail(e, "LM-head normalize launch");
+  return ok();
+}
+
+// --------------------------------------------------------------------------- attention
+size_t spec_attention_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int D, int cap) {
+  if (B <= 0 || max_rows <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || cap <= 0) return 0;
+  return plan_attention(B, Hkv, cap).bytes;
+}
+
+int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
+                          const spec_bf16* Vnew, int ldkv, const int32_t* cu_rows,
+                          const int32_t* ctx_len, int B, int max_rows, spec_bf16* Kcache,
+                          spec_bf16* Vcache, int cap, int Hq, int Hkv, int D, float scale,
+                          spec_bf16* O, int ldo, void* workspace, size_t workspace_bytes,
+                          spec_stream stream) {
+  if (B < 0) return fail(SPEC_EINVAL, "B=%d < 0", B);
+  if (B == 0) return ok();
+  if (!Q || !Knew || !Vnew || !cu_rows || !ctx_len || !Kcache || !Vcache || !O)
+    return fail(SPEC_EINVAL, "NULL tensor argument");
+  if (D != 128) return fail(SPEC_EUNSUPPORTED, "head_dim %d: only 128 is implemented", D);
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return fail(SPEC_EINVAL, "Hq=%d must be a multiple of Hkv=%d", Hq, Hkv);
+  const int G = Hq / Hkv;
+  if ((size_t)B * Hkv > kMaxCounters) return fail(SPEC_EUNSUPPORTED, "B*Hkv = %d > %zu", B * Hkv, kMaxCounters);
+  if (max_rows <= 0) return fail(SPEC_EINVAL, "max_rows must be >= 1");
+  if (G * max_rows > 64)
+    return fail(SPEC_EUNSUPPORTED, "(Hq/Hkv)*max_rows = %d > 64 query rows per kv head", G * max_rows);
+  if (cap <= 0) return fail(SPEC_EINVAL, "cap must be >= 1");
+  if (ldq < Hq * D || ldkv < Hkv * D || ldo < Hq * D || ldq % 8 || ldkv % 8 || ldo % 8)
+    return fail(SPEC_EINVAL, "bad leading dimensions");
+  if (!aligned16(Q) || !aligned16(Knew) || !aligned16(Vnew) || !aligned16(Kcache) ||
+      !aligned16(Vcache) || !aligned16(O))
+    return fail(SPEC_EINVAL, "bf16 tensors must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(SPEC_EINVAL, "scale must be finite");
+  AttnPlan p = plan_attention(B, Hkv, cap);
+  if (!workspace || workspace_bytes < p.bytes)
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  CUtensorMap tk, tv;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)cap, (cuuint64_t)B * Hkv};
+  cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)cap * D * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache")) return rc;
+  if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache")) return rc;
+  char* ws = static_cast<char*>(workspace);
+  AttnArgs a{};
+  a.Q = Q; a.ldq = ldq; a.Knew = Knew; a.Vnew = Vnew; a.ldkv = ldkv;
+  a.cu_rows = cu_rows; a.ctx_len = ctx_len; a.Kc = Kcache; a.Vc = Vcache; a.cap = cap;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = G; a.max_rows = max_rows;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.O = O; a.ldo = ldo;
+  a.chunk = p.chunk; a.max_chunks = p.max_chunks;
+  a.partial = reinterpret_cast<float*>(ws + p.partial_off);
+  a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
+  a.status = d->status;
+  cudaError_t e = launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+// --------------------------------------------------------------------------- sampler
+int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok, const float* U,
+                       const int32_t* cu_rows, int B, int V, float tie_eps, int32_t* n_acc,
+                       int32_t* out_tok, int32_t* near_tie, spec_stream stream) {
+  if (B < 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes B=%d V=%d", B, V);
+  if (B == 0) return ok();
+  if (!P || !Q || !draft_tok || !U || !cu_rows || !n_acc || !out_tok || !near_tie)
+    return fail(SPEC_EINVAL, "NULL argument");
+  if (!(tie_eps >= 0.f)) return fail(SPEC_EINVAL, "tie_eps must be >= 0");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = launch_reject_sample(P, Q, draft_tok, U, cu_rows, B, V, tie_eps, n_acc, out_tok,
+                                       near_tie, d->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reject_sample launch");
+  return ok();
+}
+
+// --------------------------------------------------------------------------- glue
+int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, float eps,
+                 spec_bf16* Y, int ldy, spec_stream stream) {
+  if (M < 0 || N <= 0) return fail(SPEC_EINVAL, "bad sizes");
+  if (M == 0) return ok();
+  if (!X || !w || !Y) return fail(SPEC_EINVAL, "NULL argument");
+  if (N % 8 || N > 16384) return fail(SPEC_EUNSUPPORTED, "N=%d must be a multiple of 8 and <= 16384", N);
+  if (ldx < N || ldy < N || ldx % 8 || ldy % 8) return fail(SPEC_EINVAL, "bad leading dimensions");
+  if (!aligned16(X) || !aligned16(w) || !aligned16(Y)) return fail(SPEC_EINVAL, "16-byte alignment");
+  if (!(eps >= 0.f)) return fail(SPEC_EINVAL, "eps must be >= 0");
+  cudaError_t e = launch_rmsnorm(X, M, N, ldx, w, eps, Y, ldy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+  return ok();
+}
+
+int spec_rope(spec_bf16* Q, int ldq, int Hq, spec_bf16* K, int ldk, int Hkv, int D,
+              const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, float theta,
+              spec_stream stream) {
+  if (M < 0 || B < 0) return fail(SPEC_EINVAL, "bad sizes");
+  if (M == 0) return ok();
+  if (B == 0) return fail(SPEC_EINVAL, "rows without sequences");
+  if (!Q || !K || !cu_rows || !ctx_len) return fail(SPEC_EINVAL, "NULL argument");
+  if (D <= 0 || D % 2 || D > 256) return fail(SPEC_EUNSUPPORTED, "D=%d must be even and <= 256", D);
+  if (Hq < 0 || Hkv < 0 || ldq < Hq * D || ldk < Hkv * D) return fail(SPEC_EINVAL, "bad heads / strides");
+  if (!(theta > 0.f)) return fail(SPEC_EINVAL, "theta must be > 0");
+  cudaError_t e = launch_rope(Q, ldq, Hq, K, ldk, Hkv, D, cu_rows, ctx_len, B, M, theta,
+                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+  return ok();
+}
+
+int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int lda,
+                  spec_stream stream) {
+  if (M < 0 || I <= 0) return fail(SPEC_EINVAL, "bad sizes");
+  if (M == 0) return ok();
+  if (!GU || !A) return fail(SPEC_EINVAL, "NULL argument");
+  if (I % 8 || ldgu < 2 * I || lda < I || ldgu % 8 || lda % 8) return fail(SPEC_EINVAL, "bad sizes / strides");
+  if (!aligned16(GU) || !aligned16(A)) return fail(SPEC_EINVAL, "16-byte alignment");
+  cudaError_t e = launch_silu_mul(GU, M, I, ldgu, A, lda, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "silu_mul launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "linear_tc.cuh"
+
+namespace spec {
+
+// ---- tcgen05 GEMM: token tile widths instantiated (multiples of 16 up to 256)
+constexpr int kMaxBN = 256;
+int linear_tc_smem_bytes(int BN);
+int linear_tc_tmem_cols(int BN);
+cudaError_t launch_linear_tc_bf16(int BN, const CUtensorMap& tw, const CUtensorMap& tx,
+                                  const LinearArgs& a, dim3 grid, cudaStream_t s);
+cudaError_t launch_linear_tc_lmhead(int BN, bool greedy, const CUtensorMap& tw,
+                                    const CUtensorMap& tx, const LinearArgs& a, dim3 grid,
+                                    cudaStream_t s);
+
+// ---- CUDA-core skinny GEMM (M <= 4)
+struct GemvArgs {
+  const uint16_t* X; int ldx;
+  const uint16_t* W; int ldw;
+  uint16_t* Y; int ldy;
+  const uint16_t* residual; int ldr;
+  int M, N, K;
+  int splits;           // K split count
+  int k_per_split;      // multiple of 256 elements
+  float* partial;       // [splits][M][N]
+  unsigned* counters;   // [ceil(N / rows_per_group)]
+};
+int gemv_k_slice(int M);   // K elements per split for an M-row pass
+cudaError_t launch_gemv(const GemvArgs& a, int grid, cudaStream_t s);
+
+// ---- softmax normalisation of the LM head output
+cudaError_t launch_lmhead_normalize(float* P, const float2* stats, int M, int V, int n_tiles,
+                                    bool greedy, cudaStream_t s);
+
+// ---- verify attention
+struct AttnArgs {
+  const uint16_t* Q; int ldq;
+  const uint16_t* Knew; const uint16_t* Vnew; int ldkv;
+  const int32_t* cu_rows; const int32_t* ctx_len;
+  uint16_t* Kc; uint16_t* Vc; int cap;
+  int B, Hq, Hkv, G, max_rows;
+  float scale_log2;     // softmax scale * log2(e)
+  uint16_t* O; int ldo;
+  int chunk;            // keys per CTA (multiple of 64)
+  int max_chunks;
+  float* partial;       // [B*Hkv][max_chunks][64][128 + 2]
+  unsigned* counters;   // [B*Hkv]
+  unsigned* status;
+};
+cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                             cudaStream_t s);
+
+// ---- rejection sampler
+cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* draft,
+                                 const float* U, const int32_t* cu_rows, int B, int V,
+                                 float tie_eps, int32_t* n_acc, int32_t* out_tok,
+                                 int32_t* near_tie, unsigned* status, cudaStream_t s);
+
+// ---- glue
+cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
+                           uint16_t* Y, int ldy, cudaStream_t s);
+cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int Hkv, int D,
+                        const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, float theta,
+                        cudaStream_t s);
+cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
+                            cudaStream_t s);
+
+}  // namespace spec

@@ -1,0 +1,152 @@
+"""Verify-round driver for a Qwen3-8B-shaped decoder stack, built on the C ABI.
+
+This is the caller's side of the library boundary: it owns device buffers
+(torch allocations), walks the layers and issues one library call per step
+of the verify pass, all on the current stream so that a whole round can be
+captured in one CUDA graph.  It computes nothing itself.
+
+Layer reading (the pages give only the shape: 36 layers, 32 query / 8 kv
+heads of 128, grouped-query attention, a 151936-token vocabulary): pre-RMSNorm
+(eps 1e-6), fused QKV projection, RoPE (theta 1e6, rotate-half) on q and k,
+causal verify attention over the cache, O projection + residual, RMSNorm,
+fused gate/up projection, SwiGLU, down projection + residual; final RMSNorm
+and LM head.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import binding as S
+
+
+@dataclass
+class Dims:
+    d: int = 4096
+    Hq: int = 32
+    Hkv: int = 8
+    D: int = 128
+    I: int = 12288
+    V: int = 151936
+    layers: int = 36
+    eps: float = 1e-6
+    theta: float = 1e6
+
+    @property
+    def qkv(self) -> int:
+        return (self.Hq + 2 * self.Hkv) * self.D
+
+
+@dataclass
+class LayerW:
+    w_qkv: torch.Tensor      # [(Hq + 2 Hkv) D, d]
+    w_o: torch.Tensor        # [d, Hq D]
+    w_gu: torch.Tensor       # [2 I, d]  gate rows then up rows
+    w_down: torch.Tensor     # [d, I]
+    attn_norm: torch.Tensor  # [d]
+    mlp_norm: torch.Tensor   # [d]
+
+
+@dataclass
+class StackW:
+    layers: list = field(default_factory=list)
+    final_norm: torch.Tensor | None = None
+    w_lm: torch.Tensor | None = None
+
+
+def random_stack(dims: Dims, seed: int, device, std: float = 0.02, with_head: bool = True) -> StackW:
+    """Random-init bf16 weights N(0, std^2) of the stack's shapes (norm weights = 1)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def w(rows, cols):
+        t = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+        t.normal_(0.0, std, generator=g)
+        return t
+
+    ones = torch.ones(dims.d, dtype=torch.bfloat16, device=device)
+    sw = StackW()
+    for _ in range(dims.layers):
+        sw.layers.append(LayerW(w(dims.qkv, dims.d), w(dims.d, dims.Hq * dims.D), w(2 * dims.I, dims.d),
+                                w(dims.d, dims.I), ones, ones))
+    sw.final_norm = ones
+    if with_head:
+        sw.w_lm = w(dims.V, dims.d)
+    return sw
+
+
+class VerifyEngine:
+    """Buffers + call sequence of one verify pass / round for up to ``max_M`` rows."""
+
+    def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, max_M: int, max_rows: int,
+                 device=None):
+        self.dims = dims
+        self.w = weights
+        self.kc = kcaches
+        self.vc = vcaches
+        self.max_M = max_M
+        self.max_rows = max_rows
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.device = dev
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.x = torch.empty((max_M, dims.d), **bf)
+        self.h = torch.empty((max_M, dims.d), **bf)
+        self.qkv = torch.empty((max_M, dims.qkv), **bf)
+        self.o = torch.empty((max_M, dims.Hq * dims.D), **bf)
+        self.gu = torch.empty((max_M, 2 * dims.I), **bf)
+        self.a = torch.empty((max_M, dims.I), **bf)
+        self.P = torch.empty((max_M, dims.V), dtype=torch.float32, device=dev) if weights.w_lm is not None else None
+        B, cap = (kcaches[0].shape[0], kcaches[0].shape[2]) if kcaches else (1, 1)
+        need = 0
+        for M in range(1, max_M + 1):
+            for (n, k) in ((dims.qkv, dims.d), (dims.d, dims.Hq * dims.D), (2 * dims.I, dims.d),
+                           (dims.d, dims.I)):
+                need = max(need, S.spec_linear_workspace_bytes(M, n, k))
+        if kcaches:
+            need = max(need, S.spec_attention_workspace_bytes(B, max_rows, dims.Hq, dims.Hkv, dims.D, cap))
+        if weights.w_lm is not None:
+            need = max(need, S.spec_lmhead_workspace_bytes(max_M, dims.d, dims.V))
+        self.ws = S.Workspace(dev, need)
+
+    # ------------------------------------------------------------------ one layer
+    def layer(self, li: int, M: int, cu_rows, ctx_len, B: int, max_rows: int):
+        dm, lw = self.dims, self.w.layers[li]
+        x, h, qkv, o, gu, a = (self.x[:M], self.h[:M], self.qkv[:M], self.o[:M], self.gu[:M], self.a[:M])
+        hq = dm.Hq * dm.D
+        hk = dm.Hkv * dm.D
+        S.spec_rmsnorm(x, lw.attn_norm, dm.eps, Y=h)
+        S.spec_verify_linear(h, lw.w_qkv, Y=qkv, ws=self.ws)
+        q, k, v = qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:]
+        S.spec_rope(q, k, cu_rows, ctx_len, dm.D, dm.theta)
+        S.spec_verify_attention(q, k, v, cu_rows, ctx_len, self.kc[li], self.vc[li], max_rows, O=o,
+                                ws=self.ws)
+        S.spec_verify_linear(o, lw.w_o, Y=x, residual=x, ws=self.ws)
+        S.spec_rmsnorm(x, lw.mlp_norm, dm.eps, Y=h)
+        S.spec_verify_linear(h, lw.w_gu, Y=gu, ws=self.ws)
+        S.spec_silu_mul(gu, A=a)
+        S.spec_verify_linear(a, lw.w_down, Y=x, residual=x, ws=self.ws)
+
+    def verify_pass(self, x0, cu_rows, ctx_len, temperature: float, max_rows: int | None = None,
+                    n_layers: int | None = None):
+        """All layers + LM head over the packed rows; returns P [M, V] (fp32 view)."""
+        M = x0.shape[0]
+        B = cu_rows.numel() - 1
+        max_rows = self.max_rows if max_rows is None else max_rows
+        if M > self.max_M:
+            raise ValueError("more rows than the engine was sized for")
+        if x0.data_ptr() != self.x.data_ptr():
+            self.x[:M].copy_(x0)
+        L = len(self.w.layers) if n_layers is None else n_layers
+        for li in range(L):
+            self.layer(li, M, cu_rows, ctx_len, B, max_rows)
+        if self.w.w_lm is None:
+            return None
+        S.spec_rmsnorm(self.x[:M], self.w.final_norm, self.dims.eps, Y=self.h[:M])
+        return S.spec_lmhead_softmax(self.h[:M], self.w.w_lm, temperature, P=self.P[:M], ws=self.ws)
+
+    def verify_round(self, x0, cu_rows, ctx_len, q, drafts, U, temperature: float,
+                     tie_eps: float = 1e-5, max_rows: int | None = None, out=None):
+        """Verify pass + rejection sampler; returns (n_acc, out_tok, near_tie)."""
+        P = self.verify_pass(x0, cu_rows, ctx_len, temperature, max_rows)
+        return S.spec_reject_sample(P, q, drafts, U, cu_rows, tie_eps, out=out)

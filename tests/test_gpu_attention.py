@@ -1,0 +1,99 @@
+"""GPU parity of spec_verify_attention against the oracle (outputs and cache append)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import bf16 as obf, ops as oops
+
+from gpu_util import assert_close_rel, bf16_dev, bits_of, dev, f64_of_bf16
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def run_case(lib, gammas, ctx, Hq, Hkv, seed, cap=None, fused_qkv=True):
+    batch = synth.RaggedBatch(gammas, ctx, cap)
+    M, B = batch.M, batch.B
+    G = Hq // Hkv
+    width = (Hq + 2 * Hkv) * D
+    qkv = synth.normal_bf16_bits(seed, (M, width), 1.0)
+    kc = synth.normal_bf16_bits(seed + 1, (B, Hkv, batch.cap, D), 1.0)
+    vc = synth.normal_bf16_bits(seed + 2, (B, Hkv, batch.cap, D), 1.0)
+    qkv_d = bf16_dev(qkv)
+    hq, hk = Hq * D, Hkv * D
+    if fused_qkv:
+        Qd, Kd, Vd = qkv_d[:, :hq], qkv_d[:, hq:hq + hk], qkv_d[:, hq + hk:]
+    else:
+        Qd, Kd, Vd = (qkv_d[:, :hq].contiguous(), qkv_d[:, hq:hq + hk].contiguous(),
+                      qkv_d[:, hq + hk:].contiguous())
+    kcd, vcd = bf16_dev(kc), bf16_dev(vc)
+    scale = 1.0 / math.sqrt(D)
+    O = lib.spec_verify_attention(Qd, Kd, Vd, dev(batch.cu_rows), dev(batch.ctx_len), kcd, vcd,
+                                  batch.max_rows, scale=scale)
+    lib.spec_device_status()
+    q = obf.decode(qkv[:, :hq]).reshape(M, Hq, D)
+    k = obf.decode(qkv[:, hq:hq + hk]).reshape(M, Hkv, D)
+    v = obf.decode(qkv[:, hq + hk:]).reshape(M, Hkv, D)
+    Oref, Kref, Vref = oops.verify_attention(q, k, v, batch.cu_rows, obf.decode(kc), obf.decode(vc),
+                                             batch.ctx_len, scale)
+    assert_close_rel(f64_of_bf16(O).reshape(M, Hq, D), Oref, f"attention B={B} G={G}")
+    # the cache append is a byte copy: bit-exact
+    assert np.array_equal(obf.decode(bits_of(kcd)), Kref)
+    assert np.array_equal(obf.decode(bits_of(vcd)), Vref)
+    return batch
+
+
+@pytest.mark.parametrize("gammas,ctx,Hq,Hkv", [
+    ([0], [0], 4, 1),                         # a single key: output = its value
+    ([4], [37], 32, 8),                       # config-1-like row count, GQA 4
+    ([2, 0, 5], [7, 70, 0], 8, 2),            # ragged, one empty context
+    ([10, 3, 7, 1], [130, 64, 511, 1000], 32, 8),   # 11 rows x 4 heads = 44 rows (4 m-tiles)
+    ([3, 3], [300, 2], 16, 4),                # 16 rows: one m-tile
+    ([6, 1], [90, 63], 16, 8),                # G = 2
+    ([15], [5], 4, 1),                        # G*rows = 64 exactly
+])
+def test_attention_small(lib, gammas, ctx, Hq, Hkv):
+    run_case(lib, gammas, ctx, Hq, Hkv, seed=sum(ctx) + len(gammas))
+
+
+def test_attention_split_kv_long_context(lib):
+    # long contexts with few sequences: several key chunks per (sequence, kv head)
+    run_case(lib, [4, 2], [3000, 4096], 32, 8, seed=77)
+
+
+def test_attention_separate_qkv_buffers(lib):
+    run_case(lib, [4, 1], [200, 17], 32, 8, seed=5, fused_qkv=False)
+
+
+def test_attention_cap_with_slack(lib):
+    run_case(lib, [3, 9], [100, 500], 32, 8, seed=6, cap=700)
+
+
+def test_attention_row_equals_single_decode(lib):
+    """Row j of a verify block equals a one-row call at context ctx + j (caches after j steps)."""
+    gam, ctx, Hq, Hkv = 5, 150, 32, 8
+    width = (Hq + 2 * Hkv) * D
+    M = gam + 1
+    qkv = bf16_dev(synth.normal_bf16_bits(31, (M, width), 1.0))
+    kc0 = bf16_dev(synth.normal_bf16_bits(32, (1, Hkv, 200, D), 1.0))
+    vc0 = bf16_dev(synth.normal_bf16_bits(33, (1, Hkv, 200, D), 1.0))
+    hq, hk = Hq * D, Hkv * D
+    kc, vc = kc0.clone(), vc0.clone()
+    Ov = lib.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:],
+                                   dev(np.array([0, M], np.int32)), dev(np.array([ctx], np.int32)),
+                                   kc, vc, M)
+    kd, vd = kc0.clone(), vc0.clone()
+    rows = []
+    for j in range(M):
+        r = qkv[j:j + 1]
+        rows.append(lib.spec_verify_attention(r[:, :hq], r[:, hq:hq + hk], r[:, hq + hk:],
+                                              dev(np.array([0, 1], np.int32)),
+                                              dev(np.array([ctx + j], np.int32)), kd, vd, 1))
+    lib.spec_device_status()
+    Od = torch.cat(rows)
+    assert torch.equal(kc, kd) and torch.equal(vc, vd)
+    assert_close_rel(f64_of_bf16(Ov), f64_of_bf16(Od), "verify vs sequential decode", rel=1e-2)

@@ -1,0 +1,93 @@
+"""GPU parity of spec_verify_linear (CUDA-core and tcgen05 paths) against the oracle."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import bf16 as obf, ops as oops
+
+from gpu_util import assert_close_rel, bf16_dev, f64_of_bf16
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # (M, N, K): ragged tails in every dimension, several M tiles, split-K on and off
+    (1, 256, 512), (2, 384, 1000), (3, 200, 264), (4, 1024, 4096),
+    (5, 512, 4096), (7, 136, 72), (16, 640, 264), (17, 256, 520), (40, 1024, 512),
+    (100, 256, 768), (256, 384, 128), (300, 384, 512), (513, 128, 256),
+]
+
+
+def run_case(lib, M, N, K, residual, seed, gemv_max_m=4, splits=0, std=0.05):
+    X = synth.normal_bf16_bits(seed, (M, K), 1.0)
+    W = synth.normal_bf16_bits(seed + 1, (N, K), std)
+    R = synth.normal_bf16_bits(seed + 2, (M, N), 1.0) if residual else None
+    lib.spec_set_option("gemv_max_m", gemv_max_m)
+    lib.spec_set_option("linear_splits", splits)
+    try:
+        Y = lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), residual=bf16_dev(R) if residual else None)
+        lib.spec_device_status()
+    finally:
+        lib.spec_set_option("gemv_max_m", 4)
+        lib.spec_set_option("linear_splits", 0)
+    ref = oops.linear(obf.decode(X), obf.decode(W), obf.decode(R) if residual else None)
+    assert_close_rel(f64_of_bf16(Y), ref, f"linear M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("residual", [False, True])
+def test_linear_default_path(lib, M, N, K, residual):
+    run_case(lib, M, N, K, residual, seed=M * 7 + N + K)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_linear_tensor_core_path_at_tiny_m(lib, M):
+    run_case(lib, M, 768, 1024, True, seed=40 + M, gemv_max_m=0)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_linear_forced_splits(lib, splits):
+    run_case(lib, 24, 512, 1536, True, seed=90 + splits, gemv_max_m=0, splits=splits)
+
+
+def test_linear_residual_aliases_output(lib):
+    import torch
+    M, N, K = 6, 256, 512
+    X = synth.normal_bf16_bits(5, (M, K), 1.0)
+    W = synth.normal_bf16_bits(6, (N, K), 0.05)
+    R = synth.normal_bf16_bits(7, (M, N), 1.0)
+    Yd = bf16_dev(R).clone()
+    lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), Y=Yd, residual=Yd)
+    lib.spec_device_status()
+    ref = oops.linear(obf.decode(X), obf.decode(W), obf.decode(R))
+    assert_close_rel(f64_of_bf16(Yd), ref, "aliased residual")
+
+
+def test_linear_repeat_reuses_workspace(lib):
+    """Counters return to zero: the same workspace serves many split-K calls."""
+    ws = lib.Workspace()
+    X = synth.normal_bf16_bits(8, (5, 4096), 1.0)
+    W = synth.normal_bf16_bits(9, (4096, 4096), 0.02)
+    ref = oops.linear(obf.decode(X), obf.decode(W))
+    Xd, Wd = bf16_dev(X), bf16_dev(W)
+    lib.spec_set_option("gemv_max_m", 0)
+    try:
+        for _ in range(3):
+            Y = lib.spec_verify_linear(Xd, Wd, ws=ws)
+            assert_close_rel(f64_of_bf16(Y), ref, "repeat")
+    finally:
+        lib.spec_set_option("gemv_max_m", 4)
+    lib.spec_device_status()
+
+
+def test_linear_strided_output_slice(lib):
+    """Y written into a column slice of a wider buffer (leading dimension > N)."""
+    import torch
+    M, N, K = 9, 256, 384
+    X = synth.normal_bf16_bits(11, (M, K), 1.0)
+    W = synth.normal_bf16_bits(12, (N, K), 0.05)
+    big = torch.zeros((M, 3 * N), dtype=torch.bfloat16, device="cuda")
+    lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), Y=big[:, N:2 * N])
+    lib.spec_device_status()
+    ref = oops.linear(obf.decode(X), obf.decode(W))
+    assert_close_rel(f64_of_bf16(big[:, N:2 * N]), ref, "strided Y")
+    assert torch.count_nonzero(big[:, :N]) == 0 and torch.count_nonzero(big[:, 2 * N:]) == 0

@@ -1,0 +1,94 @@
+"""CPU checks of the C ABI library: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch
+(no device is touched by these calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def built():
+    from speculative_decoding_verify_05_gb300.build import build
+    return build()
+
+
+def header_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^SPEC_API\s+[\w\s\*]+?\b(spec_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    syms = header_symbols()
+    for name in ("spec_verify_linear", "spec_verify_attention", "spec_lmhead_softmax",
+                 "spec_reject_sample"):
+        assert name in syms
+    assert len(syms) >= 14
+
+
+def test_library_exports_every_declared_symbol(built):
+    lib = ctypes.CDLL(built)
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {built}").read()
+    exported = set(re.findall(r" T (spec_\w+)", out))
+    assert exported == set(header_symbols())
+
+
+def test_binding_covers_the_header(built):
+    from speculative_decoding_verify_05_gb300 import binding
+    assert sorted(binding.EXPORTS) == header_symbols()
+    assert binding.spec_version() == 1
+
+
+def test_host_side_validation(built):
+    from speculative_decoding_verify_05_gb300 import binding as S
+    L = S._lib
+    E = S.SPEC_EINVAL
+    # null tensors, bad K, bad leading dimension
+    assert L.spec_verify_linear(None, 4, 64, 64, None, 128, 64, None, 128, None, 0, None, 0, None) == E
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.spec_verify_linear(fake, 4, 60, 64, fake, 128, 64, fake, 128, None, 0, None, 0, None) == E
+    assert b"multiple of 8" in L.spec_last_error()
+    assert L.spec_verify_linear(fake, 4, 64, 32, fake, 128, 64, fake, 128, None, 0, None, 0, None) == E
+    # misaligned pointer
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert L.spec_verify_linear(odd, 4, 64, 64, fake, 128, 64, fake, 128, None, 0, None, 0, None) == E
+    # M = 0 is a no-op that succeeds without touching anything
+    assert L.spec_verify_linear(None, 0, 64, 64, None, 128, 64, None, 128, None, 0, None, 0, None) == 0
+    # attention: unsupported head dim, too many rows per kv head
+    args = [fake, 32 * 64, fake, fake, 8 * 64, fake, fake, 2, 5, fake, fake, 64, 32, 8, 64, 0.1, fake,
+            32 * 64, None, 0, None]
+    assert L.spec_verify_attention(*args) == S.SPEC_EUNSUPPORTED
+    args = [fake, 32 * 128, fake, fake, 8 * 128, fake, fake, 2, 17, fake, fake, 64, 32, 8, 128, 0.1, fake,
+            32 * 128, None, 0, None]
+    assert L.spec_verify_attention(*args) == S.SPEC_EUNSUPPORTED
+    # workspace too small
+    args[-3] = fake
+    args[-2] = 16
+    args[8] = 4
+    assert L.spec_verify_attention(*args) == E
+    assert b"workspace" in L.spec_last_error()
+    # LM head: negative temperature, V not a multiple of 4
+    assert L.spec_lmhead_softmax(fake, 2, 64, fake, 128, -1.0, fake, fake, 1 << 30, None) == E
+    assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
+    # sampler: null outputs
+    assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # options
+    assert L.spec_set_option(b"no_such_knob", 1) == E
+    assert L.spec_set_option(b"gemv_max_m", 9) == E
+    assert L.spec_set_option(b"gemv_max_m", 4) == 0
+
+
+def test_workspace_queries_are_host_only(built):
+    from speculative_decoding_verify_05_gb300 import binding as S
+    # split-K needs counters + partials; the counter region is a fixed 64 KiB
+    n = S.spec_linear_workspace_bytes(5, 4096, 4096)
+    assert n == 0 or n > 64 * 1024
+    assert S.spec_attention_workspace_bytes(8, 5, 32, 8, 128, 4101) > 64 * 1024
+    assert S.spec_lmhead_workspace_bytes(40, 4096, 151936) >= 64 * 1024 + 40 * 1187 * 8
+    assert S.spec_linear_workspace_bytes(0, 4096, 4096) == 0
