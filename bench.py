@@ -1,0 +1,565 @@
+"""Benchmark of one speculative-decoding verify round on GB300.
+
+Workload (one "step" = one whole verify round over one batch):
+  ragged full verify round — B = 64 sequences, gamma_b ~ U{1..10} drafts each,
+  committed contexts ctx_b ~ U[128, 8192], a 36-layer Qwen3-8B-shaped stack
+  (d 4096, 32 q / 8 kv heads of 128, MLP 12288) with random-init bf16 weights
+  N(0, 0.02), the 151936-token LM head + softmax at T = 0.7, and the
+  rejection sampler with Philox uniforms (seed 0).  All inputs are synthetic.
+
+Metric: accepted tokens per second = sum_b (n_b + 1) / verify-round time,
+measured with CUDA events over K CUDA-graph replays of the round (inputs
+resident in HBM; weights + KV cache of ~93 GB are far larger than L2, so no
+flush is needed).  Extra keys: verify-round microseconds and whole-round HBM
+GB/s, the weight-read amortisation of the linear stack (M = 5 vs M = 1),
+the dominant kernel's roofline, the oracle's CPU throughput on a bounded
+sample, and the end-to-end number with host buffers.
+
+``--impl reference`` times the CPU oracle on the same workload instead.
+Under torchrun every rank runs an independent replica (weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify-round accepted tokens/sec (B*(gamma+1) rows, full stack + LM head + sampler)"
+UNIT = "tokens/s"
+WORKLOAD = ("ragged full verify round: B=64, gamma_b~U{1..10}, ctx_b~U[128,8192], 36-layer "
+            "Qwen3-8B-shaped stack + 151936-vocab LM head + rejection sampler, T=0.7, Philox seed 0")
+B, G_LO, G_HI, CTX_LO, CTX_HI = 64, 1, 10, 128, 8192
+TEMP, SIGMA, SEED = 0.7, 1.0, 0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- workload
+def make_batch():
+    import synth
+    return synth.ragged_batch(SEED, B, G_LO, G_HI, CTX_LO, CTX_HI)
+
+
+def algorithmic_bytes(batch, dims):
+    """Bytes the round must move at minimum (weights once, KV once, activations, p)."""
+    lin_w = dims.layers * 2 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    kv = dims.layers * 2 * int(np.sum(batch.ctx_len.astype(np.int64) + batch.gammas + 1)) * dims.Hkv * dims.D * 2
+    head = 2 * dims.V * dims.d + batch.M * dims.V * 4
+    return lin_w, kv, head
+
+
+def attention_bytes(batch, dims):
+    """Per attention launch: K/V cache read + new K/V + Q read + O write."""
+    keys = int(np.sum(batch.ctx_len.astype(np.int64)))
+    kv = keys * dims.Hkv * dims.D * 2 * 2
+    new = batch.M * dims.Hkv * dims.D * 2 * 2 * 2          # read new k,v and write them to the cache
+    qo = batch.M * dims.Hq * dims.D * 2 * 2
+    return kv + new + qo
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from speculative_decoding_verify_05_gb300 import binding as S
+    from speculative_decoding_verify_05_gb300 import engine as E
+    import synth
+
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+    dims = E.Dims()
+    batch = make_batch()
+    cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
+    torch.manual_seed(1234 + rank)
+
+    # ---- resident model state: weights, KV caches (random), inputs
+    sw = E.random_stack(dims, seed=1000 + rank, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(2000 + rank)
+    kcs, vcs = [], []
+    for _ in range(dims.layers):
+        k = torch.empty((B, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        k.normal_(0, 1, generator=g)
+        v.normal_(0, 1, generator=g)
+        kcs.append(k)
+        vcs.append(v)
+    eng = E.VerifyEngine(dims, sw, kcs, vcs, max_M=batch.M, max_rows=batch.max_rows, device=dev)
+    x0 = torch.empty((batch.M, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+    cu = torch.from_numpy(batch.cu_rows).to(dev)
+    ctx = torch.from_numpy(batch.ctx_len).to(dev)
+    U = torch.from_numpy(synth.uniforms_f32(SEED, batch.M)).to(dev)
+
+    # ---- draft distribution: the target's probabilities perturbed in logit space
+    # (q = softmax(log p + (sigma / T) * noise), i.e. logits + N(0, sigma^2) at temperature T)
+    eng.x[:batch.M].copy_(x0)
+    P0 = eng.verify_pass(eng.x[:batch.M], cu, ctx, TEMP).clone()
+    qrows = np.concatenate([np.arange(batch.cu_rows[b], batch.cu_rows[b] + batch.gammas[b]) for b in range(B)])
+    lp = torch.log(P0[torch.from_numpy(qrows).to(dev)].clamp_min(1e-38))
+    noise = torch.empty_like(lp).normal_(0, 1, generator=g)
+    q = torch.softmax(lp + (SIGMA / TEMP) * noise, dim=1).contiguous()
+    drafts = torch.multinomial(q, 1, generator=g).view(-1).to(torch.int32)
+    del P0, lp, noise
+    out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(batch.M, dtype=torch.int32, device=dev),
+           torch.empty(B, dtype=torch.int32, device=dev))
+
+    S.reset_launch_count()
+
+    def step():
+        eng.x[:batch.M].copy_(x0)
+        eng.verify_round(eng.x[:batch.M], cu, ctx, q, drafts, U, TEMP, out=out)
+
+    # eager warm-up (loads every kernel), then capture the round in one CUDA graph
+    step()
+    torch.cuda.synchronize()
+    S.spec_device_status()
+    stream = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    S.reset_launch_count()
+    with torch.cuda.stream(stream):
+        step()                                       # side-stream warm-up before capture
+    torch.cuda.synchronize()
+    S.reset_launch_count()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = S.launch_count()
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    S.spec_device_status()
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    ev0.record(cur)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(cur)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    n_acc = out[0].cpu().numpy()
+    near = int(out[2].sum().item())
+    accepted = int(n_acc.sum()) + B
+    S.spec_device_status()
+
+    t = torch.tensor([ms], device=dev)
+    tok = torch.tensor([float(accepted)], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tok, op=dist.ReduceOp.SUM)
+    ms_max = float(t.item())
+    value = float(tok.item()) / (ms_max / 1e3)
+
+    lin_w, kv, head = algorithmic_bytes(batch, dims)
+    round_gbs = (lin_w + kv + head) / (ms / 1e3) / 1e9
+
+    # ---- per-kernel timing (eager, CUDA events on the launching stream)
+    per = kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src)
+
+    # ---- weight-read amortisation of the linear stack: M = 5 verify vs M = 1 decode
+    lin = linear_stack_ratio(eng, dims, S, hbm_peak, peak_src)
+
+    # ---- end to end through the public API with host buffers
+    e2e = end_to_end(args, eng, batch, dims, q, drafts, x0, S, torch, dev)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = cpu_baseline(eng, batch, dims, kcs, vcs, sw, q, drafts) if world >= 1 and rank == 0 and not args.no_cpu else None
+    dominant = max(per.values(), key=lambda r: r["total_ms"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 softmax, fp64 sampler sums)",
+        "data": "synthetic (random-init weights, random KV cache and hidden states, seeded)",
+        "config": {"workload": WORKLOAD, "B": B, "M_rows": batch.M, "sum_ctx": int(batch.ctx_len.sum()),
+                   "cap": cap, "l2": "inputs larger than L2 (15.1 GB weights + %.1f GB KV read per round)" % (kv / 1e9),
+                   "graph": "whole round captured in one CUDA graph"},
+        "round_us": ms * 1e3,
+        "round_hbm_gbs": round_gbs,
+        "round_hbm_frac": round_gbs / hbm_peak,
+        "accepted_tokens_per_round": accepted,
+        "mean_acceptance_length": accepted / B,
+        "near_ties": near,
+        "roofline": dominant["roofline"],
+        "kernels": {k: {kk: vv for kk, vv in v.items() if kk != "roofline"} | {"roofline": v["roofline"]}
+                    for k, v in per.items()},
+        "linear_stack": lin,
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src, reps=3):
+    """Average launch time of each hot kernel over all 36 layers (eager, CUDA events)."""
+    import torch
+    M = batch.M
+    res = {}
+    cur = torch.cuda.current_stream()
+
+    def timeit(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record(cur)
+        for _ in range(reps):
+            fn()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * n)
+
+    L = dims.layers
+    hq, hk = dims.Hq * dims.D, dims.Hkv * dims.D
+    qkv = eng.qkv[:M]
+
+    def attn_all():
+        for li in range(L):
+            S.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:], cu, ctx,
+                                    eng.kc[li], eng.vc[li], eng.max_rows, O=eng.o[:M], ws=eng.ws)
+    t_attn = timeit(attn_all, L)
+    ab = attention_bytes(batch, dims)
+    res["verify_attention"] = {"avg_launch_us": t_attn * 1e3, "launches_per_round": L,
+                               "total_ms": t_attn * L,
+                               "roofline": {"kernel": "verify_attention", "bound": "hbm",
+                                            "achieved": ab / (t_attn / 1e3) / 1e9, "peak": hbm_peak,
+                                            "unit": "GB/s", "frac": ab / (t_attn / 1e3) / 1e9 / hbm_peak,
+                                            "traffic": None, "algorithmic_bytes": ab,
+                                            "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}}
+    shapes = {"qkv": (dims.qkv, dims.d), "o": (dims.d, hq), "gate_up": (2 * dims.I, dims.d),
+              "down": (dims.d, dims.I)}
+    xs = {"qkv": eng.h[:M], "o": eng.o[:M], "gate_up": eng.h[:M], "down": eng.a[:M]}
+    ys = {"qkv": eng.qkv[:M], "o": eng.h[:M], "gate_up": eng.gu[:M], "down": eng.h[:M]}
+    tot_t, tot_f, tot_b = 0.0, 0.0, 0.0
+    for name, (N, K) in shapes.items():
+        w_attr = {"qkv": "w_qkv", "o": "w_o", "gate_up": "w_gu", "down": "w_down"}[name]
+
+        def lin_all(name=name, w_attr=w_attr):
+            for li in range(L):
+                S.spec_verify_linear(xs[name], getattr(eng.w.layers[li], w_attr), Y=ys[name], ws=eng.ws)
+        t = timeit(lin_all, L)
+        tot_t += t * L
+        tot_f += 2.0 * M * N * K * L
+        tot_b += 2.0 * N * K * L
+    lin_tflops = tot_f / (tot_t / 1e3) / 1e12
+    res["verify_linear"] = {"avg_launch_us": tot_t / (4 * L) * 1e3, "launches_per_round": 4 * L,
+                            "total_ms": tot_t,
+                            "roofline": {"kernel": "verify_linear (tcgen05, M=%d)" % M, "bound": "tensor",
+                                         "achieved": lin_tflops, "peak": tc_sust, "unit": "TFLOP/s",
+                                         "frac": lin_tflops / tc_sust, "traffic": None,
+                                         "algorithmic_flops": tot_f / (4 * L),
+                                         "hbm_gbs": tot_b / (tot_t / 1e3) / 1e9,
+                                         "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS, in a long step)"}}
+    h = eng.h[:M]
+
+    def head():
+        S.spec_lmhead_softmax(h, eng.w.w_lm, TEMP, P=eng.P[:M], ws=eng.ws)
+    t_head = timeit(head, 1)
+    hb = 2.0 * dims.V * dims.d + 3.0 * M * dims.V * 4
+    res["lmhead_softmax"] = {"avg_launch_us": t_head * 1e3, "launches_per_round": 2, "total_ms": t_head,
+                             "roofline": {"kernel": "lmhead_softmax", "bound": "hbm",
+                                          "achieved": hb / (t_head / 1e3) / 1e9, "peak": hbm_peak,
+                                          "unit": "GB/s", "frac": hb / (t_head / 1e3) / 1e9 / hbm_peak,
+                                          "traffic": None, "algorithmic_bytes": hb,
+                                          "tflops": 2.0 * M * dims.V * dims.d / (t_head / 1e3) / 1e12,
+                                          "peak_source": f"{peak_src} hbm_gbs"}}
+    return res
+
+
+def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
+    """36-layer linear stack (QKV, O, gate/up, down) at M = 5 and M = 1 rows."""
+    import torch
+    cur = torch.cuda.current_stream()
+    out = {}
+    wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    for M in (1, 5):
+        def run():
+            for lw in eng.w.layers:
+                S.spec_verify_linear(eng.h[:M], lw.w_qkv, Y=eng.qkv[:M], ws=eng.ws)
+                S.spec_verify_linear(eng.o[:M], lw.w_o, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
+                S.spec_verify_linear(eng.h[:M], lw.w_gu, Y=eng.gu[:M], ws=eng.ws)
+                S.spec_verify_linear(eng.a[:M], lw.w_down, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            run()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(reps):
+            g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / reps
+        gbs = wbytes / (t / 1e3) / 1e9
+        out[f"m{M}_us"] = t * 1e3
+        out[f"m{M}_hbm_gbs"] = gbs
+        out[f"m{M}_hbm_frac"] = gbs / hbm_peak
+    out["ratio_m5_over_m1"] = out["m5_us"] / out["m1_us"]
+    out["weights_gb"] = wbytes / 1e9
+    out["note"] = "36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph per M; peak " + peak_src
+    return out
+
+
+def end_to_end(args, eng, batch, dims, q, drafts, x0, S, torch, dev, steps=None):
+    """Same round through the public API with pinned host inputs and a host read of the result."""
+    steps = steps or max(3, min(args.steps, 10))
+    h_x = torch.empty(x0.shape, dtype=x0.dtype, pin_memory=True).copy_(x0.cpu())
+    h_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q.cpu())
+    h_d = torch.empty(drafts.shape, dtype=drafts.dtype, pin_memory=True).copy_(drafts.cpu())
+    import synth
+    h_u = torch.from_numpy(synth.uniforms_f32(SEED, batch.M)).pin_memory()
+    h_cu = torch.from_numpy(batch.cu_rows).pin_memory()
+    h_ctx = torch.from_numpy(batch.ctx_len).pin_memory()
+    d_x = torch.empty_like(x0)
+    d_q = torch.empty_like(q)
+    d_d = torch.empty_like(drafts)
+    d_u = torch.empty(batch.M, dtype=torch.float32, device=dev)
+    d_cu = torch.empty_like(h_cu, device=dev)
+    d_ctx = torch.empty_like(h_ctx, device=dev)
+    out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(batch.M, dtype=torch.int32, device=dev),
+           torch.empty(B, dtype=torch.int32, device=dev))
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out]
+    bi = sum(t.numel() * t.element_size() for t in (h_x, h_q, h_d, h_u, h_cu, h_ctx))
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for d, h in ((d_x, h_x), (d_q, h_q), (d_d, h_d), (d_u, h_u), (d_cu, h_cu), (d_ctx, h_ctx)):
+            d.copy_(h, non_blocking=True)
+        eng.verify_round(d_x, d_cu, d_ctx, d_q, d_d, d_u, TEMP, out=out)
+        for h, d in zip(h_out, out):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    accepted = int(h_out[0].sum().item()) + B
+    return {"value": accepted / dt, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": dt * 1e3, "steps": steps,
+            "how": "eager public-API calls (binding -> C ABI) per layer, pinned H2D inputs, D2H results, wall clock"}
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_sample(n_seq, weights_np, kv_np, batch, x0_bits, q_sample, drafts_sample, U_sample):
+    """One bounded oracle run: layer 0 + LM head + sampler on the first n_seq sequences.
+
+    Returns (seconds for 36 layers + head + sampler, accepted tokens).
+    """
+    import synth
+    from oracle import bf16 as obf, ops as oops, sampler as osamp, stack as ostack
+    od = ostack.Dims()
+    sub = synth.RaggedBatch(batch.gammas[:n_seq], batch.ctx_len[:n_seq])
+    lw, final_norm, w_lm = weights_np
+    kc, vc = kv_np
+    x = obf.decode(x0_bits[:sub.M])
+    t0 = time.perf_counter()
+    x1, _, _ = ostack.layer_forward(x, lw, od, sub.cu_rows, sub.ctx_len, obf.decode(kc), obf.decode(vc))
+    t_layer = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    sw = ostack.StackWeights([], final_norm, w_lm)
+    logits = ostack.head_logits(x1, sw, od)
+    p = oops.target_probs(logits, TEMP)
+    t_head = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    n_acc, out, near = osamp.reject_sample(p.astype(np.float32), q_sample, drafts_sample, U_sample, sub.cu_rows)
+    t_samp = time.perf_counter() - t0
+    return od.layers * t_layer + t_head + t_samp, int(n_acc.sum()) + n_seq, (t_layer, t_head, t_samp)
+
+
+def cpu_baseline(eng, batch, dims, kcs, vcs, sw, q, drafts, n_seq=4):
+    """Oracle on the host cores over a bounded sample of this run's inputs (copied to the host)."""
+    import torch
+    from oracle import stack as ostack
+    import synth
+    sub = synth.RaggedBatch(batch.gammas[:n_seq], batch.ctx_len[:n_seq])
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    l0 = sw.layers[0]
+    lw = ostack.LayerWeights(bits(l0.w_qkv), bits(l0.w_o), bits(l0.w_gu), bits(l0.w_down),
+                             bits(l0.attn_norm), bits(l0.mlp_norm))
+    capn = int((sub.ctx_len + sub.gammas + 1).max())
+    kv = (bits(kcs[0][:n_seq, :, :capn]), bits(vcs[0][:n_seq, :, :capn]))
+    x0 = bits(eng.x[:sub.M])
+    # the oracle's own draft inputs for the sampled sequences: same q rows / drafts
+    q_s = q[:sub.n_drafts].cpu().numpy()
+    d_s = drafts[:sub.n_drafts].cpu().numpy()
+    U_s = synth.uniforms_f32(SEED, batch.M)[:sub.M]
+    secs, acc, parts = oracle_sample(n_seq, (lw, bits(sw.final_norm), bits(sw.w_lm)), kv, batch, x0, q_s, d_s, U_s)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": acc / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n_seq} of {B} sequences ({sub.M} rows): oracle layer 0 timed and counted 36x, "
+                      f"plus final norm + LM head + softmax + sampler; tokens = their accepted tokens",
+            "seconds_per_round": secs, "layer_s": parts[0], "head_s": parts[1], "sampler_s": parts[2]}
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    from oracle import bf16 as obf, ops as oops, stack as ostack
+    batch = make_batch()
+    dims = ostack.Dims()
+    n_seq = 2 if args.steps + args.warmup > 12 else 4
+    sub = synth.RaggedBatch(batch.gammas[:n_seq], batch.ctx_len[:n_seq])
+    capn = int((sub.ctx_len + sub.gammas + 1).max())
+    # same distributions as the GPU arm, generated on the host (numpy Philox)
+    lw = ostack.LayerWeights(
+        synth.normal_bf16_bits(1001, (dims.Hq * dims.D + 2 * dims.Hkv * dims.D, dims.d), 0.02),
+        synth.normal_bf16_bits(1002, (dims.d, dims.Hq * dims.D), 0.02),
+        synth.normal_bf16_bits(1003, (2 * dims.I, dims.d), 0.02),
+        synth.normal_bf16_bits(1004, (dims.d, dims.I), 0.02),
+        synth.f32_to_bf16_bits(np.ones(dims.d, np.float32)), synth.f32_to_bf16_bits(np.ones(dims.d, np.float32)))
+    w_lm = synth.normal_bf16_bits(1005, (dims.V, dims.d), 0.02)
+    ones = synth.f32_to_bf16_bits(np.ones(dims.d, np.float32))
+    kc = synth.normal_bf16_bits(1006, (n_seq, dims.Hkv, capn, dims.D), 1.0)
+    vc = synth.normal_bf16_bits(1007, (n_seq, dims.Hkv, capn, dims.D), 1.0)
+    x0 = synth.normal_bf16_bits(1008, (sub.M, dims.d), 1.0)
+    # draft q from the oracle's own logits for these rows (layer 0 + head stand-in, computed once)
+    x1, _, _ = ostack.layer_forward(obf.decode(x0), lw, dims, sub.cu_rows, sub.ctx_len, obf.decode(kc), obf.decode(vc))
+    logits = ostack.head_logits(x1, ostack.StackWeights([], ones, w_lm), dims)
+    q_s, d_s = synth.draft_distribution(logits, sub, SIGMA, TEMP, seed=SEED + 5)
+    U_s = synth.uniforms_f32(SEED, batch.M)[:sub.M]
+    for _ in range(args.warmup):
+        oracle_sample(n_seq, (lw, ones, w_lm), (kc, vc), batch, x0, q_s, d_s, U_s)
+    tot_s, tot_tok = 0.0, 0
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        s, acc, _ = oracle_sample(n_seq, (lw, ones, w_lm), (kc, vc), batch, x0, q_s, d_s, U_s)
+        tot_s += s
+        tot_tok += acc
+    wall = time.perf_counter() - t_wall
+    value = tot_tok / tot_s
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"first {n_seq} of {B} sequences ({sub.M} rows) of the same workload: oracle layer 0 timed and "
+              f"counted 36x, plus final norm + LM head + softmax + sampler")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy Philox, same distributions as the GPU arm)",
+            "config": {"workload": WORKLOAD, "B": B, "sampled_sequences": n_seq},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

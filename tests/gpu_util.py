@@ -46,3 +46,35 @@ def assert_close_rel(got: np.ndarray, ref: np.ndarray, what: str, rel=REL, floor
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: {bad.sum()} / {bad.size} elements out of tolerance; worst at {i}: "
                              f"got {got[i]!r} ref {ref[i]!r} (rms {scale:.3g})")
+
+
+# Attention outputs are softmax-weighted sums of values.  The probabilities
+# enter the tensor-core PV product rounded to bf16 (relative error <= 2^-9
+# each), so an output element can move by up to 2^-9 * sum_i w_i |v_i|, the
+# magnitude of the terms it sums, however small the (cancelling) result is.
+# Bar: |gpu - ref| <= 2e-2 |ref| + 2 * 2^-9 * sum_i w_i |v_i|.
+ATTN_ABS = 2.0 * 2.0 ** -9
+
+
+def assert_close_attn(got, ref, mag, what: str, rel=REL, abs_frac=ATTN_ABS):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    mag = np.asarray(mag, np.float64)
+    assert got.shape == ref.shape == mag.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = rel * np.abs(ref) + abs_frac * mag
+    bad = err > bound
+    if np.any(bad):
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} / {bad.size} elements out of tolerance; worst at {i}: "
+                             f"got {got[i]!r} ref {ref[i]!r} magnitude {mag[i]!r}")
+
+
+def assert_rows_close_l2(got, ref, what: str, rel=REL):
+    """Row-wise ||gpu - ref|| / ||ref|| <= rel: the bar for chains of several bf16 ops."""
+    got = np.asarray(got, np.float64).reshape(len(got), -1)
+    ref = np.asarray(ref, np.float64).reshape(len(ref), -1)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    r = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert r.max() <= rel, f"{what}: worst row relative L2 error {r.max():.3g} (row {int(r.argmax())})"

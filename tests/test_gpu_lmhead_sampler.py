@@ -57,8 +57,8 @@ def sampler_inputs(seed, gammas, V, conc=0.5, zero_frac=0.0):
     Q = rng.dirichlet(np.full(V, conc), size=batch.n_drafts).astype(np.float32)
     if zero_frac:
         Q[rng.random(Q.shape) < zero_frac] = 0.0
-    drafts = np.array([rng.choice(V, p=q.astype(np.float64) / q.sum()) for q in Q], np.int32) \
-        if batch.n_drafts else np.zeros(0, np.int32)
+    drafts = np.array([rng.choice(V, p=q.astype(np.float64) / q.astype(np.float64).sum()) for q in Q],
+                      np.int32) if batch.n_drafts else np.zeros(0, np.int32)
     U = synth.uniforms_f32(seed + 1, batch.M)
     return batch, P, Q, drafts, U
 
