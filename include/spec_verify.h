@@ -111,6 +111,28 @@ SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,
                        const spec_bf16* residual, int ldr,
                        void* workspace, size_t workspace_bytes, spec_stream stream);
 
+/* Allocation-free variant of spec_verify_linear.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory or
+ * pass a workspace — e.g. an op embedded in a host runtime whose allocator
+ * already owns the whole GPU, or a plugin interface that hands the op only its
+ * input and output buffers.  The caller still passes X, W, Y (and residual).
+ * Scratch comes from a library-owned static device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library
+ * holds until the process exits.  Calls whose K split needs more scratch than
+ * that return SPEC_EUNSUPPORTED and launch nothing (use spec_verify_linear with
+ * a workspace instead; small verify passes need none or a few MiB).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call outside any stream capture.
+ * Each call clears the counters it needs (an async memset on `stream`); all
+ * calls share the array, so calls that may overlap on the GPU (other streams,
+ * other host threads) race.  No cudaMalloc, cudaFree or other allocating call
+ * is made. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+SPEC_API int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ldx,
+                                        const spec_bf16* W, int N, int ldw,
+                                        spec_bf16* Y, int ldy,
+                                        const spec_bf16* residual, int ldr, spec_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Verify attention (causal GQA over the KV cache + the new block)           */
 /* ------------------------------------------------------------------------ */

@@ -28,6 +28,7 @@ _SIGS = {
     "spec_device_status": (_i, [_vp, ctypes.POINTER(_i)]),
     "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
+    "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
     "spec_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "spec_verify_attention": (_i, [_vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp, _i,
                                    _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
@@ -175,6 +176,24 @@ def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None,
         _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
         wp, wn, _stream(stream)), 1 if M else 0)
+    return Y
+
+
+def spec_verify_linear_noalloc(X, W, Y, residual=None, stream=None):
+    """Same product as spec_verify_linear, for callers that cannot allocate.
+
+    Y must be given (nothing is allocated here either); split-K scratch comes
+    from the library's static device array (see the header for the limit).
+    """
+    _need(X, torch.bfloat16, "X"); _need(W, torch.bfloat16, "W"); _need(Y, torch.bfloat16, "Y")
+    M, K = X.shape
+    N = W.shape[0]
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual")
+    _check(_lib.spec_verify_linear_noalloc(
+        _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
+        _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
+        _stream(stream)), 1 if M else 0)
     return Y
 
 

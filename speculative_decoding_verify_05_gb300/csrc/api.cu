@@ -495,3 +495,55 @@ int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int
 }
 
 }  // extern "C"
+
+// =========================================================================== allocation-free linear
+// Scratch for spec_verify_linear_noalloc: a file-scope device array (zero at
+// module load).  Host code must not pass the symbol itself to a kernel: in
+// host code it is only a stand-in, so its device address is looked up once
+// per device with that device current and cached here.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SPEC_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SPEC_OK;
+}
+}  // namespace
+
+extern "C" int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ldx,
+                                          const spec_bf16* W, int N, int ldw, spec_bf16* Y,
+                                          int ldy, const spec_bf16* residual, int ldr,
+                                          spec_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
+  if (M == 0) return ok();
+  const size_t need = spec_linear_workspace_bytes(M, N, K);
+  if (need > SPEC_NOALLOC_SCRATCH_BYTES)
+    return fail(SPEC_EUNSUPPORTED,
+                "M=%d N=%d K=%d needs %zu bytes of split-K scratch; the static scratch holds %u "
+                "(call spec_verify_linear with a workspace)", M, N, K, need,
+                (unsigned)SPEC_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(&scratch)) return rc;
+  if (need > 0) {
+    // the arrival counters must start at zero whatever an earlier call left behind
+    const size_t clear = need < kCounterBytes ? need : kCounterBytes;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clear static scratch counters");
+  }
+  return spec_verify_linear(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, scratch,
+                            SPEC_NOALLOC_SCRATCH_BYTES, stream);
+}
