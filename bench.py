@@ -364,6 +364,8 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
     cur = torch.cuda.current_stream()
     out = {}
     wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
     for M in (1, 5):
         def run():
             for lw in eng.w.layers:
@@ -392,6 +394,7 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
         out[f"m{M}_us"] = t * 1e3
         out[f"m{M}_hbm_gbs"] = gbs
         out[f"m{M}_hbm_frac"] = gbs / hbm_peak
+    out["clocks"] = clk.stop()
     out["ratio_m5_over_m1"] = out["m5_us"] / out["m1_us"]
     out["weights_gb"] = wbytes / 1e9
     out["note"] = "36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph per M; peak " + peak_src
@@ -545,6 +548,52 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_profile_case(args):
+    """Small, self-contained launches of one hot kernel for an ncu capture (no timing).
+
+    attention: one layer of B=16 ragged sequences (KV ~0.6 GB, above L2);
+    linear: one gate|up projection (201 MB of weights) at --rows rows;
+    lmhead: the LM head + softmax at --rows rows.
+    """
+    import torch
+    from speculative_decoding_verify_05_gb300 import binding as S
+    from speculative_decoding_verify_05_gb300 import engine as E
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dims = E.Dims()
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    ws = S.Workspace(dev)
+    if args.profile == "attention":
+        batch = synth.ragged_batch(SEED, 16, G_LO, G_HI, CTX_LO, CTX_HI)
+        cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
+        kc = torch.empty((16, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        vc = torch.empty_like(kc).normal_(0, 1, generator=g)
+        qkv = torch.empty((batch.M, dims.qkv), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        cu = torch.from_numpy(batch.cu_rows).to(dev)
+        ctx = torch.from_numpy(batch.ctx_len).to(dev)
+        hq, hk = dims.Hq * dims.D, dims.Hkv * dims.D
+        for _ in range(args.reps):
+            S.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:], cu, ctx, kc, vc,
+                                    batch.max_rows, ws=ws)
+    else:
+        M = args.rows
+        if args.profile == "linear":
+            W = torch.empty((2 * dims.I, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
+        else:
+            W = torch.empty((dims.V, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
+        X = torch.empty((M, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        for _ in range(args.reps):
+            if args.profile == "linear":
+                S.spec_verify_linear(X, W, ws=ws)
+            else:
+                S.spec_lmhead_softmax(X, W, TEMP, ws=ws)
+    torch.cuda.synchronize()
+    S.spec_device_status()
+    print(json.dumps({"profile": args.profile, "reps": args.reps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -552,7 +601,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--profile", choices=["attention", "linear", "lmhead"], default=None,
+                    help="run a small case of one kernel for an ncu capture instead of the benchmark")
+    ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
+    ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -151,17 +151,36 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       }
       __syncthreads();
       if (last_flag) {
+        // this CTA arrived last: sum the split partials in split order (deterministic),
+        // one warp per token column, 4 weight rows per lane, 16-byte loads
         __threadfence();
         const float* base = args.partial + (size_t)tile * args.splits * (BN * 128);
-#pragma unroll 1
-        for (int j = 0; j < BN; ++j) {
+        const int r4 = lane * 4;
+        const int n4 = n0 + r4;
+#pragma unroll 2
+        for (int j = warp; j < BN; j += 4) {
           const int m = m0 + j;
           if (m >= args.M) break;
-          float y = 0.f;
-          for (int s = 0; s < args.splits; ++s) y += __ldcg(&base[(size_t)s * (BN * 128) + j * 128 + row]);
-          if (n < args.N) {
-            if (args.residual) y += bf16f(args.residual[(size_t)m * args.ldr + n]);
-            args.Y[(size_t)m * args.ldy + n] = f2bf(y);
+          float4 acc = __ldcg(reinterpret_cast<const float4*>(base + j * 128 + r4));
+          for (int s = 1; s < args.splits; ++s) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (size_t)s * (BN * 128) + j * 128 + r4));
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
+          float y[4] = {acc.x, acc.y, acc.z, acc.w};
+          if (n4 + 3 < args.N) {
+            if (args.residual) {
+              const uint2 rr = *reinterpret_cast<const uint2*>(args.residual + (size_t)m * args.ldr + n4);
+              y[0] += bf16lo(rr.x); y[1] += bf16hi(rr.x); y[2] += bf16lo(rr.y); y[3] += bf16hi(rr.y);
+            }
+            *reinterpret_cast<uint2*>(args.Y + (size_t)m * args.ldy + n4) =
+                make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+          } else {
+            for (int e = 0; e < 4; ++e) {
+              if (n4 + e >= args.N) break;
+              float v = y[e];
+              if (args.residual) v += bf16f(args.residual[(size_t)m * args.ldr + n4 + e]);
+              args.Y[(size_t)m * args.ldy + n4 + e] = f2bf(v);
+            }
           }
         }
         if (threadIdx.x == 0) args.counters[tile] = 0u;
