@@ -323,6 +323,7 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
     xs = {"qkv": eng.h[:M], "o": eng.o[:M], "gate_up": eng.h[:M], "down": eng.a[:M]}
     ys = {"qkv": eng.qkv[:M], "o": eng.h[:M], "gate_up": eng.gu[:M], "down": eng.h[:M]}
     tot_t, tot_f, tot_b = 0.0, 0.0, 0.0
+    per_shape = {}
     for name, (N, K) in shapes.items():
         w_attr = {"qkv": "w_qkv", "o": "w_o", "gate_up": "w_gu", "down": "w_down"}[name]
 
@@ -330,12 +331,14 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
             for li in range(L):
                 S.spec_verify_linear(xs[name], getattr(eng.w.layers[li], w_attr), Y=ys[name], ws=eng.ws)
         t = timeit(lin_all, L)
+        per_shape[name] = {"us": t * 1e3, "tflops": 2.0 * M * N * K / (t / 1e3) / 1e12,
+                           "weight_gbs": 2.0 * N * K / (t / 1e3) / 1e9}
         tot_t += t * L
         tot_f += 2.0 * M * N * K * L
         tot_b += 2.0 * N * K * L
     lin_tflops = tot_f / (tot_t / 1e3) / 1e12
     res["verify_linear"] = {"avg_launch_us": tot_t / (4 * L) * 1e3, "launches_per_round": 4 * L,
-                            "total_ms": tot_t,
+                            "total_ms": tot_t, "per_shape": per_shape,
                             "roofline": {"kernel": "verify_linear (tcgen05, M=%d)" % M, "bound": "tensor",
                                          "achieved": lin_tflops, "peak": tc_sust, "unit": "TFLOP/s",
                                          "frac": lin_tflops / tc_sust, "traffic": None,
@@ -366,7 +369,8 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
     wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
-    for M in (1, 5):
+    for M, tag in ((1, "1"), (5, "5"), (1, "1_tc")):
+        S.spec_set_option("gemv_max_m", 0 if tag == "1_tc" else 4)
         def run():
             for lw in eng.w.layers:
                 S.spec_verify_linear(eng.h[:M], lw.w_qkv, Y=eng.qkv[:M], ws=eng.ws)
@@ -391,13 +395,15 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / reps
         gbs = wbytes / (t / 1e3) / 1e9
-        out[f"m{M}_us"] = t * 1e3
-        out[f"m{M}_hbm_gbs"] = gbs
-        out[f"m{M}_hbm_frac"] = gbs / hbm_peak
+        out[f"m{tag}_us"] = t * 1e3
+        out[f"m{tag}_hbm_gbs"] = gbs
+        out[f"m{tag}_hbm_frac"] = gbs / hbm_peak
+    S.spec_set_option("gemv_max_m", 4)
     out["clocks"] = clk.stop()
     out["ratio_m5_over_m1"] = out["m5_us"] / out["m1_us"]
     out["weights_gb"] = wbytes / 1e9
-    out["note"] = "36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph per M; peak " + peak_src
+    out["note"] = ("36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph "
+                   "per M; m1 = CUDA-core path, m1_tc = tensor-core path at M=1; peak " + peak_src)
     return out
 
 

@@ -76,10 +76,12 @@ SPEC_API const char* spec_last_error(void);
 SPEC_API int spec_version(void);
 
 /* Tuning knobs (process-wide): "gemv_max_m" (0..4, default 4): largest M
- * that takes the CUDA-core path of spec_verify_linear; "linear_splits" (0..64,
- * default 0 = automatic): force the K split of the tensor-core path.  Changing
- * a knob changes spec_linear_workspace_bytes.  Returns SPEC_EINVAL for an
- * unknown name or value. */
+ * that takes the CUDA-core path of spec_verify_linear; "linear_grid" (0..4096,
+ * default 0 = one CTA per SM): persistent CTAs of the tensor-core GEMM;
+ * "attention_impl" (1 = tcgen05 kernel, default; 0 = mma.sync kernel);
+ * "linear_nsub" (1 default, or 2: one tensor-core tile covers up to 512 rows).
+ * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for
+ * an unknown name or value. */
 SPEC_API int spec_set_option(const char* name, int value);
 
 /* Synchronizes `stream`, then reads and clears the current device's status

@@ -125,29 +125,19 @@ constexpr size_t kMaxCounters = kCounterBytes / 4;
 
 // --------------------------------------------------------------------------- linear plan
 int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
-int g_force_splits = 0;  // tunable: 0 = heuristic
+int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
+int g_force_grid = 0;    // tunable: persistent CTAs of the tensor-core GEMM, 0 = one per SM
+int g_nsub_max = 1;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 
 struct LinPlan {
   bool gemv = false;
-  int BN = 16, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
+  int BN = 16, NSUB = 1, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
+  int grid = 1;                 // persistent CTAs of the tensor-core path
+  bool aligned = false;         // CTA ranges cover whole tiles only
+  long long units = 0;
   int gemv_grid = 1, k_per_split = 0, groups = 0;
   size_t counters_off = 0, partial_off = 0, bytes = 0;
 };
-
-int choose_splits(int tiles, int k_steps, int sms, int min_steps) {
-  if (g_force_splits > 0) return std::min(g_force_splits, std::max(1, k_steps));
-  if (tiles >= 2 * sms) return 1;
-  const int smax = std::max(1, std::min(32, k_steps / min_steps));
-  int best = 1;
-  double best_eff = 0.0;
-  for (int s = 1; s <= smax; ++s) {
-    const double units = double(tiles) * s / sms;
-    const double eff = units / std::ceil(units);
-    if (eff >= 0.9) return s;
-    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
-  }
-  return best;
-}
 
 LinPlan plan_linear(int M, int N, int K, bool lmhead) {
   LinPlan p;
@@ -169,25 +159,44 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
     p.bytes = p.splits > 1 ? kCounterBytes + round_up(size_t(p.splits) * M * N * 4, 256) : 0;
     return p;
   }
-  p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
-  const int per = (M + p.tiles_m - 1) / p.tiles_m;
-  p.BN = std::max(16, (per + 15) / 16 * 16);
+  // up to 256 rows: one MMA of N = BN per k-substep; more rows: tiles of up to 512 rows as
+  // two MMAs of N = BN sharing each weight tile (every weight byte still read once per tile)
+  if (M <= kMaxBN) {
+    p.tiles_m = 1;
+    p.NSUB = 1;
+    p.BN = std::max(16, (M + 15) / 16 * 16);
+  } else if (g_nsub_max == 1) {
+    p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
+    const int per = (M + p.tiles_m - 1) / p.tiles_m;
+    p.NSUB = 1;
+    p.BN = std::max(16, (per + 15) / 16 * 16);
+  } else {
+    p.tiles_m = (M + 2 * kMaxBN - 1) / (2 * kMaxBN);
+    const int per = (M + p.tiles_m - 1) / p.tiles_m;
+    p.NSUB = 2;
+    p.BN = std::max(144, ((per + 1) / 2 + 15) / 16 * 16);
+  }
+  const int TN = p.BN * p.NSUB;
   p.tiles_n = (N + 127) / 128;
-  const int tiles = p.tiles_m * p.tiles_n;
+  const long long tiles = (long long)p.tiles_m * p.tiles_n;
+  p.units = tiles * p.k_tiles;
   p.counters_off = 0;
   p.partial_off = kCounterBytes;
+  // persistent stream-K: one CTA per SM, each streaming an equal share of (tile, k-step) units;
+  // the LM-head epilogue needs whole tiles, so its ranges are tile-aligned
+  p.aligned = lmhead || tiles > (long long)kMaxCounters;
+  int grid = g_force_grid > 0 ? g_force_grid : sms;
+  const long long cap_units = p.aligned ? tiles : p.units;
+  if (grid > cap_units) grid = (int)cap_units;
+  p.grid = std::max(1, grid);
   if (lmhead) {
-    p.splits = 1;
     p.bytes = kCounterBytes + round_up(size_t(M) * p.tiles_n * sizeof(float2), 256);
     return p;
   }
-  const int smem = linear_tc_smem_bytes(p.BN);
-  int cps = (228 * 1024) / (smem + 1024);
-  cps = std::max(1, std::min(cps, 512 / linear_tc_tmem_cols(p.BN)));
-  p.splits = choose_splits(tiles, p.k_tiles, sms, 4);
-  if ((size_t)tiles > kMaxCounters) p.splits = 1;
-  (void)cps;
-  p.bytes = p.splits > 1 ? kCounterBytes + round_up(size_t(tiles) * p.splits * p.BN * 128 * 4, 256) : 0;
+  bool split = false;
+  if (!p.aligned)
+    for (int c = 0; c < p.grid && !split; ++c) split = ((p.units * c / p.grid) % p.k_tiles) != 0;
+  p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * 2 * TN * 128 * 4, 256) : 0;
   return p;
 }
 
@@ -226,9 +235,19 @@ int spec_set_option(const char* name, int value) {
     g_gemv_max_m = value;
     return ok();
   }
-  if (!strcmp(name, "linear_splits")) {
-    if (value < 0 || value > 64) return fail(SPEC_EINVAL, "linear_splits must be in [0, 64]");
-    g_force_splits = value;
+  if (!strcmp(name, "attention_impl")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "attention_impl must be 0 or 1");
+    g_attn_impl = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_nsub")) {
+    if (value < 1 || value > 2) return fail(SPEC_EINVAL, "linear_nsub must be 1 or 2");
+    g_nsub_max = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_grid")) {
+    if (value < 0 || value > 4096) return fail(SPEC_EINVAL, "linear_grid must be in [0, 4096]");
+    g_force_grid = value;
     return ok();
   }
   return fail(SPEC_EINVAL, "unknown option '%s'", name);
@@ -313,13 +332,14 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
   }
   LinearArgs a{};
-  a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.splits = p.splits; a.tiles_m = p.tiles_m;
+  a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
+  a.units = p.units; a.grid = p.grid; a.aligned = p.aligned ? 1 : 0;
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
-  a.partial = p.splits > 1 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
-  a.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
+  a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
+  a.counters = p.bytes > 0 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
   a.status = d->status;
-  dim3 grid(p.tiles_m, p.tiles_n, p.splits);
-  cudaError_t e = launch_linear_tc_bf16(p.BN, tw, tx, a, grid, s);
+  dim3 grid(p.grid);
+  cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
   return ok();
 }
@@ -363,14 +383,14 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
   }
   const bool greedy = temperature == 0.f;
   LinearArgs a{};
-  a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.splits = 1; a.tiles_m = p.tiles_m;
+  a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
+  a.units = p.units; a.grid = p.grid; a.aligned = 1;
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = P;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
-  a.n_tiles = p.tiles_n;
-  dim3 grid(p.tiles_m, p.tiles_n, 1);
-  cudaError_t e = launch_linear_tc_lmhead(p.BN, greedy, tw, tx, a, grid, s);
+  dim3 grid(p.grid);
+  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   e = launch_lmhead_normalize(P, a.stats, M, V, p.tiles_n, greedy, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head normalize launch");
@@ -415,7 +435,7 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   CUtensorMap tk, tv;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)cap, (cuuint64_t)B * Hkv};
   cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)cap * D * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, g_attn_impl ? (cuuint32_t)attention_tc_key_tile() : 64u, 1};
   if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache")) return rc;
   if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache")) return rc;
   char* ws = static_cast<char*>(workspace);
@@ -429,7 +449,8 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   a.partial = reinterpret_cast<float*>(ws + p.partial_off);
   a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
   a.status = d->status;
-  cudaError_t e = launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = g_attn_impl ? launch_attention_tc(tk, tv, a, static_cast<cudaStream_t>(stream))
+                              : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok();
 }

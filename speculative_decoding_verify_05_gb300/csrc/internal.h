@@ -11,13 +11,14 @@
 
 namespace spec {
 
-// ---- tcgen05 GEMM: token tile widths instantiated (multiples of 16 up to 256)
+// ---- tcgen05 GEMM: NSUB sub-tiles of BN verify rows per CTA tile
+//      (NSUB = 1: BN = 16..256 step 16; NSUB = 2: BN = 144..256 step 16)
 constexpr int kMaxBN = 256;
-int linear_tc_smem_bytes(int BN);
-int linear_tc_tmem_cols(int BN);
-cudaError_t launch_linear_tc_bf16(int BN, const CUtensorMap& tw, const CUtensorMap& tx,
+int linear_tc_smem_bytes(int BN, int NSUB);
+bool linear_tc_supported(int BN, int NSUB);
+cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
-cudaError_t launch_linear_tc_lmhead(int BN, bool greedy, const CUtensorMap& tw,
+cudaError_t launch_linear_tc_lmhead(int BN, int NSUB, bool greedy, const CUtensorMap& tw,
                                     const CUtensorMap& tx, const LinearArgs& a, dim3 grid,
                                     cudaStream_t s);
 
@@ -57,6 +58,10 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                              cudaStream_t s);
+// tcgen05 variant: K/V tensor maps with 128-key boxes; chunk must be a multiple of 128
+int attention_tc_key_tile();
+cudaError_t launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                                cudaStream_t s);
 
 // ---- rejection sampler
 cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* draft,

@@ -1,22 +1,22 @@
 // Tensor-core (tcgen05 + TMEM + TMA) weight-streaming GEMM for the verify pass.
 //
-// Orientation: the weight is the MMA's A operand (128 weight rows per CTA
-// tile, M_mma = 128) and the verify rows are the B operand (BN tokens, the
-// MMA's N), so the accumulator tile D[n, m] = sum_k W[n, k] X[m, k] lives in
-// TMEM with one weight row per TMEM lane.  For a handful of verify rows this
-// keeps the whole 128-lane tensor core busy on the weight stream instead of
-// padding the token dimension to 128.
+// Orientation: the weight is the MMA's A operand (128 weight rows per tile,
+// M_mma = 128) and the verify rows are the B operand (BN tokens, the MMA's
+// N), so the accumulator tile D[n, m] = sum_k W[n, k] X[m, k] lives in TMEM
+// with one weight row per TMEM lane.  For a handful of verify rows this keeps
+// the whole 128-lane tensor core on the weight stream instead of padding the
+// token dimension to 128.
 //
-// Pipeline per CTA (128 threads): warp 0 / lane 0 issues TMA loads of
-// 128x64 weight tiles and BNx64 activation tiles (128-byte swizzle) into a
-// STAGES-deep shared-memory ring; warp 1 / lane 0 issues four
-// tcgen05.mma (K = 16 each) per stage and releases the stage with
-// tcgen05.commit; all four warps then drain TMEM (tcgen05.ld) in the epilogue.
-//
-// Split-K: the grid's z dimension splits the K loop.  Each split writes an
-// fp32 partial tile to the workspace; the CTA that arrives last on the
-// tile's counter (atomicAdd, no waiting) sums the partials in split order,
-// adds the residual, rounds to bf16 and resets the counter to zero.
+// Persistent stream-K schedule: one CTA per SM walks a contiguous range of
+// (tile, 64-wide k-step) units, so every SM streams the same number of weight
+// bytes whatever the matrix shape.  Roles (6 warps): warp 0 issues TMA loads
+// of 128x64 weight tiles and BNx64 activation tiles (128-byte swizzle) into a
+// STAGES-deep ring without ever draining it; warp 1 issues four
+// tcgen05.mma (K = 16) per stage into one of two TMEM accumulators; warps 2-5
+// drain the other accumulator meanwhile.  A tile whose k-steps are split
+// between CTAs is finished by the CTA that arrives last on the tile's counter
+// (an atomic, no waiting): it sums the fp32 partials in CTA order, adds the
+// residual, rounds to bf16 and resets the counter.
 #pragma once
 
 #include "common.cuh"
@@ -31,32 +31,41 @@ enum LinearEpilogue : int {
 
 struct LinearArgs {
   int M, N, K;
-  int k_tiles;          // ceil(K / 64)
-  int splits;
-  int tiles_m;
+  int k_tiles;          // 64-wide k-steps per tile
+  int tiles_m, tiles_n;
+  long long units;      // work units: tiles * k_tiles
+  int grid;             // persistent CTAs
+  int aligned;          // 1: every CTA range starts and ends on a tile boundary
   uint16_t* Y;
   int ldy;
   const uint16_t* residual;
   int ldr;
-  float* partial;       // [tiles][splits][BN][128] fp32 (split-K only)
-  unsigned* counters;   // [tiles] zero-initialised arrival counters (split-K only)
+  float* partial;       // [grid][2][BN][128] fp32 (split tiles only)
+  unsigned* counters;   // [tiles] zero-initialised arrival counters (split tiles only)
   unsigned* status;     // library status word (bounded-wait timeouts)
   float inv_temp;       // EPI_LOGITS
   float* P;             // EPI_LOGITS: [M x N] fp32
-  float2* stats;        // EPI_LOGITS / EPI_ARGMAX: [M][n_tiles] (max, sum) or (max, idx bits)
-  int n_tiles;
+  float2* stats;        // EPI_LOGITS / EPI_ARGMAX: [M][tiles_n] (max, sum) or (max, idx bits)
 };
 
-template <int BN>
+// A CTA tile is 128 weight rows x TN = NSUB * BN verify rows: NSUB MMAs of N = BN per
+// k-substep share one weight tile, so with up to 512 verify rows every weight byte is
+// read from HBM once.
+template <int BN, int NSUB>
 struct LinearCfg {
+  static constexpr int TN = BN * NSUB;
   static constexpr int A_BYTES = 128 * 64 * 2;
-  static constexpr int B_BYTES = BN * 64 * 2;
+  static constexpr int B_BYTES = TN * 64 * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES =
-      BN <= 64 ? 4 : ((200 * 1024) / STAGE_BYTES > 6 ? 6 : (200 * 1024) / STAGE_BYTES);
-  static constexpr int TMEM_COLS = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
-  // ring + barriers + tmem slot + epilogue scratch (4 warps x BN x float2), + 1 KB alignment slack
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 4 * BN * 8 + 1024;
+  static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+  // accumulator buffer: power-of-two columns >= TN; two buffers when they fit in TMEM
+  static constexpr int ACC_COLS = TN <= 16 ? 16 : (TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512))));
+  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr int TMEM_COLS = NBUF * ACC_COLS < 32 ? 32 : NBUF * ACC_COLS;
+  static constexpr int THREADS = 192;
+  // ring + barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) + alignment slack
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + 1024;
 };
 
 }  // namespace spec

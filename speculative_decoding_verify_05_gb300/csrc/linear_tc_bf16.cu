@@ -1,89 +1,86 @@
-// Instantiations of the tcgen05 verify GEMM for the bf16 (+ residual) epilogue.
+// Instantiations of the persistent tcgen05 verify GEMM for the bf16 (+ residual) epilogue.
 #include "internal.h"
 #include "linear_tc_kernel.cuh"
 
 namespace spec {
 
-template <int BN, int EPI>
+template <int BN, int NSUB, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a,
                               dim3 grid, cudaStream_t st) {
-  constexpr int smem = LinearCfg<BN>::SMEM_BYTES;
+  using Cfg = LinearCfg<BN, NSUB>;
+  constexpr int smem = Cfg::SMEM_BYTES;
   static bool configured[64] = {};   // per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<BN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<BN, NSUB, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  linear_tc_kernel<BN, EPI><<<grid, 128, smem, st>>>(tw, tx, a);
+  linear_tc_kernel<BN, NSUB, EPI><<<grid, Cfg::THREADS, smem, st>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
-int linear_tc_smem_bytes(int BN) {
-  switch (BN) {
-    case 16: return LinearCfg<16>::SMEM_BYTES;
-    case 32: return LinearCfg<32>::SMEM_BYTES;
-    case 48: return LinearCfg<48>::SMEM_BYTES;
-    case 64: return LinearCfg<64>::SMEM_BYTES;
-    case 80: return LinearCfg<80>::SMEM_BYTES;
-    case 96: return LinearCfg<96>::SMEM_BYTES;
-    case 112: return LinearCfg<112>::SMEM_BYTES;
-    case 128: return LinearCfg<128>::SMEM_BYTES;
-    case 144: return LinearCfg<144>::SMEM_BYTES;
-    case 160: return LinearCfg<160>::SMEM_BYTES;
-    case 176: return LinearCfg<176>::SMEM_BYTES;
-    case 192: return LinearCfg<192>::SMEM_BYTES;
-    case 208: return LinearCfg<208>::SMEM_BYTES;
-    case 224: return LinearCfg<224>::SMEM_BYTES;
-    case 240: return LinearCfg<240>::SMEM_BYTES;
-    case 256: return LinearCfg<256>::SMEM_BYTES;
+int linear_tc_smem_bytes(int BN, int NSUB) {
+  switch (NSUB * 1000 + BN) {
+    case 1016: return LinearCfg<16, 1>::SMEM_BYTES;
+    case 1032: return LinearCfg<32, 1>::SMEM_BYTES;
+    case 1048: return LinearCfg<48, 1>::SMEM_BYTES;
+    case 1064: return LinearCfg<64, 1>::SMEM_BYTES;
+    case 1080: return LinearCfg<80, 1>::SMEM_BYTES;
+    case 1096: return LinearCfg<96, 1>::SMEM_BYTES;
+    case 1112: return LinearCfg<112, 1>::SMEM_BYTES;
+    case 1128: return LinearCfg<128, 1>::SMEM_BYTES;
+    case 1144: return LinearCfg<144, 1>::SMEM_BYTES;
+    case 1160: return LinearCfg<160, 1>::SMEM_BYTES;
+    case 1176: return LinearCfg<176, 1>::SMEM_BYTES;
+    case 1192: return LinearCfg<192, 1>::SMEM_BYTES;
+    case 1208: return LinearCfg<208, 1>::SMEM_BYTES;
+    case 1224: return LinearCfg<224, 1>::SMEM_BYTES;
+    case 1240: return LinearCfg<240, 1>::SMEM_BYTES;
+    case 1256: return LinearCfg<256, 1>::SMEM_BYTES;
+    case 2144: return LinearCfg<144, 2>::SMEM_BYTES;
+    case 2160: return LinearCfg<160, 2>::SMEM_BYTES;
+    case 2176: return LinearCfg<176, 2>::SMEM_BYTES;
+    case 2192: return LinearCfg<192, 2>::SMEM_BYTES;
+    case 2208: return LinearCfg<208, 2>::SMEM_BYTES;
+    case 2224: return LinearCfg<224, 2>::SMEM_BYTES;
+    case 2240: return LinearCfg<240, 2>::SMEM_BYTES;
+    case 2256: return LinearCfg<256, 2>::SMEM_BYTES;
     default: return -1;
   }
 }
 
-int linear_tc_tmem_cols(int BN) {
-  switch (BN) {
-    case 16: return LinearCfg<16>::TMEM_COLS;
-    case 32: return LinearCfg<32>::TMEM_COLS;
-    case 48: return LinearCfg<48>::TMEM_COLS;
-    case 64: return LinearCfg<64>::TMEM_COLS;
-    case 80: return LinearCfg<80>::TMEM_COLS;
-    case 96: return LinearCfg<96>::TMEM_COLS;
-    case 112: return LinearCfg<112>::TMEM_COLS;
-    case 128: return LinearCfg<128>::TMEM_COLS;
-    case 144: return LinearCfg<144>::TMEM_COLS;
-    case 160: return LinearCfg<160>::TMEM_COLS;
-    case 176: return LinearCfg<176>::TMEM_COLS;
-    case 192: return LinearCfg<192>::TMEM_COLS;
-    case 208: return LinearCfg<208>::TMEM_COLS;
-    case 224: return LinearCfg<224>::TMEM_COLS;
-    case 240: return LinearCfg<240>::TMEM_COLS;
-    case 256: return LinearCfg<256>::TMEM_COLS;
-    default: return -1;
-  }
-}
+bool linear_tc_supported(int BN, int NSUB) { return linear_tc_smem_bytes(BN, NSUB) > 0; }
 
-cudaError_t launch_linear_tc_bf16(int BN, const CUtensorMap& tw, const CUtensorMap& tx,
+cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s) {
-  switch (BN) {
-    case 16: return launch_one<16, EPI_BF16>(tw, tx, a, grid, s);
-    case 32: return launch_one<32, EPI_BF16>(tw, tx, a, grid, s);
-    case 48: return launch_one<48, EPI_BF16>(tw, tx, a, grid, s);
-    case 64: return launch_one<64, EPI_BF16>(tw, tx, a, grid, s);
-    case 80: return launch_one<80, EPI_BF16>(tw, tx, a, grid, s);
-    case 96: return launch_one<96, EPI_BF16>(tw, tx, a, grid, s);
-    case 112: return launch_one<112, EPI_BF16>(tw, tx, a, grid, s);
-    case 128: return launch_one<128, EPI_BF16>(tw, tx, a, grid, s);
-    case 144: return launch_one<144, EPI_BF16>(tw, tx, a, grid, s);
-    case 160: return launch_one<160, EPI_BF16>(tw, tx, a, grid, s);
-    case 176: return launch_one<176, EPI_BF16>(tw, tx, a, grid, s);
-    case 192: return launch_one<192, EPI_BF16>(tw, tx, a, grid, s);
-    case 208: return launch_one<208, EPI_BF16>(tw, tx, a, grid, s);
-    case 224: return launch_one<224, EPI_BF16>(tw, tx, a, grid, s);
-    case 240: return launch_one<240, EPI_BF16>(tw, tx, a, grid, s);
-    case 256: return launch_one<256, EPI_BF16>(tw, tx, a, grid, s);
+  switch (NSUB * 1000 + BN) {
+    case 1016: return launch_one<16, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1032: return launch_one<32, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1048: return launch_one<48, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1064: return launch_one<64, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1080: return launch_one<80, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1096: return launch_one<96, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1112: return launch_one<112, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1128: return launch_one<128, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1144: return launch_one<144, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1160: return launch_one<160, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1176: return launch_one<176, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1192: return launch_one<192, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1208: return launch_one<208, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1224: return launch_one<224, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1240: return launch_one<240, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1256: return launch_one<256, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 2144: return launch_one<144, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2160: return launch_one<160, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2176: return launch_one<176, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2192: return launch_one<192, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2208: return launch_one<208, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2224: return launch_one<224, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2240: return launch_one<240, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2256: return launch_one<256, 2, EPI_BF16>(tw, tx, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,6 +15,14 @@ pytestmark = pytest.mark.gpu
 D = 128
 
 
+@pytest.fixture(params=[1, 0], ids=["tcgen05", "mma_sync"])
+def impl(request, lib):
+    """Run each case on both attention kernels (tcgen05 is the default)."""
+    lib.spec_set_option("attention_impl", request.param)
+    yield request.param
+    lib.spec_set_option("attention_impl", 1)
+
+
 def run_case(lib, gammas, ctx, Hq, Hkv, seed, cap=None, fused_qkv=True):
     batch = synth.RaggedBatch(gammas, ctx, cap)
     M, B = batch.M, batch.B
@@ -59,24 +67,24 @@ def run_case(lib, gammas, ctx, Hq, Hkv, seed, cap=None, fused_qkv=True):
     ([6, 1], [90, 63], 16, 8),                # G = 2
     ([15], [5], 4, 1),                        # G*rows = 64 exactly
 ])
-def test_attention_small(lib, gammas, ctx, Hq, Hkv):
+def test_attention_small(lib, impl, gammas, ctx, Hq, Hkv):
     run_case(lib, gammas, ctx, Hq, Hkv, seed=sum(ctx) + len(gammas))
 
 
-def test_attention_split_kv_long_context(lib):
+def test_attention_split_kv_long_context(lib, impl):
     # long contexts with few sequences: several key chunks per (sequence, kv head)
     run_case(lib, [4, 2], [3000, 4096], 32, 8, seed=77)
 
 
-def test_attention_separate_qkv_buffers(lib):
+def test_attention_separate_qkv_buffers(lib, impl):
     run_case(lib, [4, 1], [200, 17], 32, 8, seed=5, fused_qkv=False)
 
 
-def test_attention_cap_with_slack(lib):
+def test_attention_cap_with_slack(lib, impl):
     run_case(lib, [3, 9], [100, 500], 32, 8, seed=6, cap=700)
 
 
-def test_attention_row_equals_single_decode(lib):
+def test_attention_row_equals_single_decode(lib, impl):
     """Row j of a verify block equals a one-row call at context ctx + j (caches after j steps)."""
     gam, ctx, Hq, Hkv = 5, 150, 32, 8
     width = (Hq + 2 * Hkv) * D
@@ -108,3 +116,9 @@ def test_attention_row_equals_single_decode(lib):
                                        np.abs(f64_of_bf16(vc0)), np.array([ctx]), 1.0 / math.sqrt(D))
     assert_close_attn(f64_of_bf16(Ov).reshape(M, Hq, D), f64_of_bf16(Od).reshape(M, Hq, D), Omag,
                       "verify vs sequential decode", abs_frac=4.0 * 2.0 ** -9)
+
+
+def test_attention_config3_shapes(lib, impl):
+    """B=8, gamma=4, GQA 32/8, contexts U[512, 4096] (the verify-attention workload's shapes)."""
+    batch = synth.ragged_batch(3, 8, 4, 4, 512, 4096)
+    run_case(lib, batch.gammas, batch.ctx_len, 32, 8, seed=123)

@@ -13,22 +13,23 @@ SHAPES = [
     # (M, N, K): ragged tails in every dimension, several M tiles, split-K on and off
     (1, 256, 512), (2, 384, 1000), (3, 200, 264), (4, 1024, 4096),
     (5, 512, 4096), (7, 136, 72), (16, 640, 264), (17, 256, 520), (40, 1024, 512),
-    (100, 256, 768), (256, 384, 128), (300, 384, 512), (513, 128, 256),
+    (100, 256, 768), (256, 384, 128), (300, 384, 512), (368, 6144, 4096), (513, 128, 256),
+    (1030, 640, 320),
 ]
 
 
-def run_case(lib, M, N, K, residual, seed, gemv_max_m=4, splits=0, std=0.05):
+def run_case(lib, M, N, K, residual, seed, gemv_max_m=4, grid=0, std=0.05):
     X = synth.normal_bf16_bits(seed, (M, K), 1.0)
     W = synth.normal_bf16_bits(seed + 1, (N, K), std)
     R = synth.normal_bf16_bits(seed + 2, (M, N), 1.0) if residual else None
     lib.spec_set_option("gemv_max_m", gemv_max_m)
-    lib.spec_set_option("linear_splits", splits)
+    lib.spec_set_option("linear_grid", grid)
     try:
         Y = lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), residual=bf16_dev(R) if residual else None)
         lib.spec_device_status()
     finally:
         lib.spec_set_option("gemv_max_m", 4)
-        lib.spec_set_option("linear_splits", 0)
+        lib.spec_set_option("linear_grid", 0)
     ref = oops.linear(obf.decode(X), obf.decode(W), obf.decode(R) if residual else None)
     assert_close_rel(f64_of_bf16(Y), ref, f"linear M={M} N={N} K={K}")
 
@@ -44,9 +45,11 @@ def test_linear_tensor_core_path_at_tiny_m(lib, M):
     run_case(lib, M, 768, 1024, True, seed=40 + M, gemv_max_m=0)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_linear_forced_splits(lib, splits):
-    run_case(lib, 24, 512, 1536, True, seed=90 + splits, gemv_max_m=0, splits=splits)
+@pytest.mark.parametrize("grid", [1, 2, 3, 7, 50, 333])
+def test_linear_forced_grid(lib, grid):
+    """Persistent grids that split tiles between CTAs in many different ways."""
+    run_case(lib, 24, 512, 1536, True, seed=90 + grid, gemv_max_m=0, grid=grid)
+    run_case(lib, 300, 640, 1000, True, seed=91 + grid, gemv_max_m=0, grid=grid)
 
 
 def test_linear_residual_aliases_output(lib):
