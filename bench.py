@@ -585,11 +585,13 @@ def run_profile_case(args):
                                     batch.max_rows, ws=ws)
     else:
         M = args.rows
+        S.spec_set_option("linear_nsub", args.nsub)
         if args.profile == "linear":
-            W = torch.empty((2 * dims.I, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
+            N, K = args.n, args.k
         else:
-            W = torch.empty((dims.V, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
-        X = torch.empty((M, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+            N, K = dims.V, dims.d
+        W = torch.empty((N, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
+        X = torch.empty((M, K), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
         for _ in range(args.reps):
             if args.profile == "linear":
                 S.spec_verify_linear(X, W, ws=ws)
@@ -611,6 +613,9 @@ def main():
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
+    ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")
+    ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")
+    ap.add_argument("--nsub", type=int, default=1, help="linear_nsub knob for --profile linear/lmhead")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

@@ -76,8 +76,9 @@ SPEC_API const char* spec_last_error(void);
 SPEC_API int spec_version(void);
 
 /* Tuning knobs (process-wide): "gemv_max_m" (0..4, default 4): largest M
- * that takes the CUDA-core path of spec_verify_linear; "linear_grid" (0..4096,
- * default 0 = one CTA per SM): persistent CTAs of the tensor-core GEMM;
+ * that takes the CUDA-core path of spec_verify_linear; "persistent_grid" (0..4096,
+ * default 0 = one CTA per SM): CTAs of the persistent tensor-core GEMM and
+ * attention kernels;
  * "attention_impl" (1 = tcgen05 kernel, default; 0 = mma.sync kernel);
  * "linear_nsub" (1 default, or 2: one tensor-core tile covers up to 512 rows).
  * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for

@@ -126,7 +126,7 @@ constexpr size_t kMaxCounters = kCounterBytes / 4;
 // --------------------------------------------------------------------------- linear plan
 int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
 int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
-int g_force_grid = 0;    // tunable: persistent CTAs of the tensor-core GEMM, 0 = one per SM
+int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_nsub_max = 1;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 
 struct LinPlan {
@@ -202,20 +202,30 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
 
 // --------------------------------------------------------------------------- attention plan
 struct AttnPlan {
+  bool tc = false;               // persistent tcgen05 kernel
+  int grid = 1;
   int chunk = 256, max_chunks = 1;
   size_t counters_off = 0, partial_off = 0, bytes = 0;
 };
 
-AttnPlan plan_attention(int B, int Hkv, int cap) {
+AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
   AttnPlan p;
   const int sms = plan_sms();
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  p.tc = g_attn_impl == 1 && B <= attention_tc_max_batch() && attention_tc_rows(G, max_rows) > 0 &&
+         cap <= 16384;
+  p.counters_off = 0;
+  p.partial_off = kCounterBytes;
+  if (p.tc) {
+    p.grid = g_force_grid > 0 ? g_force_grid : sms;
+    p.bytes = kCounterBytes + round_up(size_t(p.grid) * 2 * 64 * (128 + 2) * 4, 256);
+    return p;
+  }
   const double keys = double(B) * Hkv * cap;
   int chunk = 256;
   while (chunk < 4096 && keys / (chunk * 2) >= 8.0 * sms) chunk *= 2;
   p.chunk = chunk;
   p.max_chunks = std::max(1, (cap + chunk - 1) / chunk);
-  p.counters_off = 0;
-  p.partial_off = kCounterBytes;
   p.bytes = kCounterBytes + round_up(size_t(B) * Hkv * p.max_chunks * 64 * (128 + 2) * 4, 256);
   return p;
 }
@@ -245,8 +255,8 @@ int spec_set_option(const char* name, int value) {
     g_nsub_max = value;
     return ok();
   }
-  if (!strcmp(name, "linear_grid")) {
-    if (value < 0 || value > 4096) return fail(SPEC_EINVAL, "linear_grid must be in [0, 4096]");
+  if (!strcmp(name, "persistent_grid")) {
+    if (value < 0 || value > 4096) return fail(SPEC_EINVAL, "persistent_grid must be in [0, 4096]");
     g_force_grid = value;
     return ok();
   }
@@ -400,7 +410,7 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
 // --------------------------------------------------------------------------- attention
 size_t spec_attention_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int D, int cap) {
   if (B <= 0 || max_rows <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || cap <= 0) return 0;
-  return plan_attention(B, Hkv, cap).bytes;
+  return plan_attention(B, max_rows, Hq, Hkv, cap).bytes;
 }
 
 int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
@@ -427,7 +437,7 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
       !aligned16(Vcache) || !aligned16(O))
     return fail(SPEC_EINVAL, "bf16 tensors must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(SPEC_EINVAL, "scale must be finite");
-  AttnPlan p = plan_attention(B, Hkv, cap);
+  AttnPlan p = plan_attention(B, max_rows, Hq, Hkv, cap);
   if (!workspace || workspace_bytes < p.bytes)
     return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
   DevInfo* d = nullptr;
@@ -435,7 +445,7 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   CUtensorMap tk, tv;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)cap, (cuuint64_t)B * Hkv};
   cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)cap * D * 2};
-  cuuint32_t box[3] = {64, g_attn_impl ? (cuuint32_t)attention_tc_key_tile() : 64u, 1};
+  cuuint32_t box[3] = {64, p.tc ? (cuuint32_t)attention_tc_key_tile() : 64u, 1};
   if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache")) return rc;
   if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache")) return rc;
   char* ws = static_cast<char*>(workspace);
@@ -449,8 +459,8 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   a.partial = reinterpret_cast<float*>(ws + p.partial_off);
   a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
   a.status = d->status;
-  cudaError_t e = g_attn_impl ? launch_attention_tc(tk, tv, a, static_cast<cudaStream_t>(stream))
-                              : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = p.tc ? launch_attention_tc(tk, tv, a, p.grid, static_cast<cudaStream_t>(stream))
+                       : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok();
 }

@@ -58,9 +58,12 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                              cudaStream_t s);
-// tcgen05 variant: K/V tensor maps with 128-key boxes; chunk must be a multiple of 128
+// tcgen05 variant (persistent, stream-K over 128-key tiles): K/V tensor maps with
+// 128-key boxes; `grid` persistent CTAs, partial slots [grid][2][64][128 + 2]
 int attention_tc_key_tile();
-cudaError_t launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+int attention_tc_max_batch();
+int attention_tc_rows(int G, int max_rows);   // padded query rows per kv head, -1 if unsupported
+cudaError_t launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int grid,
                                 cudaStream_t s);
 
 // ---- rejection sampler

@@ -122,3 +122,14 @@ def test_attention_config3_shapes(lib, impl):
     """B=8, gamma=4, GQA 32/8, contexts U[512, 4096] (the verify-attention workload's shapes)."""
     batch = synth.ragged_batch(3, 8, 4, 4, 512, 4096)
     run_case(lib, batch.gammas, batch.ctx_len, 32, 8, seed=123)
+
+
+@pytest.mark.parametrize("grid", [1, 5, 37, 300])
+def test_attention_persistent_grids(lib, grid):
+    """Different persistent grids cut the (sequence, kv head) pairs into different pieces."""
+    lib.spec_set_option("persistent_grid", grid)
+    try:
+        run_case(lib, [10, 3, 7, 1, 0], [130, 64, 511, 1000, 2], 32, 8, seed=40 + grid)
+        run_case(lib, [4, 2], [3000, 260], 16, 4, seed=41 + grid)
+    finally:
+        lib.spec_set_option("persistent_grid", 0)

@@ -23,13 +23,13 @@ def run_case(lib, M, N, K, residual, seed, gemv_max_m=4, grid=0, std=0.05):
     W = synth.normal_bf16_bits(seed + 1, (N, K), std)
     R = synth.normal_bf16_bits(seed + 2, (M, N), 1.0) if residual else None
     lib.spec_set_option("gemv_max_m", gemv_max_m)
-    lib.spec_set_option("linear_grid", grid)
+    lib.spec_set_option("persistent_grid", grid)
     try:
         Y = lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), residual=bf16_dev(R) if residual else None)
         lib.spec_device_status()
     finally:
         lib.spec_set_option("gemv_max_m", 4)
-        lib.spec_set_option("linear_grid", 0)
+        lib.spec_set_option("persistent_grid", 0)
     ref = oops.linear(obf.decode(X), obf.decode(W), obf.decode(R) if residual else None)
     assert_close_rel(f64_of_bf16(Y), ref, f"linear M={M} N={N} K={K}")
 
