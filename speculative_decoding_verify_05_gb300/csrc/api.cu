@@ -212,8 +212,7 @@ AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
   AttnPlan p;
   const int sms = plan_sms();
   const int G = Hkv > 0 ? Hq / Hkv : 1;
-  p.tc = g_attn_impl == 1 && B <= attention_tc_max_batch() && attention_tc_rows(G, max_rows) > 0 &&
-         cap <= 16384;
+  p.tc = g_attn_impl == 1 && B <= attention_tc_max_batch() && attention_tc_rows(G, max_rows) > 0;
   p.counters_off = 0;
   p.partial_off = kCounterBytes;
   if (p.tc) {

@@ -133,3 +133,12 @@ def test_attention_persistent_grids(lib, grid):
         run_case(lib, [4, 2], [3000, 260], 16, 4, seed=41 + grid)
     finally:
         lib.spec_set_option("persistent_grid", 0)
+
+
+def test_attention_very_long_context_many_pieces(lib, impl):
+    """A context past 16k keys; with 300 CTAs each pair is cut into ~150 pieces to merge."""
+    lib.spec_set_option("persistent_grid", 300)
+    try:
+        run_case(lib, [3], [20000], 8, 2, seed=9)
+    finally:
+        lib.spec_set_option("persistent_grid", 0)
