@@ -12,17 +12,18 @@
 //
 // Per tile:
 //   S[row, key] = Q . K_tile^T     tcgen05.mma M = 64 rows, N = 128 keys, K = 128 dims
-//   softmax: an M = 64 accumulator keeps row r in TMEM lane (r / 16) * 32 + r % 16,
-//            so lanes 0-15 of each softmax warp own one query row each: row max,
-//            exp2 and row sum stay in registers and the P row goes straight to
-//            shared memory (no staging, no cross-thread reductions)
+//   softmax: an M = 64 accumulator keeps row r in TMEM lane (r / 16) * 32 + r % 16;
+//            a split TMEM load (.16x32bx2) hands keys 0-63 of those 16 lanes to one
+//            half-warp and keys 64-127 to the other, so two threads share a row: row
+//            max, exp2 and row sum stay in registers (one shuffle each) and the P row
+//            goes straight to shared memory
 //   O[row, d] += P . V_tile        tcgen05.mma M = 64, N = 128 dims (V read MN-major), K = 128 keys
-// Roles (7 warps): 0-3 softmax + epilogue; 4 streams K tiles and stages Q; 5 issues
-// the MMAs (lane 0, event driven: whichever of QK^T or PV has its inputs ready goes
-// first); 6 streams V tiles.  K and V have separate 2-stage TMA rings, Q, P, S and O
-// are double buffered.  The newest gamma_b + 1 keys come from Knew/Vnew: the K and V
-// warps patch them into the tile(s) holding keys >= ctx after the load lands, then copy
-// them into the cache.
+// Roles (8 warps): 0-3 softmax + epilogue; 4 and 6 only issue the TMA loads of K
+// (2-stage ring) and V (3-stage ring: a V tile waits for the softmax, a K tile only for
+// QK^T); 5 issues the MMAs (lane 0, event driven: whichever of QK^T or PV has its inputs
+// ready goes first); 7 stages each pair's Q rows and patches the newest gamma_b + 1 keys
+// (from Knew/Vnew) into the tiles holding keys >= ctx once their loads land, writing the
+// same rows into the cache.  P, S and O are double buffered, Q single buffered.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,23 +33,25 @@ namespace {
 constexpr int D = 128;
 constexpr int KT = 128;                  // keys per tile = MMA N of QK^T, MMA K of PV
 constexpr int QR = 64;                   // query rows per (b, h) pair = MMA M
-constexpr int ST = 2;                    // K and V ring stages
+constexpr int ST_K = 2;                  // K ring stages
+constexpr int ST_V = 3;                  // V ring stages
 constexpr int KV_HALF = KT * 128;        // 128 keys x 64 dims (128 B rows), 16 KB
 constexpr int KV_TILE = 2 * KV_HALF;     // 32 KB
 constexpr int Q_HALF = QR * 128;         // 64 rows x 64 bf16, 8 KB
-constexpr int THREADS = 224;
+constexpr int THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;      // S x2 then O x2, 128 columns each
 constexpr int MAX_B = 1024;              // sequences per call handled by this kernel
 constexpr int META_N = MAX_B + 8;        // entries per metadata array
 
 constexpr int OFF_K = 0;
-constexpr int OFF_V = ST * KV_TILE;
-constexpr int OFF_Q = 2 * ST * KV_TILE;             // 2 buffers x two 64-dim halves
-constexpr int OFF_P = OFF_Q + 2 * 2 * Q_HALF;       // 2 buffers x [64 rows][128 keys] as two halves
-constexpr int OFF_META = OFF_P + 2 * 2 * Q_HALF;    // unit prefix, tiles, ctx, cu_rows per sequence
-constexpr int OFF_BAR = OFF_META + 4 * META_N * 4;
+constexpr int OFF_V = ST_K * KV_TILE;
+constexpr int OFF_Q = OFF_V + ST_V * KV_TILE;       // two 64-dim halves
+constexpr int OFF_P = OFF_Q + 2 * Q_HALF;           // 2 buffers x [64 rows][128 keys] as two halves
+constexpr int OFF_META = OFF_P + 2 * 2 * Q_HALF;    // unit prefix, ctx, cu_rows per sequence
+constexpr int OFF_BAR = OFF_META + 3 * META_N * 4;
 constexpr int OFF_FLAG = OFF_BAR + 256;
 constexpr int SMEM = OFF_FLAG + 16 + 1024;          // + alignment slack
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 // Non-blocking probe of an mbarrier phase (the event-driven MMA loop polls several barriers).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
@@ -84,24 +87,34 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint3
   return d;
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 TMEM lanes, 128 columns split between the half-warps: threads 0-15 get columns
+// [c, c + 64) of lanes base .. base + 15, threads 16-31 columns [c + 64, c + 128) of the same
+// lanes (one asm with its wait, so no register is read before the load completes).
+__device__ __forceinline__ void tmem_ld_split64(uint32_t taddr, float* v) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
-      " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64+0], 64;\n"
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64+32], 64;\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+// The matching store of 16 columns per half-warp (columns [c, c + 16) and [c + 64, c + 80)).
+__device__ __forceinline__ void tmem_st_split16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 64, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Per-sequence metadata in shared memory.
 struct Meta {
   const int* pfx;   // [B + 1] first unit of sequence b (pfx[B] = total units)
-  const int* ntl;   // [B] key tiles per (b, h) pair
   const int* ctx;   // [B] cached context length
   const int* cu;    // [B + 1] verify-row offsets
 };
@@ -113,10 +126,10 @@ struct Cursor {
 };
 __device__ __forceinline__ void cur_seq(Cursor& c, const Meta& m, int B) {
   if (c.b < B) {
-    c.nt = m.ntl[c.b];
     c.ctx = m.ctx[c.b];
     c.r0 = m.cu[c.b];
     c.Mb = m.cu[c.b + 1] - c.r0;
+    c.nt = (c.ctx + c.Mb + KT - 1) / KT;
   }
 }
 __device__ __forceinline__ Cursor cur_at(const Meta& m, int B, long long u) {
@@ -157,9 +170,10 @@ __device__ __forceinline__ int cta_of(long long total, int grid, long long u) {
   return c;
 }
 
-__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float* v, float f) {
+// 64 consecutive outputs v[d] * f rounded to bf16 (eight 16-byte stores).
+__device__ __forceinline__ void store_half_bf16(uint16_t* dst, const float* v, float f) {
 #pragma unroll
-  for (int d = 0; d < D; d += 8)
+  for (int d = 0; d < 64; d += 8)
     *reinterpret_cast<uint4*>(dst + d) =
         make_uint4(pack_bf16x2(v[d] * f, v[d + 1] * f), pack_bf16x2(v[d + 2] * f, v[d + 3] * f),
                    pack_bf16x2(v[d + 4] * f, v[d + 5] * f), pack_bf16x2(v[d + 6] * f, v[d + 7] * f));
@@ -206,25 +220,24 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int* s_pfx = reinterpret_cast<int*>(smem + OFF_META);
-  int* s_ntl = s_pfx + META_N;
-  int* s_ctx = s_ntl + META_N;
+  int* s_ctx = s_pfx + META_N;
   int* s_cu = s_ctx + META_N;
-  const Meta meta{s_pfx, s_ntl, s_ctx, s_cu};
+  const Meta meta{s_pfx, s_ctx, s_cu};
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* k_full = bars;             // [ST]  K tile ready (tail tiles: after the patch)
-  uint64_t* v_full = bars + 2;         // [ST]
-  uint64_t* k_empty = bars + 4;        // [ST]  QK^T done with the K stage
-  uint64_t* v_empty = bars + 6;        // [ST]  PV done with the V stage
-  uint64_t* k_land = bars + 8;         //       tail K load landed (K warp only)
-  uint64_t* v_land = bars + 9;         //       tail V load landed (V warp only)
-  uint64_t* s_full = bars + 10;        // [2]   S in TMEM
-  uint64_t* s_empty = bars + 12;       // [2]   softmax has read S
-  uint64_t* p_full = bars + 14;        // [2]   P in smem, O rescaled
-  uint64_t* pv_done = bars + 16;       // [2]   PV finished (P buffer free, O current)
-  uint64_t* q_full = bars + 18;        // [2]   Q of a pair staged
-  uint64_t* q_empty = bars + 20;       // [2]   last QK^T of a pair done
-  uint64_t* o_empty = bars + 22;       // [2]   epilogue has read the O buffer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+  uint64_t* k_full = bars;             // [ST_K] K tile ready (tiles with new keys: after the patch)
+  uint64_t* k_empty = bars + 2;        // [ST_K] QK^T done with the K stage
+  uint64_t* k_land = bars + 4;         // [ST_K] load landed of a tile that gets new keys
+  uint64_t* v_full = bars + 6;         // [ST_V]
+  uint64_t* v_empty = bars + 9;        // [ST_V] PV done with the V stage
+  uint64_t* v_land = bars + 12;        // [ST_V]
+  uint64_t* s_full = bars + 15;        // [2]    S in TMEM
+  uint64_t* s_empty = bars + 17;       // [2]    softmax has read S
+  uint64_t* p_full = bars + 19;        // [2]    P in smem, O rescaled
+  uint64_t* pv_done = bars + 21;       // [2]    PV finished (P buffer free, O current)
+  uint64_t* o_empty = bars + 23;       // [2]    epilogue has read the O buffer
+  uint64_t* q_full = bars + 25;        //        Q of a pair staged
+  uint64_t* q_empty = bars + 26;       //        last QK^T of a pair done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
   unsigned* last_flag = reinterpret_cast<unsigned*>(smem + OFF_FLAG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -238,23 +251,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   if (tid == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < ST_K; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&k_land[s], 1);
     }
-    mbar_init(k_land, 1);
-    mbar_init(v_land, 1);
+    for (int s = 0; s < ST_V; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_land[s], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 128);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
       mbar_init(&o_empty[i], 128);
     }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -269,9 +284,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int ctx = s_ctx[b];
         const int mb = s_cu[b + 1] - s_cu[b];
         bad |= (mb <= 0 || mb > a.max_rows || ctx < 0 || ctx + mb > a.cap || G * mb > QR);
-        const int nt = mb > 0 ? (ctx + mb + KT - 1) / KT : 1;
-        s_ntl[b] = nt > 0 ? nt : 1;
-        units = s_ntl[b] * Hkv;
+        units = (mb > 0 && ctx >= 0) ? (ctx + mb + KT - 1) / KT * Hkv : 0;
       }
       int incl = units;
 #pragma unroll
@@ -299,43 +312,42 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const long long n_units = ue - ub;
 
   if (warp == 4 || warp == 6) {
-    // ------------------------------------------------------------ producers: K (+Q) and V
-    const bool is_k = warp == 4;
-    const CUtensorMap* tm = is_k ? &tmK : &tmV;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* empty = is_k ? k_empty : v_empty;
-    uint64_t* land = is_k ? k_land : v_land;
-    uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
-    const uint16_t* src_new = is_k ? a.Knew : a.Vnew;
-    uint16_t* cache = is_k ? a.Kc : a.Vc;
-    bool ok = true;
-    int piece = -1, n_tail = 0;
-    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
-    for (long long i = 0; i < n_units && ok; ++i, cur_next(c, meta, B, Hkv)) {
-      const int s = (int)(i % ST);
-      const int key0 = c.t * KT;
-      const int bh = c.b * Hkv + c.h;
-      const bool tail = key0 + KT > c.ctx;
-      if (i >= ST) ok = mbar_wait(&empty[s], (uint32_t)(((i / ST) - 1) & 1), a.status, is_k ? 0x211u : 0x212u);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      uint8_t* st = ring + s * KV_TILE;
-      if (lane == 0) {
-        uint64_t* bar = tail ? land : &full[s];
+    // ------------------------------------------------------------ TMA producers: K and V
+    if (lane == 0 && n_units > 0) {
+      const bool is_k = warp == 4;
+      const int nst = is_k ? ST_K : ST_V;
+      const CUtensorMap* tm = is_k ? &tmK : &tmV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint64_t* land = is_k ? k_land : v_land;
+      uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
+      Cursor c = cur_at(meta, B, ub);
+      for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
+        const int s = (int)(i % nst);
+        const int key0 = c.t * KT;
+        if (i >= nst &&
+            !mbar_wait(&empty[s], (uint32_t)(((i / nst) - 1) & 1), a.status, is_k ? 0x211u : 0x212u))
+          break;
+        uint64_t* bar = (key0 + KT > c.ctx) ? &land[s] : &full[s];
+        uint8_t* st = ring + s * KV_TILE;
+        const int bh = c.b * Hkv + c.h;
         mbar_arrive_expect_tx(bar, KV_TILE);
         tma_load_3d(st, tm, bar, 0, key0, bh);
         tma_load_3d(st + KV_HALF, tm, bar, 64, key0, bh);
       }
-      if (is_k && (c.u == ub || c.t == 0)) {
-        // a new pair: stage its Q rows (row j = token row j / G, head j % G), zero-padded to 64.
-        // The K ring wait above means QK^T of tile i - 2 is done, so the Q buffer of the pair
-        // before the previous one is normally free already.
+    }
+    __syncwarp();
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ Q staging + new-key patches
+    bool ok = true;
+    int piece = -1;
+    int n_land_k[ST_K] = {0, 0}, n_land_v[ST_V] = {0, 0, 0};
+    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
+    for (long long i = 0; i < n_units && ok; ++i, cur_next(c, meta, B, Hkv)) {
+      if (c.u == ub || c.t == 0) {
+        // a new pair: its Q rows (row j = token row j / G, head j % G), zero-padded to 64,
+        // loaded into registers first, stored once QK^T of the previous pair is done
         ++piece;
-        const int qb = piece & 1;
-        if (piece >= 2) ok = mbar_wait(&q_empty[qb], ((piece >> 1) - 1) & 1, a.status, 0x210u);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        uint8_t* qd = smem + OFF_Q + qb * 2 * Q_HALF;
         const int R = G * c.Mb, ch = lane & 15;
         uint4 v[32];
 #pragma unroll
@@ -347,6 +359,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             v[k] = *reinterpret_cast<const uint4*>(a.Q + (size_t)(c.r0 + tr) * a.ldq + (size_t)(c.h * G + g) * D + ch * 8);
           }
         }
+        if (piece >= 1) ok = mbar_wait(q_empty, (uint32_t)((piece - 1) & 1), a.status, 0x210u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint8_t* qd = smem + OFF_Q;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int j = 2 * k + (lane >> 4);
@@ -354,17 +370,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full[qb]);
+        if (lane == 0) mbar_arrive(q_full);
       }
-      if (tail) {
-        ok = mbar_wait(land, (uint32_t)(n_tail & 1), a.status, is_k ? 0x213u : 0x214u);
-        ++n_tail;
+      if (c.t * KT + KT > c.ctx) {
+        const int bh = c.b * Hkv + c.h;
+        const int sk = (int)(i % ST_K), sv = (int)(i % ST_V);
+        ok = mbar_wait(&k_land[sk], (uint32_t)(n_land_k[sk]++ & 1), a.status, 0x213u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        patch_tail(st, src_new, cache, c, a.ldkv, a.cap, bh, lane);
+        patch_tail(smem + OFF_K + sk * KV_TILE, a.Knew, a.Kc, c, a.ldkv, a.cap, bh, lane);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (lane == 0) mbar_arrive(&k_full[sk]);
+        ok = mbar_wait(&v_land[sv], (uint32_t)(n_land_v[sv]++ & 1), a.status, 0x214u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        patch_tail(smem + OFF_V + sv * KV_TILE, a.Vnew, a.Vc, c, a.ldkv, a.cap, bh, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v_full[sv]);
       }
     }
   } else if (warp == 5) {
@@ -372,6 +396,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     if (lane == 0 && n_units > 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(QR, KT);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(QR, D) | (1u << 16);   // B (V) MN-major
+      const uint32_t q_addr = smem_u32(smem + OFF_Q);
       Cursor cs = cur_at(meta, B, ub), cp = cs;
       long long ns = 0, np = 0;          // next QK^T, next PV
       int piece_s = -1, piece_p = -1;
@@ -383,14 +408,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           const bool first = (cs.u == ub || cs.t == 0);
           const bool last = (cs.u + 1 == ue) || (cs.t + 1 == cs.nt);
           const int pc = first ? piece_s + 1 : piece_s;
-          const int qb = pc & 1, s = (int)(ns % ST);
-          if ((!first || mbar_test(&q_full[qb], (uint32_t)((pc >> 1) & 1))) &&
-              mbar_test(&k_full[s], (uint32_t)((ns / ST) & 1)) &&
+          const int s = (int)(ns % ST_K);
+          if ((!first || mbar_test(q_full, (uint32_t)(pc & 1))) &&
+              mbar_test(&k_full[s], (uint32_t)((ns / ST_K) & 1)) &&
               (ns < 2 || mbar_test(&s_empty[ns & 1], (uint32_t)(((ns >> 1) - 1) & 1)))) {
             piece_s = pc;
             tc_fence_after();
             const uint32_t k_addr = smem_u32(smem + OFF_K + s * KV_TILE);
-            const uint32_t q_addr = smem_u32(smem + OFF_Q + qb * 2 * Q_HALF);
             const uint32_t d_s = tmem + (uint32_t)(ns & 1) * KT;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -400,7 +424,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             }
             umma_commit(&k_empty[s]);
             umma_commit(&s_full[ns & 1]);
-            if (last) umma_commit(&q_empty[qb]);
+            if (last) umma_commit(q_empty);
             ++ns;
             cur_next(cs, meta, B, Hkv);
             did = true;
@@ -409,9 +433,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (np < ns) {
           const bool first = (cp.u == ub || cp.t == 0);
           const int pc = first ? piece_p + 1 : piece_p;
-          const int ob = pc & 1, s = (int)(np % ST);
+          const int ob = pc & 1, s = (int)(np % ST_V);
           if (mbar_test(&p_full[np & 1], (uint32_t)((np >> 1) & 1)) &&
-              mbar_test(&v_full[s], (uint32_t)((np / ST) & 1)) &&
+              mbar_test(&v_full[s], (uint32_t)((np / ST_V) & 1)) &&
               (!first || pc < 2 || mbar_test(&o_empty[ob], (uint32_t)(((pc >> 1) - 1) & 1)))) {
             piece_p = pc;
             tc_fence_after();
@@ -446,12 +470,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue warps
-    // Lanes 0-15 of warp q own query row 16 q + lane (TMEM lane 32 q + lane); lanes 16-31 only
-    // take part in the warp-wide TMEM instructions.  After a timed-out wait a thread stops
-    // waiting but keeps the same control flow, so the named barriers below stay matched.
+    // Query row 16 q + (lane % 16) of warp q sits in TMEM lane 32 q + lane % 16; the two
+    // half-warps share it, lanes 0-15 taking keys (and output dims) 0-63, lanes 16-31 keys
+    // 64-127.  After a timed-out wait a thread stops waiting but keeps the same control
+    // flow, so the named barriers below stay matched.
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     const int row = warp * 16 + (lane & 15);
-    const bool owner = lane < 16;
+    const int half = lane >> 4;
     const float scale = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -471,64 +496,70 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const uint32_t t_o = tmem + 2 * KT + (uint32_t)ob * D + lane_off;
       const int key0 = c.t * KT;
       const bool tail = key0 + KT > c.ctx;
-      // key k of the tile is visible to this row iff k <= lim (rows past the group clamp to the last)
-      const int lim = c.ctx + min(row / G, c.Mb - 1) - key0;
+      // key k of this thread's half is visible to the row iff k <= lim (rows past the group
+      // clamp to the last one)
+      const int lim = c.ctx + min(row / G, c.Mb - 1) - key0 - half * 64;
       ok = ok && mbar_wait(&s_full[i & 1], (uint32_t)((i >> 1) & 1), a.status, 0x231u);
       tc_fence_after();
-      float sv[KT];
-      tmem_ld_cols<64>(tmem + (uint32_t)(i & 1) * KT + lane_off, sv);
-      tmem_ld_cols<64>(tmem + (uint32_t)(i & 1) * KT + 64 + lane_off, sv + 64);
+      float sv[64];
+      tmem_ld_split64(tmem + (uint32_t)(i & 1) * KT + lane_off, sv);
       tc_fence_before();
       mbar_arrive(&s_empty[i & 1]);
-      float mx = -INFINITY;
+      // scaled logits and their maximum (8 independent chains)
+      float mx8[8];
 #pragma unroll
-      for (int k = 0; k < KT; ++k) {
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
         float v = sv[k] * scale;
         if (tail && k > lim) v = -INFINITY;
         sv[k] = v;
-        mx = fmaxf(mx, v);
+        mx8[k & 7] = fmaxf(mx8[k & 7], v);
       }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       // the running max only moves when the tile max exceeds it by more than 2^8: P <= 256
       // stays representable, and O, l keep using one common max, so the result is unchanged
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const bool grew = m_new != m_run;
       const float base = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = ex2(m_run - base);
-      float sm = 0.f;
+      float sm8[8];
 #pragma unroll
-      for (int k = 0; k < KT; ++k) {
+      for (int e = 0; e < 8; ++e) sm8[e] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
         sv[k] = ex2(sv[k] - base);
-        sm += sv[k];
+        sm8[k & 7] += sv[k];
       }
+      float sm = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      sm += __shfl_xor_sync(0xffffffffu, sm, 16);
       l_run = l_run * alpha + sm;
       m_run = m_new;
       // P buffer i & 1 was last read by PV(i - 2)
       if (i >= 2) ok = ok && mbar_wait(&pv_done[i & 1], (uint32_t)(((i >> 1) - 1) & 1), a.status, 0x232u);
-      if (owner) {
-        uint8_t* prow = smem + OFF_P + (int)(i & 1) * 2 * Q_HALF;
+      {
+        uint8_t* prow = smem + OFF_P + (int)(i & 1) * 2 * Q_HALF + half * Q_HALF;
 #pragma unroll
-        for (int k = 0; k < KT; k += 8) {
+        for (int k = 0; k < 64; k += 8) {
           const uint4 wv = make_uint4(pack_bf16x2(sv[k], sv[k + 1]), pack_bf16x2(sv[k + 2], sv[k + 3]),
                                       pack_bf16x2(sv[k + 4], sv[k + 5]), pack_bf16x2(sv[k + 6], sv[k + 7]));
-          *reinterpret_cast<uint4*>(prow + (k >> 6) * Q_HALF + sw128_off(row, k & 63)) = wv;
+          *reinterpret_cast<uint4*>(prow + sw128_off(row, k)) = wv;
         }
       }
-      if (!first && __any_sync(0xffffffffu, owner && grew)) {
+      if (!first && __any_sync(0xffffffffu, grew)) {
         // O must hold PV(i - 1) before it is rescaled; PV(i) waits for this tile's p_full
         ok = ok && mbar_wait(&pv_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), a.status, 0x234u);
         tc_fence_after();
-        const float f = owner ? alpha : 1.f;
+        float ov[64];
+        tmem_ld_split64(t_o, ov);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float ov[64];
-          tmem_ld_cols<64>(t_o + half * 64, ov);
+        for (int cc = 0; cc < 64; cc += 16) {
+          float o16[16];
 #pragma unroll
-          for (int cc = 0; cc < 64; cc += 16) {
-            float o16[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) o16[e] = ov[cc + e] * f;
-            tmem_st16(t_o + half * 64 + cc, o16);
-          }
+          for (int e = 0; e < 16; ++e) o16[e] = ov[cc + e] * alpha;
+          tmem_st_split16(t_o + cc, o16);
         }
         tmem_st_wait();
       }
@@ -537,30 +568,30 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       mbar_arrive(&p_full[i & 1]);
       if (!last) continue;
 
-      // ---- piece epilogue: the row's O once this tile's PV is done
+      // ---- piece epilogue: this thread's 64 output dims of the row once the tile's PV is done
       ok = ok && mbar_wait(&pv_done[i & 1], (uint32_t)((i >> 1) & 1), a.status, 0x233u);
       tc_fence_after();
-      float ov[D];
-      tmem_ld_cols<64>(t_o, ov);
-      tmem_ld_cols<64>(t_o + 64, ov + 64);
+      float ov[64];
+      tmem_ld_split64(t_o, ov);
       tc_fence_before();
       mbar_arrive(&o_empty[ob]);
       const int bh = c.b * Hkv + c.h;
       const long long pair0 = u - c.t;
       const long long pair_last = pair0 + c.nt - 1;
       const bool complete = (pair0 >= ub) && (u == pair_last);
-      if (owner && row < R) {
+      if (row < R) {
         if (complete) {
           const int tr = row / G, g = row - tr * G;
-          store_row_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D, ov, 1.f / l_run);
+          store_half_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D + half * 64, ov, 1.f / l_run);
         } else {
           // slot 0: the piece that opens this CTA's range; slot 1: the piece that closes it
           const int slot = (pair0 < ub) ? 0 : 1;
           float* pb = a.partial + ((size_t)blockIdx.x * 2 + slot) * (QR * (D + 2));
 #pragma unroll
-          for (int d = 0; d < D; d += 4)
-            __stcg(reinterpret_cast<float4*>(pb + row * D + d), make_float4(ov[d], ov[d + 1], ov[d + 2], ov[d + 3]));
-          __stcg(reinterpret_cast<float2*>(pb + QR * D + row * 2), make_float2(m_run, l_run));
+          for (int d = 0; d < 64; d += 4)
+            __stcg(reinterpret_cast<float4*>(pb + row * D + half * 64 + d),
+                   make_float4(ov[d], ov[d + 1], ov[d + 2], ov[d + 3]));
+          if (half == 0) __stcg(reinterpret_cast<float2*>(pb + QR * D + row * 2), make_float2(m_run, l_run));
         }
       }
       if (complete) continue;
@@ -580,40 +611,35 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       __threadfence();
       const int c_lo = cta_of(total, grid, pair0);
       const int c_hi = cta_of(total, grid, pair_last);
-      // one query row per owner thread: weights exp2(m_c - M) / L, then the weighted sum of
-      // the contributors' O rows
-      if (owner && row < R) {
-        float M = -INFINITY;
-        for (int c2 = c_lo; c2 <= c_hi; ++c2) {
-          const int sl = (range_begin(total, grid, c2) > pair0) ? 0 : 1;
-          M = fmaxf(M, __ldcg(a.partial + ((size_t)c2 * 2 + sl) * (QR * (D + 2)) + QR * D + row * 2));
-        }
-        const float mb = M == -INFINITY ? 0.f : M;
-        float L = 0.f;
-        for (int c2 = c_lo; c2 <= c_hi; ++c2) {
-          const int sl = (range_begin(total, grid, c2) > pair0) ? 0 : 1;
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-              a.partial + ((size_t)c2 * 2 + sl) * (QR * (D + 2)) + QR * D + row * 2));
-          L += ml.y * ex2(ml.x - mb);
-        }
-        float acc[D];
+      // one pass over the contributors in CTA order (each one's (m, l) and O half-row loaded
+      // together), rescaling the running sums to the running maximum
+      if (row < R) {
+        float M = -INFINITY, L = 0.f;
+        float acc[64];
 #pragma unroll
-        for (int d = 0; d < D; ++d) acc[d] = 0.f;
+        for (int d = 0; d < 64; ++d) acc[d] = 0.f;
         for (int c2 = c_lo; c2 <= c_hi; ++c2) {
           const int sl = (range_begin(total, grid, c2) > pair0) ? 0 : 1;
           const float* pk = a.partial + ((size_t)c2 * 2 + sl) * (QR * (D + 2));
-          const float f = ex2(__ldcg(pk + QR * D + row * 2) - mb);
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(pk + QR * D + row * 2));
+          float4 v[16];
 #pragma unroll
-          for (int d = 0; d < D; d += 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(pk + row * D + d));
-            acc[d] += f * v.x;
-            acc[d + 1] += f * v.y;
-            acc[d + 2] += f * v.z;
-            acc[d + 3] += f * v.w;
+          for (int q = 0; q < 16; ++q) v[q] = __ldcg(reinterpret_cast<const float4*>(pk + row * D + half * 64 + q * 4));
+          const float mn = fmaxf(M, ml.x);
+          if (mn == -INFINITY) continue;                       // nothing visible in either yet
+          const float fo = ex2(M - mn), fc = ex2(ml.x - mn);  // 2^-inf = 0
+          L = L * fo + ml.y * fc;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            acc[4 * q] = acc[4 * q] * fo + v[q].x * fc;
+            acc[4 * q + 1] = acc[4 * q + 1] * fo + v[q].y * fc;
+            acc[4 * q + 2] = acc[4 * q + 2] * fo + v[q].z * fc;
+            acc[4 * q + 3] = acc[4 * q + 3] * fo + v[q].w * fc;
           }
+          M = mn;
         }
         const int tr = row / G, g = row - tr * G;
-        store_row_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D, acc, 1.f / L);
+        store_half_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D + half * 64, acc, 1.f / L);
       }
       if (tid == 0) a.counters[bh] = 0u;
     }
