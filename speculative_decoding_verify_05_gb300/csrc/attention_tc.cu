@@ -22,8 +22,9 @@
 // (2-stage ring) and V (3-stage ring: a V tile waits for the softmax, a K tile only for
 // QK^T); 5 issues the MMAs (lane 0, event driven: whichever of QK^T or PV has its inputs
 // ready goes first); 7 stages each pair's Q rows and patches the newest gamma_b + 1 keys
-// (from Knew/Vnew) into the tiles holding keys >= ctx once their loads land, writing the
-// same rows into the cache.  P, S and O are double buffered, Q single buffered.
+// (from Knew) into the K tiles holding keys >= ctx once their loads land; the softmax
+// warps do the same for V (zeroing the rows past the block) just before that tile's PV.
+// Both write the new rows into the cache too.  Q, S and O are double buffered, P single.
 #include "common.cuh"
 #include "internal.h"
 
@@ -45,9 +46,9 @@ constexpr int META_N = MAX_B + 8;        // entries per metadata array
 
 constexpr int OFF_K = 0;
 constexpr int OFF_V = ST_K * KV_TILE;
-constexpr int OFF_Q = OFF_V + ST_V * KV_TILE;       // two 64-dim halves
-constexpr int OFF_P = OFF_Q + 2 * Q_HALF;           // 2 buffers x [64 rows][128 keys] as two halves
-constexpr int OFF_META = OFF_P + 2 * 2 * Q_HALF;    // unit prefix, ctx, cu_rows per sequence
+constexpr int OFF_Q = OFF_V + ST_V * KV_TILE;       // 2 buffers x two 64-dim halves
+constexpr int OFF_P = OFF_Q + 2 * 2 * Q_HALF;       // [64 rows][128 keys] as two 64-key halves
+constexpr int OFF_META = OFF_P + 2 * Q_HALF;        // unit prefix, ctx, cu_rows per sequence
 constexpr int OFF_BAR = OFF_META + 3 * META_N * 4;
 constexpr int OFF_FLAG = OFF_BAR + 256;
 constexpr int SMEM = OFF_FLAG + 16 + 1024;          // + alignment slack
@@ -179,39 +180,55 @@ __device__ __forceinline__ void store_half_bf16(uint16_t* dst, const float* v, f
                    pack_bf16x2(v[d + 4] * f, v[d + 5] * f), pack_bf16x2(v[d + 6] * f, v[d + 7] * f));
 }
 
-// A tile holding keys >= ctx (the last one or two of a pair; one warp): its keys in
-// ctx .. ctx + Mb - 1 come from the new block `src` (row stride ldkv, head h), keys past
-// them are zeroed, and the same new rows are written into the cache of pair bh.  Only the
-// CTA owning the tile loads those cache rows, and its load has landed.  All loads are
-// issued before the first store (one memory round trip).
-__device__ __forceinline__ void patch_tail(uint8_t* stage, const uint16_t* src, uint16_t* cache, const Cursor& c,
-                                           int ldkv, int cap, int bh, int lane) {
+// A tile holding keys >= ctx (the last one or two of a pair): its rows rr0 .. rr0 + n_new - 1
+// are keys first_new .. first_new + n_new - 1 of the new block.
+struct TailRows {
+  int rr0, n_new, first_new;
+};
+__device__ __forceinline__ TailRows tail_rows(const Cursor& c) {
   const int key0 = c.t * KT;
-  const int rr0 = c.ctx > key0 ? c.ctx - key0 : 0;
-  const int end = c.ctx + c.Mb - key0 < KT ? c.ctx + c.Mb - key0 : KT;
-  const int n_new = end - rr0;                          // new keys inside this tile (>= 1)
-  const int first_new = key0 + rr0 - c.ctx;             // index of the first one in the block
-  uint4 v[32];
+  TailRows g;
+  g.rr0 = c.ctx > key0 ? c.ctx - key0 : 0;
+  g.n_new = min(c.ctx + c.Mb - key0, KT) - g.rr0;    // >= 1
+  g.first_new = key0 + g.rr0 - c.ctx;
+  return g;
+}
+// NT threads load the new rows of head h from `src` (row stride ldkv) into registers:
+// 16-byte chunk t + NT k of the n_new x 16 chunks (the block has at most 64 rows).
+template <int NT>
+__device__ __forceinline__ void tail_load(uint4 (&v)[1024 / NT], const uint16_t* src, const Cursor& c,
+                                          const TailRows& g, int ldkv, int t) {
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int idx = lane + 32 * k, j = idx >> 4, ch = idx & 15;
+  for (int k = 0; k < 1024 / NT; ++k) {
+    const int idx = t + NT * k, j = idx >> 4, ch = idx & 15;
     v[k] = make_uint4(0, 0, 0, 0);
-    if (j < n_new)
-      v[k] = *reinterpret_cast<const uint4*>(src + (size_t)(c.r0 + first_new + j) * ldkv + (size_t)c.h * D + ch * 8);
+    if (j < g.n_new)
+      v[k] = *reinterpret_cast<const uint4*>(src + (size_t)(c.r0 + g.first_new + j) * ldkv + (size_t)c.h * D + ch * 8);
   }
+}
+// ... and store them into the landed stage and into the cache rows of pair bh.  Only the CTA
+// owning the tile loads those cache rows, and its load has landed.  With `zero_rest` the stage
+// rows past the new block are zeroed: whatever the cache holds there would meet P = 0 in P . V
+// (K needs no zeros: masked scores are replaced, not multiplied).
+template <int NT>
+__device__ __forceinline__ void tail_store(const uint4 (&v)[1024 / NT], uint8_t* stage, uint16_t* cache,
+                                           const Cursor& c, const TailRows& g, int cap, int bh, int t,
+                                           bool zero_rest) {
+  const int key0 = c.t * KT;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int idx = lane + 32 * k, j = idx >> 4, ch = idx & 15;
-    if (j < n_new) {
-      const int rr = rr0 + j;
+  for (int k = 0; k < 1024 / NT; ++k) {
+    const int idx = t + NT * k, j = idx >> 4, ch = idx & 15;
+    if (j < g.n_new) {
+      const int rr = g.rr0 + j;
       *reinterpret_cast<uint4*>(stage + (ch >> 3) * KV_HALF + sw128_off(rr, (ch & 7) * 8)) = v[k];
       *reinterpret_cast<uint4*>(cache + ((size_t)bh * cap + key0 + rr) * D + ch * 8) = v[k];
     }
   }
-  for (int idx = (rr0 + n_new) * 16 + lane; idx < KT * 16; idx += 32) {
-    const int rr = idx >> 4, ch = idx & 15;
-    *reinterpret_cast<uint4*>(stage + (ch >> 3) * KV_HALF + sw128_off(rr, (ch & 7) * 8)) = make_uint4(0, 0, 0, 0);
-  }
+  if (zero_rest)
+    for (int idx = (g.rr0 + g.n_new) * 16 + t; idx < KT * 16; idx += NT) {
+      const int rr = idx >> 4, ch = idx & 15;
+      *reinterpret_cast<uint4*>(stage + (ch >> 3) * KV_HALF + sw128_off(rr, (ch & 7) * 8)) = make_uint4(0, 0, 0, 0);
+    }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -232,11 +249,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* v_land = bars + 12;        // [ST_V]
   uint64_t* s_full = bars + 15;        // [2]    S in TMEM
   uint64_t* s_empty = bars + 17;       // [2]    softmax has read S
-  uint64_t* p_full = bars + 19;        // [2]    P in smem, O rescaled
-  uint64_t* pv_done = bars + 21;       // [2]    PV finished (P buffer free, O current)
-  uint64_t* o_empty = bars + 23;       // [2]    epilogue has read the O buffer
-  uint64_t* q_full = bars + 25;        //        Q of a pair staged
-  uint64_t* q_empty = bars + 26;       //        last QK^T of a pair done
+  uint64_t* p_full = bars + 19;        //        P in smem, O rescaled
+  uint64_t* pv_done = bars + 20;       //        PV finished (P free, O current)
+  uint64_t* o_empty = bars + 21;       // [2]    epilogue has read the O buffer
+  uint64_t* q_full = bars + 23;        // [2]    Q of a pair staged
+  uint64_t* q_empty = bars + 25;       // [2]    last QK^T of a pair done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
   unsigned* last_flag = reinterpret_cast<unsigned*>(smem + OFF_FLAG);
 
@@ -264,12 +281,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 128);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&pv_done[i], 1);
       mbar_init(&o_empty[i], 128);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -338,16 +355,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     __syncwarp();
   } else if (warp == 7) {
-    // ------------------------------------------------------------ Q staging + new-key patches
+    // ------------------------------------------------------------ Q staging + new K rows
     bool ok = true;
     int piece = -1;
-    int n_land_k[ST_K] = {0, 0}, n_land_v[ST_V] = {0, 0, 0};
+    int n_land_k[ST_K] = {0, 0};
     Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
     for (long long i = 0; i < n_units && ok; ++i, cur_next(c, meta, B, Hkv)) {
       if (c.u == ub || c.t == 0) {
         // a new pair: its Q rows (row j = token row j / G, head j % G), zero-padded to 64,
-        // loaded into registers first, stored once QK^T of the previous pair is done
+        // loaded into registers first, stored once QK^T of the pair two back is done
         ++piece;
+        const int qb = piece & 1;
         const int R = G * c.Mb, ch = lane & 15;
         uint4 v[32];
 #pragma unroll
@@ -359,10 +377,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             v[k] = *reinterpret_cast<const uint4*>(a.Q + (size_t)(c.r0 + tr) * a.ldq + (size_t)(c.h * G + g) * D + ch * 8);
           }
         }
-        if (piece >= 1) ok = mbar_wait(q_empty, (uint32_t)((piece - 1) & 1), a.status, 0x210u);
+        if (piece >= 2) ok = mbar_wait(&q_empty[qb], (uint32_t)(((piece >> 1) - 1) & 1), a.status, 0x210u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        uint8_t* qd = smem + OFF_Q;
+        uint8_t* qd = smem + OFF_Q + qb * 2 * Q_HALF;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int j = 2 * k + (lane >> 4);
@@ -370,25 +388,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(q_full);
+        if (lane == 0) mbar_arrive(&q_full[qb]);
       }
       if (c.t * KT + KT > c.ctx) {
-        const int bh = c.b * Hkv + c.h;
-        const int sk = (int)(i % ST_K), sv = (int)(i % ST_V);
+        const int sk = (int)(i % ST_K);
+        const TailRows g = tail_rows(c);
+        uint4 v[32];
+        tail_load<32>(v, a.Knew, c, g, a.ldkv, lane);
         ok = mbar_wait(&k_land[sk], (uint32_t)(n_land_k[sk]++ & 1), a.status, 0x213u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        patch_tail(smem + OFF_K + sk * KV_TILE, a.Knew, a.Kc, c, a.ldkv, a.cap, bh, lane);
+        tail_store<32>(v, smem + OFF_K + sk * KV_TILE, a.Kc, c, g, a.cap, c.b * Hkv + c.h, lane, false);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[sk]);
-        ok = mbar_wait(&v_land[sv], (uint32_t)(n_land_v[sv]++ & 1), a.status, 0x214u);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        patch_tail(smem + OFF_V + sv * KV_TILE, a.Vnew, a.Vc, c, a.ldkv, a.cap, bh, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&v_full[sv]);
       }
     }
   } else if (warp == 5) {
@@ -396,7 +409,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     if (lane == 0 && n_units > 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(QR, KT);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(QR, D) | (1u << 16);   // B (V) MN-major
-      const uint32_t q_addr = smem_u32(smem + OFF_Q);
       Cursor cs = cur_at(meta, B, ub), cp = cs;
       long long ns = 0, np = 0;          // next QK^T, next PV
       int piece_s = -1, piece_p = -1;
@@ -408,13 +420,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           const bool first = (cs.u == ub || cs.t == 0);
           const bool last = (cs.u + 1 == ue) || (cs.t + 1 == cs.nt);
           const int pc = first ? piece_s + 1 : piece_s;
-          const int s = (int)(ns % ST_K);
-          if ((!first || mbar_test(q_full, (uint32_t)(pc & 1))) &&
+          const int qb = pc & 1, s = (int)(ns % ST_K);
+          if ((!first || mbar_test(&q_full[qb], (uint32_t)((pc >> 1) & 1))) &&
               mbar_test(&k_full[s], (uint32_t)((ns / ST_K) & 1)) &&
               (ns < 2 || mbar_test(&s_empty[ns & 1], (uint32_t)(((ns >> 1) - 1) & 1)))) {
             piece_s = pc;
             tc_fence_after();
             const uint32_t k_addr = smem_u32(smem + OFF_K + s * KV_TILE);
+            const uint32_t q_addr = smem_u32(smem + OFF_Q + qb * 2 * Q_HALF);
             const uint32_t d_s = tmem + (uint32_t)(ns & 1) * KT;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -424,7 +437,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             }
             umma_commit(&k_empty[s]);
             umma_commit(&s_full[ns & 1]);
-            if (last) umma_commit(q_empty);
+            if (last) umma_commit(&q_empty[qb]);
             ++ns;
             cur_next(cs, meta, B, Hkv);
             did = true;
@@ -434,13 +447,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           const bool first = (cp.u == ub || cp.t == 0);
           const int pc = first ? piece_p + 1 : piece_p;
           const int ob = pc & 1, s = (int)(np % ST_V);
-          if (mbar_test(&p_full[np & 1], (uint32_t)((np >> 1) & 1)) &&
+          if (mbar_test(p_full, (uint32_t)(np & 1)) &&
               mbar_test(&v_full[s], (uint32_t)((np / ST_V) & 1)) &&
               (!first || pc < 2 || mbar_test(&o_empty[ob], (uint32_t)(((pc >> 1) - 1) & 1)))) {
             piece_p = pc;
             tc_fence_after();
             const uint32_t v_addr = smem_u32(smem + OFF_V + s * KV_TILE);
-            const uint32_t p_addr = smem_u32(smem + OFF_P + (int)(np & 1) * 2 * Q_HALF);
+            const uint32_t p_addr = smem_u32(smem + OFF_P);
             const uint32_t t_o = tmem + 2 * KT + (uint32_t)ob * D;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -450,7 +463,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                         (!first || kk > 0) ? 1u : 0u);
             }
             umma_commit(&v_empty[s]);
-            umma_commit(&pv_done[np & 1]);
+            umma_commit(pv_done);
             ++np;
             cur_next(cp, meta, B, Hkv);
             did = true;
@@ -481,6 +494,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int piece = -1;
+    int n_land_v[ST_V] = {0, 0, 0};
     Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
     for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
       const long long u = c.u;
@@ -496,6 +510,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const uint32_t t_o = tmem + 2 * KT + (uint32_t)ob * D + lane_off;
       const int key0 = c.t * KT;
       const bool tail = key0 + KT > c.ctx;
+      // a tile with new keys: their V rows are fetched now and patched in before this tile's PV
+      TailRows g{};
+      uint4 vnew[8];
+      if (tail) {
+        g = tail_rows(c);
+        tail_load<128>(vnew, a.Vnew, c, g, a.ldkv, tid);
+      }
       // key k of this thread's half is visible to the row iff k <= lim (rows past the group
       // clamp to the last one)
       const int lim = c.ctx + min(row / G, c.Mb - 1) - key0 - half * 64;
@@ -537,10 +558,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       sm += __shfl_xor_sync(0xffffffffu, sm, 16);
       l_run = l_run * alpha + sm;
       m_run = m_new;
-      // P buffer i & 1 was last read by PV(i - 2)
-      if (i >= 2) ok = ok && mbar_wait(&pv_done[i & 1], (uint32_t)(((i >> 1) - 1) & 1), a.status, 0x232u);
+      // P was last read by PV(i - 1), which also has to be in O before O is rescaled
+      if (i >= 1) ok = ok && mbar_wait(pv_done, (uint32_t)((i - 1) & 1), a.status, 0x232u);
       {
-        uint8_t* prow = smem + OFF_P + (int)(i & 1) * 2 * Q_HALF + half * Q_HALF;
+        uint8_t* prow = smem + OFF_P + half * Q_HALF;
 #pragma unroll
         for (int k = 0; k < 64; k += 8) {
           const uint4 wv = make_uint4(pack_bf16x2(sv[k], sv[k + 1]), pack_bf16x2(sv[k + 2], sv[k + 3]),
@@ -549,8 +570,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
       }
       if (!first && __any_sync(0xffffffffu, grew)) {
-        // O must hold PV(i - 1) before it is rescaled; PV(i) waits for this tile's p_full
-        ok = ok && mbar_wait(&pv_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), a.status, 0x234u);
         tc_fence_after();
         float ov[64];
         tmem_ld_split64(t_o, ov);
@@ -563,13 +582,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         tmem_st_wait();
       }
+      if (tail) {
+        const int sv_ = (int)(i % ST_V);
+        ok = ok && mbar_wait(&v_land[sv_], (uint32_t)(n_land_v[sv_]++ & 1), a.status, 0x214u);
+        tail_store<128>(vnew, smem + OFF_V + sv_ * KV_TILE, a.Vc, c, g, a.cap, c.b * Hkv + c.h, tid, true);
+        fence_proxy_async_smem();
+        bar_compute();
+        if (tid == 0) mbar_arrive(&v_full[sv_]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[i & 1]);
+      mbar_arrive(p_full);
       if (!last) continue;
 
       // ---- piece epilogue: this thread's 64 output dims of the row once the tile's PV is done
-      ok = ok && mbar_wait(&pv_done[i & 1], (uint32_t)((i >> 1) & 1), a.status, 0x233u);
+      ok = ok && mbar_wait(pv_done, (uint32_t)(i & 1), a.status, 0x233u);
       tc_fence_after();
       float ov[64];
       tmem_ld_split64(t_o, ov);
