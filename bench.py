@@ -124,23 +124,10 @@ def attention_bytes(batch, dims):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def run_gpu(args):
+def build_round(dev, rank, S, E, synth):
+    """Resident state of the benchmark round (weights, KV caches, inputs, draft distribution)
+    and a function that runs one full verify round on it."""
     import torch
-    import torch.distributed as dist
-
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from speculative_decoding_verify_05_gb300 import binding as S
-    from speculative_decoding_verify_05_gb300 import engine as E
-    import synth
-
-    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
     dims = E.Dims()
     batch = make_batch()
     cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
@@ -177,11 +164,35 @@ def run_gpu(args):
     out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(batch.M, dtype=torch.int32, device=dev),
            torch.empty(B, dtype=torch.int32, device=dev))
 
-    S.reset_launch_count()
-
     def step():
         eng.x[:batch.M].copy_(x0)
         eng.verify_round(eng.x[:batch.M], cu, ctx, q, drafts, U, TEMP, out=out)
+
+    return dict(dims=dims, batch=batch, cap=cap, sw=sw, kcs=kcs, vcs=vcs, eng=eng, x0=x0, cu=cu, ctx=ctx,
+                U=U, q=q, drafts=drafts, out=out, step=step)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from speculative_decoding_verify_05_gb300 import binding as S
+    from speculative_decoding_verify_05_gb300 import engine as E
+    import synth
+
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+    st = build_round(dev, rank, S, E, synth)
+    dims, batch, cap, sw, kcs, vcs, eng = (st[k] for k in ("dims", "batch", "cap", "sw", "kcs", "vcs", "eng"))
+    x0, cu, ctx, q, drafts, out, step = (st[k] for k in ("x0", "cu", "ctx", "q", "drafts", "out", "step"))
+    S.reset_launch_count()
 
     # eager warm-up (loads every kernel), then capture the round in one CUDA graph
     step()
@@ -557,6 +568,7 @@ def run_reference(args):
 def run_profile_case(args):
     """Small, self-contained launches of one hot kernel for an ncu capture (no timing).
 
+    round: one full verify round of the benchmark workload (for the launch list);
     attention: one layer of B=16 ragged sequences (KV ~0.6 GB, above L2);
     linear: one gate|up projection (201 MB of weights) at --rows rows;
     lmhead: the LM head + softmax at --rows rows.
@@ -571,7 +583,16 @@ def run_profile_case(args):
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     ws = S.Workspace(dev)
-    if args.profile == "attention":
+    if args.profile == "round":
+        # the benchmark's full verify round, run eagerly: once to warm up, then once inside
+        # the NVTX range "round" (ncu --nvtx --nvtx-include "round/" lists only that one)
+        st = build_round(dev, 0, S, E, synth)
+        st["step"]()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("round")
+        st["step"]()
+        torch.cuda.nvtx.range_pop()
+    elif args.profile == "attention":
         batch = synth.ragged_batch(SEED, 16, G_LO, G_HI, CTX_LO, CTX_HI)
         cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
         kc = torch.empty((16, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
@@ -609,7 +630,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--profile", choices=["attention", "linear", "lmhead"], default=None,
+    ap.add_argument("--profile", choices=["round", "attention", "linear", "lmhead"], default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")

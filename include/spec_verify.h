@@ -72,6 +72,12 @@ enum {
 /* Message of the last failing call on this host thread ("" if none). */
 SPEC_API const char* spec_last_error(void);
 
+/* Number of library kernels the last call on this host thread enqueued (0 after
+ * a failing call): spec_verify_linear enqueues one, or two when the GEMM split
+ * some tiles' k-steps between CTAs (the second sums their pieces);
+ * spec_lmhead_softmax two; the other compute calls one.  For launch accounting. */
+SPEC_API int spec_launches(void);
+
 /* Library ABI version (increments on any signature change). */
 SPEC_API int spec_version(void);
 
@@ -80,6 +86,9 @@ SPEC_API int spec_version(void);
  * default 0 = one CTA per SM): CTAs of the persistent tensor-core GEMM and
  * attention kernels;
  * "attention_impl" (1 = tcgen05 kernel, default; 0 = mma.sync kernel);
+ * "attention_pair_cost" (0..64, default 12): work the tcgen05 attention kernel
+ * charges for starting a (sequence, kv head) pair, in quarters of a 128-key
+ * tile, when it splits the key tiles evenly between CTAs;
  * "linear_nsub" (1 default, or 2: one tensor-core tile covers up to 512 rows).
  * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for
  * an unknown name or value. */

@@ -24,6 +24,7 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 _SIGS = {
     "spec_last_error": (ctypes.c_char_p, []),
     "spec_version": (_i, []),
+    "spec_launches": (_i, []),
     "spec_set_option": (_i, [ctypes.c_char_p, _i]),
     "spec_device_status": (_i, [_vp, ctypes.POINTER(_i)]),
     "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
@@ -64,11 +65,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 _lib = load()
 
 
-def _check(rc: int, kernels: int = 0) -> None:
+def _check(rc: int, compute: bool = False) -> None:
+    """Raise on an error code; after a compute call, add the kernels it enqueued."""
     global _launches
     if rc != SPEC_OK:
         raise SpecError(rc, _lib.spec_last_error().decode())
-    _launches += kernels
+    if compute:
+        _launches += _lib.spec_launches()
 
 
 # Number of library kernels launched through this binding (for launch accounting).
@@ -175,7 +178,7 @@ def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None,
     _check(_lib.spec_verify_linear(
         _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
-        wp, wn, _stream(stream)), 1 if M else 0)
+        wp, wn, _stream(stream)), True)
     return Y
 
 
@@ -193,7 +196,7 @@ def spec_verify_linear_noalloc(X, W, Y, residual=None, stream=None):
     _check(_lib.spec_verify_linear_noalloc(
         _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
-        _stream(stream)), 1 if M else 0)
+        _stream(stream)), True)
     return Y
 
 
@@ -229,7 +232,7 @@ def spec_verify_attention(Q, Knew, Vnew, cu_rows, ctx_len, Kcache, Vcache, max_r
     _check(_lib.spec_verify_attention(
         _p(Q), _rowmajor(Q, "Q"), _p(Knew), _p(Vnew), ldkv, _p(cu_rows), _p(ctx_len), B,
         int(max_rows), _p(Kcache), _p(Vcache), cap, Hq, Hkv, D, float(scale), _p(O),
-        _rowmajor(O, "O"), wp, wn, _stream(stream)), 1 if B else 0)
+        _rowmajor(O, "O"), wp, wn, _stream(stream)), True)
     return O
 
 
@@ -250,7 +253,7 @@ def spec_lmhead_softmax(H, Wlm, temperature: float, P=None, ws: Workspace | None
     _need(P, torch.float32, "P")
     wp, wn = _ws_args(ws, spec_lmhead_workspace_bytes(M, K, V), H.device)
     _check(_lib.spec_lmhead_softmax(_p(H), M, K, _p(Wlm), V, float(temperature), _p(P), wp, wn,
-                                    _stream(stream)), 2 if M else 0)
+                                    _stream(stream)), True)
     return P
 
 
@@ -270,8 +273,7 @@ def spec_reject_sample(P, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5, out=N
         if not t.is_contiguous():
             raise ValueError("sampler inputs must be contiguous")
     _check(_lib.spec_reject_sample(_p(P), _p(Q), _p(draft_tok), _p(U), _p(cu_rows), B, V,
-                                   float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)),
-           1 if B else 0)
+                                   float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)), True)
     return n_acc, out_tok, near
 
 
@@ -282,7 +284,7 @@ def spec_rmsnorm(X, w, eps: float = 1e-6, Y=None, stream=None):
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _check(_lib.spec_rmsnorm(_p(X), M, N, _rowmajor(X, "X"), _p(w), float(eps), _p(Y),
-                             _rowmajor(Y, "Y"), _stream(stream)), 1 if M else 0)
+                             _rowmajor(Y, "Y"), _stream(stream)), True)
     return Y
 
 
@@ -293,7 +295,7 @@ def spec_rope(Q, K, cu_rows, ctx_len, D: int, theta: float = 1e6, stream=None):
     B = cu_rows.numel() - 1
     _check(_lib.spec_rope(_p(Q), _rowmajor(Q, "Q"), Q.shape[1] // D, _p(K), _rowmajor(K, "K"),
                           K.shape[1] // D, D, _p(cu_rows), _p(ctx_len), B, M, float(theta),
-                          _stream(stream)), 1 if M else 0)
+                          _stream(stream)), True)
 
 
 def spec_silu_mul(GU, A=None, stream=None):
@@ -304,5 +306,5 @@ def spec_silu_mul(GU, A=None, stream=None):
     if A is None:
         A = torch.empty((M, inter), dtype=torch.bfloat16, device=GU.device)
     _check(_lib.spec_silu_mul(_p(GU), M, inter, _rowmajor(GU, "GU"), _p(A), _rowmajor(A, "A"),
-                              _stream(stream)), 1 if M else 0)
+                              _stream(stream)), True)
     return A

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kVersion = 1;
 thread_local std::string t_err;
+thread_local int t_launches = 0;   // kernels the last call on this thread launched
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -31,10 +32,12 @@ int fail(int code, const char* fmt, ...) {
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
   t_err = buf;
+  t_launches = 0;
   return code;
 }
-int ok() {
+int ok(int launched = 0) {
   t_err.clear();
+  t_launches = launched;
   return SPEC_OK;
 }
 int cuda_fail(cudaError_t e, const char* what) {
@@ -126,8 +129,9 @@ constexpr size_t kMaxCounters = kCounterBytes / 4;
 // --------------------------------------------------------------------------- linear plan
 int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
 int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
+int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
-int g_nsub_max = 1;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
+int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 
 struct LinPlan {
   bool gemv = false;
@@ -165,7 +169,9 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
     p.tiles_m = 1;
     p.NSUB = 1;
     p.BN = std::max(16, (M + 15) / 16 * 16);
-  } else if (g_nsub_max == 1) {
+  } else if (g_nsub_max == 1 || lmhead) {
+    // (the LM head keeps two accumulator buffers so each tile's epilogue overlaps the next
+    // tile's MMAs: it has ~1200 tiles, each with a long softmax-statistics epilogue)
     p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
     const int per = (M + p.tiles_m - 1) / p.tiles_m;
     p.NSUB = 1;
@@ -235,6 +241,7 @@ AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
 extern "C" {
 
 const char* spec_last_error(void) { return t_err.c_str(); }
+int spec_launches(void) { return t_launches; }
 int spec_version(void) { return kVersion; }
 
 int spec_set_option(const char* name, int value) {
@@ -242,6 +249,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "gemv_max_m")) {
     if (value < 0 || value > 4) return fail(SPEC_EINVAL, "gemv_max_m must be in [0, 4]");
     g_gemv_max_m = value;
+    return ok();
+  }
+  if (!strcmp(name, "attention_pair_cost")) {
+    if (value < 0 || value > 64) return fail(SPEC_EINVAL, "attention_pair_cost must be in [0, 64]");
+    g_attn_pair_cost = value;
     return ok();
   }
   if (!strcmp(name, "attention_impl")) {
@@ -325,7 +337,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     a.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
     cudaError_t e = launch_gemv(a, p.gemv_grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
-    return ok();
+    return ok(1);
   }
   CUtensorMap tw, tx;
   {
@@ -345,12 +357,16 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   a.units = p.units; a.grid = p.grid; a.aligned = p.aligned ? 1 : 0;
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
-  a.counters = p.bytes > 0 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
   a.status = d->status;
+  a.tn = p.BN * p.NSUB;
   dim3 grid(p.grid);
   cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
-  return ok();
+  if (p.bytes == 0) return ok(1);
+  // some tiles had their k-steps split between CTAs: a second kernel sums their pieces
+  e = launch_linear_reduce(a, plan_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+  return ok(2);
 }
 
 // --------------------------------------------------------------------------- LM head
@@ -403,7 +419,7 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   e = launch_lmhead_normalize(P, a.stats, M, V, p.tiles_n, greedy, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head normalize launch");
-  return ok();
+  return ok(2);
 }
 
 // --------------------------------------------------------------------------- attention
@@ -458,10 +474,11 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   a.partial = reinterpret_cast<float*>(ws + p.partial_off);
   a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
   a.status = d->status;
+  a.pair_cost = g_attn_pair_cost;
   cudaError_t e = p.tc ? launch_attention_tc(tk, tv, a, p.grid, static_cast<cudaStream_t>(stream))
                        : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-  return ok();
+  return ok(1);
 }
 
 // --------------------------------------------------------------------------- sampler
@@ -478,7 +495,7 @@ int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
   cudaError_t e = launch_reject_sample(P, Q, draft_tok, U, cu_rows, B, V, tie_eps, n_acc, out_tok,
                                        near_tie, d->status, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "reject_sample launch");
-  return ok();
+  return ok(1);
 }
 
 // --------------------------------------------------------------------------- glue
@@ -493,7 +510,7 @@ int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, 
   if (!(eps >= 0.f)) return fail(SPEC_EINVAL, "eps must be >= 0");
   cudaError_t e = launch_rmsnorm(X, M, N, ldx, w, eps, Y, ldy, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
-  return ok();
+  return ok(1);
 }
 
 int spec_rope(spec_bf16* Q, int ldq, int Hq, spec_bf16* K, int ldk, int Hkv, int D,
@@ -509,7 +526,7 @@ int spec_rope(spec_bf16* Q, int ldq, int Hq, spec_bf16* K, int ldk, int Hkv, int
   cudaError_t e = launch_rope(Q, ldq, Hq, K, ldk, Hkv, D, cu_rows, ctx_len, B, M, theta,
                               static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rope launch");
-  return ok();
+  return ok(1);
 }
 
 int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int lda,
@@ -521,7 +538,7 @@ int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int
   if (!aligned16(GU) || !aligned16(A)) return fail(SPEC_EINVAL, "16-byte alignment");
   cudaError_t e = launch_silu_mul(GU, M, I, ldgu, A, lda, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "silu_mul launch");
-  return ok();
+  return ok(1);
 }
 
 }  // extern "C"

@@ -160,15 +160,45 @@ __device__ __forceinline__ void cur_next(Cursor& c, const Meta& m, int B, int Hk
   }
 }
 
-__device__ __forceinline__ long long range_begin(long long total, int grid, int c) {
-  return total * c / grid;
+// Cost-balanced split of the tile list: a tile costs WT, starting a pair costs wp more, so
+// unit u of pair p = b Hkv + h ends at cumulative cost C(u) = WT (u + 1) + wp (p + 1) and CTA
+// c owns the units with floor((C(u) - 1) grid / Ctot) == c.  CTAs that cover many short
+// pairs (each with its own epilogue, tail patch and possibly a merge) get fewer tiles.
+constexpr long long WT = 4;
+struct Part {
+  long long U, Ctot;   // units, total cost
+  int P, grid, Hkv, wp;
+};
+__device__ __forceinline__ long long cost_end(const Part& q, long long u, int p) {
+  return WT * (u + 1) + (long long)q.wp * (p + 1);
 }
-__device__ __forceinline__ int cta_of(long long total, int grid, long long u) {
-  int c = (int)(((u + 1) * grid - 1) / total);
-  if (c >= grid) c = grid - 1;
-  while (c + 1 < grid && range_begin(total, grid, c + 1) <= u) ++c;
-  while (c > 0 && range_begin(total, grid, c) > u) --c;
-  return c;
+__device__ __forceinline__ int cta_of(const Part& q, long long u, int p) {
+  const long long c = (cost_end(q, u, p) - 1) * q.grid / q.Ctot;
+  return c < q.grid - 1 ? (int)c : q.grid - 1;
+}
+// first unit of pair p; nt = its tiles
+__device__ __forceinline__ long long pair_first(const Meta& m, int Hkv, int p, int& nt) {
+  const int b = p / Hkv, h = p - b * Hkv;
+  nt = (m.ctx[b] + m.cu[b + 1] - m.cu[b] + KT - 1) / KT;
+  return m.pfx[b] + (long long)h * nt;
+}
+// first unit owned by CTA c (U for c >= grid): the smallest u with C(u) >= T(c)
+__device__ long long range_start(const Part& q, const Meta& m, int c) {
+  if (c <= 0 || q.U == 0) return 0;
+  if (c >= q.grid) return q.U;
+  const long long T = ((long long)c * q.Ctot + q.grid - 1) / q.grid + 1;
+  if (T > q.Ctot) return q.U;             // more CTAs than cost units: this one and the rest are empty
+  int lo = 0, hi = q.P - 1, nt;
+  while (lo < hi) {                       // first pair whose last unit reaches T (C(U - 1) = Ctot)
+    const int mid = (lo + hi) >> 1;
+    const long long f = pair_first(m, q.Hkv, mid, nt);
+    if (cost_end(q, f + nt - 1, mid) >= T) hi = mid; else lo = mid + 1;
+  }
+  const long long f = pair_first(m, q.Hkv, lo, nt);
+  const long long need = T - (long long)q.wp * (lo + 1);    // WT (u + 1) >= need
+  long long t = (need > 0 ? (need + WT - 1) / WT : 0) - 1 - f;
+  t = t < 0 ? 0 : (t > nt - 1 ? nt - 1 : t);
+  return f + t;
 }
 
 // 64 consecutive outputs v[d] * f rounded to bf16 (eight 16-byte stores).
@@ -256,6 +286,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* q_empty = bars + 25;       // [2]    last QK^T of a pair done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
   unsigned* last_flag = reinterpret_cast<unsigned*>(smem + OFF_FLAG);
+  long long* s_range = reinterpret_cast<long long*>(bars + 28);   // this CTA's [ub, ue)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv, G = a.G;
@@ -317,15 +348,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       s_pfx[B] = bad ? 0 : carry;          // nothing to do when the ragged arrays are invalid
       if (bad && blockIdx.x == 0) set_status(a.status, 0x2F1u);
     }
+    __syncwarp();
+    if (lane == 0) {
+      const long long U = s_pfx[B];
+      const Part q{U, WT * U + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
+      s_range[0] = range_start(q, meta, blockIdx.x);
+      s_range[1] = range_start(q, meta, blockIdx.x + 1);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long total = s_pfx[B];
-  const int grid = gridDim.x;
-  const long long ub = total > 0 ? range_begin(total, grid, blockIdx.x) : 0;
-  const long long ue = total > 0 ? range_begin(total, grid, blockIdx.x + 1) : 0;
+  const Part part{total, WT * total + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
+  const long long ub = s_range[0], ue = s_range[1];
   const long long n_units = ue - ub;
 
   if (warp == 4 || warp == 6) {
@@ -636,17 +673,26 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       bar_compute();
       if (!merge) continue;
       __threadfence();
-      const int c_lo = cta_of(total, grid, pair0);
-      const int c_hi = cta_of(total, grid, pair_last);
+      const int p_id = c.b * Hkv + c.h;
+      const int c_lo = cta_of(part, pair0, p_id);
+      const int c_hi = cta_of(part, pair_last, p_id);
       // one pass over the contributors in CTA order (each one's (m, l) and O half-row loaded
-      // together), rescaling the running sums to the running maximum
+      // together), rescaling the running sums to the running maximum.  The first contributor
+      // left its piece in slot 1 (the pair starts inside its range), the others in slot 0;
+      // a CTA between them with an empty range contributed nothing.
       if (row < R) {
         float M = -INFINITY, L = 0.f;
         float acc[64];
 #pragma unroll
         for (int d = 0; d < 64; ++d) acc[d] = 0.f;
+        long long next_start = c_hi - c_lo >= 2 ? range_start(part, meta, c_lo + 1) : 0;
         for (int c2 = c_lo; c2 <= c_hi; ++c2) {
-          const int sl = (range_begin(total, grid, c2) > pair0) ? 0 : 1;
+          if (c2 > c_lo && c2 < c_hi) {
+            const long long st = next_start;
+            next_start = range_start(part, meta, c2 + 1);
+            if (next_start == st) continue;
+          }
+          const int sl = c2 == c_lo ? 1 : 0;
           const float* pk = a.partial + ((size_t)c2 * 2 + sl) * (QR * (D + 2));
           const float2 ml = __ldcg(reinterpret_cast<const float2*>(pk + QR * D + row * 2));
           float4 v[16];

@@ -18,6 +18,9 @@ int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
+// Second pass of a split GEMM: sums the fp32 pieces of every split tile (in CTA order), adds the
+// residual and writes bf16 Y.  `sms` sizes its grid.
+cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_linear_tc_lmhead(int BN, int NSUB, bool greedy, const CUtensorMap& tw,
                                     const CUtensorMap& tx, const LinearArgs& a, dim3 grid,
                                     cudaStream_t s);
@@ -55,6 +58,7 @@ struct AttnArgs {
   float* partial;       // [B*Hkv][max_chunks][64][128 + 2]
   unsigned* counters;   // [B*Hkv]
   unsigned* status;
+  int pair_cost;        // tcgen05 kernel: work charged per (sequence, kv head) pair, quarter tiles
 };
 cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                              cudaStream_t s);

@@ -14,9 +14,10 @@
 // STAGES-deep ring without ever draining it; warp 1 issues four
 // tcgen05.mma (K = 16) per stage into one of two TMEM accumulators; warps 2-5
 // drain the other accumulator meanwhile.  A tile whose k-steps are split
-// between CTAs is finished by the CTA that arrives last on the tile's counter
-// (an atomic, no waiting): it sums the fp32 partials in CTA order, adds the
-// residual, rounds to bf16 and resets the counter.
+// between CTAs leaves one fp32 piece per CTA in the workspace; a second, fully
+// parallel kernel sums the pieces in CTA order, adds the residual and rounds
+// to bf16 (one SM finishing a whole split tile alone would leave the rest of
+// the GPU idle at the end of the GEMM).
 #pragma once
 
 #include "common.cuh"
@@ -40,8 +41,8 @@ struct LinearArgs {
   int ldy;
   const uint16_t* residual;
   int ldr;
-  float* partial;       // [grid][2][BN][128] fp32 (split tiles only)
-  unsigned* counters;   // [tiles] zero-initialised arrival counters (split tiles only)
+  float* partial;       // [grid][2][TN][128] fp32 (split tiles only)
+  int tn;               // token columns per tile (BN * NSUB)
   unsigned* status;     // library status word (bounded-wait timeouts)
   float inv_temp;       // EPI_LOGITS
   float* P;             // EPI_LOGITS: [M x N] fp32

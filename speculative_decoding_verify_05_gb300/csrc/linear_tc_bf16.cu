@@ -85,4 +85,106 @@ cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const
   }
 }
 
+// Second pass of a split GEMM.  Every block first tabulates the CTA range starts of the
+// GEMM (beg[c] = units * c / grid, one 64-bit division per entry).  A tile is split iff a
+// range starts strictly inside it; the first such range c names the tile, whose pieces came
+// from CTAs c - 1 .. hi (the last range starting inside it).  Warp item = (c, 8 token
+// columns); lane l owns weight rows n0 + 4 l .. + 3 (one float4 per column of a piece).
+// Pieces are summed in CTA order, four contributors' loads in flight at a time, then the
+// residual is added and the sum rounded to bf16.
+__global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a) {
+  extern __shared__ long long s_beg[];                      // [grid + 1]
+  int* s_hi = reinterpret_cast<int*>(s_beg + a.grid + 1);   // [grid] -1: c names no tile
+  const int G = a.grid, TN = a.tn;
+  const long long kt = a.k_tiles;
+  for (int c = threadIdx.x; c <= G; c += blockDim.x) s_beg[c] = a.units * c / G;
+  __syncthreads();
+  for (int c = threadIdx.x; c < G; c += blockDim.x) {
+    int hi = -1;
+    if (c > 0) {
+      const long long b = s_beg[c], t0 = b / kt * kt;
+      if (b != t0 && s_beg[c - 1] <= t0) {
+        hi = c;
+        while (hi + 1 < G && s_beg[hi + 1] < t0 + kt) ++hi;
+      }
+    }
+    s_hi[c] = hi;
+  }
+  __syncthreads();
+  const int cols8 = (TN + 7) / 8;
+  const long long items = (long long)G * cols8;
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+    const int c = (int)(it / cols8);
+    const int hi = s_hi[c];
+    if (hi < 0) continue;
+    const int j0 = (int)(it - (long long)c * cols8) * 8;
+    const long long t0 = s_beg[c] / kt * kt;
+    const long long tile = t0 / kt;
+    const int m0 = (int)(tile % a.tiles_m) * TN + j0;
+    const int n4 = (int)(tile / a.tiles_m) * 128 + lane * 4;
+    float4 acc[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = c - 1; c0 <= hi; c0 += 4) {
+      float4 v[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = c0 + q;
+        // slot 0 holds a CTA's first segment: the tile is it iff the CTA starts inside it
+        const float* base = cc <= hi ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
+                                     : nullptr;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          v[q][jj] = (base && j0 + jj < TN) ? __ldcg(reinterpret_cast<const float4*>(base + (j0 + jj) * 128))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          acc[jj].x += v[q][jj].x; acc[jj].y += v[q][jj].y; acc[jj].z += v[q][jj].z; acc[jj].w += v[q][jj].w;
+        }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int m = m0 + jj;
+      if (j0 + jj >= TN || m >= a.M) continue;
+      float y[4] = {acc[jj].x, acc[jj].y, acc[jj].z, acc[jj].w};
+      if (n4 + 3 < a.N) {
+        if (a.residual) {
+          const uint2 rr = *reinterpret_cast<const uint2*>(a.residual + (size_t)m * a.ldr + n4);
+          y[0] += bf16lo(rr.x); y[1] += bf16hi(rr.x); y[2] += bf16lo(rr.y); y[3] += bf16hi(rr.y);
+        }
+        *reinterpret_cast<uint2*>(a.Y + (size_t)m * a.ldy + n4) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+      } else {
+        for (int e = 0; e < 4 && n4 + e < a.N; ++e) {
+          float v2 = y[e];
+          if (a.residual) v2 += bf16f(a.residual[(size_t)m * a.ldr + n4 + e]);
+          a.Y[(size_t)m * a.ldy + n4 + e] = f2bf(v2);
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
+  const size_t smem = (size_t)(a.grid + 1) * 8 + (size_t)a.grid * 4;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    // up to 4096 persistent CTAs: 4097 starts + 4096 ends
+    cudaError_t e = cudaFuncSetAttribute(linear_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 4097 * 8 + 4096 * 4);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 4LL * sms) blocks = 4LL * sms;
+  linear_reduce_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace spec

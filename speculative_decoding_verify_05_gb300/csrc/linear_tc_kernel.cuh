@@ -70,7 +70,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;   // [NBUF]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  unsigned* last_flag = tmem_slot + 1;
   float2* red = reinterpret_cast<float2*>(smem + STAGES * Cfg::STAGE_BYTES + 1024);  // [4][TN]
 
   const int warp = threadIdx.x >> 5;
@@ -196,7 +195,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           tc_fence_before();
           mbar_arrive(&acc_empty[acc]);
         } else {
-          // split tile: publish this CTA's fp32 partial (slot 0 = its first segment, 1 = its last)
+          // split tile: publish this CTA's fp32 piece (slot 0 = its first segment, 1 = its last);
+          // the reduce kernel that follows the GEMM sums the pieces
           const int slot = (u == ub) ? 0 : 1;
           float* part = args.partial + ((size_t)cta * 2 + slot) * (TN * 128);
 #pragma unroll 1
@@ -208,70 +208,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           }
           tc_fence_before();
           mbar_arrive(&acc_empty[acc]);
-          __threadfence();
-          bar_epi();
-          if (etid == 0) {
-            const unsigned add = (unsigned)(seg_end - u);
-            const unsigned prev = atomicAdd(&args.counters[tile], add);
-            *last_flag = (prev + add == (unsigned)kt) ? 1u : 0u;
-          }
-          bar_epi();
-          const bool last = *last_flag != 0u;
-          bar_epi();   // every thread has read the flag before it can be rewritten
-          if (last) {
-            // last arrival: sum every contributor's partial in CTA order (deterministic).
-            // Loads are batched (8 token columns x all contributors in flight per thread)
-            // so the reduction is bandwidth-, not latency-bound.
-            __threadfence();
-            const int c_lo = cta_of_unit(args, tile * kt);
-            const int c_hi = cta_of_unit(args, (tile + 1) * kt - 1);
-            const int r4 = lane * 4;
-            const int n4 = n0 + r4;
-            constexpr int JB = 8;
-            for (int j0 = ewarp; j0 < TN; j0 += 4 * JB) {
-              float4 acc[JB];
-#pragma unroll
-              for (int q2 = 0; q2 < JB; ++q2) acc[q2] = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int cc = c_lo; cc <= c_hi; ++cc) {
-                const int sl = (unit_begin(args, cc) / kt == tile) ? 0 : 1;
-                const float* base = args.partial + ((size_t)cc * 2 + sl) * (TN * 128) + r4;
-                float4 v[JB];
-#pragma unroll
-                for (int q2 = 0; q2 < JB; ++q2) {
-                  const int j = j0 + 4 * q2;
-                  v[q2] = (j < TN) ? __ldcg(reinterpret_cast<const float4*>(base + j * 128))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int q2 = 0; q2 < JB; ++q2) {
-                  acc[q2].x += v[q2].x; acc[q2].y += v[q2].y; acc[q2].z += v[q2].z; acc[q2].w += v[q2].w;
-                }
-              }
-#pragma unroll
-              for (int q2 = 0; q2 < JB; ++q2) {
-                const int j = j0 + 4 * q2;
-                const int m = m0 + j;
-                if (j >= TN || m >= args.M) continue;
-                float y[4] = {acc[q2].x, acc[q2].y, acc[q2].z, acc[q2].w};
-                if (n4 + 3 < args.N) {
-                  if (args.residual) {
-                    const uint2 rr = *reinterpret_cast<const uint2*>(args.residual + (size_t)m * args.ldr + n4);
-                    y[0] += bf16lo(rr.x); y[1] += bf16hi(rr.x); y[2] += bf16lo(rr.y); y[3] += bf16hi(rr.y);
-                  }
-                  *reinterpret_cast<uint2*>(args.Y + (size_t)m * args.ldy + n4) =
-                      make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
-                } else {
-                  for (int e = 0; e < 4; ++e) {
-                    if (n4 + e >= args.N) break;
-                    float v2 = y[e];
-                    if (args.residual) v2 += bf16f(args.residual[(size_t)m * args.ldr + n4 + e]);
-                    args.Y[(size_t)m * args.ldy + n4 + e] = f2bf(v2);
-                  }
-                }
-              }
-            }
-            if (etid == 0) args.counters[tile] = 0u;
-          }
         }
       } else {
         // LM-head epilogues (ranges are tile-aligned, so every segment is whole):

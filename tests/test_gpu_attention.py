@@ -142,3 +142,19 @@ def test_attention_very_long_context_many_pieces(lib, impl):
         run_case(lib, [3], [20000], 8, 2, seed=9)
     finally:
         lib.spec_set_option("persistent_grid", 0)
+
+
+@pytest.mark.parametrize("pair_cost", [0, 8, 64])
+@pytest.mark.parametrize("grid", [7, 0, 300])
+def test_attention_pair_cost_partitions(lib, pair_cost, grid):
+    """Cost-balanced splits (pair starts charged 0, 2 or 16 tiles) over several grids, including
+    grids with more CTAs than tiles (empty ranges between the pieces of one pair)."""
+    lib.spec_set_option("attention_pair_cost", pair_cost)
+    lib.spec_set_option("persistent_grid", grid)
+    try:
+        run_case(lib, [10, 3, 7, 1, 0, 5], [130, 64, 511, 1000, 2, 2900], 32, 8, seed=60 + grid + pair_cost)
+        run_case(lib, [0, 2], [126, 3], 8, 8, seed=61 + grid)
+        run_case(lib, [4], [130], 4, 2, seed=62 + grid)          # 4 tiles: most CTAs get nothing
+    finally:
+        lib.spec_set_option("attention_pair_cost", 12)
+        lib.spec_set_option("persistent_grid", 0)

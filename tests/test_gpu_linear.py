@@ -94,3 +94,21 @@ def test_linear_strided_output_slice(lib):
     ref = oops.linear(obf.decode(X), obf.decode(W))
     assert_close_rel(f64_of_bf16(big[:, N:2 * N]), ref, "strided Y")
     assert torch.count_nonzero(big[:, :N]) == 0 and torch.count_nonzero(big[:, 2 * N:]) == 0
+
+
+def test_linear_launch_accounting(lib):
+    """One kernel when every tile is finished by one CTA, two when split tiles need the reduce."""
+    X = bf16_dev(synth.normal_bf16_bits(3, (368, 4096), 1.0))
+    W = bf16_dev(synth.normal_bf16_bits(4, (6144, 4096), 0.02))
+    lib.reset_launch_count()
+    lib.spec_verify_linear(X, W)
+    assert lib.launch_count() == (2 if lib.spec_linear_workspace_bytes(368, 6144, 4096) > 0 else 1)
+    lib.spec_set_option("persistent_grid", 1)      # one CTA: every tile whole, no workspace
+    try:
+        assert lib.spec_linear_workspace_bytes(368, 6144, 4096) == 0
+        lib.reset_launch_count()
+        lib.spec_verify_linear(X, W)
+        assert lib.launch_count() == 1
+    finally:
+        lib.spec_set_option("persistent_grid", 0)
+    lib.spec_device_status()
