@@ -1,6 +1,8 @@
 // Layer glue of the decoder stack between the verify GEMMs and attention:
 // RMSNorm, rotary position embedding, SwiGLU.  All bandwidth-trivial (M rows
 // of a few thousand elements); fp32 math, bf16 storage, 16-byte accesses.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -60,29 +62,40 @@ rmsnorm_kernel(const uint16_t* __restrict__ X, int N, int ldx, const uint16_t* _
 
 constexpr int ROPE_THREADS = 256;
 
+// Inverse frequencies theta^(-2 i / D), computed once in fp64 on the host.
+struct RopeFreq {
+  double inv[128];
+};
+constexpr int ROPE_SMEM_B = 8192;   // sequences whose row offsets are staged in shared memory
+
 __global__ void __launch_bounds__(ROPE_THREADS)
 rope_kernel(uint16_t* __restrict__ Q, int ldq, int Hq, uint16_t* __restrict__ K, int ldk, int Hkv,
             int D, const int32_t* __restrict__ cu_rows, const int32_t* __restrict__ ctx_len, int B,
-            double theta) {
+            const __grid_constant__ RopeFreq f, int vec) {
   const int r = blockIdx.x;
   const int half = D / 2;
   __shared__ float s_cos[128];
   __shared__ float s_sin[128];
+  __shared__ int s_cu[ROPE_SMEM_B + 1];
   __shared__ int s_pos;
+  // position of row r = ctx_len[b] + (r - cu_rows[b]), b = last sequence with cu_rows[b] <= r
+  const bool staged = B <= ROPE_SMEM_B;
+  if (staged)
+    for (int i = threadIdx.x; i <= B; i += ROPE_THREADS) s_cu[i] = cu_rows[i];
+  __syncthreads();
   if (threadIdx.x == 0) {
-    int lo = 0, hi = B - 1;           // last b with cu_rows[b] <= r
+    int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (cu_rows[mid] <= r) lo = mid; else hi = mid - 1;
+      if ((staged ? s_cu[mid] : cu_rows[mid]) <= r) lo = mid; else hi = mid - 1;
     }
-    s_pos = ctx_len[lo] + (r - cu_rows[lo]);
+    s_pos = ctx_len[lo] + (r - (staged ? s_cu[lo] : cu_rows[lo]));
   }
   __syncthreads();
   if (threadIdx.x < half) {
     // angle in fp64, reduced to [-pi, pi] before the fp32 sincos
     const int i = threadIdx.x;
-    const double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
-    const double ang = (double)s_pos * inv_freq;
+    const double ang = (double)s_pos * f.inv[i];
     const double two_pi = 6.283185307179586476925286766559;
     const double red = ang - two_pi * rint(ang / two_pi);
     float sv, cv;
@@ -92,6 +105,29 @@ rope_kernel(uint16_t* __restrict__ Q, int ldq, int Hq, uint16_t* __restrict__ K,
   }
   __syncthreads();
   const int heads = Hq + Hkv;
+  if (vec) {
+    // 8 consecutive pairs (i, i + D/2) per thread: two 16-byte loads and stores
+    const int chunks = half / 8;
+    for (int idx = threadIdx.x; idx < heads * chunks; idx += ROPE_THREADS) {
+      const int hd = idx / chunks, i0 = (idx - hd * chunks) * 8;
+      uint16_t* base = hd < Hq ? Q + (size_t)r * ldq + (size_t)hd * D
+                               : K + (size_t)r * ldk + (size_t)(hd - Hq) * D;
+      const uint4 av = *reinterpret_cast<const uint4*>(base + i0);
+      const uint4 bv = *reinterpret_cast<const uint4*>(base + half + i0);
+      const uint32_t a4[4] = {av.x, av.y, av.z, av.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+      uint32_t x4[4], y4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + 2 * e;
+        const float a0 = bf16lo(a4[e]), a1 = bf16hi(a4[e]), b0 = bf16lo(b4[e]), b1 = bf16hi(b4[e]);
+        x4[e] = pack_bf16x2(a0 * s_cos[i] - b0 * s_sin[i], a1 * s_cos[i + 1] - b1 * s_sin[i + 1]);
+        y4[e] = pack_bf16x2(b0 * s_cos[i] + a0 * s_sin[i], b1 * s_cos[i + 1] + a1 * s_sin[i + 1]);
+      }
+      *reinterpret_cast<uint4*>(base + i0) = make_uint4(x4[0], x4[1], x4[2], x4[3]);
+      *reinterpret_cast<uint4*>(base + half + i0) = make_uint4(y4[0], y4[1], y4[2], y4[3]);
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < heads * half; idx += ROPE_THREADS) {
     const int hd = idx / half, i = idx - hd * half;
     uint16_t* base = hd < Hq ? Q + (size_t)r * ldq + (size_t)hd * D
@@ -138,8 +174,11 @@ cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint1
 cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int Hkv, int D,
                         const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, float theta,
                         cudaStream_t s) {
-  rope_kernel<<<M, ROPE_THREADS, 0, s>>>(Q, ldq, Hq, K, ldk, Hkv, D, cu_rows, ctx_len, B,
-                                         (double)theta);
+  RopeFreq f{};
+  for (int i = 0; i < D / 2; ++i) f.inv[i] = std::pow((double)theta, -2.0 * (double)i / (double)D);
+  const bool vec = D % 16 == 0 && ldq % 8 == 0 && ldk % 8 == 0 &&
+                   (reinterpret_cast<uintptr_t>(Q) & 15) == 0 && (reinterpret_cast<uintptr_t>(K) & 15) == 0;
+  rope_kernel<<<M, ROPE_THREADS, 0, s>>>(Q, ldq, Hq, K, ldk, Hkv, D, cu_rows, ctx_len, B, f, vec ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -6,7 +6,7 @@ import torch
 import synth
 from oracle import bf16 as obf, ops as oops, sampler as osamp, stack as ostack
 
-from gpu_util import PROB_ATOL, assert_close_rel, assert_rows_close_l2, bf16_dev, dev, f64_of_bf16
+from gpu_util import PROB_ATOL, assert_close_rel, assert_rows_close_l2, bf16_dev, bits_of, dev, f64_of_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +32,22 @@ def test_rope(lib):
     kr = oops.rope(obf.decode(Kb).reshape(batch.M, Hkv, D), pos, 1e6).reshape(batch.M, -1)
     assert_close_rel(f64_of_bf16(Qd), qr, "rope q", rel=1e-2)
     assert_close_rel(f64_of_bf16(Kd), kr, "rope k", rel=1e-2)
+
+
+def test_rope_unaligned_heads(lib):
+    """Head size 72 and rows starting 2 bytes into the buffer: the element-by-element path."""
+    batch = synth.RaggedBatch([3, 1], [100, 4000])
+    Hq, Hkv, D = 4, 2, 72
+    Qb = synth.normal_bf16_bits(5, (batch.M, Hq * D + 1), 1.0)
+    Kb = synth.normal_bf16_bits(6, (batch.M, Hkv * D + 1), 1.0)
+    Qd, Kd = bf16_dev(Qb), bf16_dev(Kb)
+    lib.spec_rope(Qd[:, 1:], Kd[:, 1:], dev(batch.cu_rows), dev(batch.ctx_len), D, 1e4)
+    pos = np.concatenate([batch.ctx_len[b] + np.arange(batch.gammas[b] + 1) for b in range(batch.B)])
+    qr = oops.rope(obf.decode(Qb[:, 1:]).reshape(batch.M, Hq, D), pos, 1e4).reshape(batch.M, -1)
+    kr = oops.rope(obf.decode(Kb[:, 1:]).reshape(batch.M, Hkv, D), pos, 1e4).reshape(batch.M, -1)
+    assert_close_rel(f64_of_bf16(Qd[:, 1:]), qr, "rope q (unaligned)", rel=1e-2)
+    assert_close_rel(f64_of_bf16(Kd[:, 1:]), kr, "rope k (unaligned)", rel=1e-2)
+    assert np.array_equal(bits_of(Qd[:, :1]), Qb[:, :1])
 
 
 def test_silu_mul(lib):
