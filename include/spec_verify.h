@@ -89,7 +89,10 @@ SPEC_API int spec_version(void);
  * "attention_pair_cost" (0..64, default 12): work the tcgen05 attention kernel
  * charges for starting a (sequence, kv head) pair, in quarters of a 128-key
  * tile, when it splits the key tiles evenly between CTAs;
- * "linear_nsub" (1 default, or 2: one tensor-core tile covers up to 512 rows).
+ * "linear_nsub" (2, default: one tensor-core tile covers up to 512 rows; 1: up
+ * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
+ * tiles split each tile's k-steps between the CTAs of a thread-block cluster
+ * and sum the pieces on chip.
  * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for
  * an unknown name or value. */
 SPEC_API int spec_set_option(const char* name, int value);

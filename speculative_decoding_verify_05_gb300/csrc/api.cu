@@ -131,12 +131,14 @@ int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
 int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
+int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 
 struct LinPlan {
   bool gemv = false;
   int BN = 16, NSUB = 1, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
   int grid = 1;                 // persistent CTAs of the tensor-core path
+  int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
   bool aligned = false;         // CTA ranges cover whole tiles only
   long long units = 0;
   int gemv_grid = 1, k_per_split = 0, groups = 0;
@@ -191,6 +193,27 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
   // persistent stream-K: one CTA per SM, each streaming an equal share of (tile, k-step) units;
   // the LM-head epilogue needs whole tiles, so its ranges are tile-aligned
   p.aligned = lmhead || tiles > (long long)kMaxCounters;
+  // few tiles: S CTAs of a cluster split each tile's k-steps and sum on chip (one wave of
+  // tiles * S CTAs).  Cost model in k-steps of one tile on one SM: the cluster kernel takes
+  // ceil(kt / S) plus ~6 for its on-chip reduction; stream-K takes ceil(units / SMs) plus
+  // ~20 when tiles are split (fp32 pieces through L2 and a second kernel)
+  if (!lmhead && g_linear_cluster && g_force_grid == 0 && tiles < sms) {
+    int best = 0;
+    long long best_cost = 0;
+    for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
+      const int cap = linear_cluster_capacity(p.BN, p.NSUB, S);
+      if (cap <= 0 || tiles * S > cap) continue;
+      const long long cost = (p.k_tiles + S - 1) / S + 6;
+      if (best == 0 || cost < best_cost) { best = S; best_cost = cost; }
+    }
+    const long long sk_cost = (p.units + sms - 1) / sms + 20;
+    if (best >= 2 && best_cost < sk_cost) {
+      p.cluster_S = best;
+      p.grid = (int)(tiles * best);
+      p.bytes = 0;
+      return p;
+    }
+  }
   int grid = g_force_grid > 0 ? g_force_grid : sms;
   const long long cap_units = p.aligned ? tiles : p.units;
   if (grid > cap_units) grid = (int)cap_units;
@@ -249,6 +272,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "gemv_max_m")) {
     if (value < 0 || value > 4) return fail(SPEC_EINVAL, "gemv_max_m must be in [0, 4]");
     g_gemv_max_m = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_cluster")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_cluster must be 0 or 1");
+    g_linear_cluster = value;
     return ok();
   }
   if (!strcmp(name, "attention_pair_cost")) {
@@ -359,6 +387,11 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
+  if (p.cluster_S > 0) {
+    cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch");
+    return ok(1);
+  }
   dim3 grid(p.grid);
   cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");

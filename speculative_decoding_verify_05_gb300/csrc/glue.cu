@@ -19,12 +19,14 @@ rmsnorm_kernel(const uint16_t* __restrict__ X, int N, int ldx, const uint16_t* _
   const uint16_t* x = X + (size_t)r * ldx;
   const int nv = N / 8;
   float v[RMS_MAX_VEC][8];
+  uint4 wv[RMS_MAX_VEC];               // weights fetched with the row (one memory round trip)
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < RMS_MAX_VEC; ++k) {
     const int c = threadIdx.x + k * RMS_THREADS;
     if (c < nv) {
       const uint4 u = *reinterpret_cast<const uint4*>(x + c * 8);
+      wv[k] = *reinterpret_cast<const uint4*>(w + c * 8);
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -49,8 +51,7 @@ rmsnorm_kernel(const uint16_t* __restrict__ X, int N, int ldx, const uint16_t* _
   for (int k = 0; k < RMS_MAX_VEC; ++k) {
     const int c = threadIdx.x + k * RMS_THREADS;
     if (c < nv) {
-      const uint4 wu = *reinterpret_cast<const uint4*>(w + c * 8);
-      const uint32_t w4[4] = {wu.x, wu.y, wu.z, wu.w};
+      const uint32_t w4[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
       uint32_t o4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)

@@ -18,6 +18,12 @@ int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
+// Cluster split-K GEMM (few tiles): CTAs that may be resident at once for clusters of S
+// (0 when the tile shape has no cluster build or S is out of range), and the launch
+// (tiles * S CTAs; no workspace).
+int linear_cluster_capacity(int BN, int NSUB, int S);
+cudaError_t launch_linear_cluster(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
+                                  const LinearArgs& a, int S, int tiles, cudaStream_t s);
 // Second pass of a split GEMM: sums the fp32 pieces of every split tile (in CTA order), adds the
 // residual and writes bf16 Y.  `sms` sizes its grid.
 cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s);

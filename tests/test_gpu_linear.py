@@ -112,3 +112,16 @@ def test_linear_launch_accounting(lib):
     finally:
         lib.spec_set_option("persistent_grid", 0)
     lib.spec_device_status()
+
+
+@pytest.mark.parametrize("M,N,K", [(368, 4096, 4096), (300, 4096, 1000), (200, 4096, 520), (17, 6144, 4096),
+                                   (513, 4096, 4096), (64, 2048, 12288)])
+def test_linear_cluster_split_k(lib, M, N, K):
+    """Few weight tiles: the cluster split-K kernel (pieces summed over distributed shared
+    memory) and the stream-K path both match the oracle."""
+    for cluster in (1, 0):
+        lib.spec_set_option("linear_cluster", cluster)
+        try:
+            run_case(lib, M, N, K, True, seed=M + N + K + cluster, gemv_max_m=0)
+        finally:
+            lib.spec_set_option("linear_cluster", 1)

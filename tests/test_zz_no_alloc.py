@@ -51,7 +51,7 @@ def test_noalloc_back_to_back_different_shapes(lib):
 
 
 def test_noalloc_rejects_scratch_beyond_the_limit(lib):
-    M, N, K = 368, 6144, 4096                          # two 184-row tiles x 48, split 3 ways
+    M, N, K = 368, 24576, 4096                         # 192 tiles of 368 rows, stream-K split
     need = lib.spec_linear_workspace_bytes(M, N, K)
     assert need > 16 << 20
     big_x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
