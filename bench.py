@@ -114,6 +114,13 @@ def algorithmic_bytes(batch, dims):
     return lin_w, kv, head
 
 
+# DRAM bytes per algorithmic byte of attention_tc_kernel, from the ncu capture summarised in
+# profiles/attention_tc_B16_ncu.md (241.4 MB of DRAM traffic for 232.3 MB of algorithmic bytes).
+# Traffic grows with the keys streamed, so the bench scales it to its own launch.  Must be re-taken
+# (or set to None) whenever that kernel changes.
+ATTN_DRAM_PER_ALG_BYTE = 1.039
+
+
 def attention_bytes(batch, dims):
     """Per attention launch: K/V cache read + new K/V + Q read + O write."""
     keys = int(np.sum(batch.ctx_len.astype(np.int64)))
@@ -327,7 +334,10 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
                                "roofline": {"kernel": "verify_attention", "bound": "hbm",
                                             "achieved": ab / (t_attn / 1e3) / 1e9, "peak": hbm_peak,
                                             "unit": "GB/s", "frac": ab / (t_attn / 1e3) / 1e9 / hbm_peak,
-                                            "traffic": None, "algorithmic_bytes": ab,
+                                            "traffic": (ab * ATTN_DRAM_PER_ALG_BYTE if ATTN_DRAM_PER_ALG_BYTE else None),
+                                            "traffic_source": "ncu dram__bytes_read+write on a B=16 launch, "
+                                                              "scaled by algorithmic bytes",
+                                            "algorithmic_bytes": ab,
                                             "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}}
     shapes = {"qkv": (dims.qkv, dims.d), "o": (dims.d, hq), "gate_up": (2 * dims.I, dims.d),
               "down": (dims.d, dims.I)}
@@ -606,7 +616,8 @@ def run_profile_case(args):
                                     batch.max_rows, ws=ws)
     else:
         M = args.rows
-        S.spec_set_option("linear_nsub", args.nsub)
+        if args.nsub:
+            S.spec_set_option("linear_nsub", args.nsub)
         if args.profile == "linear":
             N, K = args.n, args.k
         else:
@@ -636,7 +647,7 @@ def main():
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")
     ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")
-    ap.add_argument("--nsub", type=int, default=1, help="linear_nsub knob for --profile linear/lmhead")
+    ap.add_argument("--nsub", type=int, default=0, help="linear_nsub knob for --profile linear/lmhead (0: library default)")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
