@@ -139,7 +139,8 @@ struct LinPlan {
   int BN = 16, NSUB = 1, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
   int grid = 1;                 // persistent CTAs of the tensor-core path
   int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
-  bool aligned = false;         // CTA ranges cover whole tiles only
+  bool aligned = false;         // whole tiles only (no stream-K region)
+  long long dp_tiles = 0, sk_units = 0;
   long long units = 0;
   int gemv_grid = 1, k_per_split = 0, groups = 0;
   size_t counters_off = 0, partial_off = 0, bytes = 0;
@@ -218,13 +219,20 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
   const long long cap_units = p.aligned ? tiles : p.units;
   if (grid > cap_units) grid = (int)cap_units;
   p.grid = std::max(1, grid);
+  // data-parallel tiles first (every CTA gets as many whole tiles as all can), stream-K for the rest
+  if (p.aligned) {
+    p.dp_tiles = tiles;
+    p.sk_units = 0;
+  } else {
+    p.dp_tiles = tiles / p.grid * p.grid;
+    p.sk_units = (tiles - p.dp_tiles) * p.k_tiles;
+  }
   if (lmhead) {
     p.bytes = kCounterBytes + round_up(size_t(M) * p.tiles_n * sizeof(float2), 256);
     return p;
   }
   bool split = false;
-  if (!p.aligned)
-    for (int c = 0; c < p.grid && !split; ++c) split = ((p.units * c / p.grid) % p.k_tiles) != 0;
+  for (int c = 1; c < p.grid && !split && p.sk_units > 0; ++c) split = ((p.sk_units * c / p.grid) % p.k_tiles) != 0;
   p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * 2 * TN * 128 * 4, 256) : 0;
   return p;
 }
@@ -382,7 +390,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.aligned = p.aligned ? 1 : 0;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
@@ -442,7 +450,7 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
   const bool greedy = temperature == 0.f;
   LinearArgs a{};
   a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.aligned = 1;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = P;

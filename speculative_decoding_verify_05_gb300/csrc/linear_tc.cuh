@@ -7,13 +7,16 @@
 // the whole 128-lane tensor core on the weight stream instead of padding the
 // token dimension to 128.
 //
-// Persistent stream-K schedule: one CTA per SM walks a contiguous range of
-// (tile, 64-wide k-step) units, so every SM streams the same number of weight
-// bytes whatever the matrix shape.  Roles (6 warps): warp 0 issues TMA loads
+// Persistent schedule (data-parallel + stream-K): one CTA per SM first takes
+// whole tiles round-robin (as many as every CTA can get), then an equal
+// contiguous range of the (tile, 64-wide k-step) units of the remaining tiles,
+// so every SM streams the same number of weight bytes whatever the matrix shape
+// while only the remainder tiles are cut into pieces.  Roles (6 warps): warp 0 issues TMA loads
 // of 128x64 weight tiles and BNx64 activation tiles (128-byte swizzle) into a
 // STAGES-deep ring without ever draining it; warp 1 issues four
-// tcgen05.mma (K = 16) per stage into one of two TMEM accumulators; warps 2-5
-// drain the other accumulator meanwhile.  A tile whose k-steps are split
+// tcgen05.mma (K = 16) per stage into one of two TMEM accumulators; warps 2-9
+// drain the other accumulator meanwhile (two warps per TMEM lane quarter, each
+// taking half of the token columns).  A tile whose k-steps are split
 // between CTAs leaves one fp32 piece per CTA in the workspace; a second, fully
 // parallel kernel sums the pieces in CTA order, adds the residual and rounds
 // to bf16 (one SM finishing a whole split tile alone would leave the rest of
@@ -36,7 +39,8 @@ struct LinearArgs {
   int tiles_m, tiles_n;
   long long units;      // work units: tiles * k_tiles
   int grid;             // persistent CTAs
-  int aligned;          // 1: every CTA range starts and ends on a tile boundary
+  long long dp_tiles;   // tiles 0 .. dp_tiles - 1 go whole to CTAs c, c + grid, ... (data parallel)
+  long long sk_units;   // the k-steps of the other tiles, split evenly between the CTAs (stream-K)
   uint16_t* Y;
   int ldy;
   const uint16_t* residual;
@@ -64,9 +68,15 @@ struct LinearCfg {
   static constexpr int ACC_COLS = TN <= 16 ? 16 : (TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512))));
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TMEM_COLS = NBUF * ACC_COLS < 32 ? 32 : NBUF * ACC_COLS;
-  static constexpr int THREADS = 192;
-  // ring + barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) + alignment slack
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + 1024;
+  // producer warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter, each half of the columns)
+  static constexpr int THREADS = 320;
+  static constexpr int EPI_WARPS = 8;
+  // per epilogue warp: a 16-column x 32-row fp32 block (row stride 33) to turn TMEM rows into
+  // 16-byte stores along the weight rows
+  static constexpr int EPI_BUF_FLOATS = 16 * 33;
+  // ring + barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) + epilogue
+  // transpose blocks + alignment slack
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4 + 1024;
 };
 
 }  // namespace spec

@@ -85,19 +85,19 @@ cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const
   }
 }
 
-// Second pass of a split GEMM.  Every block first tabulates the CTA range starts of the
-// GEMM (beg[c] = units * c / grid, one 64-bit division per entry).  A tile is split iff a
-// range starts strictly inside it; the first such range c names the tile, whose pieces came
-// from CTAs c - 1 .. hi (the last range starting inside it).  Warp item = (c, 8 token
+// Second pass of a split GEMM.  Every block first tabulates where each CTA's stream-K range
+// starts (beg[c] = sk_units * c / grid, one 64-bit division per entry; unit u is k-step u % kt of
+// tile dp_tiles + u / kt).  A tile is split iff a range starts strictly inside it; the first such
+// range c names the tile, whose pieces came from CTAs c - 1 .. hi (the last range starting inside it).  Warp item = (c, 8 token
 // columns); lane l owns weight rows n0 + 4 l .. + 3 (one float4 per column of a piece).
-// Pieces are summed in CTA order, four contributors' loads in flight at a time, then the
-// residual is added and the sum rounded to bf16.
-__global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a) {
+// Pieces are summed in CTA order, two contributors' loads in flight at a time, then the
+// residual is added and the sum rounded to bf16.  Launched as one wave (grid-stride over items).
+__global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs a) {
   extern __shared__ long long s_beg[];                      // [grid + 1]
   int* s_hi = reinterpret_cast<int*>(s_beg + a.grid + 1);   // [grid] -1: c names no tile
   const int G = a.grid, TN = a.tn;
   const long long kt = a.k_tiles;
-  for (int c = threadIdx.x; c <= G; c += blockDim.x) s_beg[c] = a.units * c / G;
+  for (int c = threadIdx.x; c <= G; c += blockDim.x) s_beg[c] = a.sk_units * c / G;
   __syncthreads();
   for (int c = threadIdx.x; c < G; c += blockDim.x) {
     int hi = -1;
@@ -121,27 +121,29 @@ __global__ void __launch_bounds__(256) linear_reduce_kernel(const LinearArgs a) 
     if (hi < 0) continue;
     const int j0 = (int)(it - (long long)c * cols8) * 8;
     const long long t0 = s_beg[c] / kt * kt;
-    const long long tile = t0 / kt;
+    const long long tile = a.dp_tiles + t0 / kt;
     const int m0 = (int)(tile % a.tiles_m) * TN + j0;
     const int n4 = (int)(tile / a.tiles_m) * 128 + lane * 4;
     float4 acc[8];
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = c - 1; c0 <= hi; c0 += 4) {
-      float4 v[4][8];
+    for (int c0 = c - 1; c0 <= hi; c0 += 2) {
+      float4 v[2][8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const int cc = c0 + q;
-        // slot 0 holds a CTA's first segment: the tile is it iff the CTA starts inside it
-        const float* base = cc <= hi ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
-                                     : nullptr;
+        // slot 0 holds the piece that opens a CTA's stream-K range: the tile's iff the range starts
+        // inside it; a CTA with an empty range (fewer stream-K units than CTAs) left nothing
+        const float* base = (cc <= hi && s_beg[cc] < s_beg[cc + 1])
+                                ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
+                                : nullptr;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
           v[q][jj] = (base && j0 + jj < TN) ? __ldcg(reinterpret_cast<const float4*>(base + (j0 + jj) * 128))
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           acc[jj].x += v[q][jj].x; acc[jj].y += v[q][jj].y; acc[jj].z += v[q][jj].z; acc[jj].w += v[q][jj].w;
@@ -180,9 +182,10 @@ cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  // one wave: two 256-thread blocks per SM (register budget), grid-stride over the items
   const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
   long long blocks = (warps + 7) / 8;
-  if (blocks > 4LL * sms) blocks = 4LL * sms;
+  if (blocks > 2LL * sms) blocks = 2LL * sms;
   linear_reduce_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, smem, s>>>(a);
   return cudaGetLastError();
 }

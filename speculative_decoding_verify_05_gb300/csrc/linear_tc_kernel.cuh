@@ -24,37 +24,68 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
 }
-// Named barrier 2 over the four epilogue warps.
-__device__ __forceinline__ void bar_epi() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Named barrier 2 over the eight epilogue warps.
+__device__ __forceinline__ void bar_epi() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 __device__ __forceinline__ bool bar_epi_and(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.and.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      " bar.red.and.pred q, 2, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
       : "r"((uint32_t)v)
       : "memory");
   return r != 0;
 }
 
-// First work unit of persistent CTA c (c = grid gives the total), and the CTA owning unit u.
-__device__ __forceinline__ long long unit_begin(const LinearArgs& a, int c) {
-  if (a.aligned) {
-    const long long tiles = (long long)a.tiles_m * a.tiles_n;
-    return (tiles * c / a.grid) * a.k_tiles;
-  }
-  return a.units * c / a.grid;
+// Work of persistent CTA c: its data-parallel tiles c, c + grid, ... below dp_tiles, then its
+// share [sk_begin, sk_end) of the stream-K units (unit u is k-step u % kt of tile dp_tiles + u / kt).
+struct CtaWork {
+  int n_dp;
+  long long sk_begin, sk_end;
+  long long n;          // units in all
+};
+__device__ __forceinline__ long long sk_start(const LinearArgs& a, int c) { return a.sk_units * c / a.grid; }
+__device__ __forceinline__ CtaWork cta_work(const LinearArgs& a, int c) {
+  CtaWork w;
+  w.n_dp = c < a.dp_tiles ? (int)((a.dp_tiles - 1 - c) / a.grid + 1) : 0;
+  w.sk_begin = sk_start(a, c);
+  w.sk_end = sk_start(a, c + 1);
+  w.n = (long long)w.n_dp * a.k_tiles + (w.sk_end - w.sk_begin);
+  return w;
 }
-__device__ __forceinline__ int cta_of_unit(const LinearArgs& a, long long u) {
-  int c = (int)(((u + 1) * a.grid - 1) / a.units);
-  if (c >= a.grid) c = a.grid - 1;
-  while (c + 1 < a.grid && unit_begin(a, c + 1) <= u) ++c;
-  while (c > 0 && unit_begin(a, c) > u) --c;
-  return c;
+// Unit i of a CTA's list: its tile and k-step, the end of the run of units that stay in that tile
+// (a segment), whether the segment covers the tile's whole k-range, and whether it opens the CTA's
+// stream-K range (its piece then goes to partial slot 0, else slot 1).
+struct Seg {
+  long long tile, end;
+  int k;
+  bool whole, first_sk;
+};
+__device__ __forceinline__ Seg seg_at(const LinearArgs& a, const CtaWork& w, int c, long long i) {
+  const int kt = a.k_tiles;
+  const long long ndp = (long long)w.n_dp * kt;
+  Seg g;
+  if (i < ndp) {
+    const long long j = i / kt;
+    g.tile = c + j * a.grid;
+    g.k = (int)(i - j * kt);
+    g.end = (j + 1) * kt;
+    g.whole = true;
+    g.first_sk = false;
+  } else {
+    const long long u = w.sk_begin + (i - ndp), t = u / kt;
+    g.tile = a.dp_tiles + t;
+    g.k = (int)(u - t * kt);
+    const long long end_u = min(w.sk_end, (t + 1) * kt);
+    g.end = ndp + (end_u - w.sk_begin);
+    g.whole = g.k == 0 && end_u == (t + 1) * kt;
+    g.first_sk = u == w.sk_begin;
+  }
+  return g;
 }
 
 template <int BN, int NSUB, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const LinearArgs args) {
   using Cfg = LinearCfg<BN, NSUB>;
@@ -71,13 +102,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   uint64_t* acc_empty = acc_full + 2;   // [NBUF]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   float2* red = reinterpret_cast<float2*>(smem + STAGES * Cfg::STAGE_BYTES + 1024);  // [4][TN]
+  float* ebuf_all = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + 1024 + 4 * TN * 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const int kt = args.k_tiles;
-  const long long ub = unit_begin(args, cta);
-  const long long ue = unit_begin(args, cta + 1);
+  const CtaWork work = cta_work(args, cta);
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_w);
@@ -88,7 +118,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], 32 * Cfg::EPI_WARPS);
     }
     fence_barrier_init();
   }
@@ -101,15 +131,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 0) {
     // ---------------- TMA producer: one continuous stream over this CTA's units
     if (lane == 0) {
-      long long i = 0;
-      for (long long u = ub; u < ue; ++u, ++i) {
+      for (long long i = 0; i < work.n; ++i) {
         const int s = (int)(i % STAGES);
         const long long r = i / STAGES;
         if (i >= STAGES && !mbar_wait(&empty[s], (uint32_t)((r - 1) & 1), args.status, 0x101u)) break;
-        const long long tile = u / kt;
-        const int k = (int)(u - tile * kt);
-        const int m_t = (int)(tile % args.tiles_m);
-        const int n_t = (int)(tile / args.tiles_m);
+        const Seg g = seg_at(args, work, cta, i);
+        const int k = g.k;
+        const int m_t = (int)(g.tile % args.tiles_m);
+        const int n_t = (int)(g.tile / args.tiles_m);
         mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
         tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * 64, n_t * 128);
 #pragma unroll
@@ -125,9 +154,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       long long i = 0;
       int seg = 0;
       bool ok = true;
-      for (long long u = ub; u < ue && ok; ++seg) {
-        const long long tile = u / kt;
-        const long long seg_end = min(ue, (tile + 1) * kt);
+      for (long long u = 0; u < work.n && ok; ++seg) {
+        const long long seg_end = seg_at(args, work, cta, u).end;
         const int acc = seg % NBUF;
         const int use = seg / NBUF;
         if (use >= 1 && !mbar_wait(&acc_empty[acc], (uint32_t)((use - 1) & 1), args.status, 0x102u)) break;
@@ -154,17 +182,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps 2..5 drain TMEM lane quarter (warp % 4)
+    // ---------------- epilogue warps 2..9: TMEM lane quarter warp % 4, column half (warp - 2) / 4
     const int q = warp & 3;
     const int row = q * 32 + lane;            // TMEM lane = weight row within the tile
-    const int etid = threadIdx.x - 64;        // 0..127 among the epilogue threads
+    const int etid = threadIdx.x - 64;        // 0..255 among the epilogue threads
     const int ewarp = etid >> 5;
+    const int nb = TN / 16, per_half = (nb + 1) / 2;
+    const int c_begin = ((warp - 2) >> 2) * per_half * 16;
+    const int c_end = min(TN, c_begin + per_half * 16);
     int seg = 0;
     bool ok = true;
-    for (long long u = ub; u < ue; ++seg) {
-      const long long tile = u / kt;
-      const long long seg_end = min(ue, (tile + 1) * kt);
-      const bool whole = (u == tile * kt) && (seg_end == (tile + 1) * kt);
+    for (long long u = 0; u < work.n; ++seg) {
+      const Seg g = seg_at(args, work, cta, u);
+      const long long tile = g.tile;
+      const long long seg_end = g.end;
+      const bool whole = g.whole;
       const int acc = seg % NBUF;
       const int m0 = (int)(tile % args.tiles_m) * TN;
       const int n_t = (int)(tile / args.tiles_m);
@@ -177,43 +209,80 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       const uint32_t t_row = tmem + acc * Cfg::ACC_COLS + (uint32_t(q * 32) << 16);
 
       if constexpr (EPI == EPI_BF16) {
-        if (whole) {
+        // 16 columns at a time: TMEM -> this warp's transpose block -> 16-byte global accesses
+        float* ebuf = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
+        const int nq = n0 + q * 32;                     // first weight row of this warp
+        const int slot = g.first_sk ? 0 : 1;
+        float* part = whole ? nullptr : args.partial + ((size_t)cta * 2 + slot) * (TN * 128);
+        // TMEM is read 64 columns per wait (16/32/48 at the tail: TN is a multiple of 16); each
+        // 16-column block then goes through the transpose buffer
 #pragma unroll 1
-          for (int c = 0; c < TN; c += 16) {
-            float v[16];
-            tmem_ld16(t_row + c, v);
+        for (int c64 = c_begin; c64 < c_end; c64 += 64) {
+        float v64[64];
+        const int cols = c_end - c64 < 64 ? c_end - c64 : 64;
+        if (cols == 64) tmem_ld_cols<64>(t_row + c64, v64);
+        else if (cols == 48) tmem_ld_cols<48>(t_row + c64, v64);
+        else if (cols == 32) tmem_ld_cols<32>(t_row + c64, v64);
+        else tmem_ld_cols<16>(t_row + c64, v64);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int m = m0 + c + j;
-              if (m < args.M && n < args.N) {
-                float y = v[j];
-                if (args.residual) y += bf16f(args.residual[(size_t)m * args.ldr + n]);
-                args.Y[(size_t)m * args.ldy + n] = f2bf(y);
+        for (int c16 = 0; c16 < 64; c16 += 16) {
+          if (c16 >= cols) break;
+          const int c = c64 + c16;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ebuf[j * 33 + lane] = v64[c16 + j];
+          __syncwarp();
+          if (whole) {
+            // item = (token column j, 8 consecutive weight rows): one 16-byte bf16 store
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+              const int item = lane + 32 * it, j = item >> 2, r8 = (item & 3) * 8;
+              const int m = m0 + c + j, n = nq + r8;
+              if (m >= args.M) continue;
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[e] = ebuf[j * 33 + r8 + e];
+              if (n + 8 <= args.N) {
+                if (args.residual) {
+                  const uint4 rr = *reinterpret_cast<const uint4*>(args.residual + (size_t)m * args.ldr + n);
+                  const uint32_t r4[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    y[2 * h] += bf16lo(r4[h]);
+                    y[2 * h + 1] += bf16hi(r4[h]);
+                  }
+                }
+                *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n) =
+                    make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                               pack_bf16x2(y[6], y[7]));
+              } else {
+                for (int e = 0; e < 8 && n + e < args.N; ++e) {
+                  float o = y[e];
+                  if (args.residual) o += bf16f(args.residual[(size_t)m * args.ldr + n + e]);
+                  args.Y[(size_t)m * args.ldy + n + e] = f2bf(o);
+                }
               }
             }
-          }
-          tc_fence_before();
-          mbar_arrive(&acc_empty[acc]);
-        } else {
-          // split tile: publish this CTA's fp32 piece (slot 0 = its first segment, 1 = its last);
-          // the reduce kernel that follows the GEMM sums the pieces
-          const int slot = (u == ub) ? 0 : 1;
-          float* part = args.partial + ((size_t)cta * 2 + slot) * (TN * 128);
-#pragma unroll 1
-          for (int c = 0; c < TN; c += 16) {
-            float v[16];
-            tmem_ld16(t_row + c, v);
+          } else {
+            // split tile: this CTA's fp32 piece, [column][128 rows], float4 along the rows
+            // (slot 0 = the piece that opens its stream-K range, 1 = the one that closes it)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) __stcg(&part[(c + j) * 128 + row], v[j]);
+            for (int it = 0; it < 4; ++it) {
+              const int item = lane + 32 * it, j = item >> 3, r4 = (item & 7) * 4;
+              const float* src = ebuf + j * 33 + r4;
+              __stcg(reinterpret_cast<float4*>(part + (size_t)(c + j) * 128 + q * 32 + r4),
+                     make_float4(src[0], src[1], src[2], src[3]));
+            }
           }
-          tc_fence_before();
-          mbar_arrive(&acc_empty[acc]);
+          __syncwarp();
         }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
       } else {
         // LM-head epilogues (ranges are tile-aligned, so every segment is whole):
         // per token column j reduce over the tile's 128 vocabulary rows
 #pragma unroll 1
-        for (int c = 0; c < TN; c += 16) {
+        for (int c = c_begin; c < c_end; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
 #pragma unroll
@@ -227,19 +296,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
               const float mx = warp_max(zm);
               const float e = valid ? expf(z - mx) : 0.f;
               const float sm = warp_sum(e);
-              if (lane == 0) red[ewarp * TN + c + j] = make_float2(mx, sm);
+              if (lane == 0) red[q * TN + c + j] = make_float2(mx, sm);
             } else {
               float zv = valid ? v[j] : -INFINITY;
               int idx = valid ? n : 0x7fffffff;
               warp_argmax(zv, idx);
-              if (lane == 0) red[ewarp * TN + c + j] = make_float2(zv, __int_as_float(idx));
+              if (lane == 0) red[q * TN + c + j] = make_float2(zv, __int_as_float(idx));
             }
           }
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
         bar_epi();
-        for (int j = etid; j < TN; j += 128) {
+        for (int j = etid; j < TN; j += 32 * Cfg::EPI_WARPS) {
           const int m = m0 + j;
           if (m >= args.M) continue;
           float2 accv = red[j];

@@ -15,6 +15,7 @@ SHAPES = [
     (5, 512, 4096), (7, 136, 72), (16, 640, 264), (17, 256, 520), (40, 1024, 512),
     (100, 256, 768), (256, 384, 128), (300, 384, 512), (368, 6144, 4096), (513, 128, 256),
     (1030, 640, 320),
+    (200, 20480, 136),   # 160 tiles: 152 whole, the last 8 split over mostly empty stream-K ranges
 ]
 
 
