@@ -617,7 +617,7 @@ def run_profile_case(args):
     else:
         M = args.rows
         if args.nsub:
-            S.spec_set_option("linear_nsub", args.nsub)
+            S.spec_set_option("linear_nsub" if args.profile == "linear" else "lmhead_nsub", args.nsub)
         if args.profile == "linear":
             N, K = args.n, args.k
         else:

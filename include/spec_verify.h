@@ -92,7 +92,8 @@ SPEC_API int spec_version(void);
  * "linear_nsub" (2, default: one tensor-core tile covers up to 512 rows; 1: up
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
- * and sum the pieces on chip.
+ * and sum the pieces on chip; "lmhead_nsub" (1 default, or 2): the LM head's
+ * tensor-core tiles cover up to 256 or 512 rows.
  * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for
  * an unknown name or value. */
 SPEC_API int spec_set_option(const char* name, int value);

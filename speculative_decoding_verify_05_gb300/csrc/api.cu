@@ -132,7 +132,8 @@ int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
-int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
+int g_nsub_max = 2;
+int g_lmhead_nsub = 1;   // tunable: the LM head's tiles cover up to 256 (1) or 512 (2) rows      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 
 struct LinPlan {
   bool gemv = false;
@@ -172,9 +173,9 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
     p.tiles_m = 1;
     p.NSUB = 1;
     p.BN = std::max(16, (M + 15) / 16 * 16);
-  } else if (g_nsub_max == 1 || lmhead) {
-    // (the LM head keeps two accumulator buffers so each tile's epilogue overlaps the next
-    // tile's MMAs: it has ~1200 tiles, each with a long softmax-statistics epilogue)
+  } else if (lmhead ? g_lmhead_nsub == 1 : g_nsub_max == 1) {
+    // (by default the LM head keeps two accumulator buffers so each tile's epilogue overlaps
+    // the next tile's MMAs: it has ~1200 tiles, each with a long softmax-statistics epilogue)
     p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
     const int per = (M + p.tiles_m - 1) / p.tiles_m;
     p.NSUB = 1;
@@ -280,6 +281,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "gemv_max_m")) {
     if (value < 0 || value > 4) return fail(SPEC_EINVAL, "gemv_max_m must be in [0, 4]");
     g_gemv_max_m = value;
+    return ok();
+  }
+  if (!strcmp(name, "lmhead_nsub")) {
+    if (value < 1 || value > 2) return fail(SPEC_EINVAL, "lmhead_nsub must be 1 or 2");
+    g_lmhead_nsub = value;
     return ok();
   }
   if (!strcmp(name, "linear_cluster")) {
