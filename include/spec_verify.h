@@ -201,7 +201,9 @@ SPEC_API int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf
  * (exact product; q = 0 accepts), stop at the first rejection n; draw t from
  * max(0, p_{n+1} - q_{n+1}) (falling back to p_{n+1} if that is all zero) when
  * n < gamma, else from p_{gamma+1} (bonus).  t is the smallest token x with
- * sum_{y<=x} w(y) > u * sum_y w(y), summed in fp64, u = U[row gamma_b].
+ * sum_{y<=x} w(y) > u * sum_y w(y), u = U[row gamma_b]; the weights are formed
+ * in fp32 (exact sign) and summed with fp64 tile and warp prefixes, ~1e-7
+ * relative error, inside the near-tie band below.
  *   P [M x V] fp32, Q [sum gamma x V] fp32, draft_tok [sum gamma] int32,
  *   U [M] fp32 in (0,1): rows 0..gamma_b-1 = acceptance draws, row gamma_b =
  *   the draw for t.
@@ -210,15 +212,16 @@ SPEC_API int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf
  *                    (x_1..x_n, t); later slots are set to -1
  *   near_tie [B] out: decisions with |u*q - p| < tie_eps plus a final pick
  *                    whose CDF boundary is within tie_eps * sum(w) of u*sum(w)
- * Requires V >= 1, draft tokens in [0, V) (an out-of-range token is clamped
- * and flagged in the status word). */
+ * Requires 1 <= V <= 1048576, draft tokens in [0, V) (an out-of-range token
+ * is clamped and flagged in the status word). */
 SPEC_API int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
                        const float* U, const int32_t* cu_rows, int B, int V,
                        float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
                        spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
-/* Layer glue of the decoder stack (not on the pages)         */
+/* Layer glue of the decoder stack (not on the pages: the stack's layout is  */
+/* the builder's reading of a Qwen3-8B-shaped decoder)                      */
 /* ------------------------------------------------------------------------ */
 /* Y = X / sqrt(mean(X^2) + eps) * w per row; X [M x N], w [N] bf16.
  * Y may alias X.  Requires N % 8 == 0, N <= 16384. */

@@ -16,7 +16,8 @@ What it computes, and where the pages define it:
   Decode").  These are exact definitions evaluated in fp64.
 * ``sampler.reject_sample`` — the acceptance test, prefix truncation,
   residual correction and bonus token, in the order of Algorithm 1 of the
-  first page (same section), with the reading choices listed in the design doc.
+  first page (same section), with the readings of the open points stated in
+  that module's header.
 * ``ops.rmsnorm`` / ``ops.rope`` / ``ops.silu_mul`` and ``stack`` — the
   layer glue of a Qwen3-8B-shaped stack.  The pages only give the layer and
   head counts; the layer internals are the builder's reading.

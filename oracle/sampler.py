@@ -9,7 +9,7 @@ order, for a ragged batch of sequences:
 3. p' = norm(max(0, p_{n+1} - q_{n+1})) if n < gamma, else p' = p_{gamma+1}
 4. emit x_1 .. x_n and t ~ p'
 
-Readings of the points the pages leave open (each listed in the design doc):
+Readings of the points the pages leave open:
 
 * the test is done without division: accept x_i iff u_i * q_i(x_i) <= p_i(x_i)
   (the rejection condition of Algorithm 1 multiplied by q > 0; q = 0 accepts);

@@ -537,6 +537,7 @@ int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
   if (!P || !Q || !draft_tok || !U || !cu_rows || !n_acc || !out_tok || !near_tie)
     return fail(SPEC_EINVAL, "NULL argument");
   if (!(tie_eps >= 0.f)) return fail(SPEC_EINVAL, "tie_eps must be >= 0");
+  if (V > (1 << 20)) return fail(SPEC_EUNSUPPORTED, "V=%d > 1048576", V);
   DevInfo* d = nullptr;
   if (int rc = dev_info(&d)) return rc;
   cudaError_t e = launch_reject_sample(P, Q, draft_tok, U, cu_rows, B, V, tie_eps, n_acc, out_tok,

@@ -6,10 +6,16 @@
 //      i), in fp64 so that u*q is exact; n = first rejection (ballot), else
 //      gamma_b;
 //   2. the block builds the final weights w(x) = max(0, p - q) at the first
-//      rejection (p itself if that is all zero), or w = p_{gamma+1} (bonus);
-//   3. inverse CDF in token order: each thread owns a contiguous slice of the
-//      vocabulary, slice sums are scanned across the block in fp64, and the
-//      thread whose slice crosses u * sum(w) walks it to find the token.
+//      rejection (p itself if that is all zero), or w = p_{gamma+1} (bonus), in
+//      fp32 (exact sign, <= 2^-24 relative rounding per weight), and sums them
+//      per 4096-token tile with the tile totals kept in fp64;
+//   3. inverse CDF in token order: the fp64 prefix over tile totals finds the
+//      tile that crosses u * sum(w); inside it the 8-token slice sums are
+//      scanned (fp32 within a warp, fp64 across warps) and the thread whose
+//      slice crosses walks it in fp64.  Weights and sums carry ~1e-7 relative
+//      rounding, far inside the near-tie band (tie_eps, 1e-5 by default), so a
+//      pick differs from an exact fp64 one only where it is counted as a near
+//      tie.  (An all-fp64 pass is ~2 fp64 FMA/clock/SM here: 0.3 ms a round.)
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,13 +23,38 @@ namespace spec {
 namespace {
 
 constexpr int SAMPLER_THREADS = 512;
+constexpr int PER_THREAD = 8;                              // consecutive tokens per thread in a tile
+constexpr int TILE = SAMPLER_THREADS * PER_THREAD;         // 4096 tokens
+constexpr int MAX_TILES = 256;                             // V <= 1,048,576
 
-__device__ __forceinline__ double row_weight(const float* p, const float* q, int x, bool resid,
-                                             bool fallback) {
-  const double pv = (double)p[x];
-  if (!resid || fallback) return pv;
-  const double r = pv - (double)q[x];
-  return r > 0.0 ? r : 0.0;
+// This thread's 8 consecutive weights of a tile: w = max(0, p - q) at a rejection (the sign is
+// exact in fp32; the value carries <= 2^-24 relative rounding), p itself for the bonus row or
+// when the residual is empty (`use_p`).  Tokens past V weigh 0.
+__device__ __forceinline__ void load_weights(const float* prow, const float* qrow, int x0, int V, bool use_p,
+                                             bool vec, float* w) {
+  if (vec && x0 + PER_THREAD <= V) {
+    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(prow + x0));
+    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(prow + x0 + 4));
+    w[0] = p0.x; w[1] = p0.y; w[2] = p0.z; w[3] = p0.w; w[4] = p1.x; w[5] = p1.y; w[6] = p1.z; w[7] = p1.w;
+    if (!use_p) {
+      const float4 q0 = __ldcg(reinterpret_cast<const float4*>(qrow + x0));
+      const float4 q1 = __ldcg(reinterpret_cast<const float4*>(qrow + x0 + 4));
+      const float q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int e = 0; e < PER_THREAD; ++e) w[e] = fmaxf(w[e] - q[e], 0.f);
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < PER_THREAD; ++e) {
+    const int x = x0 + e;
+    float v = 0.f;
+    if (x < V) {
+      v = prow[x];
+      if (!use_p) v = fmaxf(v - qrow[x], 0.f);
+    }
+    w[e] = v;
+  }
 }
 
 __global__ void __launch_bounds__(SAMPLER_THREADS)
@@ -31,7 +62,7 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
                      const int32_t* __restrict__ draft, const float* __restrict__ U,
                      const int32_t* __restrict__ cu_rows, int V, float tie_eps,
                      int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tok,
-                     int32_t* __restrict__ near_tie, unsigned* status) {
+                     int32_t* __restrict__ near_tie, unsigned* status, int vec) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -39,15 +70,15 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
   const int gamma = cu_rows[b + 1] - r0 - 1;
   const int q0 = r0 - b;
   const double eps = (double)tie_eps;
+  const int n_tiles = (V + TILE - 1) / TILE;
 
-  __shared__ int s_n;
-  __shared__ int s_near;
-  __shared__ double s_part[SAMPLER_THREADS / 32];
-  __shared__ double s_scan[SAMPLER_THREADS];
-  __shared__ int s_pick;
-  __shared__ int s_pick_near;
+  __shared__ int s_n, s_near, s_pick, s_pick_near, s_first;
+  __shared__ float s_wp[SAMPLER_THREADS / 32][2];          // per-warp sums (residual, p)
+  __shared__ double s_tile_r[MAX_TILES], s_tile_p[MAX_TILES];
+  __shared__ float s_part_r[MAX_TILES * (SAMPLER_THREADS / 32)], s_part_p[MAX_TILES * (SAMPLER_THREADS / 32)];
+  __shared__ double s_wexcl[SAMPLER_THREADS / 32];
 
-  // ---- 1. acceptance tests (warp 0, 32 drafts per pass)
+  // ---- 1. acceptance tests (warp 0, 32 drafts per pass), exact in fp64
   if (warp == 0) {
     int n = gamma;
     int near = 0;
@@ -86,73 +117,150 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
   const int n = s_n;
   const bool resid = n < gamma;
   const float* prow = P + (size_t)(r0 + n) * V;
-  const float* qrow = resid ? Q + (size_t)(q0 + n) * V : nullptr;
+  const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow;
 
-  // ---- 2. weights: residual total (with fallback to p when it is empty)
-  const int per = (V + SAMPLER_THREADS - 1) / SAMPLER_THREADS;
-  const int x0 = min(V, tid * per), x1 = min(V, x0 + per);
-  double local = 0.0;
-  for (int x = x0; x < x1; ++x) local += row_weight(prow, qrow, x, resid, false);
-  // block total via warp shuffles + shared partials
-  double wsum = local;
+  // ---- 2. per-tile totals of the residual and of p (coalesced 16-byte loads, four tiles' loads in
+  // flight per thread, no block barrier per tile), kept in fp64
+  for (int t0 = 0; t0 < n_tiles; t0 += 4) {
+    float sr[4], sp[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  if (lane == 0) s_part[warp] = wsum;
-  __syncthreads();
-  double total = 0.0;
-  for (int w = 0; w < SAMPLER_THREADS / 32; ++w) total += s_part[w];
-  const bool fallback = resid && !(total > 0.0);
-  if (fallback) {
-    __syncthreads();
-    local = 0.0;
-    for (int x = x0; x < x1; ++x) local += row_weight(prow, qrow, x, resid, true);
-    wsum = local;
+    for (int k = 0; k < 4; ++k) {
+      sr[k] = 0.f;
+      sp[k] = 0.f;
+      const int t = t0 + k;
+      if (t >= n_tiles) continue;
+      const int x0 = t * TILE + tid * PER_THREAD;
+      float pw[PER_THREAD];
+      load_weights(prow, qrow, x0, V, true, vec, pw);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    if (lane == 0) s_part[warp] = wsum;
-    __syncthreads();
-    total = 0.0;
-    for (int w = 0; w < SAMPLER_THREADS / 32; ++w) total += s_part[w];
-  }
-
-  // ---- 3. inclusive scan of slice sums (Hillis-Steele in shared memory)
-  s_scan[tid] = local;
-  if (tid == 0) {
-    s_pick = -1;
-    s_pick_near = 0;
-  }
-  __syncthreads();
-  for (int off = 1; off < SAMPLER_THREADS; off <<= 1) {
-    const double v = tid >= off ? s_scan[tid - off] : 0.0;
-    __syncthreads();
-    s_scan[tid] += v;
-    __syncthreads();
-  }
-  const double thr = (double)U[r0 + gamma] * total;
-  const double incl = s_scan[tid];
-  const double excl = tid > 0 ? s_scan[tid - 1] : 0.0;
-  if (excl <= thr && incl > thr) {
-    // this slice holds the first token whose CDF exceeds thr
-    double cum = excl, lo = excl;
-    int pick = -1, last_pos = -1;
-    for (int x = x0; x < x1; ++x) {
-      const double w = row_weight(prow, qrow, x, resid, fallback);
-      lo = cum;
-      cum += w;
-      if (w > 0.0) last_pos = x;
-      if (cum > thr) {
-        pick = x;
-        break;
+      for (int e = 0; e < PER_THREAD; ++e) sp[k] += pw[e];
+      if (resid) {
+        float w[PER_THREAD];
+        load_weights(prow, qrow, x0, V, false, vec, w);
+#pragma unroll
+        for (int e = 0; e < PER_THREAD; ++e) sr[k] += w[e];
       }
     }
-    const double band = eps * total;
-    if (pick >= 0) {
-      s_pick = pick;
-      s_pick_near = (fabs(cum - thr) < band || (pick > 0 && fabs(lo - thr) < band)) ? 1 : 0;
-    } else if (last_pos >= 0) {
-      // the walk's rounding stayed just below thr: the crossing is at the slice end
-      s_pick = last_pos;
-      s_pick_near = 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sr[k] += __shfl_xor_sync(0xffffffffu, sr[k], o);
+        sp[k] += __shfl_xor_sync(0xffffffffu, sp[k], o);
+      }
+      if (lane == 0 && t0 + k < n_tiles) {
+        s_part_r[(t0 + k) * (SAMPLER_THREADS / 32) + warp] = sr[k];
+        s_part_p[(t0 + k) * (SAMPLER_THREADS / 32) + warp] = sp[k];
+      }
+    }
+  }
+  __syncthreads();
+  for (int t = tid; t < n_tiles; t += SAMPLER_THREADS) {
+    double tr = 0.0, tp = 0.0;
+    for (int k = 0; k < SAMPLER_THREADS / 32; ++k) {
+      tr += (double)s_part_r[t * (SAMPLER_THREADS / 32) + k];
+      tp += (double)s_part_p[t * (SAMPLER_THREADS / 32) + k];
+    }
+    s_tile_r[t] = tr;
+    s_tile_p[t] = tp;
+  }
+  __syncthreads();
+
+  // ---- 3. crossing tile of u * total (fp64 prefix over the tiles); empty residual -> p
+  __shared__ double s_thr, s_total, s_tile_excl;
+  __shared__ int s_tile, s_use_p;
+  if (tid == 0) {
+    double tot_r = 0.0, tot_p = 0.0;
+    for (int t = 0; t < n_tiles; ++t) {
+      tot_r += s_tile_r[t];
+      tot_p += s_tile_p[t];
+    }
+    const bool use_p = !resid || !(tot_r > 0.0);
+    const double* tiles = use_p ? s_tile_p : s_tile_r;
+    const double total = use_p ? tot_p : tot_r;
+    const double thr = (double)U[r0 + gamma] * total;
+    double excl = 0.0;
+    int tc = -1, last_pos = -1;
+    double last_excl = 0.0;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (tiles[t] > 0.0) { last_pos = t; last_excl = excl; }
+      if (tc < 0 && excl + tiles[t] > thr) { tc = t; s_tile_excl = excl; }
+      excl += tiles[t];
+    }
+    if (tc < 0) { tc = last_pos; s_tile_excl = last_excl; }   // rounding left thr at the very end
+    s_tile = tc;
+    s_use_p = use_p ? 1 : 0;
+    s_thr = thr;
+    s_total = total;
+    s_pick = -1;
+    s_pick_near = 0;
+    s_first = SAMPLER_THREADS;
+  }
+  __syncthreads();
+
+  // ---- 4. inside the crossing tile: block scan of the 8-token slice sums, then one thread walks
+  const int tc = s_tile;
+  if (tc >= 0) {
+    const bool use_p = s_use_p != 0;
+    const double thr = s_thr;
+    const int x0 = tc * TILE + tid * PER_THREAD;
+    float w[PER_THREAD];
+    load_weights(prow, qrow, x0, V, use_p, vec, w);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER_THREAD; ++e) s += w[e];
+    float incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    float excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl_w = 0.f;
+    if (lane == 31) s_wp[warp][0] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      double acc = s_tile_excl;
+      for (int k = 0; k < SAMPLER_THREADS / 32; ++k) {
+        s_wexcl[k] = acc;
+        acc += (double)s_wp[k][0];
+      }
+    }
+    __syncthreads();
+    const double t_excl = s_wexcl[warp] + (double)excl_w;
+    const double t_incl = s_wexcl[warp] + (double)incl;
+    if (t_incl > thr) atomicMin(&s_first, tid);
+    __syncthreads();
+    int walker = s_first;
+    if (walker == SAMPLER_THREADS) {
+      // rounding kept every prefix at or below thr: the last thread with weight walks
+      if (s > 0.f) atomicMax(&s_pick, tid);        // s_pick is -1 here: reuse it as "last positive"
+      __syncthreads();
+      walker = s_pick;
+      __syncthreads();
+      if (tid == 0) s_pick = -1;
+      __syncthreads();
+    }
+    if (tid == walker) {
+      const double band = eps * s_total;
+      double cum = t_excl, lo = t_excl;
+      int pick = -1, last_pos = -1;
+#pragma unroll
+      for (int e = 0; e < PER_THREAD; ++e) {
+        if (pick >= 0) break;
+        lo = cum;
+        cum += (double)w[e];
+        if (w[e] > 0.f) last_pos = x0 + e;
+        if (cum > thr) pick = x0 + e;
+      }
+      if (pick >= 0) {
+        s_pick = pick;
+        s_pick_near = (fabs(cum - thr) < band || (pick > 0 && fabs(lo - thr) < band)) ? 1 : 0;
+      } else if (last_pos >= 0) {
+        // the walk's rounding stayed just below thr: the crossing is at the slice end
+        s_pick = last_pos;
+        s_pick_near = 1;
+      }
     }
   }
   __syncthreads();
@@ -175,8 +283,9 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
                                  const float* U, const int32_t* cu_rows, int B, int V,
                                  float tie_eps, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* near_tie, unsigned* status, cudaStream_t s) {
+  const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
   reject_sample_kernel<<<B, SAMPLER_THREADS, 0, s>>>(P, Q, draft, U, cu_rows, V, tie_eps, n_acc,
-                                                     out_tok, near_tie, status);
+                                                     out_tok, near_tie, status, vec ? 1 : 0);
   return cudaGetLastError();
 }
 
