@@ -131,6 +131,26 @@ def attention_bytes(batch, dims):
     return kv + new + qo
 
 
+# --------------------------------------------------------------------------- ranks
+def combine_ranks(ms: float, tokens: float, device, world: int):
+    """Whole-job numbers of a replicated round: the slowest rank's time and every rank's tokens
+    (each rank runs its own B-sequence batch; nothing else crosses ranks)."""
+    import torch
+    if world <= 1:
+        return float(ms), float(tokens)
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device)
+    tok = torch.tensor([float(tokens)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(tok, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(tok.item())
+
+
+def reference_runs_here() -> bool:
+    """The reference arm (the CPU oracle) runs on rank 0 only; other ranks exit without work."""
+    return int(os.environ.get("RANK", "0")) == 0
+
+
 # --------------------------------------------------------------------------- GPU arm
 def build_round(dev, rank, S, E, synth):
     """Resident state of the benchmark round (weights, KV caches, inputs, draft distribution)
@@ -246,13 +266,8 @@ def run_gpu(args):
     accepted = int(n_acc.sum()) + B
     S.spec_device_status()
 
-    t = torch.tensor([ms], device=dev)
-    tok = torch.tensor([float(accepted)], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(tok, op=dist.ReduceOp.SUM)
-    ms_max = float(t.item())
-    value = float(tok.item()) / (ms_max / 1e3)
+    ms_max, tok_all = combine_ranks(ms, accepted, dev, world)
+    value = tok_all / (ms_max / 1e3)
 
     lin_w, kv, head = algorithmic_bytes(batch, dims)
     round_gbs = (lin_w + kv + head) / (ms / 1e3) / 1e9
@@ -525,8 +540,7 @@ def cpu_baseline(eng, batch, dims, kcs, vcs, sw, q, drafts, n_seq=4):
 
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if not reference_runs_here():
         return
     import synth
     from oracle import bf16 as obf, ops as oops, stack as ostack
