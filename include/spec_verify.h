@@ -93,7 +93,10 @@ SPEC_API int spec_version(void);
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
  * and sum the pieces on chip; "lmhead_nsub" (1 default, or 2): the LM head's
- * tensor-core tiles cover up to 256 or 512 rows.
+ * tensor-core tiles cover up to 256 or 512 rows; "pdl" (1 default, 0 off):
+ * kernels are launched with programmatic dependent launch, so each one's
+ * launch and on-chip setup overlap the end of the kernel before it on the
+ * stream (every kernel still waits for that kernel before touching memory).
  * Changing a knob can change the workspace queries.  Returns SPEC_EINVAL for
  * an unknown name or value. */
 SPEC_API int spec_set_option(const char* name, int value);

@@ -132,8 +132,9 @@ int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
-int g_nsub_max = 2;
-int g_lmhead_nsub = 1;   // tunable: the LM head's tiles cover up to 256 (1) or 512 (2) rows      // tunable: 2 lets one CTA tile cover up to 512 verify rows
+int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
+int g_lmhead_nsub = 1;   // tunable: the LM head's tiles cover up to 256 (1) or 512 (2) rows
+int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
 
 struct LinPlan {
   bool gemv = false;
@@ -269,6 +270,10 @@ AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
 
 }  // namespace
 
+namespace spec {
+bool pdl_enabled() { return g_pdl != 0; }
+}  // namespace spec
+
 // =========================================================================== C ABI
 extern "C" {
 
@@ -281,6 +286,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "gemv_max_m")) {
     if (value < 0 || value > 4) return fail(SPEC_EINVAL, "gemv_max_m must be in [0, 4]");
     g_gemv_max_m = value;
+    return ok();
+  }
+  if (!strcmp(name, "pdl")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "pdl must be 0 or 1");
+    g_pdl = value;
     return ok();
   }
   if (!strcmp(name, "lmhead_nsub")) {

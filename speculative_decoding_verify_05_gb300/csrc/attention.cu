@@ -40,6 +40,8 @@ template <int RTP>
 __global__ void __launch_bounds__(128)
 attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int WK = 4 / RTP;         // warps sharing one 16-row m-tile
   constexpr int KPW = KT / WK;        // keys of each tile handled by one warp
   constexpr int NT = KPW / 8;         // 8-key n-tiles per warp per tile
@@ -364,8 +366,8 @@ cudaError_t launch_rtp(const CUtensorMap& tk, const CUtensorMap& tv, const AttnA
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   dim3 grid(a.max_chunks, a.Hkv, a.B);
-  attention_kernel<RTP><<<grid, 128, SMEM_BYTES, s>>>(tk, tv, a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(attention_kernel<RTP>, grid, dim3(128), SMEM_BYTES, s, tk, tv, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -290,6 +290,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv, G = a.G;
+  pdl_wait();
+  pdl_trigger();
 
   // ---- per-sequence metadata: one parallel load, then a warp-0 scan of the tile counts
   for (int b = tid; b <= B; b += THREADS) {
@@ -738,8 +740,8 @@ cudaError_t launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, co
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  attention_tc_kernel<<<grid, THREADS, SMEM, s>>>(tk, tv, a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(attention_tc_kernel, dim3(grid), dim3(THREADS), SMEM, s, tk, tv, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

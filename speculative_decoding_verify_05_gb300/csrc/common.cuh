@@ -37,6 +37,14 @@ __device__ __forceinline__ void set_status(unsigned* status, unsigned site) {
   if (status) atomicCAS(status, 0u, site);
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library waits here for the kernel before it on the stream (its completion and
+// memory) before touching global memory, and lets the next one be scheduled early, so a launch and
+// its shared-memory/TMEM setup overlap the previous kernel's tail.  Both are no-ops when the launch
+// did not ask for programmatic serialization.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -24,6 +24,8 @@ struct GemvCfg {
 template <int MT>
 __global__ void __launch_bounds__(GEMV_THREADS)
 gemv_kernel(const GemvArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int T = GemvCfg<MT>::T;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (GEMV_THREADS / 32) + (threadIdx.x >> 5);
@@ -159,9 +161,9 @@ int gemv_k_slice(int M) {
 
 cudaError_t launch_gemv(const GemvArgs& a, int grid, cudaStream_t s) {
   switch (a.M) {
-    case 1: gemv_kernel<1><<<grid, GEMV_THREADS, 0, s>>>(a); break;
-    case 2: gemv_kernel<2><<<grid, GEMV_THREADS, 0, s>>>(a); break;
-    default: gemv_kernel<4><<<grid, GEMV_THREADS, 0, s>>>(a); break;
+    case 1: { cudaError_t e = launch_k(gemv_kernel<1>, dim3(grid), dim3(GEMV_THREADS), 0, s, a); if (e != cudaSuccess) return e; break; }
+    case 2: { cudaError_t e = launch_k(gemv_kernel<2>, dim3(grid), dim3(GEMV_THREADS), 0, s, a); if (e != cudaSuccess) return e; break; }
+    default: { cudaError_t e = launch_k(gemv_kernel<4>, dim3(grid), dim3(GEMV_THREADS), 0, s, a); if (e != cudaSuccess) return e; break; }
   }
   return cudaGetLastError();
 }

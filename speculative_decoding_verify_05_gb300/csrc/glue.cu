@@ -15,6 +15,8 @@ constexpr int RMS_MAX_VEC = 8;          // 8 x 8 bf16 per thread -> N <= 16384
 __global__ void __launch_bounds__(RMS_THREADS)
 rmsnorm_kernel(const uint16_t* __restrict__ X, int N, int ldx, const uint16_t* __restrict__ w,
                float eps, uint16_t* __restrict__ Y, int ldy) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const uint16_t* x = X + (size_t)r * ldx;
   const int nv = N / 8;
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(ROPE_THREADS)
 rope_kernel(uint16_t* __restrict__ Q, int ldq, int Hq, uint16_t* __restrict__ K, int ldk, int Hkv,
             int D, const int32_t* __restrict__ cu_rows, const int32_t* __restrict__ ctx_len, int B,
             const __grid_constant__ RopeFreq f, int vec) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int half = D / 2;
   __shared__ float s_cos[128];
@@ -143,6 +147,8 @@ rope_kernel(uint16_t* __restrict__ Q, int ldq, int Hq, uint16_t* __restrict__ K,
 
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ GU, int M, int I, int ldgu,
                                 uint16_t* __restrict__ A, int lda) {
+  pdl_wait();
+  pdl_trigger();
   const int per_row = I / 8;
   const size_t total = (size_t)M * per_row;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
@@ -168,8 +174,8 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ GU, int M, int I, i
 
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
                            uint16_t* Y, int ldy, cudaStream_t s) {
-  rmsnorm_kernel<<<M, RMS_THREADS, 0, s>>>(X, N, ldx, w, eps, Y, ldy);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(rmsnorm_kernel, dim3(M), dim3(RMS_THREADS), 0, s, X, N, ldx, w, eps, Y, ldy);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int Hkv, int D,
@@ -179,8 +185,9 @@ cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int 
   for (int i = 0; i < D / 2; ++i) f.inv[i] = std::pow((double)theta, -2.0 * (double)i / (double)D);
   const bool vec = D % 16 == 0 && ldq % 8 == 0 && ldk % 8 == 0 &&
                    (reinterpret_cast<uintptr_t>(Q) & 15) == 0 && (reinterpret_cast<uintptr_t>(K) & 15) == 0;
-  rope_kernel<<<M, ROPE_THREADS, 0, s>>>(Q, ldq, Hq, K, ldk, Hkv, D, cu_rows, ctx_len, B, f, vec ? 1 : 0);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(rope_kernel, dim3(M), dim3(ROPE_THREADS), 0, s, Q, ldq, Hq, K, ldk, Hkv, D, cu_rows,
+                           ctx_len, B, f, vec ? 1 : 0);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
@@ -189,8 +196,8 @@ cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t
   int grid = (int)((total + 255) / 256);
   if (grid > 152 * 16) grid = 152 * 16;
   if (grid < 1) grid = 1;
-  silu_mul_kernel<<<grid, 256, 0, s>>>(GU, M, I, ldgu, A, lda);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(silu_mul_kernel, dim3(grid), dim3(256), 0, s, GU, M, I, ldgu, A, lda);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

@@ -2,6 +2,8 @@
 // translation units.  Not part of the public interface.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -10,6 +12,26 @@
 #include "linear_tc.cuh"
 
 namespace spec {
+
+// 1: kernels are launched with programmatic stream serialization (see pdl_wait); knob "pdl".
+bool pdl_enabled();
+
+// Launch with the library's launch attributes (programmatic dependent launch when enabled).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- tcgen05 GEMM: NSUB sub-tiles of BN verify rows per CTA tile
 //      (NSUB = 1: BN = 16..256 step 16; NSUB = 2: BN = 144..256 step 16)

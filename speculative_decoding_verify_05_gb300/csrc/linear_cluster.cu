@@ -84,6 +84,9 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------- TMA producer over this rank's k-steps
@@ -240,8 +243,10 @@ struct ClusterLaunch {
     attr[0].val.clusterDim.x = S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
   }
   static int capacity(int S) {
@@ -251,7 +256,7 @@ struct ClusterLaunch {
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configure(dev)) return 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = config(S * 64, S, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, (void*)linear_cluster_kernel<BN, NSUB>, &cfg) != cudaSuccess) {
@@ -266,7 +271,7 @@ struct ClusterLaunch {
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configure(dev)) return cudaGetLastError();
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = config(tiles * S, S, st, attr);
     return cudaLaunchKernelEx(&cfg, linear_cluster_kernel<BN, NSUB>, tw, tx, a, S, cpr);
   }

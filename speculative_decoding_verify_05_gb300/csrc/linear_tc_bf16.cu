@@ -18,8 +18,8 @@ static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, cons
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  linear_tc_kernel<BN, NSUB, EPI><<<grid, Cfg::THREADS, smem, st>>>(tw, tx, a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), smem, st, tw, tx, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int linear_tc_smem_bytes(int BN, int NSUB) {
@@ -93,6 +93,8 @@ cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const
 // Pieces are summed in CTA order, two contributors' loads in flight at a time, then the
 // residual is added and the sum rounded to bf16.  Launched as one wave (grid-stride over items).
 __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ long long s_beg[];                      // [grid + 1]
   int* s_hi = reinterpret_cast<int*>(s_beg + a.grid + 1);   // [grid] -1: c names no tile
   const int G = a.grid, TN = a.tn;
@@ -186,8 +188,8 @@ cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
   const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
   long long blocks = (warps + 7) / 8;
   if (blocks > 2LL * sms) blocks = 2LL * sms;
-  linear_reduce_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(linear_reduce_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), smem, s, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

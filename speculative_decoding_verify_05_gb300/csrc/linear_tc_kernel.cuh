@@ -127,6 +127,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------- TMA producer: one continuous stream over this CTA's units

@@ -18,8 +18,8 @@ static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, cons
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  linear_tc_kernel<BN, NSUB, EPI><<<grid, Cfg::THREADS, smem, st>>>(tw, tx, a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), smem, st, tw, tx, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_linear_tc_lmhead(int BN, int NSUB, bool greedy, const CUtensorMap& tw,

@@ -63,6 +63,8 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
                      const int32_t* __restrict__ cu_rows, int V, float tie_eps,
                      int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tok,
                      int32_t* __restrict__ near_tie, unsigned* status, int vec) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -284,9 +286,9 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
                                  float tie_eps, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* near_tie, unsigned* status, cudaStream_t s) {
   const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
-  reject_sample_kernel<<<B, SAMPLER_THREADS, 0, s>>>(P, Q, draft, U, cu_rows, V, tie_eps, n_acc,
-                                                     out_tok, near_tie, status, vec ? 1 : 0);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(reject_sample_kernel, dim3(B), dim3(SAMPLER_THREADS), 0, s, P, Q, draft, U, cu_rows, V,
+                           tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec

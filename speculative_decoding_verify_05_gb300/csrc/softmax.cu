@@ -14,6 +14,8 @@ constexpr int NORM_CHUNK = 8192;   // vocabulary entries per CTA
 __global__ void __launch_bounds__(NORM_THREADS)
 lmhead_normalize_kernel(float* __restrict__ P, const float2* __restrict__ stats, int V,
                         int n_tiles, int greedy) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.y;
   const int tid = threadIdx.x;
   const float2* st = stats + (size_t)m * n_tiles;
@@ -96,8 +98,9 @@ lmhead_normalize_kernel(float* __restrict__ P, const float2* __restrict__ stats,
 cudaError_t launch_lmhead_normalize(float* P, const float2* stats, int M, int V, int n_tiles,
                                     bool greedy, cudaStream_t s) {
   dim3 grid((V + NORM_CHUNK - 1) / NORM_CHUNK, M);
-  lmhead_normalize_kernel<<<grid, NORM_THREADS, 0, s>>>(P, stats, V, n_tiles, greedy ? 1 : 0);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(lmhead_normalize_kernel, dim3(grid), dim3(NORM_THREADS), 0, s, P, stats, V, n_tiles,
+                           greedy ? 1 : 0);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spec
