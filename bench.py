@@ -152,7 +152,7 @@ def reference_runs_here() -> bool:
 
 
 # --------------------------------------------------------------------------- GPU arm
-def build_round(dev, rank, S, E, synth):
+def build_round(dev, rank, S, E, synth, fused_swiglu=True):
     """Resident state of the benchmark round (weights, KV caches, inputs, draft distribution)
     and a function that runs one full verify round on it."""
     import torch
@@ -173,7 +173,8 @@ def build_round(dev, rank, S, E, synth):
         v.normal_(0, 1, generator=g)
         kcs.append(k)
         vcs.append(v)
-    eng = E.VerifyEngine(dims, sw, kcs, vcs, max_M=batch.M, max_rows=batch.max_rows, device=dev)
+    eng = E.VerifyEngine(dims, sw, kcs, vcs, max_M=batch.M, max_rows=batch.max_rows, device=dev,
+                         fused_swiglu=fused_swiglu)
     x0 = torch.empty((batch.M, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
     cu = torch.from_numpy(batch.cu_rows).to(dev)
     ctx = torch.from_numpy(batch.ctx_len).to(dev)
@@ -217,7 +218,7 @@ def run_gpu(args):
     import synth
 
     hbm_peak, tc_peak, tc_sust, peak_src = peaks()
-    st = build_round(dev, rank, S, E, synth)
+    st = build_round(dev, rank, S, E, synth, fused_swiglu=args.swiglu == "fused")
     dims, batch, cap, sw, kcs, vcs, eng = (st[k] for k in ("dims", "batch", "cap", "sw", "kcs", "vcs", "eng"))
     x0, cu, ctx, q, drafts, out, step = (st[k] for k in ("x0", "cu", "ctx", "q", "drafts", "out", "step"))
     S.reset_launch_count()
@@ -358,7 +359,8 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
     shapes = {"qkv": (dims.qkv, dims.d), "o": (dims.d, hq), "gate_up": (2 * dims.I, dims.d),
               "down": (dims.d, dims.I)}
     xs = {"qkv": eng.h[:M], "o": eng.o[:M], "gate_up": eng.h[:M], "down": eng.a[:M]}
-    ys = {"qkv": eng.qkv[:M], "o": eng.h[:M], "gate_up": eng.gu[:M], "down": eng.h[:M]}
+    ys = {"qkv": eng.qkv[:M], "o": eng.h[:M], "gate_up": eng.a[:M] if eng.fused_swiglu else eng.gu[:M],
+          "down": eng.h[:M]}
     tot_t, tot_f, tot_b = 0.0, 0.0, 0.0
     per_shape = {}
     for name, (N, K) in shapes.items():
@@ -366,7 +368,10 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
 
         def lin_all(name=name, w_attr=w_attr):
             for li in range(L):
-                S.spec_verify_linear(xs[name], getattr(eng.w.layers[li], w_attr), Y=ys[name], ws=eng.ws)
+                if name == "gate_up" and eng.fused_swiglu:
+                    S.spec_verify_linear_swiglu(xs[name], eng.w.layers[li].w_gu, A=ys[name], ws=eng.ws)
+                else:
+                    S.spec_verify_linear(xs[name], getattr(eng.w.layers[li], w_attr), Y=ys[name], ws=eng.ws)
         t = timeit(lin_all, L)
         per_shape[name] = {"us": t * 1e3, "tflops": 2.0 * M * N * K / (t / 1e3) / 1e12,
                            "weight_gbs": 2.0 * N * K / (t / 1e3) / 1e9}
@@ -412,7 +417,10 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
             for lw in eng.w.layers:
                 S.spec_verify_linear(eng.h[:M], lw.w_qkv, Y=eng.qkv[:M], ws=eng.ws)
                 S.spec_verify_linear(eng.o[:M], lw.w_o, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
-                S.spec_verify_linear(eng.h[:M], lw.w_gu, Y=eng.gu[:M], ws=eng.ws)
+                if eng.fused_swiglu:
+                    S.spec_verify_linear_swiglu(eng.h[:M], lw.w_gu, A=eng.a[:M], ws=eng.ws)
+                else:
+                    S.spec_verify_linear(eng.h[:M], lw.w_gu, Y=eng.gu[:M], ws=eng.ws)
                 S.spec_verify_linear(eng.a[:M], lw.w_down, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
@@ -517,11 +525,15 @@ def cpu_baseline(eng, batch, dims, kcs, vcs, sw, q, drafts, n_seq=4):
     """Oracle on the host cores over a bounded sample of this run's inputs (copied to the host)."""
     import torch
     from oracle import stack as ostack
+    from speculative_decoding_verify_05_gb300 import binding as S
     import synth
     sub = synth.RaggedBatch(batch.gammas[:n_seq], batch.ctx_len[:n_seq])
     bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     l0 = sw.layers[0]
-    lw = ostack.LayerWeights(bits(l0.w_qkv), bits(l0.w_o), bits(l0.w_gu), bits(l0.w_down),
+    w_gu = bits(l0.w_gu)
+    if l0.gu_layout == "interleaved":     # back to gate rows then up rows for the oracle
+        w_gu = w_gu.reshape(-1, 2, S.GATE_UP_BLOCK, dims.d).transpose(1, 0, 2, 3).reshape(2 * dims.I, dims.d)
+    lw = ostack.LayerWeights(bits(l0.w_qkv), bits(l0.w_o), w_gu, bits(l0.w_down),
                              bits(l0.attn_norm), bits(l0.mlp_norm))
     capn = int((sub.ctx_len + sub.gammas + 1).max())
     kv = (bits(kcs[0][:n_seq, :, :capn]), bits(vcs[0][:n_seq, :, :capn]))
@@ -596,6 +608,7 @@ def run_profile_case(args):
     round: one full verify round of the benchmark workload (for the launch list);
     attention: one layer of B=16 ragged sequences (KV ~0.6 GB, above L2);
     linear: one gate|up projection (201 MB of weights) at --rows rows;
+    swiglu: the same projection with the SwiGLU epilogue (--n interleaved gate|up rows);
     lmhead: the LM head + softmax at --rows rows.
     """
     import torch
@@ -611,7 +624,7 @@ def run_profile_case(args):
     if args.profile == "round":
         # the benchmark's full verify round, run eagerly: once to warm up, then once inside
         # the NVTX range "round" (ncu --nvtx --nvtx-include "round/" lists only that one)
-        st = build_round(dev, 0, S, E, synth)
+        st = build_round(dev, 0, S, E, synth, fused_swiglu=args.swiglu == "fused")
         st["step"]()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("round")
@@ -632,8 +645,8 @@ def run_profile_case(args):
     else:
         M = args.rows
         if args.nsub:
-            S.spec_set_option("linear_nsub" if args.profile == "linear" else "lmhead_nsub", args.nsub)
-        if args.profile == "linear":
+            S.spec_set_option("lmhead_nsub" if args.profile == "lmhead" else "linear_nsub", args.nsub)
+        if args.profile in ("linear", "swiglu"):
             N, K = args.n, args.k
         else:
             N, K = dims.V, dims.d
@@ -642,6 +655,8 @@ def run_profile_case(args):
         for _ in range(args.reps):
             if args.profile == "linear":
                 S.spec_verify_linear(X, W, ws=ws)
+            elif args.profile == "swiglu":
+                S.spec_verify_linear_swiglu(X, W, ws=ws)
             else:
                 S.spec_lmhead_softmax(X, W, TEMP, ws=ws)
     torch.cuda.synchronize()
@@ -656,12 +671,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--profile", choices=["round", "attention", "linear", "lmhead"], default=None,
+    ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead"], default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")
     ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")
+    ap.add_argument("--swiglu", choices=["fused", "split"], default="fused",
+                    help="SwiGLU in the gate|up GEMM epilogue (fused) or as its own kernel (split)")
     ap.add_argument("--nsub", type=int, default=0, help="linear_nsub knob for --profile linear/lmhead (0: library default)")
     args = ap.parse_args()
     if args.profile:

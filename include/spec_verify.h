@@ -152,6 +152,25 @@ SPEC_API int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ld
                                         spec_bf16* Y, int ldy,
                                         const spec_bf16* residual, int ldr, spec_stream stream);
 
+/* Fused gate|up projection and SwiGLU activation of the MLP:
+ *   A[r, i] = silu(gate[r, i]) * up[r, i],  gate = X Wg^T, up = X Wu^T,
+ * silu(g) = g / (1 + e^-g), fp32 from the fp32 accumulators, one bf16 rounding.
+ *   X    [M x K] bf16, leading dim ldx
+ *   Wgu  [2I x K] bf16, leading dim ldw: gate and up rows interleaved in blocks
+ *        of 16, i.e. rows 32 j .. 32 j + 15 are gate rows 16 j .. 16 j + 15
+ *        and rows 32 j + 16 .. 32 j + 31 the matching up rows
+ *   A    [M x I] bf16, leading dim lda (output)
+ * Same result as spec_verify_linear into a [M x 2I] scratch followed by
+ * spec_silu_mul, except that gate and up are not rounded to bf16 first; the
+ * [M x 2I] intermediate never reaches HBM on the tensor-core path.  Requires
+ * I % 64 == 0, K % 8 == 0, leading dimensions multiples of 8, 16-byte aligned
+ * pointers.  Workspace: spec_swiglu_linear_workspace_bytes (may be 0). */
+SPEC_API size_t spec_swiglu_linear_workspace_bytes(int M, int I, int K);
+SPEC_API int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx,
+                                       const spec_bf16* Wgu, int ldw, int I,
+                                       spec_bf16* A, int lda,
+                                       void* workspace, size_t workspace_bytes, spec_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Verify attention (causal GQA over the KV cache + the new block)           */
 /* ------------------------------------------------------------------------ */

@@ -30,6 +30,9 @@ class Dims:
     layers: int = 36
     eps: float = 1e-6
     theta: float = 1e6
+    # True: gate and up are rounded to bf16 before the SwiGLU product (they are stored
+    # between two steps); False: the product takes them unrounded (one fused step)
+    gate_up_bf16: bool = False
 
 
 @dataclass
@@ -71,7 +74,9 @@ def layer_forward(x, lw: LayerWeights, dims: Dims, cu_rows, ctx_len, Kc, Vc):
     o = r16(o)
     x = r16(ops.linear(o.reshape(M, Hq * D), decode(lw.w_o), residual=x))
     h = r16(ops.rmsnorm(x, decode(lw.mlp_norm), dims.eps))
-    gu = r16(ops.linear(h, decode(lw.w_gu)))
+    gu = ops.linear(h, decode(lw.w_gu))
+    if dims.gate_up_bf16:
+        gu = r16(gu)
     a = r16(ops.silu_mul(gu[:, :dims.I], gu[:, dims.I:]))
     x = r16(ops.linear(a, decode(lw.w_down), residual=x))
     return x, Kc, Vc

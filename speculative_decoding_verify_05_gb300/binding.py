@@ -30,6 +30,8 @@ _SIGS = {
     "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
+    "spec_swiglu_linear_workspace_bytes": (_sz, [_i, _i, _i]),
+    "spec_verify_linear_swiglu": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "spec_verify_attention": (_i, [_vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp, _i,
                                    _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
@@ -198,6 +200,43 @@ def spec_verify_linear_noalloc(X, W, Y, residual=None, stream=None):
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
         _stream(stream)), True)
     return Y
+
+
+def spec_swiglu_linear_workspace_bytes(M, I, K) -> int:
+    return _lib.spec_swiglu_linear_workspace_bytes(M, I, K)
+
+
+GATE_UP_BLOCK = 16   # rows per gate / up block in the interleaved layout
+
+
+def interleave_gate_up(Wg, Wu):
+    """Weight layout of spec_verify_linear_swiglu: gate and up rows in alternating blocks of 16.
+
+    A one-time relayout of the model's weights (a copy), not part of a verify pass.
+    """
+    I, K = Wg.shape
+    b = GATE_UP_BLOCK
+    if Wu.shape != (I, K) or I % 64:
+        raise ValueError("Wg and Wu must both be [I, K] with I % 64 == 0")
+    return torch.stack((Wg.reshape(I // b, b, K), Wu.reshape(I // b, b, K)), dim=1).reshape(2 * I, K).contiguous()
+
+
+def spec_verify_linear_swiglu(X, Wgu, A=None, ws: Workspace | None = None, stream=None):
+    """A[M, I] = silu(X Wg^T) * (X Wu^T), Wgu = interleave_gate_up(Wg, Wu) of shape [2I, K]."""
+    _need(X, torch.bfloat16, "X"); _need(Wgu, torch.bfloat16, "Wgu")
+    M, K = X.shape
+    N2 = Wgu.shape[0]
+    if Wgu.shape[1] != K or N2 % 128:
+        raise ValueError("Wgu must be [2I, K] with I % 64 == 0")
+    inter = N2 // 2
+    if A is None:
+        A = torch.empty((M, inter), dtype=torch.bfloat16, device=X.device)
+    _need(A, torch.bfloat16, "A")
+    wp, wn = _ws_args(ws, spec_swiglu_linear_workspace_bytes(M, inter, K), X.device)
+    _check(_lib.spec_verify_linear_swiglu(
+        _p(X), M, K, _rowmajor(X, "X"), _p(Wgu), _rowmajor(Wgu, "Wgu"), inter,
+        _p(A), _rowmajor(A, "A"), wp, wn, _stream(stream)), True)
+    return A
 
 
 # --------------------------------------------------------------------------- attention

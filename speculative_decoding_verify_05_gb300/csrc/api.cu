@@ -148,7 +148,7 @@ struct LinPlan {
   size_t counters_off = 0, partial_off = 0, bytes = 0;
 };
 
-LinPlan plan_linear(int M, int N, int K, bool lmhead) {
+LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   LinPlan p;
   const int sms = plan_sms();
   p.k_tiles = (K + 63) / 64;
@@ -200,7 +200,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead) {
   // tiles * S CTAs).  Cost model in k-steps of one tile on one SM: the cluster kernel takes
   // ceil(kt / S) plus ~6 for its on-chip reduction; stream-K takes ceil(units / SMs) plus
   // ~20 when tiles are split (fp32 pieces through L2 and a second kernel)
-  if (!lmhead && g_linear_cluster && g_force_grid == 0 && tiles < sms) {
+  if (!lmhead && !swiglu && g_linear_cluster && g_force_grid == 0 && tiles < sms) {
     int best = 0;
     long long best_cost = 0;
     for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
@@ -411,6 +411,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
+  a.epi = EPI_BF16;
   if (p.cluster_S > 0) {
     cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch");
@@ -421,6 +422,83 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
   if (p.bytes == 0) return ok(1);
   // some tiles had their k-steps split between CTAs: a second kernel sums their pieces
+  e = launch_linear_reduce(a, plan_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+  return ok(2);
+}
+
+// --------------------------------------------------------------------------- fused SwiGLU linear
+// Scratch for the CUDA-core path: the GEMV writes the interleaved gate|up rows to the workspace,
+// after its own split-K scratch and never inside the counter region (which every kernel that
+// uses the workspace expects to find zero).
+static size_t swiglu_gemv_scratch_off(const LinPlan& p) {
+  return p.bytes > 0 ? round_up(p.bytes, 256) : kCounterBytes;
+}
+
+size_t spec_swiglu_linear_workspace_bytes(int M, int I, int K) {
+  if (M <= 0 || I <= 0 || K <= 0) return 0;
+  const LinPlan p = plan_linear(M, 2 * I, K, false, true);
+  return p.gemv ? swiglu_gemv_scratch_off(p) + round_up(size_t(M) * 2 * I * 2, 256) : p.bytes;
+}
+
+int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
+                              int I, spec_bf16* A, int lda, void* workspace, size_t workspace_bytes,
+                              spec_stream stream) {
+  if (M < 0 || I <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d I=%d K=%d", M, I, K);
+  if (M == 0) return ok();
+  if (!X || !Wgu || !A) return fail(SPEC_EINVAL, "X, Wgu and A must be non-NULL");
+  if (I % 64) return fail(SPEC_EINVAL, "I=%d must be a multiple of 64 (whole 128-row weight tiles)", I);
+  if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
+  if (ldx < K || ldw < K || lda < I) return fail(SPEC_EINVAL, "leading dimensions too small");
+  if (ldx % 8 || ldw % 8 || lda % 8) return fail(SPEC_EINVAL, "leading dimensions must be multiples of 8");
+  if (!aligned16(X) || !aligned16(Wgu) || !aligned16(A)) return fail(SPEC_EINVAL, "X, Wgu, A must be 16-byte aligned");
+  const int N = 2 * I;
+  LinPlan p = plan_linear(M, N, K, false, true);
+  const size_t need = spec_swiglu_linear_workspace_bytes(M, I, K);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (p.gemv) {
+    spec_bf16* gu = reinterpret_cast<spec_bf16*>(ws + swiglu_gemv_scratch_off(p));
+    GemvArgs g;
+    g.X = X; g.ldx = ldx; g.W = Wgu; g.ldw = ldw; g.Y = gu; g.ldy = N;
+    g.residual = nullptr; g.ldr = 0; g.M = M; g.N = N; g.K = K;
+    g.splits = p.splits; g.k_per_split = p.k_per_split;
+    g.partial = p.splits > 1 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
+    g.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + p.counters_off) : nullptr;
+    cudaError_t e = launch_gemv(g, p.gemv_grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    e = launch_swiglu_interleaved(gu, M, I, N, A, lda, s);
+    if (e != cudaSuccess) return cuda_fail(e, "swiglu launch");
+    return ok(2);
+  }
+  CUtensorMap tw, tx;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (int rc = encode_bf16(&tw, Wgu, 2, dims, str, box, "Wgu")) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
+  }
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.Y = A; a.ldy = lda; a.residual = nullptr; a.ldr = 0;
+  a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
+  a.status = d->status;
+  a.tn = p.BN * p.NSUB;
+  a.epi = EPI_SWIGLU;
+  cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid), s);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 swiglu linear launch");
+  if (p.bytes == 0) return ok(1);
   e = launch_linear_reduce(a, plan_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
   return ok(2);

@@ -27,6 +27,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return uint32_t(f2bf(lo)) | (uint32_t(f2bf(hi)) << 16);
 }
 
+// silu(g) = g / (1 + e^-g) with e^-g = 2^(-g log2 e) from the hardware base-2 exponential and
+// the reciprocal rounded to nearest (relative error a few fp32 ulps; the result is rounded to bf16).
+// For g below about -88 the exponential overflows to +inf and the result is -0.
+__device__ __forceinline__ float silu(float g) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+  return g * __frcp_rn(1.f + e);
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -163,7 +163,35 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ GU, int M, int I, i
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float g0 = bf16lo(g4[e]), g1 = bf16hi(g4[e]);
-      const float s0 = g0 / (1.f + expf(-g0)), s1 = g1 / (1.f + expf(-g1));
+      const float s0 = silu(g0), s1 = silu(g1);
+      o4[e] = pack_bf16x2(s0 * bf16lo(u4[e]), s1 * bf16hi(u4[e]));
+    }
+    *reinterpret_cast<uint4*>(A + (size_t)r * lda + c) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+  }
+}
+
+// A[m][16 j + r] = silu(GU[m][32 j + r]) * GU[m][32 j + 16 + r]: gate and up rows interleaved per
+// 16 (the layout of the fused SwiGLU linear), 8 outputs per thread.
+__global__ void swiglu_interleaved_kernel(const uint16_t* __restrict__ GU, int M, int I, int ldgu,
+                                          uint16_t* __restrict__ A, int lda) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_row = I / 8;
+  const size_t total = (size_t)M * per_row;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / per_row);
+    const int c = (int)(idx - (size_t)r * per_row) * 8;
+    const int gcol = (c / 16) * 32 + (c % 16);
+    const uint4 g = *reinterpret_cast<const uint4*>(GU + (size_t)r * ldgu + gcol);
+    const uint4 u = *reinterpret_cast<const uint4*>(GU + (size_t)r * ldgu + gcol + 16);
+    const uint32_t g4[4] = {g.x, g.y, g.z, g.w};
+    const uint32_t u4[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g0 = bf16lo(g4[e]), g1 = bf16hi(g4[e]);
+      const float s0 = silu(g0), s1 = silu(g1);
       o4[e] = pack_bf16x2(s0 * bf16lo(u4[e]), s1 * bf16hi(u4[e]));
     }
     *reinterpret_cast<uint4*>(A + (size_t)r * lda + c) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
@@ -197,6 +225,16 @@ cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t
   if (grid > 152 * 16) grid = 152 * 16;
   if (grid < 1) grid = 1;
   cudaError_t e = launch_k(silu_mul_kernel, dim3(grid), dim3(256), 0, s, GU, M, I, ldgu, A, lda);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_interleaved(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
+                                      cudaStream_t s) {
+  const size_t total = (size_t)M * (I / 8);
+  int grid = (int)((total + 255) / 256);
+  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_k(swiglu_interleaved_kernel, dim3(grid), dim3(256), 0, s, GU, M, I, ldgu, A, lda);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -40,6 +40,8 @@ int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
+cudaError_t launch_linear_tc_swiglu(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
+                                    const LinearArgs& a, dim3 grid, cudaStream_t s);
 // Cluster split-K GEMM (few tiles): CTAs that may be resident at once for clusters of S
 // (0 when the tile shape has no cluster build or S is out of range), and the launch
 // (tiles * S CTAs; no workspace).
@@ -112,5 +114,7 @@ cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int 
                         cudaStream_t s);
 cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
                             cudaStream_t s);
+cudaError_t launch_swiglu_interleaved(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
+                                      cudaStream_t s);
 
 }  // namespace spec

@@ -30,7 +30,8 @@ namespace spec {
 enum LinearEpilogue : int {
   EPI_BF16 = 0,        // Y = acc (+ residual) -> bf16
   EPI_LOGITS = 1,      // P = acc * inv_temp (fp32) + per-tile (max, sum exp) per token
-  EPI_ARGMAX = 2       // per-tile (max, argmax) per token only
+  EPI_ARGMAX = 2,      // per-tile (max, argmax) per token only
+  EPI_SWIGLU = 3       // weight rows interleaved per 64 (gate block, up block): Y = silu(gate) * up
 };
 
 struct LinearArgs {
@@ -47,6 +48,7 @@ struct LinearArgs {
   int ldr;
   float* partial;       // [grid][2][TN][128] fp32 (split tiles only)
   int tn;               // token columns per tile (BN * NSUB)
+  int epi;              // the reduce kernel's epilogue: EPI_BF16 (+ residual) or EPI_SWIGLU
   unsigned* status;     // library status word (bounded-wait timeouts)
   float inv_temp;       // EPI_LOGITS
   float* P;             // EPI_LOGITS: [M x N] fp32

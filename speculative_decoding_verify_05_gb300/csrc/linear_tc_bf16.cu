@@ -151,6 +151,25 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
           acc[jj].x += v[q][jj].x; acc[jj].y += v[q][jj].y; acc[jj].z += v[q][jj].z; acc[jj].w += v[q][jj].w;
         }
     }
+    if (a.epi == EPI_SWIGLU) {
+      // gate and up rows interleaved in blocks of 16: lane L holds rows 4L .. 4L + 3, gate rows
+      // when L % 8 < 4, and lane L + 4 holds the matching up rows
+      const bool gate = (lane & 7) < 4;
+      const int n = (int)(tile / a.tiles_m) * 64 + (lane >> 3) * 16 + (lane & 3) * 4;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float u0 = __shfl_down_sync(0xffffffffu, acc[jj].x, 4), u1 = __shfl_down_sync(0xffffffffu, acc[jj].y, 4);
+        const float u2 = __shfl_down_sync(0xffffffffu, acc[jj].z, 4), u3 = __shfl_down_sync(0xffffffffu, acc[jj].w, 4);
+        const int m = m0 + jj;
+        if (!gate || j0 + jj >= TN || m >= a.M) continue;
+        const float g[4] = {acc[jj].x, acc[jj].y, acc[jj].z, acc[jj].w}, u[4] = {u0, u1, u2, u3};
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = silu(g[e]) * u[e];
+        *reinterpret_cast<uint2*>(a.Y + (size_t)m * a.ldy + n) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+      }
+      continue;
+    }
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) {
       const int m = m0 + jj;

@@ -24,6 +24,38 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
 }
+// SwiGLU epilogue of 32 token columns of one whole tile held by one warp (v[0..31]; columns
+// past `cols` are never stored): gate and up rows are interleaved in blocks of 16, so lane l < 16
+// holds gate row l of the warp's block and lane l + 16 the matching up row.  One register
+// exchange gives lane l < 16 the up values of columns 0-15 and lane l + 16 the gate values of
+// columns 16-31; each lane writes silu(gate) * up for its 16 columns as bf16 into the warp's
+// staging buffer ([column][16 rows], column c at slot c ^ (c >> 4) so the two half-warps hit
+// different banks), and the warp stores 16-byte runs of 8 outputs along A's rows.
+__device__ __forceinline__ void swiglu_chunk32(const float* v, int cols, float* ebuf, int lane,
+                                               const LinearArgs& args, int m_first, int n_first) {
+  const bool lo = lane < 16;
+  uint16_t* eb = reinterpret_cast<uint16_t*>(ebuf);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float send = lo ? v[k + 16] : v[k];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float g = lo ? v[k] : recv;
+    const float u = lo ? recv : v[k + 16];
+    const int col = lo ? k : k + 16;
+    eb[(col ^ (col >> 4)) * 16 + (lane & 15)] = f2bf(silu(g) * u);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int item = lane + 32 * it, col = item >> 1, h = item & 1;
+    const int m = m_first + col;
+    if (col < cols && m < args.M)
+      *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n_first + h * 8) =
+          *reinterpret_cast<const uint4*>(eb + (col ^ (col >> 4)) * 16 + h * 8);
+  }
+  __syncwarp();
+}
+
 // Named barrier 2 over the eight epilogue warps.
 __device__ __forceinline__ void bar_epi() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 __device__ __forceinline__ bool bar_epi_and(bool v) {
@@ -211,7 +243,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       tc_fence_after();
       const uint32_t t_row = tmem + acc * Cfg::ACC_COLS + (uint32_t(q * 32) << 16);
 
-      if constexpr (EPI == EPI_BF16) {
+      if constexpr (EPI == EPI_BF16 || EPI == EPI_SWIGLU) {
         // 16 columns at a time: TMEM -> this warp's transpose block -> 16-byte global accesses
         float* ebuf = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
         const int nq = n0 + q * 32;                     // first weight row of this warp
@@ -221,12 +253,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         // 16-column block then goes through the transpose buffer
 #pragma unroll 1
         for (int c64 = c_begin; c64 < c_end; c64 += 64) {
-        float v64[64];
         const int cols = c_end - c64 < 64 ? c_end - c64 : 64;
+        float v64[64];
         if (cols == 64) tmem_ld_cols<64>(t_row + c64, v64);
         else if (cols == 48) tmem_ld_cols<48>(t_row + c64, v64);
         else if (cols == 32) tmem_ld_cols<32>(t_row + c64, v64);
         else tmem_ld_cols<16>(t_row + c64, v64);
+        if constexpr (EPI == EPI_SWIGLU) {
+          if (whole) {
+            // (columns past `cols` are never stored; give them defined values)
+#pragma unroll
+            for (int k = 16; k < 64; ++k)
+              if (k >= cols) v64[k] = 0.f;
+            swiglu_chunk32(v64, cols, ebuf, lane, args, m0 + c64, n_t * 64 + q * 16);
+            if (cols > 32) swiglu_chunk32(v64 + 32, cols - 32, ebuf, lane, args, m0 + c64 + 32, n_t * 64 + q * 16);
+            continue;
+          }
+        }
 #pragma unroll
         for (int c16 = 0; c16 < 64; c16 += 16) {
           if (c16 >= cols) break;

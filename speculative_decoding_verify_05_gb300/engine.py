@@ -10,7 +10,10 @@ heads of 128, grouped-query attention, a 151936-token vocabulary): pre-RMSNorm
 (eps 1e-6), fused QKV projection, RoPE (theta 1e6, rotate-half) on q and k,
 causal verify attention over the cache, O projection + residual, RMSNorm,
 fused gate/up projection, SwiGLU, down projection + residual; final RMSNorm
-and LM head.
+and LM head.  By default the SwiGLU activation runs in the gate/up GEMM's
+epilogue (spec_verify_linear_swiglu), which wants the gate and up weight rows
+interleaved in blocks of 16: the engine relays each layer's ``w_gu`` out once,
+in place, when it is built.
 """
 from __future__ import annotations
 
@@ -42,10 +45,11 @@ class Dims:
 class LayerW:
     w_qkv: torch.Tensor      # [(Hq + 2 Hkv) D, d]
     w_o: torch.Tensor        # [d, Hq D]
-    w_gu: torch.Tensor       # [2 I, d]  gate rows then up rows
+    w_gu: torch.Tensor       # [2 I, d]  gate rows then up rows (see gu_layout)
     w_down: torch.Tensor     # [d, I]
     attn_norm: torch.Tensor  # [d]
     mlp_norm: torch.Tensor   # [d]
+    gu_layout: str = "split"  # "split": gate rows then up rows; "interleaved": blocks of 16
 
 
 @dataclass
@@ -76,13 +80,35 @@ def random_stack(dims: Dims, seed: int, device, std: float = 0.02, with_head: bo
     return sw
 
 
+def set_gu_layout(lw: LayerW, layout: str) -> None:
+    """Reorders ``lw.w_gu``'s rows in place to ``layout`` (a one-time weight relayout)."""
+    if lw.gu_layout == layout:
+        return
+    w = lw.w_gu
+    I2, K = w.shape
+    I = I2 // 2
+    if layout == "interleaved":
+        w.copy_(S.interleave_gate_up(w[:I], w[I:]))
+    elif layout == "split":
+        b = S.GATE_UP_BLOCK
+        blocks = w.reshape(I // b, 2, b, K)
+        w.copy_(torch.cat((blocks[:, 0].reshape(I, K), blocks[:, 1].reshape(I, K)), dim=0))
+    else:
+        raise ValueError(f"unknown gate/up layout {layout!r}")
+    lw.gu_layout = layout
+
+
 class VerifyEngine:
     """Buffers + call sequence of one verify pass / round for up to ``max_M`` rows."""
 
     def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, max_M: int, max_rows: int,
-                 device=None):
+                 device=None, fused_swiglu: bool = True):
         self.dims = dims
         self.w = weights
+        self.fused_swiglu = fused_swiglu and dims.I % 64 == 0
+        want = "interleaved" if self.fused_swiglu else "split"
+        for lw in weights.layers:
+            set_gu_layout(lw, want)
         self.kc = kcaches
         self.vc = vcaches
         self.max_M = max_M
@@ -94,7 +120,7 @@ class VerifyEngine:
         self.h = torch.empty((max_M, dims.d), **bf)
         self.qkv = torch.empty((max_M, dims.qkv), **bf)
         self.o = torch.empty((max_M, dims.Hq * dims.D), **bf)
-        self.gu = torch.empty((max_M, 2 * dims.I), **bf)
+        self.gu = None if self.fused_swiglu else torch.empty((max_M, 2 * dims.I), **bf)
         self.a = torch.empty((max_M, dims.I), **bf)
         self.P = torch.empty((max_M, dims.V), dtype=torch.float32, device=dev) if weights.w_lm is not None else None
         B, cap = (kcaches[0].shape[0], kcaches[0].shape[2]) if kcaches else (1, 1)
@@ -103,6 +129,8 @@ class VerifyEngine:
             for (n, k) in ((dims.qkv, dims.d), (dims.d, dims.Hq * dims.D), (2 * dims.I, dims.d),
                            (dims.d, dims.I)):
                 need = max(need, S.spec_linear_workspace_bytes(M, n, k))
+            if self.fused_swiglu:
+                need = max(need, S.spec_swiglu_linear_workspace_bytes(M, dims.I, dims.d))
         if kcaches:
             need = max(need, S.spec_attention_workspace_bytes(B, max_rows, dims.Hq, dims.Hkv, dims.D, cap))
         if weights.w_lm is not None:
@@ -112,7 +140,7 @@ class VerifyEngine:
     # ------------------------------------------------------------------ one layer
     def layer(self, li: int, M: int, cu_rows, ctx_len, B: int, max_rows: int):
         dm, lw = self.dims, self.w.layers[li]
-        x, h, qkv, o, gu, a = (self.x[:M], self.h[:M], self.qkv[:M], self.o[:M], self.gu[:M], self.a[:M])
+        x, h, qkv, o, a = (self.x[:M], self.h[:M], self.qkv[:M], self.o[:M], self.a[:M])
         hq = dm.Hq * dm.D
         hk = dm.Hkv * dm.D
         S.spec_rmsnorm(x, lw.attn_norm, dm.eps, Y=h)
@@ -123,8 +151,11 @@ class VerifyEngine:
                                 ws=self.ws)
         S.spec_verify_linear(o, lw.w_o, Y=x, residual=x, ws=self.ws)
         S.spec_rmsnorm(x, lw.mlp_norm, dm.eps, Y=h)
-        S.spec_verify_linear(h, lw.w_gu, Y=gu, ws=self.ws)
-        S.spec_silu_mul(gu, A=a)
+        if self.fused_swiglu:
+            S.spec_verify_linear_swiglu(h, lw.w_gu, A=a, ws=self.ws)
+        else:
+            S.spec_verify_linear(h, lw.w_gu, Y=self.gu[:M], ws=self.ws)
+            S.spec_silu_mul(self.gu[:M], A=a)
         S.spec_verify_linear(a, lw.w_down, Y=x, residual=x, ws=self.ws)
 
     def verify_pass(self, x0, cu_rows, ctx_len, temperature: float, max_rows: int | None = None,

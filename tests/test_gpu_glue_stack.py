@@ -50,9 +50,11 @@ def test_rope_unaligned_heads(lib):
     assert np.array_equal(bits_of(Qd[:, :1]), Qb[:, :1])
 
 
-def test_silu_mul(lib):
+@pytest.mark.parametrize("std", [2.0, 60.0])
+def test_silu_mul(lib, std):
+    """std 60 puts many gate values past +-88, where e^-g overflows or underflows in fp32."""
     M, inter = 7, 12288
-    GU = synth.normal_bf16_bits(3, (M, 2 * inter), 2.0)
+    GU = synth.normal_bf16_bits(3, (M, 2 * inter), std)
     A = lib.spec_silu_mul(bf16_dev(GU))
     g = obf.decode(GU)
     ref = oops.silu_mul(g[:, :inter], g[:, inter:])
@@ -78,15 +80,17 @@ def _tiny_stack(L, seed, d=512, Hq=4, Hkv=2, I=1024, V=1024, std=0.05):
 
 
 @pytest.mark.parametrize("L,gammas,ctx,T", [(2, [3, 0, 5], [40, 9, 0], 1.0), (1, [4], [130], 0.0)])
-def test_small_stack_end_to_end(lib, L, gammas, ctx, T):
+@pytest.mark.parametrize("fused", [True, False])
+def test_small_stack_end_to_end(lib, L, gammas, ctx, T, fused):
     from speculative_decoding_verify_05_gb300 import engine as E
     dims, od, osw, gsw = _tiny_stack(L, 50 + L)
+    od.gate_up_bf16 = not fused           # the split path stores gate|up as bf16 in between
     batch = synth.RaggedBatch(gammas, ctx, cap=160)
     kc = [synth.normal_bf16_bits(200 + i, (batch.B, dims.Hkv, batch.cap, 128), 1.0) for i in range(L)]
     vc = [synth.normal_bf16_bits(300 + i, (batch.B, dims.Hkv, batch.cap, 128), 1.0) for i in range(L)]
     x0 = synth.normal_bf16_bits(7, (batch.M, dims.d), 1.0)
     eng = E.VerifyEngine(dims, gsw, [bf16_dev(k) for k in kc], [bf16_dev(v) for v in vc],
-                         max_M=batch.M, max_rows=batch.max_rows)
+                         max_M=batch.M, max_rows=batch.max_rows, fused_swiglu=fused)
     P = eng.verify_pass(bf16_dev(x0), dev(batch.cu_rows), dev(batch.ctx_len), T)
     lib.spec_device_status()
     xr, lg, Kr, Vr = ostack.verify_pass(obf.decode(x0), osw, od, batch.cu_rows, batch.ctx_len,

@@ -126,3 +126,98 @@ def test_linear_cluster_split_k(lib, M, N, K):
             run_case(lib, M, N, K, True, seed=M + N + K + cluster, gemv_max_m=0)
         finally:
             lib.spec_set_option("linear_cluster", 1)
+
+
+# --------------------------------------------------------------------------- fused gate/up + SwiGLU
+def run_swiglu(lib, M, I, K, seed, gemv_max_m=4, grid=0, std=0.05):
+    """A = silu(X Wg^T) * (X Wu^T) through spec_verify_linear_swiglu vs the oracle in fp64
+    (gate and up unrounded, as the fused kernel takes them from its fp32 accumulators)."""
+    X = synth.normal_bf16_bits(seed, (M, K), 1.0)
+    Wg = synth.normal_bf16_bits(seed + 1, (I, K), std)
+    Wu = synth.normal_bf16_bits(seed + 2, (I, K), std)
+    Wgu = lib.interleave_gate_up(bf16_dev(Wg), bf16_dev(Wu))
+    lib.spec_set_option("gemv_max_m", gemv_max_m)
+    lib.spec_set_option("persistent_grid", grid)
+    try:
+        A = lib.spec_verify_linear_swiglu(bf16_dev(X), Wgu)
+        lib.spec_device_status()
+    finally:
+        lib.spec_set_option("gemv_max_m", 4)
+        lib.spec_set_option("persistent_grid", 0)
+    x = obf.decode(X)
+    ref = oops.silu_mul(oops.linear(x, obf.decode(Wg)), oops.linear(x, obf.decode(Wu)))
+    assert_close_rel(f64_of_bf16(A), ref, f"swiglu linear M={M} I={I} K={K}")
+
+
+SWIGLU_SHAPES = [
+    # CUDA-core path (M <= 4), the smallest interleave block, ragged K, one and two
+    # sub-tiles, several M tiles, and the Qwen3-8B MLP (I = 12288, d = 4096)
+    (1, 1024, 512), (3, 64, 264), (4, 12288, 4096), (5, 12288, 4096), (37, 1024, 520),
+    (300, 640, 1000), (368, 12288, 4096), (513, 128, 256), (1030, 320, 320),
+]
+
+
+@pytest.mark.parametrize("M,I,K", SWIGLU_SHAPES)
+def test_linear_swiglu(lib, M, I, K):
+    run_swiglu(lib, M, I, K, seed=3 * M + I + K)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_linear_swiglu_tensor_core_at_tiny_m(lib, M):
+    run_swiglu(lib, M, 768, 1024, seed=60 + M, gemv_max_m=0)
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7, 50, 333])
+def test_linear_swiglu_forced_grid(lib, grid):
+    """Split tiles summed by the reduce kernel, which applies the activation itself."""
+    run_swiglu(lib, 24, 512, 1536, seed=120 + grid, gemv_max_m=0, grid=grid)
+    run_swiglu(lib, 300, 640, 1000, seed=121 + grid, gemv_max_m=0, grid=grid)
+
+
+def test_linear_swiglu_matches_unfused_pair(lib):
+    """Same rows as spec_verify_linear on the split layout followed by spec_silu_mul, up to
+    the bf16 rounding of gate and up that only the unfused pair does."""
+    M, I, K = 9, 1024, 512
+    X = bf16_dev(synth.normal_bf16_bits(11, (M, K), 1.0))
+    Wg = bf16_dev(synth.normal_bf16_bits(12, (I, K), 0.05))
+    Wu = bf16_dev(synth.normal_bf16_bits(13, (I, K), 0.05))
+    import torch
+    GU = lib.spec_verify_linear(X, torch.cat((Wg, Wu), 0))
+    A0 = lib.spec_silu_mul(GU)
+    A1 = lib.spec_verify_linear_swiglu(X, lib.interleave_gate_up(Wg, Wu))
+    lib.spec_device_status()
+    assert_close_rel(f64_of_bf16(A1), f64_of_bf16(A0), "fused vs unfused", rel=2e-2)
+
+
+def test_linear_swiglu_strided_output_and_launches(lib):
+    """Output into a column slice of a wider buffer; one launch (two when tiles are split)."""
+    import torch
+    M, I, K = 40, 1024, 512
+    X = synth.normal_bf16_bits(21, (M, K), 1.0)
+    Wg = synth.normal_bf16_bits(22, (I, K), 0.05)
+    Wu = synth.normal_bf16_bits(23, (I, K), 0.05)
+    buf = torch.zeros((M, I + 64), dtype=torch.bfloat16, device="cuda")
+    lib.reset_launch_count()
+    lib.spec_verify_linear_swiglu(bf16_dev(X), lib.interleave_gate_up(bf16_dev(Wg), bf16_dev(Wu)),
+                                  A=buf[:, 64:])
+    lib.spec_device_status()
+    assert lib.launch_count() == (2 if lib.spec_swiglu_linear_workspace_bytes(M, I, K) > 0 else 1)
+    x = obf.decode(X)
+    ref = oops.silu_mul(oops.linear(x, obf.decode(Wg)), oops.linear(x, obf.decode(Wu)))
+    assert_close_rel(f64_of_bf16(buf[:, 64:]), ref, "swiglu strided")
+    assert torch.count_nonzero(buf[:, :64]).item() == 0
+
+
+@pytest.mark.parametrize("M,I,K", [(1, 1024, 512), (3, 1024, 512), (4, 12288, 4096), (9, 1024, 512)])
+def test_linear_swiglu_leaves_counter_region_zero(lib, M, I, K):
+    """The first 64 KiB of a workspace are counters that every kernel finds zero and leaves
+    zero; the fused call's scratch lives elsewhere."""
+    import torch
+    ws = lib.Workspace()
+    ws.ensure(max(lib.spec_swiglu_linear_workspace_bytes(M, I, K), 1 << 17))
+    ws.buf.zero_()
+    X = bf16_dev(synth.normal_bf16_bits(31, (M, K), 1.0))
+    Wgu = bf16_dev(synth.normal_bf16_bits(32, (2 * I, K), 0.05))
+    lib.spec_verify_linear_swiglu(X, Wgu, ws=ws)
+    lib.spec_device_status()
+    assert torch.count_nonzero(ws.buf[:1 << 16]).item() == 0

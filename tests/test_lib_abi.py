@@ -60,6 +60,12 @@ def test_host_side_validation(built):
     assert L.spec_verify_linear(odd, 4, 64, 64, fake, 128, 64, fake, 128, None, 0, None, 0, None) == E
     # M = 0 is a no-op that succeeds without touching anything
     assert L.spec_verify_linear(None, 0, 64, 64, None, 128, 64, None, 128, None, 0, None, 0, None) == 0
+    # fused SwiGLU linear: I must be a multiple of 64, A's leading dimension at least I
+    assert L.spec_verify_linear_swiglu(fake, 4, 64, 64, fake, 64, 96, fake, 96, None, 0, None) == E
+    assert b"multiple of 64" in L.spec_last_error()
+    assert L.spec_verify_linear_swiglu(fake, 4, 64, 64, fake, 64, 128, fake, 64, None, 0, None) == E
+    assert L.spec_verify_linear_swiglu(odd, 4, 64, 64, fake, 64, 128, fake, 128, None, 0, None) == E
+    assert L.spec_verify_linear_swiglu(None, 0, 64, 64, None, 64, 128, None, 128, None, 0, None) == 0
     # attention: unsupported head dim, too many rows per kv head
     args = [fake, 32 * 64, fake, fake, 8 * 64, fake, fake, 2, 5, fake, fake, 64, 32, 8, 64, 0.1, fake,
             32 * 64, None, 0, None]
@@ -95,3 +101,28 @@ def test_workspace_queries_are_host_only(built):
     assert S.spec_attention_workspace_bytes(8, 5, 32, 8, 128, 4101) > 64 * 1024
     assert S.spec_lmhead_workspace_bytes(40, 4096, 151936) >= 64 * 1024 + 40 * 1187 * 8
     assert S.spec_linear_workspace_bytes(0, 4096, 4096) == 0
+
+
+def test_gate_up_interleave_layout(built):
+    """Rows 32 j .. 32 j + 15 are gate rows 16 j .., the next 16 the matching up rows; the
+    engine's in-place relayout goes there and back."""
+    import torch
+    from speculative_decoding_verify_05_gb300 import binding as S, engine as E
+    I, K = 192, 8
+    Wg = torch.arange(I * K, dtype=torch.float32).reshape(I, K).to(torch.bfloat16)
+    Wu = -torch.arange(I * K, dtype=torch.float32).reshape(I, K).to(torch.bfloat16) - 1
+    Wgu = S.interleave_gate_up(Wg, Wu)
+    assert Wgu.shape == (2 * I, K)
+    for j in range(I // 16):
+        assert torch.equal(Wgu[32 * j:32 * j + 16], Wg[16 * j:16 * j + 16])
+        assert torch.equal(Wgu[32 * j + 16:32 * j + 32], Wu[16 * j:16 * j + 16])
+    split = torch.cat((Wg, Wu), 0)
+    lw = E.LayerW(None, None, split.clone(), None, None, None)
+    E.set_gu_layout(lw, "interleaved")
+    assert torch.equal(lw.w_gu, Wgu) and lw.gu_layout == "interleaved"
+    E.set_gu_layout(lw, "interleaved")            # idempotent
+    assert torch.equal(lw.w_gu, Wgu)
+    E.set_gu_layout(lw, "split")
+    assert torch.equal(lw.w_gu, split) and lw.gu_layout == "split"
+    with pytest.raises(ValueError):
+        S.interleave_gate_up(Wg[:100], Wu[:100])
