@@ -677,10 +677,18 @@ def main():
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")
     ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")
+    ap.add_argument("--set", action="append", default=[], metavar="NAME=VALUE",
+                    help="library knob passed to spec_set_option before the run (repeatable)")
     ap.add_argument("--swiglu", choices=["fused", "split"], default="fused",
                     help="SwiGLU in the gate|up GEMM epilogue (fused) or as its own kernel (split)")
     ap.add_argument("--nsub", type=int, default=0, help="linear_nsub knob for --profile linear/lmhead (0: library default)")
     args = ap.parse_args()
+    if args.set and args.impl == "ours":
+        from speculative_decoding_verify_05_gb300 import binding as S
+        for kv in args.set:
+            name, _, value = kv.partition("=")
+            if S._lib.spec_set_option(name.encode(), int(value)) != 0:
+                ap.error(f"--set {kv}: {S._lib.spec_last_error().decode()}")
     if args.profile:
         run_profile_case(args)
         return

@@ -93,7 +93,10 @@ SPEC_API int spec_version(void);
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
  * and sum the pieces on chip; "lmhead_nsub" (1 default, or 2): the LM head's
- * tensor-core tiles cover up to 256 or 512 rows; "pdl" (1 default, 0 off):
+ * tensor-core tiles cover up to 256 or 512 rows; "linear_multicast" (1 =
+ * off, default; 2 or 4): the persistent tensor-core GEMM runs clusters of up
+ * to that many CTAs on adjacent weight tiles, each token tile loaded once per
+ * cluster (TMA multicast); "pdl" (1 default, 0 off):
  * kernels are launched with programmatic dependent launch, so each one's
  * launch and on-chip setup overlap the end of the kernel before it on the
  * stream (every kernel still waits for that kernel before touching memory).

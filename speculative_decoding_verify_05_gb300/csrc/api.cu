@@ -106,13 +106,19 @@ int get_encoder() {
 }
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, rank-1 entries)
+int g_w_promotion = 2;    // tunable: L2 promotion of weight-tile loads (0 none, 1 64 B, 2 128 B, 3 256 B)
+
 int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+                const cuuint64_t* strides, const cuuint32_t* box, const char* what,
+                int promotion = 3) {
   if (int rc = get_encoder()) return rc;
   cuuint32_t estr[3] = {1, 1, 1};
+  static const CUtensorMapL2promotion kPromo[4] = {
+      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_SWIZZLE_128B, kPromo[promotion & 3],
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPEC_ECUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
   return SPEC_OK;
@@ -135,12 +141,15 @@ int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
 int g_lmhead_nsub = 1;   // tunable: the LM head's tiles cover up to 256 (1) or 512 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
+int g_linear_mc = 1;     // tunable: largest cluster that shares token tiles by TMA multicast
 
 struct LinPlan {
   bool gemv = false;
   int BN = 16, NSUB = 1, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
-  int grid = 1;                 // persistent CTAs of the tensor-core path
+  int grid = 1;                 // persistent work groups of the tensor-core path (clusters of cl CTAs)
+  int cl = 1;                   // CTAs per cluster sharing each token tile (TMA multicast)
   int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
+  int x_box_rows() const { return cl > 1 ? BN * NSUB / cl : BN; }   // token rows per TMA load
   bool aligned = false;         // whole tiles only (no stream-K region)
   long long dp_tiles = 0, sk_units = 0;
   long long units = 0;
@@ -217,17 +226,33 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
       return p;
     }
   }
-  int grid = g_force_grid > 0 ? g_force_grid : sms;
-  const long long cap_units = p.aligned ? tiles : p.units;
+  // token tiles of 64+ rows (as many bytes per k-step as half a weight tile or more): clusters
+  // of cl CTAs take cl adjacent weight tiles in lockstep and load each token tile once for all
+  // of them (TMA multicast), which cuts the L2 -> SM traffic that otherwise dominates
+  int cl_cap = 0;
+  if (TN >= 64)
+    for (int c = g_linear_mc; c >= 2; c /= 2) {
+      if (TN % (8 * c) != 0 || p.tiles_n < c) continue;
+      const int cap = linear_tc_cluster_capacity(p.BN, p.NSUB, c);
+      if (cap < 1) continue;
+      p.cl = c;
+      cl_cap = cap;
+      break;
+    }
+  const long long ctiles = (long long)p.tiles_m * ((p.tiles_n + p.cl - 1) / p.cl);
+  p.units = ctiles * p.k_tiles;
+  int grid = g_force_grid > 0 ? g_force_grid : (p.cl > 1 ? std::min(cl_cap, sms / p.cl) : sms);
+  const long long cap_units = p.aligned ? ctiles : p.units;
   if (grid > cap_units) grid = (int)cap_units;
   p.grid = std::max(1, grid);
-  // data-parallel tiles first (every CTA gets as many whole tiles as all can), stream-K for the rest
+  // data-parallel tiles first (every group gets as many whole cluster tiles as all can), stream-K
+  // for the rest
   if (p.aligned) {
-    p.dp_tiles = tiles;
+    p.dp_tiles = ctiles;
     p.sk_units = 0;
   } else {
-    p.dp_tiles = tiles / p.grid * p.grid;
-    p.sk_units = (tiles - p.dp_tiles) * p.k_tiles;
+    p.dp_tiles = ctiles / p.grid * p.grid;
+    p.sk_units = (ctiles - p.dp_tiles) * p.k_tiles;
   }
   if (lmhead) {
     p.bytes = kCounterBytes + round_up(size_t(M) * p.tiles_n * sizeof(float2), 256);
@@ -235,7 +260,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   }
   bool split = false;
   for (int c = 1; c < p.grid && !split && p.sk_units > 0; ++c) split = ((p.sk_units * c / p.grid) % p.k_tiles) != 0;
-  p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * 2 * TN * 128 * 4, 256) : 0;
+  p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * p.cl * 2 * TN * 128 * 4, 256) : 0;
   return p;
 }
 
@@ -291,6 +316,16 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "pdl must be 0 or 1");
     g_pdl = value;
+    return ok();
+  }
+  if (!strcmp(name, "weight_l2_promotion")) {
+    if (value < 0 || value > 3) return fail(SPEC_EINVAL, "weight_l2_promotion must be in [0, 3]");
+    g_w_promotion = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_multicast")) {
+    if (value != 1 && value != 2 && value != 4) return fail(SPEC_EINVAL, "linear_multicast must be 1, 2 or 4");
+    g_linear_mc = value;
     return ok();
   }
   if (!strcmp(name, "lmhead_nsub")) {
@@ -396,17 +431,17 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
     cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W")) return rc;
+    if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W", g_w_promotion)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
     if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
@@ -417,7 +452,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch");
     return ok(1);
   }
-  dim3 grid(p.grid);
+  dim3 grid(p.grid * p.cl);
   cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
   if (p.bytes == 0) return ok(1);
@@ -480,23 +515,23 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
     cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, Wgu, 2, dims, str, box, "Wgu")) return rc;
+    if (int rc = encode_bf16(&tw, Wgu, 2, dims, str, box, "Wgu", g_w_promotion)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
     if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.Y = A; a.ldy = lda; a.residual = nullptr; a.ldr = 0;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
-  cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid), s);
+  cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid * p.cl), s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 swiglu linear launch");
   if (p.bytes == 0) return ok(1);
   e = launch_linear_reduce(a, plan_sms(), s);
@@ -533,23 +568,23 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)V};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, Wlm, 2, dims, str, box, "Wlm")) return rc;
+    if (int rc = encode_bf16(&tw, Wlm, 2, dims, str, box, "Wlm", g_w_promotion)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.BN};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
     if (int rc = encode_bf16(&tx, H, 2, dims, str, box, "H")) return rc;
   }
   const bool greedy = temperature == 0.f;
   LinearArgs a{};
   a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = P;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
-  dim3 grid(p.grid);
+  dim3 grid(p.grid * p.cl);
   cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   e = launch_lmhead_normalize(P, a.stats, M, V, p.tiles_n, greedy, s);

@@ -33,11 +33,37 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Same, as clusters of `cluster` CTAs along x when cluster > 1 (grid counts CTAs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---- tcgen05 GEMM: NSUB sub-tiles of BN verify rows per CTA tile
 //      (NSUB = 1: BN = 16..256 step 16; NSUB = 2: BN = 144..256 step 16)
 constexpr int kMaxBN = 256;
 int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
+// Clusters of cl CTAs of the persistent GEMM that fit on the device at once (0: none / unknown).
+int linear_tc_cluster_capacity(int BN, int NSUB, int cl);
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_linear_tc_swiglu(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,

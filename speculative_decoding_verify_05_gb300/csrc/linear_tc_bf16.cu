@@ -4,24 +4,6 @@
 
 namespace spec {
 
-template <int BN, int NSUB, int EPI>
-static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a,
-                              dim3 grid, cudaStream_t st) {
-  using Cfg = LinearCfg<BN, NSUB>;
-  constexpr int smem = Cfg::SMEM_BYTES;
-  static bool configured[64] = {};   // per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<BN, NSUB, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
-  cudaError_t e = launch_k(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), smem, st, tw, tx, a);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
 int linear_tc_smem_bytes(int BN, int NSUB) {
   switch (NSUB * 1000 + BN) {
     case 1016: return LinearCfg<16, 1>::SMEM_BYTES;
@@ -54,42 +36,65 @@ int linear_tc_smem_bytes(int BN, int NSUB) {
 
 bool linear_tc_supported(int BN, int NSUB) { return linear_tc_smem_bytes(BN, NSUB) > 0; }
 
+int linear_tc_cluster_capacity(int BN, int NSUB, int cl) {
+  if (cl < 2 || cl > 8 || BN % 16 || BN < 16 || BN > 256 || NSUB < 1 || NSUB > 2) return 0;
+  static int cache[64][3][17][9];   // [device][NSUB][BN / 16][cl]: clusters + 1, 0 = not asked yet
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (cacheable && cache[dev][NSUB][BN / 16][cl] != 0) return cache[dev][NSUB][BN / 16][cl] - 1;
+  int n = 0;
+  switch (NSUB * 1000 + BN) {
+#define X(ns, bn) \
+  case ns * 1000 + bn: n = linear_tc_clusters_resident<bn, ns, EPI_BF16>(cl); break;
+    X(1, 16) X(1, 32) X(1, 48) X(1, 64) X(1, 80) X(1, 96) X(1, 112) X(1, 128) X(1, 144) X(1, 160)
+    X(1, 176) X(1, 192) X(1, 208) X(1, 224) X(1, 240) X(1, 256)
+    X(2, 144) X(2, 160) X(2, 176) X(2, 192) X(2, 208) X(2, 224) X(2, 240) X(2, 256)
+#undef X
+    default: n = 0;
+  }
+  if (cacheable) cache[dev][NSUB][BN / 16][cl] = n + 1;
+  return n;
+}
+
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s) {
   switch (NSUB * 1000 + BN) {
-    case 1016: return launch_one<16, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1032: return launch_one<32, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1048: return launch_one<48, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1064: return launch_one<64, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1080: return launch_one<80, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1096: return launch_one<96, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1112: return launch_one<112, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1128: return launch_one<128, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1144: return launch_one<144, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1160: return launch_one<160, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1176: return launch_one<176, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1192: return launch_one<192, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1208: return launch_one<208, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1224: return launch_one<224, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1240: return launch_one<240, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 1256: return launch_one<256, 1, EPI_BF16>(tw, tx, a, grid, s);
-    case 2144: return launch_one<144, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2160: return launch_one<160, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2176: return launch_one<176, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2192: return launch_one<192, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2208: return launch_one<208, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2224: return launch_one<224, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2240: return launch_one<240, 2, EPI_BF16>(tw, tx, a, grid, s);
-    case 2256: return launch_one<256, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 1016: return launch_linear_tc_one<16, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1032: return launch_linear_tc_one<32, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1048: return launch_linear_tc_one<48, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1064: return launch_linear_tc_one<64, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1080: return launch_linear_tc_one<80, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1096: return launch_linear_tc_one<96, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1112: return launch_linear_tc_one<112, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1128: return launch_linear_tc_one<128, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1144: return launch_linear_tc_one<144, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1160: return launch_linear_tc_one<160, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1176: return launch_linear_tc_one<176, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1192: return launch_linear_tc_one<192, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1208: return launch_linear_tc_one<208, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1224: return launch_linear_tc_one<224, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1240: return launch_linear_tc_one<240, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 1256: return launch_linear_tc_one<256, 1, EPI_BF16>(tw, tx, a, grid, s);
+    case 2144: return launch_linear_tc_one<144, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2160: return launch_linear_tc_one<160, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2176: return launch_linear_tc_one<176, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2192: return launch_linear_tc_one<192, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2208: return launch_linear_tc_one<208, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2224: return launch_linear_tc_one<224, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2240: return launch_linear_tc_one<240, 2, EPI_BF16>(tw, tx, a, grid, s);
+    case 2256: return launch_linear_tc_one<256, 2, EPI_BF16>(tw, tx, a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// Second pass of a split GEMM.  Every block first tabulates where each CTA's stream-K range
-// starts (beg[c] = sk_units * c / grid, one 64-bit division per entry; unit u is k-step u % kt of
-// tile dp_tiles + u / kt).  A tile is split iff a range starts strictly inside it; the first such
-// range c names the tile, whose pieces came from CTAs c - 1 .. hi (the last range starting inside it).  Warp item = (c, 8 token
-// columns); lane l owns weight rows n0 + 4 l .. + 3 (one float4 per column of a piece).
+// Second pass of a split GEMM.  Every block first tabulates where each work group's stream-K
+// range starts (beg[c] = sk_units * c / grid, one 64-bit division per entry; unit u is k-step
+// u % kt of cluster tile dp_tiles + u / kt).  A cluster tile is split iff a range starts strictly
+// inside it; the first such range c names it, and its pieces came from groups c - 1 .. hi (the
+// last range starting inside it): rank r of each of those clusters left the piece of weight tile
+// (t / tiles_m) cl + r.  Warp item = (c, r, 8 token columns); lane l owns weight rows
+// n0 + 4 l .. + 3 (one float4 per column of a piece).
 // Pieces are summed in CTA order, two contributors' loads in flight at a time, then the
 // residual is added and the sum rounded to bf16.  Launched as one wave (grid-stride over items).
 __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs a) {
@@ -113,19 +118,23 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
     s_hi[c] = hi;
   }
   __syncthreads();
+  const int CL = a.cl > 1 ? a.cl : 1;
   const int cols8 = (TN + 7) / 8;
-  const long long items = (long long)G * cols8;
+  const long long items = (long long)G * CL * cols8;
   const int lane = threadIdx.x & 31;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
-    const int c = (int)(it / cols8);
+    const int cr = (int)(it / cols8);
+    const int c = cr / CL, r = cr - c * CL;
     const int hi = s_hi[c];
     if (hi < 0) continue;
-    const int j0 = (int)(it - (long long)c * cols8) * 8;
+    const int j0 = (int)(it - (long long)cr * cols8) * 8;
     const long long t0 = s_beg[c] / kt * kt;
-    const long long tile = a.dp_tiles + t0 / kt;
-    const int m0 = (int)(tile % a.tiles_m) * TN + j0;
-    const int n4 = (int)(tile / a.tiles_m) * 128 + lane * 4;
+    const long long ctile = a.dp_tiles + t0 / kt;
+    const int n_t = (int)(ctile / a.tiles_m) * CL + r;
+    if (n_t >= a.tiles_n) continue;
+    const int m0 = (int)(ctile % a.tiles_m) * TN + j0;
+    const int n4 = n_t * 128 + lane * 4;
     float4 acc[8];
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
         // slot 0 holds the piece that opens a CTA's stream-K range: the tile's iff the range starts
         // inside it; a CTA with an empty range (fewer stream-K units than CTAs) left nothing
         const float* base = (cc <= hi && s_beg[cc] < s_beg[cc + 1])
-                                ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
+                                ? a.partial + ((size_t)(cc * CL + r) * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
                                 : nullptr;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
       // gate and up rows interleaved in blocks of 16: lane L holds rows 4L .. 4L + 3, gate rows
       // when L % 8 < 4, and lane L + 4 holds the matching up rows
       const bool gate = (lane & 7) < 4;
-      const int n = (int)(tile / a.tiles_m) * 64 + (lane >> 3) * 16 + (lane & 3) * 4;
+      const int n = n_t * 64 + (lane >> 3) * 16 + (lane & 3) * 4;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float u0 = __shfl_down_sync(0xffffffffu, acc[jj].x, 4), u1 = __shfl_down_sync(0xffffffffu, acc[jj].y, 4);
@@ -204,7 +213,7 @@ cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   // one wave: two 256-thread blocks per SM (register budget), grid-stride over the items
-  const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
+  const long long warps = (long long)a.grid * (a.cl > 1 ? a.cl : 1) * ((a.tn + 7) / 8);
   long long blocks = (warps + 7) / 8;
   if (blocks > 2LL * sms) blocks = 2LL * sms;
   cudaError_t e = launch_k(linear_reduce_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), smem, s, a);

@@ -91,6 +91,8 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"attention_pair_cost", 65) == E
     assert L.spec_set_option(b"attention_pair_cost", -1) == E
     assert L.spec_set_option(b"attention_pair_cost", 8) == 0
+    assert L.spec_set_option(b"linear_multicast", 3) == E
+    assert L.spec_set_option(b"linear_multicast", 4) == 0
 
 
 def test_workspace_queries_are_host_only(built):
