@@ -152,7 +152,7 @@ def reference_runs_here() -> bool:
 
 
 # --------------------------------------------------------------------------- GPU arm
-def build_round(dev, rank, S, E, synth, fused_swiglu=True):
+def build_round(dev, rank, S, E, synth, fused_swiglu=True, fused_sampler=True):
     """Resident state of the benchmark round (weights, KV caches, inputs, draft distribution)
     and a function that runs one full verify round on it."""
     import torch
@@ -174,7 +174,7 @@ def build_round(dev, rank, S, E, synth, fused_swiglu=True):
         kcs.append(k)
         vcs.append(v)
     eng = E.VerifyEngine(dims, sw, kcs, vcs, max_M=batch.M, max_rows=batch.max_rows, device=dev,
-                         fused_swiglu=fused_swiglu)
+                         fused_swiglu=fused_swiglu, fused_sampler=fused_sampler)
     x0 = torch.empty((batch.M, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
     cu = torch.from_numpy(batch.cu_rows).to(dev)
     ctx = torch.from_numpy(batch.ctx_len).to(dev)
@@ -218,7 +218,8 @@ def run_gpu(args):
     import synth
 
     hbm_peak, tc_peak, tc_sust, peak_src = peaks()
-    st = build_round(dev, rank, S, E, synth, fused_swiglu=args.swiglu == "fused")
+    st = build_round(dev, rank, S, E, synth, fused_swiglu=args.swiglu == "fused",
+                     fused_sampler=args.sampler == "fused")
     dims, batch, cap, sw, kcs, vcs, eng = (st[k] for k in ("dims", "batch", "cap", "sw", "kcs", "vcs", "eng"))
     x0, cu, ctx, q, drafts, out, step = (st[k] for k in ("x0", "cu", "ctx", "q", "drafts", "out", "step"))
     S.reset_launch_count()
@@ -274,7 +275,8 @@ def run_gpu(args):
     round_gbs = (lin_w + kv + head) / (ms / 1e3) / 1e9
 
     # ---- per-kernel timing (eager, CUDA events on the launching stream)
-    per = kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src)
+    per = kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src,
+                         sampler_inputs=(q, drafts, st["U"], out))
 
     # ---- weight-read amortisation of the linear stack: M = 5 verify vs M = 1 decode
     lin = linear_stack_ratio(eng, dims, S, hbm_peak, peak_src)
@@ -318,7 +320,8 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src, reps=3):
+def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src, reps=3,
+                   sampler_inputs=None):
     """Average launch time of each hot kernel over all 36 layers (eager, CUDA events)."""
     import torch
     M = batch.M
@@ -393,13 +396,31 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
         S.spec_lmhead_softmax(h, eng.w.w_lm, TEMP, P=eng.P[:M], ws=eng.ws)
     t_head = timeit(head, 1)
     hb = 2.0 * dims.V * dims.d + 3.0 * M * dims.V * 4
-    res["lmhead_softmax"] = {"avg_launch_us": t_head * 1e3, "launches_per_round": 2, "total_ms": t_head,
+    res["lmhead_softmax"] = {"avg_launch_us": t_head * 1e3, "launches_per_round": 0 if eng.fused_sampler else 2,
+                             "total_ms": 0.0 if eng.fused_sampler else t_head,
                              "roofline": {"kernel": "lmhead_softmax", "bound": "hbm",
                                           "achieved": hb / (t_head / 1e3) / 1e9, "peak": hbm_peak,
                                           "unit": "GB/s", "frac": hb / (t_head / 1e3) / 1e9 / hbm_peak,
                                           "traffic": None, "algorithmic_bytes": hb,
                                           "tflops": 2.0 * M * dims.V * dims.d / (t_head / 1e3) / 1e12,
                                           "peak_source": f"{peak_src} hbm_gbs"}}
+    if sampler_inputs is not None:
+        q, drafts, U, out = sampler_inputs
+        B = cu.numel() - 1
+
+        def fused():
+            S.spec_lmhead_reject_sample(h, eng.w.w_lm, TEMP, q, drafts, U, cu, out=out, ws=eng.ws)
+        t_f = timeit(fused, 1)
+        # weights + logits written once + the final rows' logits and q read back by the sampler
+        fb = 2.0 * dims.V * dims.d + 1.0 * M * dims.V * 4 + 2.0 * B * dims.V * 4
+        res["lmhead_reject_sample"] = {
+            "avg_launch_us": t_f * 1e3, "launches_per_round": 2 if eng.fused_sampler else 0,
+            "total_ms": t_f if eng.fused_sampler else 0.0,
+            "roofline": {"kernel": "lmhead_reject_sample (fused)", "bound": "hbm",
+                         "achieved": fb / (t_f / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": fb / (t_f / 1e3) / 1e9 / hbm_peak, "traffic": None, "algorithmic_bytes": fb,
+                         "tflops": 2.0 * M * dims.V * dims.d / (t_f / 1e3) / 1e12,
+                         "peak_source": f"{peak_src} hbm_gbs"}}
     return res
 
 
@@ -624,7 +645,8 @@ def run_profile_case(args):
     if args.profile == "round":
         # the benchmark's full verify round, run eagerly: once to warm up, then once inside
         # the NVTX range "round" (ncu --nvtx --nvtx-include "round/" lists only that one)
-        st = build_round(dev, 0, S, E, synth, fused_swiglu=args.swiglu == "fused")
+        st = build_round(dev, 0, S, E, synth, fused_swiglu=args.swiglu == "fused",
+                         fused_sampler=args.sampler == "fused")
         st["step"]()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("round")
@@ -679,6 +701,8 @@ def main():
     ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")
     ap.add_argument("--set", action="append", default=[], metavar="NAME=VALUE",
                     help="library knob passed to spec_set_option before the run (repeatable)")
+    ap.add_argument("--sampler", choices=["fused", "split"], default="fused",
+                    help="LM head -> sampler in one call without materialising p (fused), or softmax + sampler")
     ap.add_argument("--swiglu", choices=["fused", "split"], default="fused",
                     help="SwiGLU in the gate|up GEMM epilogue (fused) or as its own kernel (split)")
     ap.add_argument("--nsub", type=int, default=0, help="linear_nsub knob for --profile linear/lmhead (0: library default)")

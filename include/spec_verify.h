@@ -212,8 +212,8 @@ SPEC_API int spec_verify_attention(const spec_bf16* Q, int ldq,
  * ([P1] Algorithm 1).  Greedy ties go to the lowest token index.
  *   H   [M x K] bf16 (final-normed hidden states), W_lm [V x K] bf16
  *   P   [M x V] fp32 out
- * Requires V % 128 == 0, K % 8 == 0, temperature >= 0.
- * Workspace: spec_lmhead_workspace_bytes. */
+ * Requires V % 4 == 0, K % 8 == 0, temperature >= 0; H row-major with leading
+ * dimension K.  Workspace: spec_lmhead_workspace_bytes. */
 SPEC_API size_t spec_lmhead_workspace_bytes(int M, int K, int V);
 SPEC_API int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
                         float temperature, float* P,
@@ -243,6 +243,30 @@ SPEC_API int spec_reject_sample(const float* P, const float* Q, const int32_t* d
                        const float* U, const int32_t* cu_rows, int B, int V,
                        float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
                        spec_stream stream);
+
+/* Fused LM head -> sampler: the same n_acc / out_tok / near_tie as
+ * spec_lmhead_softmax followed by spec_reject_sample on the same inputs (bit
+ * for bit), without materialising p.  The acceptance test needs p_i(x_i) only
+ * at the draft token and the row's softmax normaliser ([P1] Algorithm 1, the
+ * accept step), and only the final row's full distribution is read; so the
+ * GEMM writes z / T and per-tile (max, sum e^z) statistics into the workspace,
+ * and the sampler evaluates p_x = e^(z_x - max) / sum for the entries it reads
+ * (a one-hot at the argmax when temperature == 0, where no logits are stored).
+ * The normalisation pass and the M x V probability write / read go away.
+ *   H [M x K] bf16, W_lm [V x K] bf16; the M verify rows are the rows that
+ *   cu_rows [B + 1] packs (cu_rows[B] <= M is checked on the device: a
+ *   sequence outside the M rows is skipped and the status word set);
+ *   Q, draft_tok, U, tie_eps, n_acc, out_tok, near_tie as for
+ *   spec_reject_sample.
+ * Requires K % 8 == 0, V % 4 == 0, V <= 1048576, temperature >= 0, M >= B.
+ * Workspace: spec_lmhead_sample_workspace_bytes (the logits, M x V x 4 bytes,
+ * plus statistics; statistics only when temperature == 0). */
+SPEC_API size_t spec_lmhead_sample_workspace_bytes(int M, int K, int V, float temperature);
+SPEC_API int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                                       float temperature, const float* Q, const int32_t* draft_tok,
+                                       const float* U, const int32_t* cu_rows, int B, float tie_eps,
+                                       int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                                       void* workspace, size_t workspace_bytes, spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Layer glue of the decoder stack (not on the pages: the stack's layout is  */

@@ -38,6 +38,9 @@ _SIGS = {
     "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "spec_reject_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _vp, _vp, _vp, _vp]),
+    "spec_lmhead_sample_workspace_bytes": (_sz, [_i, _i, _i, _f]),
+    "spec_lmhead_reject_sample": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _vp,
+                                       _vp, _sz, _vp]),
     "spec_rmsnorm": (_i, [_vp, _i, _i, _i, _vp, _f, _vp, _i, _vp]),
     "spec_rope": (_i, [_vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp]),
     "spec_silu_mul": (_i, [_vp, _i, _i, _i, _vp, _i, _vp]),
@@ -313,6 +316,36 @@ def spec_reject_sample(P, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5, out=N
             raise ValueError("sampler inputs must be contiguous")
     _check(_lib.spec_reject_sample(_p(P), _p(Q), _p(draft_tok), _p(U), _p(cu_rows), B, V,
                                    float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)), True)
+    return n_acc, out_tok, near
+
+
+def spec_lmhead_sample_workspace_bytes(M, K, V, temperature) -> int:
+    return _lib.spec_lmhead_sample_workspace_bytes(M, K, V, float(temperature))
+
+
+def spec_lmhead_reject_sample(H, W_lm, temperature: float, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5,
+                              out=None, ws: Workspace | None = None, stream=None):
+    """Fused LM head -> sampler; returns (n_acc [B], out_tok [M], near_tie [B]) int32 device tensors."""
+    _need(H, torch.bfloat16, "H"); _need(W_lm, torch.bfloat16, "W_lm")
+    _need(Q, torch.float32, "Q"); _need(U, torch.float32, "U")
+    _need(draft_tok, torch.int32, "draft_tok"); _need(cu_rows, torch.int32, "cu_rows")
+    M, K = H.shape
+    V = W_lm.shape[0]
+    if W_lm.shape[1] != K:
+        raise ValueError("W_lm must be [V, K]")
+    for t in (H, W_lm, Q, U, draft_tok, cu_rows):
+        if not t.is_contiguous():
+            raise ValueError("fused sampler inputs must be contiguous")
+    B = cu_rows.numel() - 1
+    if out is None:
+        dev = H.device
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(M, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    n_acc, out_tok, near = out
+    wp, wn = _ws_args(ws, spec_lmhead_sample_workspace_bytes(M, K, V, temperature), H.device)
+    _check(_lib.spec_lmhead_reject_sample(_p(H), M, K, _p(W_lm), V, float(temperature), _p(Q), _p(draft_tok),
+                                          _p(U), _p(cu_rows), B, float(tie_eps), _p(n_acc), _p(out_tok),
+                                          _p(near), wp, wn, _stream(stream)), True)
     return n_acc, out_tok, near
 
 

@@ -545,24 +545,11 @@ size_t spec_lmhead_workspace_bytes(int M, int K, int V) {
   return plan_linear(M, V, K, true).bytes;
 }
 
-int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
-                        float temperature, float* P, void* workspace, size_t workspace_bytes,
-                        spec_stream stream) {
-  if (M < 0 || K <= 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d", M, K, V);
-  if (M == 0) return ok();
-  if (!H || !Wlm || !P) return fail(SPEC_EINVAL, "H, Wlm and P must be non-NULL");
-  if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
-  if (V % 4) return fail(SPEC_EINVAL, "V=%d must be a multiple of 4", V);
-  if (!(temperature >= 0.f) || std::isinf(temperature))
-    return fail(SPEC_EINVAL, "temperature must be finite and >= 0");
-  if (!aligned16(H) || !aligned16(Wlm) || !aligned16(P))
-    return fail(SPEC_EINVAL, "H, Wlm, P must be 16-byte aligned");
-  LinPlan p = plan_linear(M, V, K, true);
-  if (!workspace || workspace_bytes < p.bytes)
-    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
-  DevInfo* d = nullptr;
-  if (int rc = dev_info(&d)) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The LM-head GEMM: z / T of every row into Z (T > 0) and per-128-token-tile statistics (max,
+// sum of exp; or max, argmax when T = 0) into the workspace after its counter region.
+static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+                              float* Z, void* workspace, const LinPlan& p, DevInfo* d, cudaStream_t s,
+                              float2** stats_out) {
   CUtensorMap tw, tx;
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)V};
@@ -582,13 +569,81 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
   a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
-  a.P = P;
+  a.P = Z;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
-  dim3 grid(p.grid * p.cl);
-  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, grid, s);
+  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid * p.cl), s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
-  e = launch_lmhead_normalize(P, a.stats, M, V, p.tiles_n, greedy, s);
+  *stats_out = a.stats;
+  return SPEC_OK;
+}
+
+static int check_lmhead_args(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature) {
+  if (!H || !Wlm) return fail(SPEC_EINVAL, "H and Wlm must be non-NULL");
+  if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
+  if (V % 4) return fail(SPEC_EINVAL, "V=%d must be a multiple of 4", V);
+  if (!(temperature >= 0.f) || std::isinf(temperature))
+    return fail(SPEC_EINVAL, "temperature must be finite and >= 0");
+  if (!aligned16(H) || !aligned16(Wlm)) return fail(SPEC_EINVAL, "H, Wlm must be 16-byte aligned");
+  (void)M;
+  return SPEC_OK;
+}
+
+int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                        float temperature, float* P, void* workspace, size_t workspace_bytes,
+                        spec_stream stream) {
+  if (M < 0 || K <= 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d", M, K, V);
+  if (M == 0) return ok();
+  if (int rc = check_lmhead_args(H, M, K, Wlm, V, temperature)) return rc;
+  if (!P) return fail(SPEC_EINVAL, "P must be non-NULL");
+  if (!aligned16(P)) return fail(SPEC_EINVAL, "P must be 16-byte aligned");
+  LinPlan p = plan_linear(M, V, K, true);
+  if (!workspace || workspace_bytes < p.bytes)
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float2* stats = nullptr;
+  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, P, workspace, p, d, s, &stats)) return rc;
+  cudaError_t e = launch_lmhead_normalize(P, stats, M, V, p.tiles_n, temperature == 0.f, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head normalize launch");
+  return ok(2);
+}
+
+// --------------------------------------------------------------------------- fused LM head -> sampler
+// Workspace: counters + per-tile statistics, then (T > 0) the logits z / T [M x V] fp32.
+static size_t fused_logits_off(const LinPlan& p) { return round_up(p.bytes, 256); }
+
+size_t spec_lmhead_sample_workspace_bytes(int M, int K, int V, float temperature) {
+  if (M <= 0 || K <= 0 || V <= 0) return 0;
+  const LinPlan p = plan_linear(M, V, K, true);
+  return temperature == 0.f ? p.bytes : fused_logits_off(p) + round_up(size_t(M) * V * 4, 256);
+}
+
+int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+                              const float* Q, const int32_t* draft_tok, const float* U, const int32_t* cu_rows,
+                              int B, float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                              void* workspace, size_t workspace_bytes, spec_stream stream) {
+  if (M < 0 || K <= 0 || V <= 0 || B < 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d B=%d", M, K, V, B);
+  if (B == 0) return ok();
+  if (M < B) return fail(SPEC_EINVAL, "M=%d verify rows cannot hold B=%d sequences", M, B);
+  if (int rc = check_lmhead_args(H, M, K, Wlm, V, temperature)) return rc;
+  if (!Q || !draft_tok || !U || !cu_rows || !n_acc || !out_tok || !near_tie)
+    return fail(SPEC_EINVAL, "NULL argument");
+  if (!(tie_eps >= 0.f)) return fail(SPEC_EINVAL, "tie_eps must be >= 0");
+  if (V > (1 << 20)) return fail(SPEC_EUNSUPPORTED, "V=%d > 1048576", V);
+  const LinPlan p = plan_linear(M, V, K, true);
+  const size_t need = spec_lmhead_sample_workspace_bytes(M, K, V, temperature);
+  if (!workspace || workspace_bytes < need) return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool greedy = temperature == 0.f;
+  float* Z = greedy ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + fused_logits_off(p));
+  float2* stats = nullptr;
+  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, Z, workspace, p, d, s, &stats)) return rc;
+  cudaError_t e = launch_reject_sample_logits(Z, stats, p.tiles_n, greedy, Q, draft_tok, U, cu_rows, B, M, V,
+                                              tie_eps, n_acc, out_tok, near_tie, d->status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fused sampler launch");
   return ok(2);
 }
 

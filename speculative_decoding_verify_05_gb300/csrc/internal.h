@@ -131,6 +131,13 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
                                  const float* U, const int32_t* cu_rows, int B, int V,
                                  float tie_eps, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* near_tie, unsigned* status, cudaStream_t s);
+// Fused LM-head path: p from the logits Z = z / T [M x V] and the GEMM's per-tile statistics
+// stats [M][n_stats] (or the argmax statistics when greedy; Z unused).
+cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int n_stats, bool greedy,
+                                        const float* Q, const int32_t* draft, const float* U,
+                                        const int32_t* cu_rows, int B, int M, int V, float tie_eps,
+                                        int32_t* n_acc, int32_t* out_tok, int32_t* near_tie, unsigned* status,
+                                        cudaStream_t s);
 
 // ---- glue
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,

@@ -16,8 +16,18 @@
 //      rounding, far inside the near-tie band (tie_eps, 1e-5 by default), so a
 //      pick differs from an exact fp64 one only where it is counted as a near
 //      tie.  (An all-fp64 pass is ~2 fp64 FMA/clock/SM here: 0.3 ms a round.)
+//
+// The probabilities come either as a materialised p [M x V] (spec_reject_sample) or, for the
+// fused LM-head -> sampler path (spec_lmhead_reject_sample), as the LM head's logits z / T and
+// per-tile statistics: p_x = expf(z_x - max) * inv with the row's normaliser computed here by
+// the same code as the normalisation kernel (bit-identical p; one warp per row, 16 rows at a
+// time), or a one-hot row at the argmax when the temperature is 0.  Only the rows the sampler
+// reads are ever evaluated.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "lmhead_norm.cuh"
 
 namespace spec {
 namespace {
@@ -27,15 +37,39 @@ constexpr int PER_THREAD = 8;                              // consecutive tokens
 constexpr int TILE = SAMPLER_THREADS * PER_THREAD;         // 4096 tokens
 constexpr int MAX_TILES = 256;                             // V <= 1,048,576
 
+// Where a row's probabilities come from.
+enum { P_GIVEN = 0, P_LOGITS = 1, P_ARGMAX = 2 };
+struct RowP {
+  const float* v;   // P_GIVEN: the p row; P_LOGITS: the z / T row
+  float mx, inv;    // P_LOGITS: p_x = expf(z_x - mx) * inv
+  int am;           // P_ARGMAX: p_x = (x == am)
+};
+template <int MODE>
+__device__ __forceinline__ float p_at(const RowP& r, int x) {
+  if constexpr (MODE == P_GIVEN) return r.v[x];
+  else if constexpr (MODE == P_LOGITS) return expf(r.v[x] - r.mx) * r.inv;
+  else return x == r.am ? 1.f : 0.f;
+}
+
 // This thread's 8 consecutive weights of a tile: w = max(0, p - q) at a rejection (the sign is
 // exact in fp32; the value carries <= 2^-24 relative rounding), p itself for the bonus row or
 // when the residual is empty (`use_p`).  Tokens past V weigh 0.
-__device__ __forceinline__ void load_weights(const float* prow, const float* qrow, int x0, int V, bool use_p,
+template <int MODE>
+__device__ __forceinline__ void load_weights(const RowP& pr, const float* qrow, int x0, int V, bool use_p,
                                              bool vec, float* w) {
   if (vec && x0 + PER_THREAD <= V) {
-    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(prow + x0));
-    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(prow + x0 + 4));
-    w[0] = p0.x; w[1] = p0.y; w[2] = p0.z; w[3] = p0.w; w[4] = p1.x; w[5] = p1.y; w[6] = p1.z; w[7] = p1.w;
+    if constexpr (MODE == P_ARGMAX) {
+#pragma unroll
+      for (int e = 0; e < PER_THREAD; ++e) w[e] = (x0 + e == pr.am) ? 1.f : 0.f;
+    } else {
+      const float4 p0 = __ldcg(reinterpret_cast<const float4*>(pr.v + x0));
+      const float4 p1 = __ldcg(reinterpret_cast<const float4*>(pr.v + x0 + 4));
+      w[0] = p0.x; w[1] = p0.y; w[2] = p0.z; w[3] = p0.w; w[4] = p1.x; w[5] = p1.y; w[6] = p1.z; w[7] = p1.w;
+      if constexpr (MODE == P_LOGITS) {
+#pragma unroll
+        for (int e = 0; e < PER_THREAD; ++e) w[e] = expf(w[e] - pr.mx) * pr.inv;
+      }
+    }
     if (!use_p) {
       const float4 q0 = __ldcg(reinterpret_cast<const float4*>(qrow + x0));
       const float4 q1 = __ldcg(reinterpret_cast<const float4*>(qrow + x0 + 4));
@@ -50,19 +84,23 @@ __device__ __forceinline__ void load_weights(const float* prow, const float* qro
     const int x = x0 + e;
     float v = 0.f;
     if (x < V) {
-      v = prow[x];
+      v = p_at<MODE>(pr, x);
       if (!use_p) v = fmaxf(v - qrow[x], 0.f);
     }
     w[e] = v;
   }
 }
 
+// P: p [M x V] (P_GIVEN) or z / T [M x V] (P_LOGITS, unused for P_ARGMAX); stats: the LM head's
+// per-tile statistics [M][n_stats] (P_LOGITS, P_ARGMAX).
+template <int MODE>
 __global__ void __launch_bounds__(SAMPLER_THREADS)
-reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
+reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ stats, int n_stats,
+                     const float* __restrict__ Q,
                      const int32_t* __restrict__ draft, const float* __restrict__ U,
                      const int32_t* __restrict__ cu_rows, int V, float tie_eps,
                      int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tok,
-                     int32_t* __restrict__ near_tie, unsigned* status, int vec) {
+                     int32_t* __restrict__ near_tie, unsigned* status, int vec, int m_rows) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -70,6 +108,14 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
   const int warp = tid >> 5, lane = tid & 31;
   const int r0 = cu_rows[b];
   const int gamma = cu_rows[b + 1] - r0 - 1;
+  if (r0 < 0 || gamma < 0 || cu_rows[b + 1] > m_rows) {   // rows outside the verify pass's M rows
+    if (tid == 0) {
+      set_status(status, 0x3F1u);
+      n_acc[b] = 0;
+      near_tie[b] = 0;
+    }
+    return;
+  }
   const int q0 = r0 - b;
   const double eps = (double)tie_eps;
   const int n_tiles = (V + TILE - 1) / TILE;
@@ -79,12 +125,35 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
   __shared__ double s_tile_r[MAX_TILES], s_tile_p[MAX_TILES];
   __shared__ float s_part_r[MAX_TILES * (SAMPLER_THREADS / 32)], s_part_p[MAX_TILES * (SAMPLER_THREADS / 32)];
   __shared__ double s_wexcl[SAMPLER_THREADS / 32];
+  __shared__ float s_mx[32], s_inv[32];
+  __shared__ int s_am[32], s_done;
 
-  // ---- 1. acceptance tests (warp 0, 32 drafts per pass), exact in fp64
-  if (warp == 0) {
-    int n = gamma;
-    int near = 0;
-    for (int base = 0; base < gamma; base += 32) {
+  // ---- 1. acceptance tests, 32 drafts per pass (warp 0), exact in fp64; rows base .. base + 31
+  // (and the final row, which is one of them) get their normaliser first when p is not given
+  if (tid == 0) {
+    s_n = gamma;
+    s_near = 0;
+    s_done = 0;
+  }
+  __syncthreads();
+  int base = 0;
+  for (;; base += 32) {
+    const int rows = min(32, gamma + 1 - base);
+    // one warp per row: 16 rows at a time
+    if constexpr (MODE == P_LOGITS) {
+      for (int j = warp; j < rows; j += SAMPLER_THREADS / 32) {
+        float mx, inv;
+        lm_row_norm_warp(stats + (size_t)(r0 + base + j) * n_stats, n_stats, mx, inv);
+        if (lane == 0) { s_mx[j] = mx; s_inv[j] = inv; }
+      }
+    } else if constexpr (MODE == P_ARGMAX) {
+      for (int j = warp; j < rows; j += SAMPLER_THREADS / 32) {
+        const int am = lm_row_argmax_warp(stats + (size_t)(r0 + base + j) * n_stats, n_stats);
+        if (lane == 0) s_am[j] = am;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
       const int i = base + lane;
       bool reject = false, tie = false;
       if (i < gamma) {
@@ -93,7 +162,8 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
           set_status(status, 0x3F0u);
           x = x < 0 ? 0 : V - 1;
         }
-        const double p = (double)P[(size_t)(r0 + i) * V + x];
+        const RowP pr{P + (size_t)(r0 + i) * V, s_mx[lane], s_inv[lane], s_am[lane]};
+        const double p = (double)p_at<MODE>(pr, x);
         const double q = (double)Q[(size_t)(q0 + i) * V + x];
         const double uq = (double)U[r0 + i] * q;       // exact: 24 x 24 bit product
         reject = !(uq <= p);
@@ -101,25 +171,26 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
       }
       const unsigned rej = __ballot_sync(0xffffffffu, reject);
       const unsigned ties = __ballot_sync(0xffffffffu, tie);
-      if (rej) {
-        const int first = __ffs(rej) - 1;                 // decisions 0..first were taken
-        const unsigned taken = (first == 31) ? 0xffffffffu : ((1u << (first + 1)) - 1u);
-        near += __popc(ties & taken);
-        n = base + first;
-        break;
+      if (lane == 0) {
+        if (rej) {
+          const int first = __ffs(rej) - 1;                 // decisions 0..first were taken
+          const unsigned taken = (first == 31) ? 0xffffffffu : ((1u << (first + 1)) - 1u);
+          s_near += __popc(ties & taken);
+          s_n = base + first;
+          s_done = 1;
+        } else {
+          s_near += __popc(ties);
+          if (base + 32 > gamma) s_done = 1;             // every draft accepted: n = gamma
+        }
       }
-      near += __popc(ties);
     }
-    if (lane == 0) {
-      s_n = n;
-      s_near = near;
-    }
+    __syncthreads();
+    if (s_done) break;
   }
-  __syncthreads();
   const int n = s_n;
   const bool resid = n < gamma;
-  const float* prow = P + (size_t)(r0 + n) * V;
-  const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow;
+  const RowP prow{P + (size_t)(r0 + n) * V, s_mx[n - base], s_inv[n - base], s_am[n - base]};
+  const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow.v;
 
   // ---- 2. per-tile totals of the residual and of p (coalesced 16-byte loads, four tiles' loads in
   // flight per thread, no block barrier per tile), kept in fp64
@@ -133,12 +204,12 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
       if (t >= n_tiles) continue;
       const int x0 = t * TILE + tid * PER_THREAD;
       float pw[PER_THREAD];
-      load_weights(prow, qrow, x0, V, true, vec, pw);
+      load_weights<MODE>(prow, qrow, x0, V, true, vec, pw);
 #pragma unroll
       for (int e = 0; e < PER_THREAD; ++e) sp[k] += pw[e];
       if (resid) {
         float w[PER_THREAD];
-        load_weights(prow, qrow, x0, V, false, vec, w);
+        load_weights<MODE>(prow, qrow, x0, V, false, vec, w);
 #pragma unroll
         for (int e = 0; e < PER_THREAD; ++e) sr[k] += w[e];
       }
@@ -207,7 +278,7 @@ reject_sample_kernel(const float* __restrict__ P, const float* __restrict__ Q,
     const double thr = s_thr;
     const int x0 = tc * TILE + tid * PER_THREAD;
     float w[PER_THREAD];
-    load_weights(prow, qrow, x0, V, use_p, vec, w);
+    load_weights<MODE>(prow, qrow, x0, V, use_p, vec, w);
     float s = 0.f;
 #pragma unroll
     for (int e = 0; e < PER_THREAD; ++e) s += w[e];
@@ -286,8 +357,24 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
                                  float tie_eps, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* near_tie, unsigned* status, cudaStream_t s) {
   const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
-  cudaError_t e = launch_k(reject_sample_kernel, dim3(B), dim3(SAMPLER_THREADS), 0, s, P, Q, draft, U, cu_rows, V,
-                           tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0);
+  cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
+                           static_cast<const float2*>(nullptr), 0, Q, draft, U, cu_rows, V, tie_eps, n_acc,
+                           out_tok, near_tie, status, vec ? 1 : 0, INT_MAX);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int n_stats, bool greedy,
+                                        const float* Q, const int32_t* draft, const float* U,
+                                        const int32_t* cu_rows, int B, int M, int V, float tie_eps,
+                                        int32_t* n_acc, int32_t* out_tok, int32_t* near_tie, unsigned* status,
+                                        cudaStream_t s) {
+  const bool vec = V % 4 == 0 && (greedy || (reinterpret_cast<uintptr_t>(Z) & 15) == 0) &&
+                   (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
+  cudaError_t e = greedy
+      ? launch_k(reject_sample_kernel<P_ARGMAX>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q, draft,
+                 U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M)
+      : launch_k(reject_sample_kernel<P_LOGITS>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q, draft,
+                 U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -102,9 +102,11 @@ class VerifyEngine:
     """Buffers + call sequence of one verify pass / round for up to ``max_M`` rows."""
 
     def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, max_M: int, max_rows: int,
-                 device=None, fused_swiglu: bool = True):
+                 device=None, fused_swiglu: bool = True, fused_sampler: bool = True):
         self.dims = dims
         self.w = weights
+        # verify_round: LM head and sampler in one call that never materialises p
+        self.fused_sampler = fused_sampler
         self.fused_swiglu = fused_swiglu and dims.I % 64 == 0
         want = "interleaved" if self.fused_swiglu else "split"
         for lw in weights.layers:
@@ -135,6 +137,8 @@ class VerifyEngine:
             need = max(need, S.spec_attention_workspace_bytes(B, max_rows, dims.Hq, dims.Hkv, dims.D, cap))
         if weights.w_lm is not None:
             need = max(need, S.spec_lmhead_workspace_bytes(max_M, dims.d, dims.V))
+            if fused_sampler:
+                need = max(need, S.spec_lmhead_sample_workspace_bytes(max_M, dims.d, dims.V, 1.0))
         self.ws = S.Workspace(dev, need)
 
     # ------------------------------------------------------------------ one layer
@@ -158,9 +162,8 @@ class VerifyEngine:
             S.spec_silu_mul(self.gu[:M], A=a)
         S.spec_verify_linear(a, lw.w_down, Y=x, residual=x, ws=self.ws)
 
-    def verify_pass(self, x0, cu_rows, ctx_len, temperature: float, max_rows: int | None = None,
-                    n_layers: int | None = None):
-        """All layers + LM head over the packed rows; returns P [M, V] (fp32 view)."""
+    def _stack(self, x0, cu_rows, ctx_len, max_rows, n_layers):
+        """All layers and the final RMSNorm over the packed rows; the normed rows are in self.h."""
         M = x0.shape[0]
         B = cu_rows.numel() - 1
         max_rows = self.max_rows if max_rows is None else max_rows
@@ -171,13 +174,24 @@ class VerifyEngine:
         L = len(self.w.layers) if n_layers is None else n_layers
         for li in range(L):
             self.layer(li, M, cu_rows, ctx_len, B, max_rows)
+        if self.w.w_lm is not None:
+            S.spec_rmsnorm(self.x[:M], self.w.final_norm, self.dims.eps, Y=self.h[:M])
+        return M
+
+    def verify_pass(self, x0, cu_rows, ctx_len, temperature: float, max_rows: int | None = None,
+                    n_layers: int | None = None):
+        """All layers + LM head over the packed rows; returns P [M, V] (fp32 view)."""
+        M = self._stack(x0, cu_rows, ctx_len, max_rows, n_layers)
         if self.w.w_lm is None:
             return None
-        S.spec_rmsnorm(self.x[:M], self.w.final_norm, self.dims.eps, Y=self.h[:M])
         return S.spec_lmhead_softmax(self.h[:M], self.w.w_lm, temperature, P=self.P[:M], ws=self.ws)
 
     def verify_round(self, x0, cu_rows, ctx_len, q, drafts, U, temperature: float,
                      tie_eps: float = 1e-5, max_rows: int | None = None, out=None):
         """Verify pass + rejection sampler; returns (n_acc, out_tok, near_tie)."""
-        P = self.verify_pass(x0, cu_rows, ctx_len, temperature, max_rows)
-        return S.spec_reject_sample(P, q, drafts, U, cu_rows, tie_eps, out=out)
+        if not self.fused_sampler:
+            P = self.verify_pass(x0, cu_rows, ctx_len, temperature, max_rows)
+            return S.spec_reject_sample(P, q, drafts, U, cu_rows, tie_eps, out=out)
+        M = self._stack(x0, cu_rows, ctx_len, max_rows, None)
+        return S.spec_lmhead_reject_sample(self.h[:M], self.w.w_lm, temperature, q, drafts, U, cu_rows, tie_eps,
+                                           out=out, ws=self.ws)

@@ -1,0 +1,115 @@
+"""GPU parity of the fused LM head -> sampler (spec_lmhead_reject_sample).
+
+Two bars: (1) on identical inputs it returns exactly what spec_lmhead_softmax followed by
+spec_reject_sample returns (it evaluates the same fp32 probabilities, only where it reads
+them); (2) against the oracle chain (fp64 logits, fp64 softmax, the oracle sampler) every
+sequence that neither side flags as a near tie has the same acceptance count and tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import bf16 as obf, ops as oops, sampler as osamp
+
+from gpu_util import bf16_dev, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def chain_inputs(seed, gammas, V, K, T, w_std=0.05, sigma=1.0):
+    """Hidden rows and LM-head weights (bf16), the oracle's logits, and draft distributions that
+    are the target's perturbed in logit space (so drafts are accepted often, rejected sometimes)."""
+    rng = np.random.default_rng(seed)
+    batch = synth.RaggedBatch(gammas, np.zeros(len(gammas), np.int32))
+    H = synth.normal_bf16_bits(seed, (batch.M, K), 1.0)
+    W = synth.normal_bf16_bits(seed + 1, (V, K), w_std)
+    logits = oops.linear(obf.decode(H), obf.decode(W))
+    qrows = np.concatenate([np.arange(batch.cu_rows[b], batch.cu_rows[b] + batch.gammas[b])
+                            for b in range(batch.B)]).astype(np.int64)
+    z = logits[qrows] / (T if T > 0 else 1.0) + sigma * rng.standard_normal((len(qrows), V))
+    z -= z.max(axis=1, keepdims=True)
+    Q = np.exp(z)
+    Q /= Q.sum(axis=1, keepdims=True)
+    Q = Q.astype(np.float32)
+    drafts = np.array([rng.choice(V, p=q.astype(np.float64) / q.astype(np.float64).sum()) for q in Q],
+                      np.int32) if len(qrows) else np.zeros(0, np.int32)
+    U = synth.uniforms_f32(seed + 2, batch.M)
+    return batch, H, W, logits, Q, drafts, U
+
+
+def run_fused(lib, batch, H, W, T, Q, drafts, U):
+    V = W.shape[0]
+    Qd = dev(Q) if Q.size else torch.zeros((1, V), dtype=torch.float32, device="cuda")
+    Dd = dev(drafts) if drafts.size else torch.zeros(1, dtype=torch.int32, device="cuda")
+    n, t, near = lib.spec_lmhead_reject_sample(bf16_dev(H), bf16_dev(W), T, Qd, Dd, dev(U), dev(batch.cu_rows))
+    lib.spec_device_status()
+    return n.cpu().numpy(), t.cpu().numpy(), near.cpu().numpy(), Qd, Dd
+
+
+CASES = [
+    ([4, 0, 7, 2], 4096, 512, 1.0),
+    ([3] * 16, 151936, 1024, 0.7),
+    ([5, 1, 0, 9], 8192, 512, 0.0),        # greedy: one-hot rows, no logits stored
+    ([40, 2], 4096, 256, 1.0),             # more than 32 drafts: acceptance in two passes
+    ([0], 4096, 256, 0.5),                 # bonus row only
+    ([6, 6, 1], 1000, 264, 1.3),           # vocabulary not a multiple of the 128-token tile
+]
+
+
+@pytest.mark.parametrize("gammas,V,K,T", CASES)
+def test_fused_equals_softmax_then_sampler(lib, gammas, V, K, T):
+    batch, H, W, _, Q, drafts, U = chain_inputs(len(gammas) * 7 + V + K, gammas, V, K, T)
+    n, t, near, Qd, Dd = run_fused(lib, batch, H, W, T, Q, drafts, U)
+    P = lib.spec_lmhead_softmax(bf16_dev(H), bf16_dev(W), T)
+    n2, t2, near2 = lib.spec_reject_sample(P, Qd, Dd, dev(U), dev(batch.cu_rows))
+    lib.spec_device_status()
+    assert np.array_equal(n, n2.cpu().numpy())
+    assert np.array_equal(t, t2.cpu().numpy())
+    assert np.array_equal(near, near2.cpu().numpy())
+
+
+# Peaked target rows (weights of std 0.2: logits spread by ~4.5 at K = 512) keep most decisions out
+# of the absolute 1e-5 near-tie band; flat rows over a large vocabulary put p itself near 1e-4.
+ORACLE_CASES = [
+    ([4, 0, 7, 2] * 8, 4096, 512, 1.0),
+    ([3] * 16, 151936, 512, 0.7),
+    ([5, 1, 0, 9] * 4, 8192, 512, 0.0),
+    ([40, 2, 33], 4096, 256, 1.0),
+    ([6, 6, 1] * 6, 1000, 264, 1.3),
+]
+
+
+@pytest.mark.parametrize("gammas,V,K,T", ORACLE_CASES)
+def test_fused_matches_oracle_chain(lib, gammas, V, K, T):
+    batch, H, W, logits, Q, drafts, U = chain_inputs(len(gammas) * 7 + V + K, gammas, V, K, T, w_std=0.2)
+    n, t, near, _, _ = run_fused(lib, batch, H, W, T, Q, drafts, U)
+    p = oops.target_probs(logits, T)
+    n_ref, t_ref, near_ref = osamp.reject_sample(p, Q, drafts, U, batch.cu_rows)
+    clean = (near == 0) & (near_ref == 0)
+    assert clean.mean() >= 0.5, clean
+    assert np.array_equal(n[clean], n_ref[clean])
+    for b in np.nonzero(clean)[0]:
+        r0 = batch.cu_rows[b]
+        assert np.array_equal(t[r0:r0 + n[b] + 1], t_ref[r0:r0 + n[b] + 1]), b
+        assert np.all(t[r0 + n[b] + 1:batch.cu_rows[b + 1]] == -1)
+
+
+def test_fused_accepts_and_rejects(lib):
+    """The inputs drive both branches: some drafts accepted, some sequences stop early."""
+    gammas = [6] * 24
+    batch, H, W, _, Q, drafts, U = chain_inputs(77, gammas, 4096, 512, 1.0, sigma=0.7)
+    n, _, _, _, _ = run_fused(lib, batch, H, W, 1.0, Q, drafts, U)
+    assert n.sum() > 0 and np.any(n < 6)
+
+
+def test_fused_rows_outside_the_pass_are_flagged(lib):
+    """cu_rows naming more rows than H has: that sequence is skipped and the status word set."""
+    batch, H, W, _, Q, drafts, U = chain_inputs(5, [3, 2], 1024, 256, 1.0)
+    cu = batch.cu_rows.copy()
+    cu[-1] += 4                                   # the last sequence runs past the M rows
+    Ud = dev(np.concatenate([U, np.full(4, 0.5, np.float32)]))
+    lib.spec_lmhead_reject_sample(bf16_dev(H), bf16_dev(W), 1.0, dev(Q), dev(drafts), Ud, dev(cu))
+    with pytest.raises(lib.SpecError):
+        lib.spec_device_status()
+    lib.spec_device_status()                      # cleared

@@ -84,6 +84,16 @@ def test_host_side_validation(built):
     assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
     # sampler: null outputs
     assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # fused LM head -> sampler: fewer rows than sequences, null outputs, small workspace
+    assert L.spec_lmhead_reject_sample(fake, 2, 64, fake, 128, 1.0, fake, fake, fake, fake, 3, 1e-5,
+                                       fake, fake, fake, fake, 1 << 30, None) == E
+    assert L.spec_lmhead_reject_sample(fake, 4, 64, fake, 128, 1.0, fake, fake, fake, fake, 3, 1e-5,
+                                       None, fake, fake, fake, 1 << 30, None) == E
+    assert L.spec_lmhead_reject_sample(fake, 4, 64, fake, 128, 1.0, fake, fake, fake, fake, 3, 1e-5,
+                                       fake, fake, fake, fake, 16, None) == E
+    assert b"workspace" in L.spec_last_error()
+    assert L.spec_lmhead_reject_sample(fake, 4, 64, fake, 128, 1.0, fake, fake, fake, fake, 0, 1e-5,
+                                       None, None, None, None, 0, None) == 0
     # options
     assert L.spec_set_option(b"no_such_knob", 1) == E
     assert L.spec_set_option(b"gemv_max_m", 9) == E
@@ -103,6 +113,10 @@ def test_workspace_queries_are_host_only(built):
     assert S.spec_attention_workspace_bytes(8, 5, 32, 8, 128, 4101) > 64 * 1024
     assert S.spec_lmhead_workspace_bytes(40, 4096, 151936) >= 64 * 1024 + 40 * 1187 * 8
     assert S.spec_linear_workspace_bytes(0, 4096, 4096) == 0
+    # the fused LM head keeps the logits (fp32) unless it is greedy
+    full = S.spec_lmhead_sample_workspace_bytes(40, 4096, 151936, 1.0)
+    greedy = S.spec_lmhead_sample_workspace_bytes(40, 4096, 151936, 0.0)
+    assert full >= greedy + 40 * 151936 * 4 and greedy == S.spec_lmhead_workspace_bytes(40, 4096, 151936)
 
 
 def test_gate_up_interleave_layout(built):
