@@ -43,6 +43,7 @@ WORKLOAD = ("ragged full verify round: B=64, gamma_b~U{1..10}, ctx_b~U[128,8192]
             "Qwen3-8B-shaped stack + 151936-vocab LM head + rejection sampler, T=0.7, Philox seed 0")
 B, G_LO, G_HI, CTX_LO, CTX_HI = 64, 1, 10, 128, 8192
 TEMP, SIGMA, SEED = 0.7, 1.0, 0
+TYPICAL_EPS, TYPICAL_DELTA = 0.09, 0.3   # typical acceptance: threshold floor and entropy slope
 
 
 def peaks():
@@ -421,6 +422,25 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
                          "frac": fb / (t_f / 1e3) / 1e9 / hbm_peak, "traffic": None, "algorithmic_bytes": fb,
                          "tflops": 2.0 * M * dims.V * dims.d / (t_f / 1e3) / 1e12,
                          "peak_source": f"{peak_src} hbm_gbs"}}
+        # typical acceptance (lossy variant) on the same rows: the probabilities of this round
+        S.spec_lmhead_softmax(h, eng.w.w_lm, TEMP, P=eng.P[:M], ws=eng.ws)
+        t_out = (torch.empty_like(out[0]), torch.empty_like(out[1]), torch.empty_like(out[2]))
+
+        def typical():
+            S.spec_typical_sample(eng.P[:M], drafts, U, cu, TYPICAL_EPS, TYPICAL_DELTA, out=t_out)
+        t_t = timeit(typical, 1)
+        n_t = t_out[0].cpu().numpy().astype(np.int64)
+        gam = batch.gammas.astype(np.int64)
+        # rows read: one entropy pass per tested draft (n + 1 tests, gamma when all pass) + the final row
+        rows = int(np.minimum(n_t + 1, gam).sum() + B)
+        tb = rows * dims.V * 4.0
+        res["typical_sample"] = {
+            "avg_launch_us": t_t * 1e3, "launches_per_round": 0, "total_ms": 0.0,
+            "epsilon": TYPICAL_EPS, "delta": TYPICAL_DELTA,
+            "accepted_tokens_per_round": int(n_t.sum()) + B,
+            "roofline": {"kernel": "typical_sample", "bound": "hbm", "achieved": tb / (t_t / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": tb / (t_t / 1e3) / 1e9 / hbm_peak,
+                         "traffic": None, "algorithmic_bytes": tb, "peak_source": f"{peak_src} hbm_gbs"}}
     return res
 
 

@@ -244,6 +244,25 @@ SPEC_API int spec_reject_sample(const float* P, const float* Q, const int32_t* d
                        float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
                        spec_stream stream);
 
+/* Typical acceptance, the lossy accept rule ([P3] "Exactness is a choice"):
+ * keep draft x_i iff p_i(x_i) > max(epsilon, delta * exp(-H_i)), H_i =
+ * -sum_x p_i(x) ln p_i(x) the entropy of the target row (epsilon the floor of
+ * the bar, delta its entropy slope; the page's formula is lost, this is the
+ * reading of its words), stopping at the first draft that fails (n_b); the
+ * token after the kept prefix is drawn from the target row p_{n+1} itself by
+ * the same inverse CDF as spec_reject_sample (no residual, so Q is not an
+ * argument).  The output is no longer distributed as p; at temperature 0
+ * (one-hot rows) it equals the exact rule's.  Entropies are summed from fp32
+ * terms with fp64 across warps; near_tie counts tests with
+ * |p_i(x_i) - threshold| < tie_eps and final picks as for spec_reject_sample.
+ *   P, draft_tok, U, cu_rows, n_acc, out_tok, near_tie: as spec_reject_sample
+ *   (U rows 0 .. gamma_b - 1 are not used).
+ * Requires epsilon, delta finite and >= 0, 1 <= V <= 1048576. */
+SPEC_API int spec_typical_sample(const float* P, const int32_t* draft_tok, const float* U,
+                                 const int32_t* cu_rows, int B, int V, float epsilon, float delta,
+                                 float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                                 spec_stream stream);
+
 /* Fused LM head -> sampler: the same n_acc / out_tok / near_tie as
  * spec_lmhead_softmax followed by spec_reject_sample on the same inputs (bit
  * for bit), without materialising p.  The acceptance test needs p_i(x_i) only

@@ -38,6 +38,7 @@ _SIGS = {
     "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "spec_reject_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _vp, _vp, _vp, _vp]),
+    "spec_typical_sample": (_i, [_vp, _vp, _vp, _vp, _i, _i, _f, _f, _f, _vp, _vp, _vp, _vp]),
     "spec_lmhead_sample_workspace_bytes": (_sz, [_i, _i, _i, _f]),
     "spec_lmhead_reject_sample": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _vp,
                                        _vp, _sz, _vp]),
@@ -316,6 +317,26 @@ def spec_reject_sample(P, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5, out=N
             raise ValueError("sampler inputs must be contiguous")
     _check(_lib.spec_reject_sample(_p(P), _p(Q), _p(draft_tok), _p(U), _p(cu_rows), B, V,
                                    float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)), True)
+    return n_acc, out_tok, near
+
+
+def spec_typical_sample(P, draft_tok, U, cu_rows, epsilon: float, delta: float, tie_eps: float = 1e-5, out=None,
+                        stream=None):
+    """Typical acceptance; returns (n_acc [B], out_tok [M], near_tie [B]) int32 device tensors."""
+    _need(P, torch.float32, "P"); _need(U, torch.float32, "U")
+    _need(draft_tok, torch.int32, "draft_tok"); _need(cu_rows, torch.int32, "cu_rows")
+    M, V = P.shape
+    B = cu_rows.numel() - 1
+    if out is None:
+        dev = P.device
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(M, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    n_acc, out_tok, near = out
+    for t in (P, U, draft_tok, cu_rows):
+        if not t.is_contiguous():
+            raise ValueError("sampler inputs must be contiguous")
+    _check(_lib.spec_typical_sample(_p(P), _p(draft_tok), _p(U), _p(cu_rows), B, V, float(epsilon), float(delta),
+                                    float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)), True)
     return n_acc, out_tok, near
 
 

@@ -724,6 +724,25 @@ int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
   return ok(1);
 }
 
+int spec_typical_sample(const float* P, const int32_t* draft_tok, const float* U, const int32_t* cu_rows, int B,
+                        int V, float epsilon, float delta, float tie_eps, int32_t* n_acc, int32_t* out_tok,
+                        int32_t* near_tie, spec_stream stream) {
+  if (B < 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes B=%d V=%d", B, V);
+  if (B == 0) return ok();
+  if (!P || !draft_tok || !U || !cu_rows || !n_acc || !out_tok || !near_tie)
+    return fail(SPEC_EINVAL, "NULL argument");
+  if (!(tie_eps >= 0.f)) return fail(SPEC_EINVAL, "tie_eps must be >= 0");
+  if (!(epsilon >= 0.f) || !(delta >= 0.f) || std::isinf(epsilon) || std::isinf(delta))
+    return fail(SPEC_EINVAL, "epsilon and delta must be finite and >= 0");
+  if (V > (1 << 20)) return fail(SPEC_EUNSUPPORTED, "V=%d > 1048576", V);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = launch_typical_sample(P, draft_tok, U, cu_rows, B, V, epsilon, delta, tie_eps, n_acc, out_tok,
+                                        near_tie, d->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "typical_sample launch");
+  return ok(1);
+}
+
 // --------------------------------------------------------------------------- glue
 int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, float eps,
                  spec_bf16* Y, int ldy, spec_stream stream) {

@@ -139,6 +139,11 @@ cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int
                                         int32_t* n_acc, int32_t* out_tok, int32_t* near_tie, unsigned* status,
                                         cudaStream_t s);
 
+// Typical acceptance (lossy): p [M x V] given; Q not used.
+cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const float* U, const int32_t* cu_rows,
+                                  int B, int V, float t_eps, float t_delta, float tie_eps, int32_t* n_acc,
+                                  int32_t* out_tok, int32_t* near_tie, unsigned* status, cudaStream_t s);
+
 // ---- glue
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
                            uint16_t* Y, int ldy, cudaStream_t s);

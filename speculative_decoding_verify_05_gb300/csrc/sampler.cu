@@ -93,14 +93,19 @@ __device__ __forceinline__ void load_weights(const RowP& pr, const float* qrow, 
 
 // P: p [M x V] (P_GIVEN) or z / T [M x V] (P_LOGITS, unused for P_ARGMAX); stats: the LM head's
 // per-tile statistics [M][n_stats] (P_LOGITS, P_ARGMAX).
-template <int MODE>
+// TYPICAL: the lossy accept rule instead of step 1 ("How Speculative Decoding Works (and When It
+// Doesn't)", "Exactness is a choice"): keep x_i iff p_i(x_i) > max(t_eps, t_delta * e^(-H_i)),
+// H_i the entropy of row i, stop at the first failure; the final token is drawn from the target
+// row p_{n+1} itself (no residual).  Q is not read.
+template <int MODE, bool TYPICAL>
 __global__ void __launch_bounds__(SAMPLER_THREADS)
 reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ stats, int n_stats,
                      const float* __restrict__ Q,
                      const int32_t* __restrict__ draft, const float* __restrict__ U,
                      const int32_t* __restrict__ cu_rows, int V, float tie_eps,
                      int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tok,
-                     int32_t* __restrict__ near_tie, unsigned* status, int vec, int m_rows) {
+                     int32_t* __restrict__ near_tie, unsigned* status, int vec, int m_rows,
+                     float t_eps, float t_delta) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -137,6 +142,42 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
   }
   __syncthreads();
   int base = 0;
+  if constexpr (TYPICAL) {
+    // one draft row at a time: block-wide entropy pass (fp32 terms, fp64 across warps), then the
+    // threshold test by thread 0; the loop ends at the first draft that fails
+    for (int i = 0; i < gamma; ++i) {
+      const RowP pr{P + (size_t)(r0 + i) * V, 0.f, 0.f, 0};
+      float h = 0.f;
+      for (int x0 = tid * PER_THREAD; x0 < V; x0 += TILE) {
+        float w[PER_THREAD];
+        load_weights<MODE>(pr, pr.v, x0, V, true, vec, w);
+#pragma unroll
+        for (int e = 0; e < PER_THREAD; ++e) h -= w[e] > 0.f ? w[e] * logf(w[e]) : 0.f;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+      if (lane == 0) s_wp[warp][1] = h;
+      __syncthreads();
+      if (tid == 0) {
+        double H = 0.0;
+        for (int k = 0; k < SAMPLER_THREADS / 32; ++k) H += (double)s_wp[k][1];
+        const double tau = fmax((double)t_eps, (double)t_delta * exp(-H));
+        int x = draft[q0 + i];
+        if (x < 0 || x >= V) {           // invalid draft token: flag it, read a valid slot
+          set_status(status, 0x3F0u);
+          x = x < 0 ? 0 : V - 1;
+        }
+        const double px = (double)p_at<MODE>(pr, x);
+        if (fabs(px - tau) < eps) ++s_near;
+        if (!(px > tau)) {
+          s_n = i;
+          s_done = 1;
+        }
+      }
+      __syncthreads();
+      if (s_done) break;
+    }
+  } else
   for (;; base += 32) {
     const int rows = min(32, gamma + 1 - base);
     // one warp per row: 16 rows at a time
@@ -188,8 +229,9 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
     if (s_done) break;
   }
   const int n = s_n;
-  const bool resid = n < gamma;
-  const RowP prow{P + (size_t)(r0 + n) * V, s_mx[n - base], s_inv[n - base], s_am[n - base]};
+  const bool resid = !TYPICAL && n < gamma;
+  const int ri = (MODE == P_GIVEN) ? 0 : n - base;   // the final row's normaliser slot
+  const RowP prow{P + (size_t)(r0 + n) * V, s_mx[ri], s_inv[ri], s_am[ri]};
   const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow.v;
 
   // ---- 2. per-tile totals of the residual and of p (coalesced 16-byte loads, four tiles' loads in
@@ -357,9 +399,9 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
                                  float tie_eps, int32_t* n_acc, int32_t* out_tok,
                                  int32_t* near_tie, unsigned* status, cudaStream_t s) {
   const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
-  cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
+  cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
                            static_cast<const float2*>(nullptr), 0, Q, draft, U, cu_rows, V, tie_eps, n_acc,
-                           out_tok, near_tie, status, vec ? 1 : 0, INT_MAX);
+                           out_tok, near_tie, status, vec ? 1 : 0, INT_MAX, 0.f, 0.f);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -371,10 +413,21 @@ cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int
   const bool vec = V % 4 == 0 && (greedy || (reinterpret_cast<uintptr_t>(Z) & 15) == 0) &&
                    (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
   cudaError_t e = greedy
-      ? launch_k(reject_sample_kernel<P_ARGMAX>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q, draft,
-                 U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M)
-      : launch_k(reject_sample_kernel<P_LOGITS>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q, draft,
-                 U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M);
+      ? launch_k(reject_sample_kernel<P_ARGMAX, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q,
+                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f)
+      : launch_k(reject_sample_kernel<P_LOGITS, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q,
+                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const float* U, const int32_t* cu_rows,
+                                  int B, int V, float t_eps, float t_delta, float tie_eps, int32_t* n_acc,
+                                  int32_t* out_tok, int32_t* near_tie, unsigned* status, cudaStream_t s) {
+  const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0;
+  cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN, true>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
+                           static_cast<const float2*>(nullptr), 0, static_cast<const float*>(nullptr), draft, U,
+                           cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, INT_MAX, t_eps,
+                           t_delta);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -84,6 +84,9 @@ def test_host_side_validation(built):
     assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
     # sampler: null outputs
     assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # typical acceptance: negative floor, infinite slope
+    assert L.spec_typical_sample(fake, fake, fake, fake, 3, 8, -0.1, 0.3, 1e-5, fake, fake, fake, None) == E
+    assert L.spec_typical_sample(fake, fake, fake, fake, 3, 8, 0.1, float("inf"), 1e-5, fake, fake, fake, None) == E
     # fused LM head -> sampler: fewer rows than sequences, null outputs, small workspace
     assert L.spec_lmhead_reject_sample(fake, 2, 64, fake, 128, 1.0, fake, fake, fake, fake, 3, 1e-5,
                                        fake, fake, fake, fake, 1 << 30, None) == E
