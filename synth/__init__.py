@@ -131,3 +131,29 @@ def draft_distribution(logits: np.ndarray, batch: RaggedBatch, sigma: float,
     for i in np.nonzero(q32[np.arange(len(rows)), tok] == 0)[0]:
         tok[i] = int(np.argmax(q32[i]))
     return q32, tok.astype(np.int32)
+
+
+def ngram_histories(seed: int, B: int, len_lo: int, len_hi: int, vocab: int, copy_frac: float):
+    """Packed token histories for the n-gram drafter: tokens [sum L] int32 and cu_len [B+1].
+
+    Each history (length ~ U[len_lo, len_hi]) is built from segments of 8..64 tokens; a segment
+    is, with probability copy_frac, a span copied from earlier in the same history (the
+    copy-heavy regime: editing, quoting, repeating the prompt), else fresh uniform tokens.
+    """
+    rng = philox(seed)
+    lens = rng.integers(len_lo, len_hi + 1, size=B)
+    out = []
+    for L in lens:
+        h = []
+        while len(h) < L:
+            seg = int(rng.integers(8, 65))
+            if h and len(h) > 16 and rng.random() < copy_frac:
+                start = int(rng.integers(0, len(h) - 8))
+                span = h[start:start + seg]
+                h.extend(span)
+            else:
+                h.extend(int(t) for t in rng.integers(0, vocab, size=seg))
+        out.append(np.asarray(h[:L], np.int32))
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum([len(x) for x in out])
+    return np.concatenate(out) if out else np.zeros(0, np.int32), cu
