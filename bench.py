@@ -279,6 +279,8 @@ def run_gpu(args):
     per = kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, peak_src,
                          sampler_inputs=(q, drafts, st["U"], out))
 
+    per["ngram_propose"] = ngram_timing(S, hbm_peak, peak_src, dev)
+
     # ---- weight-read amortisation of the linear stack: M = 5 verify vs M = 1 decode
     lin = linear_stack_ratio(eng, dims, S, hbm_peak, peak_src)
 
@@ -442,6 +444,33 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
                          "peak": hbm_peak, "unit": "GB/s", "frac": tb / (t_t / 1e3) / 1e9 / hbm_peak,
                          "traffic": None, "algorithmic_bytes": tb, "peak_source": f"{peak_src} hbm_gbs"}}
     return res
+
+
+def ngram_timing(S, hbm_peak, peak_src, dev, reps=5):
+    """The weightless drafter on B = 64 copy-heavy histories of 128..8192 tokens (k = 4, window 3..8,
+    the pages' example configuration); not part of the verify round."""
+    import torch
+    import synth
+    tokens, cu = synth.ngram_histories(SEED + 7, B=B, len_lo=CTX_LO, len_hi=CTX_HI, vocab=151936, copy_frac=0.8)
+    td, cd = torch.from_numpy(tokens).to(dev), torch.from_numpy(cu).to(dev)
+    out = (torch.empty((B, 4), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    S.spec_ngram_propose(td, cd, 4, 3, 8, out=out)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(reps):
+        S.spec_ngram_propose(td, cd, 4, 3, 8, out=out)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / reps
+    hb = float(tokens.nbytes)   # every history read at least once
+    n = out[1].cpu().numpy()
+    return {"avg_launch_us": t * 1e3, "launches_per_round": 0, "total_ms": 0.0, "sequences": B,
+            "history_tokens": int(len(tokens)), "with_drafts": int((n > 0).sum()), "drafts": int(n.sum()),
+            "roofline": {"kernel": "ngram_propose", "bound": "hbm", "achieved": hb / (t / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": hb / (t / 1e3) / 1e9 / hbm_peak,
+                         "traffic": None, "algorithmic_bytes": hb, "peak_source": f"{peak_src} hbm_gbs"}}
 
 
 def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):

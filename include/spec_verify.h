@@ -175,6 +175,25 @@ SPEC_API int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx
                                        void* workspace, size_t workspace_bytes, spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* n-gram prompt-lookup drafter (the weightless drafter)                     */
+/* ------------------------------------------------------------------------ */
+/* [P2] "Under the Hood" (N-gram: match the recent context against earlier
+ * text, copy what followed) and "Cheat Sheet" (num_speculative_tokens k,
+ * prompt_lookup_min / prompt_lookup_max).  Per sequence with history
+ * h[0 .. L-1]: for n = n_max down to n_min, the latest start j with
+ * h[j .. j+n-1] == h[L-n .. L-1] and j + n <= L - 1; the first n that has one
+ * wins and the drafts are h[j+n .. min(j+n+k, L) - 1]; no match, no drafts.
+ *   tokens  [sum L] int32, history b at tokens[cu_len[b] .. cu_len[b+1] - 1]
+ *   cu_len  [B + 1] int32 device array (non-decreasing; a negative length is
+ *           flagged in the status word and gives no drafts)
+ *   drafts  [B x k] int32 out, -1 after the n_drafts[b] proposed tokens
+ *   n_drafts [B] int32 out
+ * Requires 1 <= k <= 4096, 1 <= n_min <= n_max <= 64.  One kernel, no
+ * workspace. */
+SPEC_API int spec_ngram_propose(const int32_t* tokens, const int32_t* cu_len, int B, int k, int n_min,
+                                int n_max, int32_t* drafts, int32_t* n_drafts, spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Verify attention (causal GQA over the KV cache + the new block)           */
 /* ------------------------------------------------------------------------ */
 /* Row j of sequence b sits at position ctx_len[b] + j and attends the

@@ -38,6 +38,7 @@ _SIGS = {
     "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "spec_reject_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _vp, _vp, _vp, _vp]),
+    "spec_ngram_propose": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "spec_typical_sample": (_i, [_vp, _vp, _vp, _vp, _i, _i, _f, _f, _f, _vp, _vp, _vp, _vp]),
     "spec_lmhead_sample_workspace_bytes": (_sz, [_i, _i, _i, _f]),
     "spec_lmhead_reject_sample": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _vp,
@@ -318,6 +319,21 @@ def spec_reject_sample(P, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5, out=N
     _check(_lib.spec_reject_sample(_p(P), _p(Q), _p(draft_tok), _p(U), _p(cu_rows), B, V,
                                    float(tie_eps), _p(n_acc), _p(out_tok), _p(near), _stream(stream)), True)
     return n_acc, out_tok, near
+
+
+def spec_ngram_propose(tokens, cu_len, k: int, n_min: int, n_max: int, out=None, stream=None):
+    """n-gram prompt lookup; returns (drafts [B, k] (-1 padded), n_drafts [B]) int32 device tensors."""
+    _need(tokens, torch.int32, "tokens"); _need(cu_len, torch.int32, "cu_len")
+    if not (tokens.is_contiguous() and cu_len.is_contiguous()):
+        raise ValueError("tokens and cu_len must be contiguous")
+    B = cu_len.numel() - 1
+    if out is None:
+        out = (torch.empty((B, k), dtype=torch.int32, device=tokens.device),
+               torch.empty(B, dtype=torch.int32, device=tokens.device))
+    drafts, n = out
+    _check(_lib.spec_ngram_propose(_p(tokens), _p(cu_len), B, int(k), int(n_min), int(n_max), _p(drafts), _p(n),
+                                   _stream(stream)), True)
+    return drafts, n
 
 
 def spec_typical_sample(P, draft_tok, U, cu_rows, epsilon: float, delta: float, tie_eps: float = 1e-5, out=None,

@@ -743,6 +743,24 @@ int spec_typical_sample(const float* P, const int32_t* draft_tok, const float* U
   return ok(1);
 }
 
+// --------------------------------------------------------------------------- n-gram drafter
+int spec_ngram_propose(const int32_t* tokens, const int32_t* cu_len, int B, int k, int n_min, int n_max,
+                       int32_t* drafts, int32_t* n_drafts, spec_stream stream) {
+  if (B < 0) return fail(SPEC_EINVAL, "B=%d < 0", B);
+  if (B == 0) return ok();
+  if (!tokens || !cu_len || !drafts || !n_drafts) return fail(SPEC_EINVAL, "NULL argument");
+  if (k < 1 || k > 4096) return fail(SPEC_EINVAL, "k=%d must be in [1, 4096]", k);
+  if (n_min < 1 || n_max < n_min || n_max > NGRAM_MAX_WINDOW)
+    return fail(SPEC_EINVAL, "window [%d, %d] must satisfy 1 <= n_min <= n_max <= %d", n_min, n_max,
+                NGRAM_MAX_WINDOW);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = launch_ngram_propose(tokens, cu_len, B, k, n_min, n_max, drafts, n_drafts, d->status,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ngram_propose launch");
+  return ok(1);
+}
+
 // --------------------------------------------------------------------------- glue
 int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, float eps,
                  spec_bf16* Y, int ldy, spec_stream stream) {

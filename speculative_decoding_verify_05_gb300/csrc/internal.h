@@ -144,6 +144,11 @@ cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const fl
                                   int B, int V, float t_eps, float t_delta, float tie_eps, int32_t* n_acc,
                                   int32_t* out_tok, int32_t* near_tie, unsigned* status, cudaStream_t s);
 
+// ---- n-gram prompt-lookup drafter
+constexpr int NGRAM_MAX_WINDOW = 64;
+cudaError_t launch_ngram_propose(const int32_t* tokens, const int32_t* cu_len, int B, int k, int n_min, int n_max,
+                                 int32_t* drafts, int32_t* n_drafts, unsigned* status, cudaStream_t s);
+
 // ---- glue
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
                            uint16_t* Y, int ldy, cudaStream_t s);

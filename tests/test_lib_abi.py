@@ -84,6 +84,11 @@ def test_host_side_validation(built):
     assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
     # sampler: null outputs
     assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # n-gram drafter: empty window, window past the limit, k = 0
+    assert L.spec_ngram_propose(fake, fake, 2, 4, 3, 2, fake, fake, None) == E
+    assert L.spec_ngram_propose(fake, fake, 2, 4, 1, 65, fake, fake, None) == E
+    assert L.spec_ngram_propose(fake, fake, 2, 0, 1, 4, fake, fake, None) == E
+    assert L.spec_ngram_propose(None, None, 0, 4, 1, 4, None, None, None) == 0
     # typical acceptance: negative floor, infinite slope
     assert L.spec_typical_sample(fake, fake, fake, fake, 3, 8, -0.1, 0.3, 1e-5, fake, fake, fake, None) == E
     assert L.spec_typical_sample(fake, fake, fake, fake, 3, 8, 0.1, float("inf"), 1e-5, fake, fake, fake, None) == E
