@@ -284,6 +284,9 @@ def run_gpu(args):
     # ---- weight-read amortisation of the linear stack: M = 5 verify vs M = 1 decode
     lin = linear_stack_ratio(eng, dims, S, hbm_peak, peak_src)
 
+    # ---- the draft side (the step before the verify pass), off with --no-draft
+    draft = draft_timing(S, E, batch, dev, ms) if not args.no_draft else None
+
     # ---- end to end through the public API with host buffers
     e2e = end_to_end(args, eng, batch, dims, q, drafts, x0, S, torch, dev)
 
@@ -312,6 +315,7 @@ def run_gpu(args):
         "kernels": {k: {kk: vv for kk, vv in v.items() if kk != "roofline"} | {"roofline": v["roofline"]}
                     for k, v in per.items()},
         "linear_stack": lin,
+        "draft_phase": draft,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "clocks": clk,
@@ -443,6 +447,62 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
             "roofline": {"kernel": "typical_sample", "bound": "hbm", "achieved": tb / (t_t / 1e3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s", "frac": tb / (t_t / 1e3) / 1e9 / hbm_peak,
                          "traffic": None, "algorithmic_bytes": tb, "peak_source": f"{peak_src} hbm_gbs"}}
+    return res
+
+
+def draft_timing(S, E, batch, dev, round_ms, gamma=4, reps=5):
+    """The step before the verify pass: gamma decode steps of a Qwen3-0.6B-shaped draft stack (28
+    layers, d 1024, random init) at M = B rows over the benchmark batch's contexts, captured in
+    one CUDA graph.  c_hat = one draft step / one verify round (the pages' draft-cost ratio)."""
+    import torch
+    import synth
+    dims = E.draft_dims()
+    cap = int((batch.ctx_len + gamma + 1).max() + 15) // 16 * 16
+    sw = E.random_stack(dims, seed=3000, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(3001)
+    kcs, vcs = [], []
+    for _ in range(dims.layers):
+        k = torch.empty((B, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        kcs.append(k)
+        vcs.append(torch.empty_like(k).normal_(0, 1, generator=g))
+    eng = E.DraftEngine(dims, sw, kcs, vcs, B, gamma, device=dev)
+    tok0 = torch.randint(0, dims.V, (B,), dtype=torch.int32, device=dev, generator=g)
+    ctx = torch.from_numpy(batch.ctx_len).to(dev)
+    U = torch.from_numpy(synth.uniforms_f32(SEED + 11, gamma * B).reshape(gamma, B)).to(dev)
+    Q = torch.empty((B * gamma, dims.V), dtype=torch.float32, device=dev)
+    drafts = torch.empty(B * gamma, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        eng.draft(tok0, ctx, U, TEMP, Q, drafts)
+    torch.cuda.synchronize()
+    S.spec_device_status()
+    graph = torch.cuda.CUDAGraph()
+    S.reset_launch_count()
+    with torch.cuda.graph(graph, stream=stream):
+        eng.draft(tok0, ctx, U, TEMP, Q, drafts)
+    launches = S.launch_count()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    S.spec_device_status()
+    t = e0.elapsed_time(e1) / reps
+    wbytes = 2.0 * (dims.layers * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d
+                                   + dims.d * dims.I) + dims.V * dims.d)
+    kv = float(batch.ctx_len.sum()) * dims.layers * dims.Hkv * dims.D * 2 * 2
+    res = {"model": "Qwen3-0.6B-shaped (28 layers, d 1024, 16/8 heads, I 3072, tied LM head), random init",
+           "B": B, "gamma": gamma, "phase_ms": t, "step_us": t / gamma * 1e3, "launches_per_phase": launches,
+           "c_hat": (t / gamma) / round_ms, "step_hbm_gbs": (wbytes + kv) / (t / gamma / 1e3) / 1e9,
+           "step_algorithmic_bytes": wbytes + kv}
+    del eng, kcs, vcs, sw, graph
+    torch.cuda.empty_cache()
     return res
 
 
@@ -742,6 +802,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-draft", action="store_true", help="skip the draft-phase measurement")
     ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead"], default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")

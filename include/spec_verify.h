@@ -237,6 +237,12 @@ SPEC_API size_t spec_lmhead_workspace_bytes(int M, int K, int V);
 SPEC_API int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
                         float temperature, float* P,
                         void* workspace, size_t workspace_bytes, spec_stream stream);
+/* Same, writing row m of P at P + m*ldp (ldp >= V, a multiple of 4): lets a
+ * decode step put its rows straight into a larger packed array (the draft
+ * side writes step i of sequence b at row b*gamma + i of the verify pass's q). */
+SPEC_API int spec_lmhead_softmax_ld(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                                    float temperature, float* P, long long ldp,
+                                    void* workspace, size_t workspace_bytes, spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Rejection sampler (one CTA per sequence)                                  */
@@ -262,6 +268,13 @@ SPEC_API int spec_reject_sample(const float* P, const float* Q, const int32_t* d
                        const float* U, const int32_t* cu_rows, int B, int V,
                        float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
                        spec_stream stream);
+
+/* One token per row: out_tok[r] = the smallest x with sum_{y<=x} p_r(y) >
+ * U[r] * sum_y p_r(y) (the sampler's inverse CDF, fp64 prefixes), p_r at
+ * P + r*ldp.  The draft side's sampling step; rows of zero mass give V - 1.
+ * Requires ldp >= V, 1 <= V <= 1048576. */
+SPEC_API int spec_sample_rows(const float* P, long long ldp, int M, int V, const float* U, int32_t* out_tok,
+                              spec_stream stream);
 
 /* Typical acceptance, the lossy accept rule ([P3] "Exactness is a choice"):
  * keep draft x_i iff p_i(x_i) > max(epsilon, delta * exp(-H_i)), H_i =
@@ -314,6 +327,12 @@ SPEC_API int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const s
  * Y may alias X.  Requires N % 8 == 0, N <= 16384. */
 SPEC_API int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, float eps,
                  spec_bf16* Y, int ldy, spec_stream stream);
+
+/* X[r] = table[ids[r]] (token-embedding rows feeding a decode step), d bf16
+ * per row; ids outside [0, V) are flagged in the status word and read row 0.
+ * Requires d, ldt, ldx multiples of 8, ldt, ldx >= d, 16-byte aligned. */
+SPEC_API int spec_embed(const int32_t* ids, int M, const spec_bf16* table, int V, int d, int ldt,
+               spec_bf16* X, int ldx, spec_stream stream);
 
 /* In-place rotary embedding (rotate-half pairs (i, i + D/2), frequency
  * theta^(-2i/D)) on Hq query heads at Q + r*ldq + h*D and Hkv key heads at

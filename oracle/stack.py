@@ -139,3 +139,40 @@ def decode_steps(x0, sw: StackWeights, dims: Dims, cu_rows, ctx_len, Kcaches, Vc
                 logits = np.zeros((x0.shape[0], lg.shape[1]))
             logits[idx] = lg
     return X, logits, Kc, Vc
+
+
+def draft_decode(tok0, table, sw: StackWeights, dims: Dims, ctx_len, Kcaches, Vcaches, U, temperature: float,
+                 gamma: int):
+    """gamma autoregressive decode steps of a (draft-shaped) stack for B sequences, one row each.
+
+    The step before the verify pass ("Speculative Decoding Spends Arithmetic You May Not Have",
+    Algorithm 1: the draft model proposes x_1 .. x_gamma one at a time, keeping q_1 .. q_gamma).
+    Step i feeds the embedding row of each sequence's current token (table [V, d] bf16 bits;
+    the last committed token at step 0) at position ctx_b + i, runs the stack and the LM head
+    (sw.w_lm), forms q = softmax(logits / T) (one-hot argmax at T = 0) and draws the next token
+    with the sampler's inverse CDF and U[i, b].  Returns (q [B, gamma, V] fp64, drafts [B, gamma]
+    int64, logits [B, gamma, V] fp64, caches).
+    """
+    from . import ops
+    from .sampler import inverse_cdf_pick
+    tok = np.asarray(tok0, np.int64).copy()
+    B = len(tok)
+    emb = decode(np.asarray(table))
+    cu = np.arange(B + 1)
+    ctx = np.asarray(ctx_len, np.int64)
+    Kc = [np.array(k, dtype=np.float64, copy=True) for k in Kcaches]
+    Vc = [np.array(v, dtype=np.float64, copy=True) for v in Vcaches]
+    V = emb.shape[0]
+    q = np.zeros((B, gamma, V))
+    logits = np.zeros((B, gamma, V))
+    drafts = np.zeros((B, gamma), np.int64)
+    for i in range(gamma):
+        x = emb[tok]
+        _, lg, Kc, Vc = verify_pass(x, sw, dims, cu, ctx + i, Kc, Vc)
+        p = ops.target_probs(lg, temperature)
+        t, _ = inverse_cdf_pick(p, np.asarray(U[i], np.float64), 0.0)
+        q[:, i] = p
+        logits[:, i] = lg
+        drafts[:, i] = t
+        tok = t
+    return q, drafts, logits, Kc, Vc

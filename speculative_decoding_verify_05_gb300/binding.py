@@ -37,8 +37,11 @@ _SIGS = {
                                    _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
     "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
+    "spec_lmhead_softmax_ld": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, ctypes.c_longlong, _vp, _sz, _vp]),
+    "spec_embed": (_i, [_vp, _i, _vp, _i, _i, _i, _vp, _i, _vp]),
     "spec_reject_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _vp, _vp, _vp, _vp]),
     "spec_ngram_propose": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "spec_sample_rows": (_i, [_vp, ctypes.c_longlong, _i, _i, _vp, _vp, _vp]),
     "spec_typical_sample": (_i, [_vp, _vp, _vp, _vp, _i, _i, _f, _f, _f, _vp, _vp, _vp, _vp]),
     "spec_lmhead_sample_workspace_bytes": (_sz, [_i, _i, _i, _f]),
     "spec_lmhead_reject_sample": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _vp,
@@ -295,10 +298,31 @@ def spec_lmhead_softmax(H, Wlm, temperature: float, P=None, ws: Workspace | None
     if P is None:
         P = torch.empty((M, V), dtype=torch.float32, device=H.device)
     _need(P, torch.float32, "P")
+    if P.shape != (M, V) or P.stride(1) != 1:
+        raise ValueError("P must be [M, V] with unit column stride")
     wp, wn = _ws_args(ws, spec_lmhead_workspace_bytes(M, K, V), H.device)
-    _check(_lib.spec_lmhead_softmax(_p(H), M, K, _p(Wlm), V, float(temperature), _p(P), wp, wn,
-                                    _stream(stream)), True)
+    if P.stride(0) == V:
+        _check(_lib.spec_lmhead_softmax(_p(H), M, K, _p(Wlm), V, float(temperature), _p(P), wp, wn,
+                                        _stream(stream)), True)
+    else:   # rows of a larger array (e.g. one decode step's rows of a packed q)
+        _check(_lib.spec_lmhead_softmax_ld(_p(H), M, K, _p(Wlm), V, float(temperature), _p(P), P.stride(0),
+                                           wp, wn, _stream(stream)), True)
     return P
+
+
+def spec_embed(ids, table, X=None, stream=None):
+    """X[r] = table[ids[r]] (bf16 rows)."""
+    _need(ids, torch.int32, "ids"); _need(table, torch.bfloat16, "table")
+    M = ids.numel()
+    V, d = table.shape
+    if X is None:
+        X = torch.empty((M, d), dtype=torch.bfloat16, device=table.device)
+    _need(X, torch.bfloat16, "X")
+    if not ids.is_contiguous():
+        raise ValueError("ids must be contiguous")
+    _check(_lib.spec_embed(_p(ids), M, _p(table), V, d, _rowmajor(table, "table"), _p(X), _rowmajor(X, "X"),
+                           _stream(stream)), True)
+    return X
 
 
 # --------------------------------------------------------------------------- sampler
@@ -334,6 +358,16 @@ def spec_ngram_propose(tokens, cu_len, k: int, n_min: int, n_max: int, out=None,
     _check(_lib.spec_ngram_propose(_p(tokens), _p(cu_len), B, int(k), int(n_min), int(n_max), _p(drafts), _p(n),
                                    _stream(stream)), True)
     return drafts, n
+
+
+def spec_sample_rows(P, U, out=None, stream=None):
+    """One token per row of P [M, V] (rows may be strided) drawn with U [M]; returns out [M] int32."""
+    _need(P, torch.float32, "P"); _need(U, torch.float32, "U")
+    M, V = P.shape
+    if out is None:
+        out = torch.empty(M, dtype=torch.int32, device=P.device)
+    _check(_lib.spec_sample_rows(_p(P), _rowmajor(P, "P"), M, V, _p(U), _p(out), _stream(stream)), True)
+    return out
 
 
 def spec_typical_sample(P, draft_tok, U, cu_rows, epsilon: float, delta: float, tie_eps: float = 1e-5, out=None,

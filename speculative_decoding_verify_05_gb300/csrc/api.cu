@@ -548,7 +548,7 @@ size_t spec_lmhead_workspace_bytes(int M, int K, int V) {
 // The LM-head GEMM: z / T of every row into Z (T > 0) and per-128-token-tile statistics (max,
 // sum of exp; or max, argmax when T = 0) into the workspace after its counter region.
 static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
-                              float* Z, void* workspace, const LinPlan& p, DevInfo* d, cudaStream_t s,
+                              float* Z, long long ldz, void* workspace, const LinPlan& p, DevInfo* d, cudaStream_t s,
                               float2** stats_out) {
   CUtensorMap tw, tx;
   {
@@ -570,6 +570,7 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = Z;
+  a.ldp = ldz;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
   cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid * p.cl), s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
@@ -591,10 +592,16 @@ static int check_lmhead_args(const spec_bf16* H, int M, int K, const spec_bf16* 
 int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
                         float temperature, float* P, void* workspace, size_t workspace_bytes,
                         spec_stream stream) {
+  return spec_lmhead_softmax_ld(H, M, K, Wlm, V, temperature, P, V, workspace, workspace_bytes, stream);
+}
+
+int spec_lmhead_softmax_ld(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+                           float* P, long long ldp, void* workspace, size_t workspace_bytes, spec_stream stream) {
   if (M < 0 || K <= 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d", M, K, V);
   if (M == 0) return ok();
   if (int rc = check_lmhead_args(H, M, K, Wlm, V, temperature)) return rc;
   if (!P) return fail(SPEC_EINVAL, "P must be non-NULL");
+  if (ldp < V || ldp % 4) return fail(SPEC_EINVAL, "ldp=%lld must be >= V and a multiple of 4", ldp);
   if (!aligned16(P)) return fail(SPEC_EINVAL, "P must be 16-byte aligned");
   LinPlan p = plan_linear(M, V, K, true);
   if (!workspace || workspace_bytes < p.bytes)
@@ -603,8 +610,8 @@ int spec_lmhead_softmax(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, 
   if (int rc = dev_info(&d)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float2* stats = nullptr;
-  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, P, workspace, p, d, s, &stats)) return rc;
-  cudaError_t e = launch_lmhead_normalize(P, stats, M, V, p.tiles_n, temperature == 0.f, s);
+  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, P, ldp, workspace, p, d, s, &stats)) return rc;
+  cudaError_t e = launch_lmhead_normalize(P, ldp, stats, M, V, p.tiles_n, temperature == 0.f, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head normalize launch");
   return ok(2);
 }
@@ -640,7 +647,7 @@ int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16*
   const bool greedy = temperature == 0.f;
   float* Z = greedy ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + fused_logits_off(p));
   float2* stats = nullptr;
-  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, Z, workspace, p, d, s, &stats)) return rc;
+  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, Z, V, workspace, p, d, s, &stats)) return rc;
   cudaError_t e = launch_reject_sample_logits(Z, stats, p.tiles_n, greedy, Q, draft_tok, U, cu_rows, B, M, V,
                                               tie_eps, n_acc, out_tok, near_tie, d->status, s);
   if (e != cudaSuccess) return cuda_fail(e, "fused sampler launch");
@@ -724,6 +731,20 @@ int spec_reject_sample(const float* P, const float* Q, const int32_t* draft_tok,
   return ok(1);
 }
 
+int spec_sample_rows(const float* P, long long ldp, int M, int V, const float* U, int32_t* out_tok,
+                     spec_stream stream) {
+  if (M < 0 || V <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d V=%d", M, V);
+  if (M == 0) return ok();
+  if (!P || !U || !out_tok) return fail(SPEC_EINVAL, "NULL argument");
+  if (ldp < V) return fail(SPEC_EINVAL, "ldp=%lld < V=%d", ldp, V);
+  if (V > (1 << 20)) return fail(SPEC_EUNSUPPORTED, "V=%d > 1048576", V);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = launch_sample_rows(P, ldp, M, V, U, out_tok, d->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sample_rows launch");
+  return ok(1);
+}
+
 int spec_typical_sample(const float* P, const int32_t* draft_tok, const float* U, const int32_t* cu_rows, int B,
                         int V, float epsilon, float delta, float tie_eps, int32_t* n_acc, int32_t* out_tok,
                         int32_t* near_tie, spec_stream stream) {
@@ -773,6 +794,21 @@ int spec_rmsnorm(const spec_bf16* X, int M, int N, int ldx, const spec_bf16* w, 
   if (!(eps >= 0.f)) return fail(SPEC_EINVAL, "eps must be >= 0");
   cudaError_t e = launch_rmsnorm(X, M, N, ldx, w, eps, Y, ldy, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+  return ok(1);
+}
+
+int spec_embed(const int32_t* ids, int M, const spec_bf16* table, int V, int d, int ldt, spec_bf16* X, int ldx,
+               spec_stream stream) {
+  if (M < 0 || V <= 0 || d <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d V=%d d=%d", M, V, d);
+  if (M == 0) return ok();
+  if (!ids || !table || !X) return fail(SPEC_EINVAL, "NULL argument");
+  if (d % 8 || ldt < d || ldx < d || ldt % 8 || ldx % 8)
+    return fail(SPEC_EINVAL, "d, ldt, ldx must be multiples of 8 with ldt, ldx >= d");
+  if (!aligned16(table) || !aligned16(X)) return fail(SPEC_EINVAL, "table and X must be 16-byte aligned");
+  DevInfo* dv = nullptr;
+  if (int rc = dev_info(&dv)) return rc;
+  cudaError_t e = launch_embed(ids, M, table, V, d, ldt, X, ldx, dv->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "embed launch");
   return ok(1);
 }
 

@@ -198,6 +198,28 @@ __global__ void swiglu_interleaved_kernel(const uint16_t* __restrict__ GU, int M
   }
 }
 
+// X[r] = table[ids[r]]: the token-embedding row gather that feeds a decode step, 8 bf16 per
+// thread (16-byte loads and stores).  An id outside [0, V) is flagged and row 0 is used.
+__global__ void embed_kernel(const int32_t* __restrict__ ids, int M, const uint16_t* __restrict__ table, int V,
+                             int d, int ldt, uint16_t* __restrict__ X, int ldx, unsigned* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_row = d / 8;
+  const size_t total = (size_t)M * per_row;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / per_row);
+    const int c = (int)(idx - (size_t)r * per_row) * 8;
+    int id = ids[r];
+    if (id < 0 || id >= V) {
+      if (c == 0) set_status(status, 0x5F0u);
+      id = 0;
+    }
+    *reinterpret_cast<uint4*>(X + (size_t)r * ldx + c) =
+        *reinterpret_cast<const uint4*>(table + (size_t)id * ldt + c);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
@@ -235,6 +257,16 @@ cudaError_t launch_swiglu_interleaved(const uint16_t* GU, int M, int I, int ldgu
   if (grid > 152 * 16) grid = 152 * 16;
   if (grid < 1) grid = 1;
   cudaError_t e = launch_k(swiglu_interleaved_kernel, dim3(grid), dim3(256), 0, s, GU, M, I, ldgu, A, lda);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_embed(const int32_t* ids, int M, const uint16_t* table, int V, int d, int ldt, uint16_t* X,
+                         int ldx, unsigned* status, cudaStream_t s) {
+  const size_t total = (size_t)M * (d / 8);
+  int grid = (int)((total + 255) / 256);
+  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_k(embed_kernel, dim3(grid), dim3(256), 0, s, ids, M, table, V, d, ldt, X, ldx, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -97,7 +97,7 @@ int gemv_k_slice(int M);   // K elements per split for an M-row pass
 cudaError_t launch_gemv(const GemvArgs& a, int grid, cudaStream_t s);
 
 // ---- softmax normalisation of the LM head output
-cudaError_t launch_lmhead_normalize(float* P, const float2* stats, int M, int V, int n_tiles,
+cudaError_t launch_lmhead_normalize(float* P, long long ldp, const float2* stats, int M, int V, int n_tiles,
                                     bool greedy, cudaStream_t s);
 
 // ---- verify attention
@@ -139,6 +139,9 @@ cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int
                                         int32_t* n_acc, int32_t* out_tok, int32_t* near_tie, unsigned* status,
                                         cudaStream_t s);
 
+// One token per row of p (rows at P + r*ldp) by the sampler's inverse CDF with U[r].
+cudaError_t launch_sample_rows(const float* P, long long ldp, int M, int V, const float* U, int32_t* out_tok,
+                               unsigned* status, cudaStream_t s);
 // Typical acceptance (lossy): p [M x V] given; Q not used.
 cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const float* U, const int32_t* cu_rows,
                                   int B, int V, float t_eps, float t_delta, float tie_eps, int32_t* n_acc,
@@ -157,6 +160,8 @@ cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int 
                         cudaStream_t s);
 cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
                             cudaStream_t s);
+cudaError_t launch_embed(const int32_t* ids, int M, const uint16_t* table, int V, int d, int ldt, uint16_t* X,
+                         int ldx, unsigned* status, cudaStream_t s);
 cudaError_t launch_swiglu_interleaved(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
                                       cudaStream_t s);
 

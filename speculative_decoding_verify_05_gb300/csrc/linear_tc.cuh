@@ -53,7 +53,8 @@ struct LinearArgs {
   int epi;              // the reduce kernel's epilogue: EPI_BF16 (+ residual) or EPI_SWIGLU
   unsigned* status;     // library status word (bounded-wait timeouts)
   float inv_temp;       // EPI_LOGITS
-  float* P;             // EPI_LOGITS: [M x N] fp32
+  float* P;             // EPI_LOGITS: [M x N] fp32, leading dimension ldp
+  long long ldp;
   float2* stats;        // EPI_LOGITS / EPI_ARGMAX: [M][tiles_n] (max, sum) or (max, idx bits)
 };
 

@@ -367,7 +367,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const bool valid = (n < args.N);
             if constexpr (EPI == EPI_LOGITS) {
               const float z = v[j] * args.inv_temp;
-              if (m < args.M && valid) args.P[(size_t)m * args.N + n] = z;
+              if (m < args.M && valid) args.P[(size_t)m * args.ldp + n] = z;
               const float zm = valid ? z : -INFINITY;
               const float mx = warp_max(zm);
               const float e = valid ? expf(z - mx) : 0.f;

@@ -105,19 +105,20 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
                      const int32_t* __restrict__ cu_rows, int V, float tie_eps,
                      int32_t* __restrict__ n_acc, int32_t* __restrict__ out_tok,
                      int32_t* __restrict__ near_tie, unsigned* status, int vec, int m_rows,
-                     float t_eps, float t_delta) {
+                     float t_eps, float t_delta, long long ldp) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int r0 = cu_rows[b];
-  const int gamma = cu_rows[b + 1] - r0 - 1;
-  if (r0 < 0 || gamma < 0 || cu_rows[b + 1] > m_rows) {   // rows outside the verify pass's M rows
+  // cu_rows == nullptr: one row per sequence and no drafts (plain sampling of row b)
+  const int r0 = cu_rows ? cu_rows[b] : b;
+  const int gamma = cu_rows ? cu_rows[b + 1] - r0 - 1 : 0;
+  if (r0 < 0 || gamma < 0 || r0 + gamma + 1 > m_rows) {   // rows outside the verify pass's M rows
     if (tid == 0) {
       set_status(status, 0x3F1u);
-      n_acc[b] = 0;
-      near_tie[b] = 0;
+      if (n_acc) n_acc[b] = 0;
+      if (near_tie) near_tie[b] = 0;
     }
     return;
   }
@@ -146,7 +147,7 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
     // one draft row at a time: block-wide entropy pass (fp32 terms, fp64 across warps), then the
     // threshold test by thread 0; the loop ends at the first draft that fails
     for (int i = 0; i < gamma; ++i) {
-      const RowP pr{P + (size_t)(r0 + i) * V, 0.f, 0.f, 0};
+      const RowP pr{P + (size_t)(r0 + i) * ldp, 0.f, 0.f, 0};
       float h = 0.f;
       for (int x0 = tid * PER_THREAD; x0 < V; x0 += TILE) {
         float w[PER_THREAD];
@@ -203,7 +204,7 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
           set_status(status, 0x3F0u);
           x = x < 0 ? 0 : V - 1;
         }
-        const RowP pr{P + (size_t)(r0 + i) * V, s_mx[lane], s_inv[lane], s_am[lane]};
+        const RowP pr{P + (size_t)(r0 + i) * ldp, s_mx[lane], s_inv[lane], s_am[lane]};
         const double p = (double)p_at<MODE>(pr, x);
         const double q = (double)Q[(size_t)(q0 + i) * V + x];
         const double uq = (double)U[r0 + i] * q;       // exact: 24 x 24 bit product
@@ -231,7 +232,7 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
   const int n = s_n;
   const bool resid = !TYPICAL && n < gamma;
   const int ri = (MODE == P_GIVEN) ? 0 : n - base;   // the final row's normaliser slot
-  const RowP prow{P + (size_t)(r0 + n) * V, s_mx[ri], s_inv[ri], s_am[ri]};
+  const RowP prow{P + (size_t)(r0 + n) * ldp, s_mx[ri], s_inv[ri], s_am[ri]};
   const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow.v;
 
   // ---- 2. per-tile totals of the residual and of p (coalesced 16-byte loads, four tiles' loads in
@@ -382,8 +383,8 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
 
   if (tid == 0) {
     const int t = s_pick >= 0 ? s_pick : V - 1;   // no positive weight at all: last token
-    n_acc[b] = n;
-    near_tie[b] = s_near + s_pick_near;
+    if (n_acc) n_acc[b] = n;
+    if (near_tie) near_tie[b] = s_near + s_pick_near;
     out_tok[r0 + n] = t;
   }
   for (int k = tid; k <= gamma; k += SAMPLER_THREADS) {
@@ -401,7 +402,7 @@ cudaError_t launch_reject_sample(const float* P, const float* Q, const int32_t* 
   const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
   cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
                            static_cast<const float2*>(nullptr), 0, Q, draft, U, cu_rows, V, tie_eps, n_acc,
-                           out_tok, near_tie, status, vec ? 1 : 0, INT_MAX, 0.f, 0.f);
+                           out_tok, near_tie, status, vec ? 1 : 0, INT_MAX, 0.f, 0.f, (long long)V);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -414,9 +415,11 @@ cudaError_t launch_reject_sample_logits(const float* Z, const float2* stats, int
                    (reinterpret_cast<uintptr_t>(Q) & 15) == 0;
   cudaError_t e = greedy
       ? launch_k(reject_sample_kernel<P_ARGMAX, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q,
-                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f)
+                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f,
+                 (long long)V)
       : launch_k(reject_sample_kernel<P_LOGITS, false>, dim3(B), dim3(SAMPLER_THREADS), 0, s, Z, stats, n_stats, Q,
-                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f);
+                 draft, U, cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, M, 0.f, 0.f,
+                 (long long)V);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -427,7 +430,18 @@ cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const fl
   cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN, true>, dim3(B), dim3(SAMPLER_THREADS), 0, s, P,
                            static_cast<const float2*>(nullptr), 0, static_cast<const float*>(nullptr), draft, U,
                            cu_rows, V, tie_eps, n_acc, out_tok, near_tie, status, vec ? 1 : 0, INT_MAX, t_eps,
-                           t_delta);
+                           t_delta, (long long)V);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_sample_rows(const float* P, long long ldp, int M, int V, const float* U, int32_t* out_tok,
+                               unsigned* status, cudaStream_t s) {
+  const bool vec = V % 4 == 0 && ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0;
+  cudaError_t e = launch_k(reject_sample_kernel<P_GIVEN, false>, dim3(M), dim3(SAMPLER_THREADS), 0, s, P,
+                           static_cast<const float2*>(nullptr), 0, static_cast<const float*>(nullptr),
+                           static_cast<const int32_t*>(nullptr), U, static_cast<const int32_t*>(nullptr), V, 0.f,
+                           static_cast<int32_t*>(nullptr), out_tok, static_cast<int32_t*>(nullptr), status,
+                           vec ? 1 : 0, M, 0.f, 0.f, ldp);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

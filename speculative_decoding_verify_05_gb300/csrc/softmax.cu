@@ -13,7 +13,7 @@ constexpr int NORM_THREADS = 256;
 constexpr int NORM_CHUNK = 8192;   // vocabulary entries per CTA
 
 __global__ void __launch_bounds__(NORM_THREADS)
-lmhead_normalize_kernel(float* __restrict__ P, const float2* __restrict__ stats, int V,
+lmhead_normalize_kernel(float* __restrict__ P, long long ldp, const float2* __restrict__ stats, int V,
                         int n_tiles, int greedy) {
   pdl_wait();
   pdl_trigger();
@@ -22,7 +22,7 @@ lmhead_normalize_kernel(float* __restrict__ P, const float2* __restrict__ stats,
   const float2* st = stats + (size_t)m * n_tiles;
   __shared__ float s_mx, s_inv;
   __shared__ int s_am;
-  float* row = P + (size_t)m * V;
+  float* row = P + (size_t)m * ldp;
   const int x0 = blockIdx.x * NORM_CHUNK;
   const int x1 = min(V, x0 + NORM_CHUNK);
 
@@ -69,10 +69,10 @@ lmhead_normalize_kernel(float* __restrict__ P, const float2* __restrict__ stats,
 
 }  // namespace
 
-cudaError_t launch_lmhead_normalize(float* P, const float2* stats, int M, int V, int n_tiles,
+cudaError_t launch_lmhead_normalize(float* P, long long ldp, const float2* stats, int M, int V, int n_tiles,
                                     bool greedy, cudaStream_t s) {
   dim3 grid((V + NORM_CHUNK - 1) / NORM_CHUNK, M);
-  cudaError_t e = launch_k(lmhead_normalize_kernel, dim3(grid), dim3(NORM_THREADS), 0, s, P, stats, V, n_tiles,
+  cudaError_t e = launch_k(lmhead_normalize_kernel, dim3(grid), dim3(NORM_THREADS), 0, s, P, ldp, stats, V, n_tiles,
                            greedy ? 1 : 0);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

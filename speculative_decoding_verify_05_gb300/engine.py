@@ -41,6 +41,12 @@ class Dims:
         return (self.Hq + 2 * self.Hkv) * self.D
 
 
+def draft_dims() -> Dims:
+    """A Qwen3-0.6B-shaped draft stack: 28 layers, d 1024, 16 query / 8 kv heads of 128, I 3072,
+    vocabulary 151936 shared with the target (LM head tied to the embedding table)."""
+    return Dims(d=1024, Hq=16, Hkv=8, D=128, I=3072, V=151936, layers=28)
+
+
 @dataclass
 class LayerW:
     w_qkv: torch.Tensor      # [(Hq + 2 Hkv) D, d]
@@ -195,3 +201,47 @@ class VerifyEngine:
         M = self._stack(x0, cu_rows, ctx_len, max_rows, None)
         return S.spec_lmhead_reject_sample(self.h[:M], self.w.w_lm, temperature, q, drafts, U, cu_rows, tie_eps,
                                            out=out, ws=self.ws)
+
+
+class DraftEngine:
+    """The step before the verify pass: gamma autoregressive decode steps of a draft-shaped stack
+    for B sequences at M = B rows ("Speculative Decoding Spends Arithmetic You May Not Have",
+    Algorithm 1: the draft proposes x_1 .. x_gamma one at a time and keeps q_1 .. q_gamma).
+
+    Step i: embedding rows of the current tokens (spec_embed; the LM head is tied to the
+    embedding table), the stack at positions ctx_b + i (verify attention with one row per
+    sequence writes that row's K/V into the draft cache), the LM head writing q_i straight into
+    row b * gamma + i of the packed q that the verify sampler reads (spec_lmhead_softmax_ld),
+    and the next token drawn from q_i (spec_sample_rows, uniform U[i, b]).  All arithmetic in
+    the library's kernels; the engine only sequences the calls and advances positions.
+    """
+
+    def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, B: int, gamma: int, device=None):
+        self.dims = dims
+        self.B = B
+        self.gamma = gamma
+        self.eng = VerifyEngine(dims, weights, kcaches, vcaches, max_M=B, max_rows=1, device=device,
+                                fused_sampler=False)
+        dev = self.eng.device
+        self.table = weights.w_lm
+        self.cu = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        self.ctx = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+        self.step_tok = torch.empty((gamma + 1, B), dtype=torch.int32, device=dev)
+        self.steps = torch.arange(gamma, dtype=torch.int32, device=dev)[:, None]
+
+    def draft(self, tok0, ctx_len, U, temperature: float, Q, drafts):
+        """tok0 [B] int32 (each sequence's last committed token), ctx_len [B] int32 (tokens in the
+        draft cache), U [gamma, B] fp32; writes Q [B * gamma, V] fp32 (q rows, sequence-major) and
+        drafts [B * gamma] int32 (sequence b's drafts at b * gamma ..)."""
+        B, g, V = self.B, self.gamma, self.dims.V
+        e = self.eng
+        self.step_tok[0].copy_(tok0)
+        torch.add(ctx_len[None, :], self.steps, out=self.ctx)     # positions ctx_b + i
+        Qv = Q.view(B, g, V)
+        for i in range(g):
+            S.spec_embed(self.step_tok[i], self.table, X=e.x[:B])
+            e._stack(e.x[:B], self.cu, self.ctx[i], 1, None)
+            S.spec_lmhead_softmax(e.h[:B], self.table, temperature, P=Qv[:, i, :], ws=e.ws)
+            S.spec_sample_rows(Qv[:, i, :], U[i], out=self.step_tok[i + 1])
+        drafts.view(B, g).copy_(self.step_tok[1:].t())
+

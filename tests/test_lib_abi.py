@@ -84,6 +84,10 @@ def test_host_side_validation(built):
     assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
     # sampler: null outputs
     assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # draft side: embedding with d not a multiple of 8, sampling rows with ldp < V, LM head ldp < V
+    assert L.spec_embed(fake, 4, fake, 100, 12, 12, fake, 12, None) == E
+    assert L.spec_sample_rows(fake, 10, 4, 16, fake, fake, None) == E
+    assert L.spec_lmhead_softmax_ld(fake, 2, 64, fake, 128, 1.0, fake, 64, fake, 1 << 30, None) == E
     # n-gram drafter: empty window, window past the limit, k = 0
     assert L.spec_ngram_propose(fake, fake, 2, 4, 3, 2, fake, fake, None) == E
     assert L.spec_ngram_propose(fake, fake, 2, 4, 1, 65, fake, fake, None) == E
