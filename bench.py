@@ -366,6 +366,41 @@ def kernel_timings(eng, batch, dims, cu, ctx, S, hbm_peak, tc_peak, tc_sust, pea
                                                               "scaled by algorithmic bytes",
                                             "algorithmic_bytes": ab,
                                             "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}}
+    # paged KV (128-key pages, randomly permuted) over layer 0's cache contents vs the contiguous launch
+    Bc, Hkv_, cap_, D_ = eng.kc[0].shape
+    max_pages = (cap_ + 127) // 128
+    n_pages = Bc * max_pages
+    gp = torch.Generator(device=eng.device)
+    gp.manual_seed(5)
+    kpool = torch.zeros((Hkv_, n_pages, 128, D_), dtype=torch.bfloat16, device=eng.device)
+    vpool = torch.zeros_like(kpool)
+    t_pgs = {}
+    for alloc in ("in_order", "random"):
+        if alloc == "random":   # pages scattered over the whole pool (worst case for locality)
+            perm = torch.randperm(n_pages, generator=gp, device=eng.device).to(torch.int32)
+        else:                   # each sequence's pages consecutive, as a bump allocator hands them out
+            perm = torch.arange(n_pages, dtype=torch.int32, device=eng.device)
+        table = perm.view(Bc, max_pages).contiguous()
+        for src, pool in ((eng.kc[0], kpool), (eng.vc[0], vpool)):
+            padded = torch.zeros((Bc, Hkv_, max_pages * 128, D_), dtype=torch.bfloat16, device=eng.device)
+            padded[:, :, :cap_] = src
+            pool[:, table.view(-1).long()] = padded.view(Bc, Hkv_, max_pages, 128, D_).permute(1, 0, 2, 3, 4).reshape(
+                Hkv_, n_pages, 128, D_)
+            del padded
+
+        def attn_paged(table=table):
+            S.spec_verify_attention_paged(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:], cu, ctx, kpool, vpool,
+                                          table, eng.max_rows, O=eng.o[:M], ws=eng.ws)
+        t_pgs[alloc] = timeit(attn_paged, 1)
+    t_pg = t_pgs["in_order"]
+    res["verify_attention_paged"] = {
+        "avg_launch_us": t_pg * 1e3, "launches_per_round": 0, "total_ms": 0.0, "page_keys": 128,
+        "vs_contiguous": t_pg / t_attn, "random_pages_us": t_pgs["random"] * 1e3,
+        "random_vs_contiguous": t_pgs["random"] / t_attn,
+        "roofline": {"kernel": "verify_attention (paged)", "bound": "hbm", "achieved": ab / (t_pg / 1e3) / 1e9,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": ab / (t_pg / 1e3) / 1e9 / hbm_peak,
+                     "traffic": None, "algorithmic_bytes": ab, "peak_source": f"{peak_src} hbm_gbs"}}
+    del kpool, vpool
     shapes = {"qkv": (dims.qkv, dims.d), "o": (dims.d, hq), "gate_up": (2 * dims.I, dims.d),
               "down": (dims.d, dims.I)}
     xs = {"qkv": eng.h[:M], "o": eng.o[:M], "gate_up": eng.h[:M], "down": eng.a[:M]}

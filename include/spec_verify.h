@@ -224,6 +224,28 @@ SPEC_API int spec_verify_attention(const spec_bf16* Q, int ldq,
                           spec_bf16* O, int ldo,
                           void* workspace, size_t workspace_bytes, spec_stream stream);
 
+/* Same pass over a paged cache: Kpool, Vpool [Hkv][num_pages][128][D] bf16
+ * (in/out; one pool per kv head, page ids shared across heads, so pages
+ * handed out in order give each head one unbroken run of keys) and
+ * block_table [B x max_pages] int32 (device): keys
+ * 128 t .. 128 t + 127 of sequence b live in page block_table[b * max_pages + t]
+ * (one page = one 128-key tile of the kernel).  ctx_len[b] + gamma_b + 1 <=
+ * 128 * max_pages is checked on the device as for cap; a page id outside
+ * [0, num_pages) is flagged in the status word (page 0 is read instead).  The
+ * new keys / values go into their pages.  Pages need not be distinct across
+ * sequences for reading (shared prefixes), but pages that receive new rows
+ * must belong to one sequence.  Needs the tcgen05 kernel (attention_impl 1).
+ * Workspace: spec_attention_paged_workspace_bytes. */
+SPEC_API size_t spec_attention_paged_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int D, int max_pages);
+SPEC_API int spec_verify_attention_paged(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
+                                         const spec_bf16* Vnew, int ldkv, const int32_t* cu_rows,
+                                         const int32_t* ctx_len, int B, int max_rows,
+                                         spec_bf16* Kpool, spec_bf16* Vpool, int num_pages,
+                                         const int32_t* block_table, int max_pages,
+                                         int Hq, int Hkv, int D, float scale,
+                                         spec_bf16* O, int ldo, void* workspace, size_t workspace_bytes,
+                                         spec_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* LM head + softmax: P = softmax((H W_lm^T) / T); T == 0 -> one-hot argmax  */
 /* ------------------------------------------------------------------------ */

@@ -35,6 +35,9 @@ _SIGS = {
     "spec_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "spec_verify_attention": (_i, [_vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp, _i,
                                    _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
+    "spec_attention_paged_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "spec_verify_attention_paged": (_i, [_vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _i,
+                                         _i, _i, _i, _f, _vp, _i, _vp, _sz, _vp]),
     "spec_lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_lmhead_softmax": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "spec_lmhead_softmax_ld": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, ctypes.c_longlong, _vp, _sz, _vp]),
@@ -279,6 +282,41 @@ def spec_verify_attention(Q, Knew, Vnew, cu_rows, ctx_len, Kcache, Vcache, max_r
     _check(_lib.spec_verify_attention(
         _p(Q), _rowmajor(Q, "Q"), _p(Knew), _p(Vnew), ldkv, _p(cu_rows), _p(ctx_len), B,
         int(max_rows), _p(Kcache), _p(Vcache), cap, Hq, Hkv, D, float(scale), _p(O),
+        _rowmajor(O, "O"), wp, wn, _stream(stream)), True)
+    return O
+
+
+def spec_attention_paged_workspace_bytes(B, max_rows, Hq, Hkv, D, max_pages) -> int:
+    return _lib.spec_attention_paged_workspace_bytes(B, max_rows, Hq, Hkv, D, max_pages)
+
+
+def spec_verify_attention_paged(Q, Knew, Vnew, cu_rows, ctx_len, Kpool, Vpool, block_table, max_rows: int,
+                                scale: float | None = None, O=None, ws: Workspace | None = None, stream=None):
+    """Verify attention over a paged cache: Kpool/Vpool [Hkv, num_pages, 128, D], block_table
+    [B, max_pages] int32 (page of each 128-key block of each sequence)."""
+    for t, n in ((Q, "Q"), (Knew, "Knew"), (Vnew, "Vnew"), (Kpool, "Kpool"), (Vpool, "Vpool")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_rows, torch.int32, "cu_rows"); _need(ctx_len, torch.int32, "ctx_len")
+    _need(block_table, torch.int32, "block_table")
+    Hkv, num_pages, page, D = Kpool.shape
+    if page != 128 or not (Kpool.is_contiguous() and Vpool.is_contiguous() and Vpool.shape == Kpool.shape):
+        raise ValueError("Kpool/Vpool must be contiguous [Hkv, num_pages, 128, D]")
+    if not block_table.is_contiguous() or block_table.dim() != 2:
+        raise ValueError("block_table must be a contiguous [B, max_pages] tensor")
+    B, max_pages = block_table.shape
+    M = Q.shape[0]
+    Hq = Q.shape[1] // D
+    ldkv = _rowmajor(Knew, "Knew")
+    if _rowmajor(Vnew, "Vnew") != ldkv:
+        raise ValueError("Knew and Vnew must share a leading dimension")
+    if O is None:
+        O = torch.empty((M, Hq * D), dtype=torch.bfloat16, device=Q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    wp, wn = _ws_args(ws, spec_attention_paged_workspace_bytes(B, max_rows, Hq, Hkv, D, max_pages), Q.device)
+    _check(_lib.spec_verify_attention_paged(
+        _p(Q), _rowmajor(Q, "Q"), _p(Knew), _p(Vnew), ldkv, _p(cu_rows), _p(ctx_len), B, int(max_rows),
+        _p(Kpool), _p(Vpool), num_pages, _p(block_table), max_pages, Hq, Hkv, D, float(scale), _p(O),
         _rowmajor(O, "O"), wp, wn, _stream(stream)), True)
     return O
 

@@ -3,6 +3,7 @@
 // Nothing here allocates device memory; workspaces come from the caller.
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -660,12 +661,13 @@ size_t spec_attention_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int 
   return plan_attention(B, max_rows, Hq, Hkv, cap).bytes;
 }
 
-int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
-                          const spec_bf16* Vnew, int ldkv, const int32_t* cu_rows,
-                          const int32_t* ctx_len, int B, int max_rows, spec_bf16* Kcache,
-                          spec_bf16* Vcache, int cap, int Hq, int Hkv, int D, float scale,
-                          spec_bf16* O, int ldo, void* workspace, size_t workspace_bytes,
-                          spec_stream stream) {
+// Contiguous cache (block_table == nullptr: [B][Hkv][cap][D]) or paged pools ([Hkv][num_pages][128][D],
+// key tile t of sequence b in page block_table[b * max_pages + t]; cap = max_pages * 128 keys).
+static int verify_attention_impl(const spec_bf16* Q, int ldq, const spec_bf16* Knew, const spec_bf16* Vnew,
+                                 int ldkv, const int32_t* cu_rows, const int32_t* ctx_len, int B, int max_rows,
+                                 spec_bf16* Kcache, spec_bf16* Vcache, int cap, const int32_t* block_table,
+                                 int max_pages, int num_pages, int Hq, int Hkv, int D, float scale, spec_bf16* O,
+                                 int ldo, void* workspace, size_t workspace_bytes, spec_stream stream) {
   if (B < 0) return fail(SPEC_EINVAL, "B=%d < 0", B);
   if (B == 0) return ok();
   if (!Q || !Knew || !Vnew || !cu_rows || !ctx_len || !Kcache || !Vcache || !O)
@@ -685,14 +687,19 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
     return fail(SPEC_EINVAL, "bf16 tensors must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(SPEC_EINVAL, "scale must be finite");
   AttnPlan p = plan_attention(B, max_rows, Hq, Hkv, cap);
+  if (block_table && !p.tc)
+    return fail(SPEC_EUNSUPPORTED, "the paged cache needs the tcgen05 attention kernel (attention_impl 1)");
   if (!workspace || workspace_bytes < p.bytes)
     return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
   DevInfo* d = nullptr;
   if (int rc = dev_info(&d)) return rc;
   CUtensorMap tk, tv;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)cap, (cuuint64_t)B * Hkv};
-  cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)cap * D * 2};
-  cuuint32_t box[3] = {64, p.tc ? (cuuint32_t)attention_tc_key_tile() : 64u, 1};
+  const int kt = attention_tc_key_tile();
+  const cuuint64_t rows = block_table ? (cuuint64_t)kt : (cuuint64_t)cap;
+  const cuuint64_t zs = block_table ? (cuuint64_t)num_pages * Hkv : (cuuint64_t)B * Hkv;
+  cuuint64_t dims[3] = {(cuuint64_t)D, rows, zs};
+  cuuint64_t str[2] = {(cuuint64_t)D * 2, rows * D * 2};
+  cuuint32_t box[3] = {64, p.tc ? (cuuint32_t)kt : 64u, 1};
   if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache")) return rc;
   if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache")) return rc;
   char* ws = static_cast<char*>(workspace);
@@ -707,10 +714,43 @@ int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
   a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
   a.status = d->status;
   a.pair_cost = g_attn_pair_cost;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
   cudaError_t e = p.tc ? launch_attention_tc(tk, tv, a, p.grid, static_cast<cudaStream_t>(stream))
                        : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok(1);
+}
+
+int spec_verify_attention(const spec_bf16* Q, int ldq, const spec_bf16* Knew,
+                          const spec_bf16* Vnew, int ldkv, const int32_t* cu_rows,
+                          const int32_t* ctx_len, int B, int max_rows, spec_bf16* Kcache,
+                          spec_bf16* Vcache, int cap, int Hq, int Hkv, int D, float scale,
+                          spec_bf16* O, int ldo, void* workspace, size_t workspace_bytes,
+                          spec_stream stream) {
+  return verify_attention_impl(Q, ldq, Knew, Vnew, ldkv, cu_rows, ctx_len, B, max_rows, Kcache, Vcache, cap,
+                               nullptr, 0, 0, Hq, Hkv, D, scale, O, ldo, workspace, workspace_bytes, stream);
+}
+
+size_t spec_attention_paged_workspace_bytes(int B, int max_rows, int Hq, int Hkv, int D, int max_pages) {
+  if (max_pages <= 0) return 0;
+  return spec_attention_workspace_bytes(B, max_rows, Hq, Hkv, D, max_pages * attention_tc_key_tile());
+}
+
+int spec_verify_attention_paged(const spec_bf16* Q, int ldq, const spec_bf16* Knew, const spec_bf16* Vnew,
+                                int ldkv, const int32_t* cu_rows, const int32_t* ctx_len, int B, int max_rows,
+                                spec_bf16* Kpool, spec_bf16* Vpool, int num_pages, const int32_t* block_table,
+                                int max_pages, int Hq, int Hkv, int D, float scale, spec_bf16* O, int ldo,
+                                void* workspace, size_t workspace_bytes, spec_stream stream) {
+  if (B > 0 && !block_table) return fail(SPEC_EINVAL, "block_table must be non-NULL");
+  if (B > 0 && (num_pages <= 0 || max_pages <= 0))
+    return fail(SPEC_EINVAL, "num_pages=%d and max_pages=%d must be >= 1", num_pages, max_pages);
+  if ((long long)max_pages * attention_tc_key_tile() > INT32_MAX / 2)
+    return fail(SPEC_EINVAL, "max_pages=%d too large", max_pages);
+  return verify_attention_impl(Q, ldq, Knew, Vnew, ldkv, cu_rows, ctx_len, B, max_rows, Kpool, Vpool,
+                               max_pages * attention_tc_key_tile(), block_table, max_pages, num_pages, Hq, Hkv, D,
+                               scale, O, ldo, workspace, workspace_bytes, stream);
 }
 
 // --------------------------------------------------------------------------- sampler

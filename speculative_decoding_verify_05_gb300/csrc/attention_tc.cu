@@ -223,6 +223,32 @@ __device__ __forceinline__ TailRows tail_rows(const Cursor& c) {
   g.first_new = key0 + g.rr0 - c.ctx;
   return g;
 }
+// Where key tile t of pair (b, h) lives: the TMA coordinates (z, y) of its first key and the
+// cache row of that key (rows of D elements).  Contiguous cache: z = b Hkv + h, y = t KT, row =
+// z cap + y.  Paged cache (one pool per kv head, [Hkv][num_pages][KT][D]): page = block_table[b][t]
+// (an id outside the pool is flagged and page 0 is used instead), z = h num_pages + page, y = 0,
+// row = z KT; pages allocated in order then give each head one unbroken run, as the contiguous
+// cache does.
+struct KvTile {
+  int z, y;
+  size_t row;
+};
+__device__ __forceinline__ KvTile kv_tile_page(const AttnArgs& a, int page, int h) {
+  if (page < 0 || page >= a.num_pages) {
+    set_status(a.status, 0x2F2u);
+    page = 0;
+  }
+  const int z = h * a.num_pages + page;
+  return KvTile{z, 0, (size_t)z * KT};
+}
+__device__ __forceinline__ KvTile kv_tile(const AttnArgs& a, int b, int h, int t) {
+  if (a.block_table == nullptr) {
+    const int z = b * a.Hkv + h;
+    return KvTile{z, t * KT, (size_t)z * a.cap + (size_t)t * KT};
+  }
+  return kv_tile_page(a, a.block_table[(size_t)b * a.max_pages + t], h);
+}
+
 // NT threads load the new rows of head h from `src` (row stride ldkv) into registers:
 // 16-byte chunk t + NT k of the n_new x 16 chunks (the block has at most 64 rows).
 template <int NT>
@@ -242,16 +268,14 @@ __device__ __forceinline__ void tail_load(uint4 (&v)[1024 / NT], const uint16_t*
 // (K needs no zeros: masked scores are replaced, not multiplied).
 template <int NT>
 __device__ __forceinline__ void tail_store(const uint4 (&v)[1024 / NT], uint8_t* stage, uint16_t* cache,
-                                           const Cursor& c, const TailRows& g, int cap, int bh, int t,
-                                           bool zero_rest) {
-  const int key0 = c.t * KT;
+                                           const TailRows& g, size_t row0, int t, bool zero_rest) {
 #pragma unroll
   for (int k = 0; k < 1024 / NT; ++k) {
     const int idx = t + NT * k, j = idx >> 4, ch = idx & 15;
     if (j < g.n_new) {
       const int rr = g.rr0 + j;
       *reinterpret_cast<uint4*>(stage + (ch >> 3) * KV_HALF + sw128_off(rr, (ch & 7) * 8)) = v[k];
-      *reinterpret_cast<uint4*>(cache + ((size_t)bh * cap + key0 + rr) * D + ch * 8) = v[k];
+      *reinterpret_cast<uint4*>(cache + (row0 + rr) * D + ch * 8) = v[k];
     }
   }
   if (zero_rest)
@@ -333,7 +357,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       if (b < B) {
         const int ctx = s_ctx[b];
         const int mb = s_cu[b + 1] - s_cu[b];
-        bad |= (mb <= 0 || mb > a.max_rows || ctx < 0 || ctx + mb > a.cap || G * mb > QR);
+        const int cap_keys = a.block_table ? a.max_pages * KT : a.cap;
+        bad |= (mb <= 0 || mb > a.max_rows || ctx < 0 || ctx + mb > cap_keys || G * mb > QR);
         units = (mb > 0 && ctx >= 0) ? (ctx + mb + KT - 1) / KT * Hkv : 0;
       }
       int incl = units;
@@ -378,18 +403,41 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       uint64_t* land = is_k ? k_land : v_land;
       uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
       Cursor c = cur_at(meta, B, ub);
+      // paged cache: the block-table entries are read PF units ahead of the loads that use them
+      // (a second cursor), so a page lookup's latency never sits in front of a TMA issue
+      constexpr int PF = 4;
+      int pq[PF] = {0, 0, 0, 0};
+      Cursor ca = c;
+      const bool paged = a.block_table != nullptr;
+      if (paged) {
+#pragma unroll
+        for (int j = 0; j < PF; ++j)
+          if (j < n_units) {
+            if (j > 0) cur_next(ca, meta, B, Hkv);
+            pq[j] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
+          }
+      }
       for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
         const int s = (int)(i % nst);
         const int key0 = c.t * KT;
+        const int page = pq[0];
+        if (paged) {
+#pragma unroll
+          for (int j = 0; j + 1 < PF; ++j) pq[j] = pq[j + 1];
+          if (i + PF < n_units) {
+            cur_next(ca, meta, B, Hkv);
+            pq[PF - 1] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
+          }
+        }
         if (i >= nst &&
             !mbar_wait(&empty[s], (uint32_t)(((i / nst) - 1) & 1), a.status, is_k ? 0x211u : 0x212u))
           break;
         uint64_t* bar = (key0 + KT > c.ctx) ? &land[s] : &full[s];
         uint8_t* st = ring + s * KV_TILE;
-        const int bh = c.b * Hkv + c.h;
+        const KvTile kt = paged ? kv_tile_page(a, page, c.h) : kv_tile(a, c.b, c.h, c.t);
         mbar_arrive_expect_tx(bar, KV_TILE);
-        tma_load_3d(st, tm, bar, 0, key0, bh);
-        tma_load_3d(st + KV_HALF, tm, bar, 64, key0, bh);
+        tma_load_3d(st, tm, bar, 0, kt.y, kt.z);
+        tma_load_3d(st + KV_HALF, tm, bar, 64, kt.y, kt.z);
       }
     }
     __syncwarp();
@@ -437,7 +485,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         ok = mbar_wait(&k_land[sk], (uint32_t)(n_land_k[sk]++ & 1), a.status, 0x213u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        tail_store<32>(v, smem + OFF_K + sk * KV_TILE, a.Kc, c, g, a.cap, c.b * Hkv + c.h, lane, false);
+        tail_store<32>(v, smem + OFF_K + sk * KV_TILE, a.Kc, g, kv_tile(a, c.b, c.h, c.t).row, lane, false);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&k_full[sk]);
@@ -624,7 +672,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       if (tail) {
         const int sv_ = (int)(i % ST_V);
         ok = ok && mbar_wait(&v_land[sv_], (uint32_t)(n_land_v[sv_]++ & 1), a.status, 0x214u);
-        tail_store<128>(vnew, smem + OFF_V + sv_ * KV_TILE, a.Vc, c, g, a.cap, c.b * Hkv + c.h, tid, true);
+        tail_store<128>(vnew, smem + OFF_V + sv_ * KV_TILE, a.Vc, g, kv_tile(a, c.b, c.h, c.t).row, tid, true);
         fence_proxy_async_smem();
         bar_compute();
         if (tid == 0) mbar_arrive(&v_full[sv_]);

@@ -115,6 +115,10 @@ struct AttnArgs {
   unsigned* counters;   // [B*Hkv]
   unsigned* status;
   int pair_cost;        // tcgen05 kernel: work charged per (sequence, kv head) pair, quarter tiles
+  // paged cache (tcgen05 kernel only; nullptr: the contiguous [B][Hkv][cap][D] layout): Kc / Vc are
+  // pools [Hkv][num_pages][128][D] and key tile t of sequence b is page block_table[b * max_pages + t]
+  const int32_t* block_table;
+  int max_pages, num_pages;
 };
 cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                              cudaStream_t s);

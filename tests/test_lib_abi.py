@@ -84,6 +84,11 @@ def test_host_side_validation(built):
     assert L.spec_lmhead_softmax(fake, 2, 64, fake, 126, 1.0, fake, fake, 1 << 30, None) == E
     # sampler: null outputs
     assert L.spec_reject_sample(fake, fake, fake, fake, fake, 3, 8, 1e-5, None, fake, fake, None) == E
+    # paged attention: no block table, no pages
+    assert L.spec_verify_attention_paged(fake, 32 * 128, fake, fake, 8 * 128, fake, fake, 2, 5, fake, fake, 4,
+                                         None, 2, 32, 8, 128, 0.1, fake, 32 * 128, fake, 1 << 30, None) == E
+    assert L.spec_verify_attention_paged(fake, 32 * 128, fake, fake, 8 * 128, fake, fake, 2, 5, fake, fake, 0,
+                                         fake, 2, 32, 8, 128, 0.1, fake, 32 * 128, fake, 1 << 30, None) == E
     # draft side: embedding with d not a multiple of 8, sampling rows with ldp < V, LM head ldp < V
     assert L.spec_embed(fake, 4, fake, 100, 12, 12, fake, 12, None) == E
     assert L.spec_sample_rows(fake, 10, 4, 16, fake, fake, None) == E
