@@ -107,11 +107,12 @@ int get_encoder() {
 }
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, rank-1 entries)
+constexpr CUtensorMapSwizzle kLinSwizzle = LIN_BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 int g_w_promotion = 2;    // tunable: L2 promotion of weight-tile loads (0 none, 1 64 B, 2 128 B, 3 256 B)
 
 int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                 const cuuint64_t* strides, const cuuint32_t* box, const char* what,
-                int promotion = 3) {
+                int promotion = 3, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   if (int rc = get_encoder()) return rc;
   cuuint32_t estr[3] = {1, 1, 1};
   static const CUtensorMapL2promotion kPromo[4] = {
@@ -119,7 +120,7 @@ int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* 
       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, kPromo[promotion & 3],
+                        swizzle, kPromo[promotion & 3],
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPEC_ECUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
   return SPEC_OK;
@@ -161,7 +162,7 @@ struct LinPlan {
 LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   LinPlan p;
   const int sms = plan_sms();
-  p.k_tiles = (K + 63) / 64;
+  p.k_tiles = (K + LIN_BK - 1) / LIN_BK;
   if (!lmhead && M <= g_gemv_max_m && M <= 4) {
     p.gemv = true;
     const int ks = gemv_k_slice(M);
@@ -216,10 +217,10 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
     for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
       const int cap = linear_cluster_capacity(p.BN, p.NSUB, S);
       if (cap <= 0 || tiles * S > cap) continue;
-      const long long cost = (p.k_tiles + S - 1) / S + 6;
+      const long long cost = (p.k_tiles + S - 1) / S + 6 * 64 / LIN_BK;
       if (best == 0 || cost < best_cost) { best = S; best_cost = cost; }
     }
-    const long long sk_cost = (p.units + sms - 1) / sms + 20;
+    const long long sk_cost = (p.units + sms - 1) / sms + 20 * 64 / LIN_BK;
     if (best >= 2 && best_cost < sk_cost) {
       p.cluster_S = best;
       p.grid = (int)(tiles * best);
@@ -431,14 +432,14 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
-    cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W", g_w_promotion)) return rc;
+    cuuint32_t box[2] = {LIN_BK, 128};
+    if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W", g_w_promotion, kLinSwizzle)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
-    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
+    cuuint32_t box[2] = {LIN_BK, (cuuint32_t)p.x_box_rows()};
+    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X", 3, kLinSwizzle)) return rc;
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
@@ -515,14 +516,14 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
-    cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, Wgu, 2, dims, str, box, "Wgu", g_w_promotion)) return rc;
+    cuuint32_t box[2] = {LIN_BK, 128};
+    if (int rc = encode_bf16(&tw, Wgu, 2, dims, str, box, "Wgu", g_w_promotion, kLinSwizzle)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
-    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X")) return rc;
+    cuuint32_t box[2] = {LIN_BK, (cuuint32_t)p.x_box_rows()};
+    if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X", 3, kLinSwizzle)) return rc;
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
@@ -555,14 +556,14 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)V};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, 128};
-    if (int rc = encode_bf16(&tw, Wlm, 2, dims, str, box, "Wlm", g_w_promotion)) return rc;
+    cuuint32_t box[2] = {LIN_BK, 128};
+    if (int rc = encode_bf16(&tw, Wlm, 2, dims, str, box, "Wlm", g_w_promotion, kLinSwizzle)) return rc;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.x_box_rows()};
-    if (int rc = encode_bf16(&tx, H, 2, dims, str, box, "H")) return rc;
+    cuuint32_t box[2] = {LIN_BK, (cuuint32_t)p.x_box_rows()};
+    if (int rc = encode_bf16(&tx, H, 2, dims, str, box, "H", 3, kLinSwizzle)) return rc;
   }
   const bool greedy = temperature == 0.f;
   LinearArgs a{};

@@ -147,6 +147,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ----------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor for a K-major operand stored by TMA with 64-byte swizzling:
+// rows of 32 bf16 (64 B), 8-row atoms 512 B apart.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= uint64_t((smem_addr & 0x3FFFFu) >> 4);          // start address
+  d |= uint64_t(1) << 16;                               // leading byte offset (unused here)
+  d |= uint64_t(512 >> 4) << 32;                        // stride byte offset: 8 rows * 64 B
+  d |= uint64_t(1) << 46;                               // descriptor version for sm_100 family
+  d |= uint64_t(4) << 61;                               // layout: 64-byte swizzle
+  return d;
+}
 // Shared-memory matrix descriptor for a K-major operand stored by TMA with
 // 128-byte swizzling: rows of 64 bf16 (128 B), 8-row atoms 1024 B apart.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {

@@ -95,10 +95,10 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
         const int i = k - k0, s = i % STAGES;
         if (i >= STAGES && !mbar_wait(&empty[s], (uint32_t)((i / STAGES - 1) & 1), args.status, 0x141u)) break;
         mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * 64, n_t * 128);
+        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
 #pragma unroll
         for (int sub = 0; sub < NSUB; ++sub)
-          tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * 128, &tm_x, &full[s], k * 64, m_t * TN + sub * BN);
+          tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);
       }
     }
     __syncwarp();
@@ -113,10 +113,10 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
         const uint32_t a = smem_u32(sA + s * Cfg::A_BYTES);
         const uint32_t b = smem_u32(sB + s * Cfg::B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < LIN_BK / 16; ++kk)
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            umma_bf16(tmem + sub * BN, umma_desc_sw128(a + kk * 32), umma_desc_sw128(b + sub * BN * 128 + kk * 32),
+            umma_bf16(tmem + sub * BN, umma_desc_lin(a + kk * 32), umma_desc_lin(b + sub * BN * LIN_ROW_BYTES + kk * 32),
                       idesc, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&empty[s]);
       }

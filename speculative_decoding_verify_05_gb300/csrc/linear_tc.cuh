@@ -58,17 +58,28 @@ struct LinearArgs {
   float2* stats;        // EPI_LOGITS / EPI_ARGMAX: [M][tiles_n] (max, sum) or (max, idx bits)
 };
 
+// k-step of the tensor-core GEMMs: LIN_BK bf16 per operand row and stage (one swizzle row of
+// LIN_ROW_BYTES): 64 with 128-byte swizzle, or 32 with 64-byte swizzle.  Half-size stages keep
+// more of the shared-memory ring in flight while the tensor core works on one of them, but each
+// weight row then arrives in 64-byte pieces: measured on GB300 the 32-wide step was 1.3-1.7x
+// slower on every verify shape (gate|up 89 -> 115 us, LM head 0.74 -> 1.22 ms), so 64 it is.
+constexpr int LIN_BK = 64;
+constexpr int LIN_ROW_BYTES = LIN_BK * 2;
+__device__ __forceinline__ uint64_t umma_desc_lin(uint32_t smem_addr) {
+  return LIN_BK == 64 ? umma_desc_sw128(smem_addr) : umma_desc_sw64(smem_addr);
+}
+
 // A CTA tile is 128 weight rows x TN = NSUB * BN verify rows: NSUB MMAs of N = BN per
 // k-substep share one weight tile, so with up to 512 verify rows every weight byte is
 // read from HBM once.
 template <int BN, int NSUB>
 struct LinearCfg {
   static constexpr int TN = BN * NSUB;
-  static constexpr int A_BYTES = 128 * 64 * 2;
-  static constexpr int B_BYTES = TN * 64 * 2;
+  static constexpr int A_BYTES = 128 * LIN_ROW_BYTES;
+  static constexpr int B_BYTES = TN * LIN_ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
   // accumulator buffer: power-of-two columns >= TN; two buffers when they fit in TMEM
   static constexpr int ACC_COLS = TN <= 16 ? 16 : (TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512))));
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;

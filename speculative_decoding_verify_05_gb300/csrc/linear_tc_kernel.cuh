@@ -186,14 +186,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const int m_t = (int)(g.tile % args.tiles_m);
         const int n_t = (int)(g.tile / args.tiles_m) * CL + rank;   // past the last tile: zero fill
         mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * 64, n_t * 128);
+        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
         if (CL == 1) {
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * 128, &tm_x, &full[s], k * 64, m_t * TN + sub * BN);
+            tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);
         } else {
           const int rows = TN / CL;
-          tma_load_2d_mc(sB + s * Cfg::B_BYTES + rank * rows * 128, &tm_x, &full[s], k * 64,
+          tma_load_2d_mc(sB + s * Cfg::B_BYTES + rank * rows * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK,
                          m_t * TN + rank * rows, mc_mask);
         }
         issued = i + 1;
@@ -226,10 +226,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           const uint32_t a = smem_u32(sA + s * Cfg::A_BYTES);
           const uint32_t b = smem_u32(sB + s * Cfg::B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < LIN_BK / 16; ++kk)
 #pragma unroll
             for (int sub = 0; sub < NSUB; ++sub)
-              umma_bf16(d + sub * BN, umma_desc_sw128(a + kk * 32), umma_desc_sw128(b + sub * BN * 128 + kk * 32),
+              umma_bf16(d + sub * BN, umma_desc_lin(a + kk * 32), umma_desc_lin(b + sub * BN * LIN_ROW_BYTES + kk * 32),
                         idesc, (uu > u || kk > 0) ? 1u : 0u);
           if (CL > 1) umma_commit_mc(&empty[s], mc_mask);
           else umma_commit(&empty[s]);
