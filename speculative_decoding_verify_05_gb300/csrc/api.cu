@@ -151,6 +151,8 @@ struct LinPlan {
   int grid = 1;                 // persistent work groups of the tensor-core path (clusters of cl CTAs)
   int cl = 1;                   // CTAs per cluster sharing each token tile (TMA multicast)
   int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
+  int rem_S = 0;                // > 0: whole tiles on the persistent kernel, then the remaining
+  long long rem_tiles = 0;      //      rem_tiles on the cluster split-K kernel (S = rem_S)
   int x_box_rows() const { return cl > 1 ? BN * NSUB / cl : BN; }   // token rows per TMA load
   bool aligned = false;         // whole tiles only (no stream-K region)
   long long dp_tiles = 0, sk_units = 0;
@@ -211,7 +213,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   // tiles * S CTAs).  Cost model in k-steps of one tile on one SM: the cluster kernel takes
   // ceil(kt / S) plus ~6 for its on-chip reduction; stream-K takes ceil(units / SMs) plus
   // ~20 when tiles are split (fp32 pieces through L2 and a second kernel)
-  if (!lmhead && !swiglu && g_linear_cluster && g_force_grid == 0 && tiles < sms) {
+  if (!lmhead && g_linear_cluster && g_force_grid == 0 && tiles < sms) {
     int best = 0;
     long long best_cost = 0;
     for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
@@ -243,6 +245,31 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
     }
   const long long ctiles = (long long)p.tiles_m * ((p.tiles_n + p.cl - 1) / p.cl);
   p.units = ctiles * p.k_tiles;
+  // many tiles, not a multiple of the SM count: the whole tiles one per CTA (none split) on the
+  // persistent kernel, then the remainder on the cluster split-K kernel (on-chip sums: no fp32
+  // pieces through L2, no reduce kernel), when that costs fewer k-steps than stream-K
+  if (!lmhead && g_linear_cluster && g_force_grid == 0 && p.cl == 1 && tiles > sms && tiles % sms != 0 &&
+      !p.aligned) {
+    const long long rem = tiles % sms;
+    int best = 0;
+    long long best_cost = 0;
+    for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
+      const int cap = linear_cluster_capacity(p.BN, p.NSUB, S);
+      if (cap <= 0 || rem * S > cap) continue;
+      const long long cost = (p.k_tiles + S - 1) / S + 6 * 64 / LIN_BK;
+      if (best == 0 || cost < best_cost) { best = S; best_cost = cost; }
+    }
+    const long long sk_cost = (p.units + sms - 1) / sms + 20 * 64 / LIN_BK;
+    if (best >= 2 && (tiles / sms) * p.k_tiles + best_cost < sk_cost) {
+      p.rem_S = best;
+      p.rem_tiles = rem;
+      p.grid = sms;
+      p.dp_tiles = tiles - rem;
+      p.sk_units = 0;
+      p.bytes = 0;
+      return p;
+    }
+  }
   int grid = g_force_grid > 0 ? g_force_grid : (p.cl > 1 ? std::min(cl_cap, sms / p.cl) : sms);
   const long long cap_units = p.aligned ? ctiles : p.units;
   if (grid > cap_units) grid = (int)cap_units;
@@ -457,6 +484,11 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   dim3 grid(p.grid * p.cl);
   cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
+  if (p.rem_S > 0) {   // the tiles after a.dp_tiles: cluster split-K
+    e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.rem_S, (int)p.rem_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch (remainder)");
+    return ok(2);
+  }
   if (p.bytes == 0) return ok(1);
   // some tiles had their k-steps split between CTAs: a second kernel sums their pieces
   e = launch_linear_reduce(a, plan_sms(), s);
@@ -533,8 +565,18 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
+  if (p.cluster_S > 0) {
+    cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cluster swiglu linear launch");
+    return ok(1);
+  }
   cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid * p.cl), s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 swiglu linear launch");
+  if (p.rem_S > 0) {
+    e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.rem_S, (int)p.rem_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cluster swiglu linear launch (remainder)");
+    return ok(2);
+  }
   if (p.bytes == 0) return ok(1);
   e = launch_linear_reduce(a, plan_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");

@@ -64,7 +64,9 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int tile = blockIdx.x / S;                 // a cluster is S consecutive blocks
+  // a cluster is S consecutive blocks; tiles start at args.dp_tiles (the tiles before it are whole
+  // tiles of a persistent launch that ran first)
+  const int tile = (int)args.dp_tiles + blockIdx.x / S;
   const int kt = args.k_tiles;
   const int k0 = (int)((long long)kt * rank / S), k1 = (int)((long long)kt * (rank + 1) / S);
   const int m_t = tile % args.tiles_m, n_t = tile / args.tiles_m;
@@ -171,7 +173,43 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   // Item = (chunk, 8 consecutive weight rows): 4 tokens x 8 rows, so the residual and Y move
   // in 16-byte pieces (8 bf16 of one token row).
   const int n_chunks = min(cpr, TN / 4 - (int)rank * cpr);
-  const int items = (n_chunks > 0 ? n_chunks : 0) * 16;
+  if (args.epi == EPI_SWIGLU) {
+    // gate and up rows interleaved per 16: item = (chunk, 8 gate rows r8..r8+7 with r8 % 32 < 16);
+    // the matching up rows are r8+16..; 8 outputs per token at column n_t 64 + (r8 / 32) 16 + r8 % 32
+    const int sitems = (n_chunks > 0 ? n_chunks : 0) * 8;
+    for (int it = threadIdx.x; it < sitems; it += 192) {
+      const int kk = it >> 3, q8 = it & 7, r8 = (q8 >> 1) * 32 + (q8 & 1) * 8;
+      float g[8][4], u[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 vg = slots[kk * 128 + slot_row(r8 + i)];
+        const float4 vu = slots[kk * 128 + slot_row(r8 + 16 + i)];
+        g[i][0] = vg.x; g[i][1] = vg.y; g[i][2] = vg.z; g[i][3] = vg.w;
+        u[i][0] = vu.x; u[i][1] = vu.y; u[i][2] = vu.z; u[i][3] = vu.w;
+      }
+      for (int s2 = 1; s2 < S; ++s2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 vg = slots[(s2 * cpr + kk) * 128 + slot_row(r8 + i)];
+          const float4 vu = slots[(s2 * cpr + kk) * 128 + slot_row(r8 + 16 + i)];
+          g[i][0] += vg.x; g[i][1] += vg.y; g[i][2] += vg.z; g[i][3] += vg.w;
+          u[i][0] += vu.x; u[i][1] += vu.y; u[i][2] += vu.z; u[i][3] += vu.w;
+        }
+      }
+      const int n = n_t * 64 + (r8 >> 5) * 16 + (r8 & 31);
+      const int mb = m_t * TN + ((int)rank * cpr + kk) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (mb + e >= args.M) break;
+        uint32_t o4[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          o4[h] = pack_bf16x2(silu(g[2 * h][e]) * u[2 * h][e], silu(g[2 * h + 1][e]) * u[2 * h + 1][e]);
+        *reinterpret_cast<uint4*>(args.Y + (size_t)(mb + e) * args.ldy + n) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+  }
+  const int items = (args.epi == EPI_SWIGLU || n_chunks <= 0) ? 0 : n_chunks * 16;
   for (int it = threadIdx.x; it < items; it += 192) {
     const int kk = it >> 4, r8 = (it & 15) * 8;
     float acc[8][4];
