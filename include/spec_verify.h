@@ -155,6 +155,27 @@ SPEC_API int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ld
                                         spec_bf16* Y, int ldy,
                                         const spec_bf16* residual, int ldr, spec_stream stream);
 
+/* Fused QKV projection and rotary embedding: Y = X W^T, then the first
+ * rope_heads 128-column heads of Y (the query and key heads of a fused QKV
+ * output) rotated as spec_rope does (rotate-half pairs (i, i + 64)), with the
+ * rotation of row r taken from cs (spec_rope_table).  When the projection has
+ * few weight tiles (the cluster split-K plan) the rotation happens on the
+ * fp32 sums before the single rounding to bf16 and no extra kernel runs;
+ * otherwise Y is rounded, then rotated by a second kernel (one more bf16
+ * rounding of q and k, within the linear tolerance).
+ *   X, W, Y as spec_verify_linear (no residual); cs [M x 64] pairs of fp32
+ *   (cos, sin), 16-byte aligned.  Requires rope_heads * 128 <= N.
+ * Workspace: spec_linear_workspace_bytes(M, N, K). */
+SPEC_API int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                                     int ldw, spec_bf16* Y, int ldy, const float* cs, int rope_heads,
+                                     void* workspace, size_t workspace_bytes, spec_stream stream);
+/* The rotation table of a verify pass: cs[r][i] = (cos, sin) of p_r * theta^(-2i/D),
+ * i < D/2, p_r = ctx_len[b] + (r - cu_rows[b]) the position of row r; the angle is
+ * formed and reduced mod 2 pi in fp64, then one fp32 sincos (as spec_rope).
+ *   cs [M x D/2] pairs of fp32 out.  Requires D even, D <= 256, theta > 0. */
+SPEC_API int spec_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, int D, float theta,
+                             float* cs, spec_stream stream);
+
 /* Fused gate|up projection and SwiGLU activation of the MLP:
  *   A[r, i] = silu(gate[r, i]) * up[r, i],  gate = X Wg^T, up = X Wu^T,
  * silu(g) = g / (1 + e^-g), fp32 from the fp32 accumulators, one bf16 rounding.

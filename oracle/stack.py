@@ -33,6 +33,9 @@ class Dims:
     # True: gate and up are rounded to bf16 before the SwiGLU product (they are stored
     # between two steps); False: the product takes them unrounded (one fused step)
     gate_up_bf16: bool = False
+    # True: q and k are rounded to bf16 before RoPE (projection and rotation as two steps); False:
+    # rotated from the unrounded projection, one rounding (RoPE in the projection's epilogue)
+    qkv_bf16_before_rope: bool = False
 
 
 @dataclass
@@ -64,10 +67,12 @@ def layer_forward(x, lw: LayerWeights, dims: Dims, cu_rows, ctx_len, Kc, Vc):
     pos = np.concatenate([ctx_len[b] + np.arange(cu_rows[b + 1] - cu_rows[b])
                           for b in range(len(cu_rows) - 1)]) if M else np.zeros(0)
     h = r16(ops.rmsnorm(x, decode(lw.attn_norm), dims.eps))
-    qkv = r16(ops.linear(h, decode(lw.w_qkv)))
+    qkv = ops.linear(h, decode(lw.w_qkv))
+    if dims.qkv_bf16_before_rope:
+        qkv = r16(qkv)
     q = qkv[:, :Hq * D].reshape(M, Hq, D)
     k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(M, Hkv, D)
-    v = qkv[:, (Hq + Hkv) * D:].reshape(M, Hkv, D)
+    v = r16(qkv[:, (Hq + Hkv) * D:]).reshape(M, Hkv, D)
     q = r16(ops.rope(q, pos, dims.theta))
     k = r16(ops.rope(k, pos, dims.theta))
     o, Kc, Vc = ops.verify_attention(q, k, v, cu_rows, Kc, Vc, ctx_len, 1.0 / np.sqrt(D))

@@ -30,6 +30,8 @@ _SIGS = {
     "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
+    "spec_verify_linear_rope": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
+    "spec_rope_table": (_i, [_vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "spec_swiglu_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear_swiglu": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_attention_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -210,6 +212,37 @@ def spec_verify_linear_noalloc(X, W, Y, residual=None, stream=None):
         _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
         _stream(stream)), True)
+    return Y
+
+
+def spec_rope_table(cu_rows, ctx_len, M: int, D: int, theta: float = 1e6, cs=None, stream=None):
+    """(cos, sin) per verify row and frequency: cs [M, D/2, 2] fp32."""
+    _need(cu_rows, torch.int32, "cu_rows"); _need(ctx_len, torch.int32, "ctx_len")
+    B = cu_rows.numel() - 1
+    if cs is None:
+        cs = torch.empty((M, D // 2, 2), dtype=torch.float32, device=cu_rows.device)
+    _need(cs, torch.float32, "cs")
+    if not cs.is_contiguous():
+        raise ValueError("cs must be contiguous")
+    _check(_lib.spec_rope_table(_p(cu_rows), _p(ctx_len), B, M, D, float(theta), _p(cs), _stream(stream)), True)
+    return cs
+
+
+def spec_verify_linear_rope(X, W, cs, rope_heads: int, Y=None, ws: Workspace | None = None, stream=None):
+    """Y = X W^T with the first rope_heads 128-column heads rotated by the table cs [M, 64, 2]."""
+    _need(X, torch.bfloat16, "X"); _need(W, torch.bfloat16, "W"); _need(cs, torch.float32, "cs")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("W must be [N, K]")
+    if not cs.is_contiguous() or cs.shape[0] < M:
+        raise ValueError("cs must be a contiguous table with a row per verify row")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _need(Y, torch.bfloat16, "Y")
+    wp, wn = _ws_args(ws, spec_linear_workspace_bytes(M, N, K), X.device)
+    _check(_lib.spec_verify_linear_rope(_p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y),
+                                        _rowmajor(Y, "Y"), _p(cs), int(rope_heads), wp, wn, _stream(stream)), True)
     return Y
 
 

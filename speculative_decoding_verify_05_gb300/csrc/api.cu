@@ -496,6 +496,79 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   return ok(2);
 }
 
+// --------------------------------------------------------------------------- linear + RoPE
+int spec_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, int D, float theta, float* cs,
+                    spec_stream stream) {
+  if (M < 0 || B < 0) return fail(SPEC_EINVAL, "bad sizes M=%d B=%d", M, B);
+  if (M == 0) return ok();
+  if (B == 0) return fail(SPEC_EINVAL, "rows without sequences");
+  if (!cu_rows || !ctx_len || !cs) return fail(SPEC_EINVAL, "NULL argument");
+  if (D <= 0 || D % 2 || D > 256) return fail(SPEC_EUNSUPPORTED, "D=%d must be even and <= 256", D);
+  if (!(theta > 0.f) || std::isinf(theta)) return fail(SPEC_EINVAL, "theta must be finite and > 0");
+  cudaError_t e = launch_rope_table(cu_rows, ctx_len, B, M, D, theta, reinterpret_cast<float2*>(cs),
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope_table launch");
+  return ok(1);
+}
+
+int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                            spec_bf16* Y, int ldy, const float* cs, int rope_heads, void* workspace,
+                            size_t workspace_bytes, spec_stream stream) {
+  constexpr int HD = 128;   // head size: one weight tile of the GEMM is one head
+  if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
+  if (M == 0) return ok();
+  if (rope_heads < 0 || (long long)rope_heads * HD > N)
+    return fail(SPEC_EINVAL, "rope_heads=%d heads of 128 do not fit in N=%d", rope_heads, N);
+  if (rope_heads > 0 && !cs) return fail(SPEC_EINVAL, "cs must be non-NULL");
+  if (rope_heads > 0 && !aligned16(cs)) return fail(SPEC_EINVAL, "cs must be 16-byte aligned");
+  const LinPlan p = plan_linear(M, N, K, false);
+  if (rope_heads > 0 && p.cluster_S > 0 && !p.gemv) {
+    // few weight tiles: the cluster split-K kernel rotates the q / k heads in its epilogue
+    if (!X || !W || !Y) return fail(SPEC_EINVAL, "X, W and Y must be non-NULL");
+    if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
+    if (ldx < K || ldw < K || ldy < N || ldx % 8 || ldw % 8 || ldy % 8)
+      return fail(SPEC_EINVAL, "bad leading dimensions");
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return fail(SPEC_EINVAL, "X, W, Y must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    if (int rc = dev_info(&d)) return rc;
+    CUtensorMap tw, tx;
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+      cuuint64_t str[1] = {(cuuint64_t)ldw * 2};
+      cuuint32_t box[2] = {LIN_BK, 128};
+      if (int rc = encode_bf16(&tw, W, 2, dims, str, box, "W", g_w_promotion, kLinSwizzle)) return rc;
+    }
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+      cuuint64_t str[1] = {(cuuint64_t)ldx * 2};
+      cuuint32_t box[2] = {LIN_BK, (cuuint32_t)p.x_box_rows()};
+      if (int rc = encode_bf16(&tx, X, 2, dims, str, box, "X", 3, kLinSwizzle)) return rc;
+    }
+    LinearArgs a{};
+    a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
+    a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+    a.Y = Y; a.ldy = ldy; a.residual = nullptr; a.ldr = 0;
+    a.status = d->status;
+    a.tn = p.BN * p.NSUB;
+    a.epi = EPI_ROPE;
+    a.rope_cs = reinterpret_cast<const float2*>(cs);
+    a.rope_tiles = rope_heads;
+    cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cluster linear + rope launch");
+    return ok(1);
+  }
+  // otherwise the plain product, then the rotation from the table
+  if (int rc = spec_verify_linear(X, M, K, ldx, W, N, ldw, Y, ldy, nullptr, 0, workspace, workspace_bytes, stream))
+    return rc;
+  const int n_lin = t_launches;
+  if (rope_heads == 0) return ok(n_lin);
+  cudaError_t e = launch_rope_apply(Y, ldy, rope_heads, HD, reinterpret_cast<const float2*>(cs), M,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope_apply launch");
+  return ok(n_lin + 1);
+}
+
 // --------------------------------------------------------------------------- fused SwiGLU linear
 // Scratch for the CUDA-core path: the GEMV writes the interleaved gate|up rows to the workspace,
 // after its own split-K scratch and never inside the counter region (which every kernel that

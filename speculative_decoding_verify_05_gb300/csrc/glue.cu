@@ -65,6 +65,26 @@ rmsnorm_kernel(const uint16_t* __restrict__ X, int N, int ldx, const uint16_t* _
 
 constexpr int ROPE_THREADS = 256;
 
+// (cos, sin) of pos * inv: the angle is formed and reduced to [-pi, pi] in fp64, then one fp32
+// sincos (an fp32 angle would be off by up to 5e-4 rad at position 8192).
+__device__ __forceinline__ float2 rope_cs(int pos, double inv) {
+  const double ang = (double)pos * inv;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double red = ang - two_pi * rint(ang / two_pi);
+  float sv, cv;
+  sincosf((float)red, &sv, &cv);
+  return make_float2(cv, sv);
+}
+// Position of row r = ctx_len[b] + (r - cu_rows[b]), b the last sequence with cu_rows[b] <= r.
+__device__ __forceinline__ int row_position(int r, const int32_t* cu_rows, const int32_t* ctx_len, int B) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_rows[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return ctx_len[lo] + (r - cu_rows[lo]);
+}
+
 // Inverse frequencies theta^(-2 i / D), computed once in fp64 on the host.
 struct RopeFreq {
   double inv[128];
@@ -98,15 +118,9 @@ rope_kernel(uint16_t* __restrict__ Q, int ldq, int Hq, uint16_t* __restrict__ K,
   }
   __syncthreads();
   if (threadIdx.x < half) {
-    // angle in fp64, reduced to [-pi, pi] before the fp32 sincos
-    const int i = threadIdx.x;
-    const double ang = (double)s_pos * f.inv[i];
-    const double two_pi = 6.283185307179586476925286766559;
-    const double red = ang - two_pi * rint(ang / two_pi);
-    float sv, cv;
-    sincosf((float)red, &sv, &cv);
-    s_cos[i] = cv;
-    s_sin[i] = sv;
+    const float2 cs = rope_cs(s_pos, f.inv[threadIdx.x]);
+    s_cos[threadIdx.x] = cs.x;
+    s_sin[threadIdx.x] = cs.y;
   }
   __syncthreads();
   const int heads = Hq + Hkv;
@@ -220,6 +234,38 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, int M, const uint1
   }
 }
 
+// cs[r][i] = (cos, sin) of row r's position times theta^(-2 i / D), i < D / 2: the rotation of a
+// verify pass, computed once and read by every layer's fused QKV epilogue (or rope_apply_kernel).
+__global__ void rope_table_kernel(const int32_t* __restrict__ cu_rows, const int32_t* __restrict__ ctx_len, int B,
+                                  int M, int half, const __grid_constant__ RopeFreq f, float2* __restrict__ cs) {
+  pdl_wait();
+  pdl_trigger();
+  const int total = M * half;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+    const int r = idx / half, i = idx - r * half;
+    cs[idx] = rope_cs(row_position(r, cu_rows, ctx_len, B), f.inv[i]);
+  }
+}
+
+// In-place rotate-half on `heads` heads of D at Y + r*ldy + h*D, angles from the table.
+__global__ void __launch_bounds__(ROPE_THREADS)
+rope_apply_kernel(uint16_t* __restrict__ Y, int ldy, int heads, int D, const float2* __restrict__ cs) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x;
+  const int half = D / 2;
+  const float2* row = cs + (size_t)r * half;
+  for (int idx = threadIdx.x; idx < heads * half; idx += ROPE_THREADS) {
+    const int hd = idx / half, i = idx - hd * half;
+    uint16_t* base = Y + (size_t)r * ldy + (size_t)hd * D;
+    const float a = bf16f(base[i]);
+    const float b = bf16f(base[i + half]);
+    const float2 t = row[i];
+    base[i] = f2bf(a * t.x - b * t.y);
+    base[i + half] = f2bf(b * t.x + a * t.y);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
@@ -267,6 +313,23 @@ cudaError_t launch_embed(const int32_t* ids, int M, const uint16_t* table, int V
   if (grid > 152 * 16) grid = 152 * 16;
   if (grid < 1) grid = 1;
   cudaError_t e = launch_k(embed_kernel, dim3(grid), dim3(256), 0, s, ids, M, table, V, d, ldt, X, ldx, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, int D, float theta,
+                              float2* cs, cudaStream_t s) {
+  RopeFreq f{};
+  for (int i = 0; i < D / 2; ++i) f.inv[i] = std::pow((double)theta, -2.0 * (double)i / (double)D);
+  const int total = M * (D / 2);
+  int grid = (total + 255) / 256;
+  if (grid > 152 * 8) grid = 152 * 8;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_k(rope_table_kernel, dim3(grid), dim3(256), 0, s, cu_rows, ctx_len, B, M, D / 2, f, cs);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_rope_apply(uint16_t* Y, int ldy, int heads, int D, const float2* cs, int M, cudaStream_t s) {
+  cudaError_t e = launch_k(rope_apply_kernel, dim3(M), dim3(ROPE_THREADS), 0, s, Y, ldy, heads, D, cs);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -162,6 +162,9 @@ cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint1
 cudaError_t launch_rope(uint16_t* Q, int ldq, int Hq, uint16_t* K, int ldk, int Hkv, int D,
                         const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, float theta,
                         cudaStream_t s);
+cudaError_t launch_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, int D, float theta,
+                              float2* cs, cudaStream_t s);
+cudaError_t launch_rope_apply(uint16_t* Y, int ldy, int heads, int D, const float2* cs, int M, cudaStream_t s);
 cudaError_t launch_silu_mul(const uint16_t* GU, int M, int I, int ldgu, uint16_t* A, int lda,
                             cudaStream_t s);
 cudaError_t launch_embed(const int32_t* ids, int M, const uint16_t* table, int V, int d, int ldt, uint16_t* X,

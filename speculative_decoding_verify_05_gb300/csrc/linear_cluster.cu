@@ -209,7 +209,51 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
       }
     }
   }
-  const int items = (args.epi == EPI_SWIGLU || n_chunks <= 0) ? 0 : n_chunks * 16;
+  // RoPE heads: item = (chunk, 8 dims r8..r8+7 of the first half); the pair dims r8+64.. rotate
+  // with them: (a, b) -> (a c - b s, b c + a s), c, s from row m's table entry for dim r8 + i
+  const bool rope = args.epi == EPI_ROPE && n_t < args.rope_tiles;
+  if (rope) {
+    const int ritems = (n_chunks > 0 ? n_chunks : 0) * 8;
+    for (int it = threadIdx.x; it < ritems; it += 192) {
+      const int kk = it >> 3, r8 = (it & 7) * 8;
+      float a[8][4], b[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 va = slots[kk * 128 + slot_row(r8 + i)];
+        const float4 vb = slots[kk * 128 + slot_row(r8 + 64 + i)];
+        a[i][0] = va.x; a[i][1] = va.y; a[i][2] = va.z; a[i][3] = va.w;
+        b[i][0] = vb.x; b[i][1] = vb.y; b[i][2] = vb.z; b[i][3] = vb.w;
+      }
+      for (int s2 = 1; s2 < S; ++s2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 va = slots[(s2 * cpr + kk) * 128 + slot_row(r8 + i)];
+          const float4 vb = slots[(s2 * cpr + kk) * 128 + slot_row(r8 + 64 + i)];
+          a[i][0] += va.x; a[i][1] += va.y; a[i][2] += va.z; a[i][3] += va.w;
+          b[i][0] += vb.x; b[i][1] += vb.y; b[i][2] += vb.z; b[i][3] += vb.w;
+        }
+      }
+      const int n = n_t * 128 + r8;
+      const int mb = m_t * TN + ((int)rank * cpr + kk) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = mb + e;
+        if (m >= args.M) break;
+        const float2* cs = args.rope_cs + (size_t)m * 64 + r8;
+        uint32_t x4[4], y4[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 c0 = cs[2 * h], c1 = cs[2 * h + 1];
+          const float a0 = a[2 * h][e], a1 = a[2 * h + 1][e], b0 = b[2 * h][e], b1 = b[2 * h + 1][e];
+          x4[h] = pack_bf16x2(a0 * c0.x - b0 * c0.y, a1 * c1.x - b1 * c1.y);
+          y4[h] = pack_bf16x2(b0 * c0.x + a0 * c0.y, b1 * c1.x + a1 * c1.y);
+        }
+        *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n) = make_uint4(x4[0], x4[1], x4[2], x4[3]);
+        *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n + 64) = make_uint4(y4[0], y4[1], y4[2], y4[3]);
+      }
+    }
+  }
+  const int items = (args.epi == EPI_SWIGLU || rope || n_chunks <= 0) ? 0 : n_chunks * 16;
   for (int it = threadIdx.x; it < items; it += 192) {
     const int kk = it >> 4, r8 = (it & 15) * 8;
     float acc[8][4];

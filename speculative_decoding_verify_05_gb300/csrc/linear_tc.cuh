@@ -31,7 +31,9 @@ enum LinearEpilogue : int {
   EPI_BF16 = 0,        // Y = acc (+ residual) -> bf16
   EPI_LOGITS = 1,      // P = acc * inv_temp (fp32) + per-tile (max, sum exp) per token
   EPI_ARGMAX = 2,      // per-tile (max, argmax) per token only
-  EPI_SWIGLU = 3       // weight rows interleaved per 64 (gate block, up block): Y = silu(gate) * up
+  EPI_SWIGLU = 3,      // weight rows interleaved per 16 (gate block, up block): Y = silu(gate) * up
+  EPI_ROPE = 4         // cluster kernel: 128-column heads n_t < rope_tiles rotated (rotate-half) with
+                       // the per-row (cos, sin) table rope_cs [M][64] before rounding
 };
 
 struct LinearArgs {
@@ -52,6 +54,8 @@ struct LinearArgs {
   int tn;               // token columns per tile (BN * NSUB)
   int epi;              // the reduce kernel's epilogue: EPI_BF16 (+ residual) or EPI_SWIGLU
   unsigned* status;     // library status word (bounded-wait timeouts)
+  const float2* rope_cs;  // EPI_ROPE
+  int rope_tiles;
   float inv_temp;       // EPI_LOGITS
   float* P;             // EPI_LOGITS: [M x N] fp32, leading dimension ldp
   long long ldp;

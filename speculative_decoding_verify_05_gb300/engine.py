@@ -108,11 +108,13 @@ class VerifyEngine:
     """Buffers + call sequence of one verify pass / round for up to ``max_M`` rows."""
 
     def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, max_M: int, max_rows: int,
-                 device=None, fused_swiglu: bool = True, fused_sampler: bool = True):
+                 device=None, fused_swiglu: bool = True, fused_sampler: bool = True, fused_rope: bool = True):
         self.dims = dims
         self.w = weights
         # verify_round: LM head and sampler in one call that never materialises p
         self.fused_sampler = fused_sampler
+        # RoPE applied by the QKV projection from a per-pass (cos, sin) table (head size 128 only)
+        self.fused_rope = fused_rope and dims.D == 128
         self.fused_swiglu = fused_swiglu and dims.I % 64 == 0
         want = "interleaved" if self.fused_swiglu else "split"
         for lw in weights.layers:
@@ -130,6 +132,7 @@ class VerifyEngine:
         self.o = torch.empty((max_M, dims.Hq * dims.D), **bf)
         self.gu = None if self.fused_swiglu else torch.empty((max_M, 2 * dims.I), **bf)
         self.a = torch.empty((max_M, dims.I), **bf)
+        self.cs = torch.empty((max_M, dims.D // 2, 2), dtype=torch.float32, device=dev)
         self.P = torch.empty((max_M, dims.V), dtype=torch.float32, device=dev) if weights.w_lm is not None else None
         B, cap = (kcaches[0].shape[0], kcaches[0].shape[2]) if kcaches else (1, 1)
         need = 0
@@ -154,9 +157,13 @@ class VerifyEngine:
         hq = dm.Hq * dm.D
         hk = dm.Hkv * dm.D
         S.spec_rmsnorm(x, lw.attn_norm, dm.eps, Y=h)
-        S.spec_verify_linear(h, lw.w_qkv, Y=qkv, ws=self.ws)
+        if self.fused_rope:
+            S.spec_verify_linear_rope(h, lw.w_qkv, self.cs[:M], dm.Hq + dm.Hkv, Y=qkv, ws=self.ws)
+        else:
+            S.spec_verify_linear(h, lw.w_qkv, Y=qkv, ws=self.ws)
         q, k, v = qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:]
-        S.spec_rope(q, k, cu_rows, ctx_len, dm.D, dm.theta)
+        if not self.fused_rope:
+            S.spec_rope(q, k, cu_rows, ctx_len, dm.D, dm.theta)
         S.spec_verify_attention(q, k, v, cu_rows, ctx_len, self.kc[li], self.vc[li], max_rows, O=o,
                                 ws=self.ws)
         S.spec_verify_linear(o, lw.w_o, Y=x, residual=x, ws=self.ws)
@@ -178,6 +185,8 @@ class VerifyEngine:
         if x0.data_ptr() != self.x.data_ptr():
             self.x[:M].copy_(x0)
         L = len(self.w.layers) if n_layers is None else n_layers
+        if self.fused_rope and L > 0:
+            S.spec_rope_table(cu_rows, ctx_len, M, self.dims.D, self.dims.theta, cs=self.cs[:M])
         for li in range(L):
             self.layer(li, M, cu_rows, ctx_len, B, max_rows)
         if self.w.w_lm is not None:

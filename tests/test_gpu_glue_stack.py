@@ -168,3 +168,42 @@ def test_config1_round(lib):
     if near.cpu().numpy()[0] == 0 and near_ref[0] == 0:
         assert int(n.cpu()[0]) == int(n_ref[0])
         assert np.array_equal(t.cpu().numpy(), t_ref)
+
+
+def test_rope_table(lib):
+    batch = synth.RaggedBatch([4, 0, 10, 2], [8190, 0, 333, 70000])
+    D, theta = 128, 1e6
+    cs = lib.spec_rope_table(dev(batch.cu_rows), dev(batch.ctx_len), batch.M, D, theta)
+    lib.spec_device_status()
+    pos = np.concatenate([batch.ctx_len[b] + np.arange(batch.gammas[b] + 1) for b in range(batch.B)])
+    ang = pos[:, None].astype(np.float64) * theta ** (-2.0 * np.arange(D // 2) / D)[None, :]
+    got = cs.cpu().numpy().astype(np.float64)
+    assert np.abs(got[..., 0] - np.cos(ang)).max() < 2e-6
+    assert np.abs(got[..., 1] - np.sin(ang)).max() < 2e-6
+
+
+@pytest.mark.parametrize("M,Hq,Hkv,K", [(368, 32, 8, 4096), (5, 32, 8, 4096), (37, 8, 4, 512)])
+def test_linear_rope_fused(lib, M, Hq, Hkv, K):
+    """Q/K heads rotated by the projection (cluster epilogue at 368 rows, GEMM + rotate otherwise)."""
+    rng = np.random.default_rng(M)
+    B = max(1, M // 6)
+    gam = np.full(B, M // B - 1)
+    gam[-1] += M - int((gam + 1).sum())
+    batch = synth.RaggedBatch(gam, rng.integers(0, 8000, size=B))
+    D = 128
+    N = (Hq + 2 * Hkv) * D
+    X = synth.normal_bf16_bits(M + 1, (M, K), 1.0)
+    W = synth.normal_bf16_bits(M + 2, (N, K), 0.02)
+    cs = lib.spec_rope_table(dev(batch.cu_rows), dev(batch.ctx_len), M, D, 1e6)
+    lib.reset_launch_count()
+    Y = lib.spec_verify_linear_rope(bf16_dev(X), bf16_dev(W), cs, Hq + Hkv)
+    fused = lib.launch_count() == 1          # rotated in the epilogue; else GEMM, then rotate
+    lib.spec_device_status()
+    pos = np.concatenate([batch.ctx_len[b] + np.arange(batch.gammas[b] + 1) for b in range(batch.B)])
+    y = oops.linear(obf.decode(X), obf.decode(W))
+    if not fused:                            # the two-step path rotates the bf16-rounded q and k
+        y = obf.round_to_bf16(y)
+    ref = y.copy()
+    qk = y[:, :(Hq + Hkv) * D].reshape(M, Hq + Hkv, D)
+    ref[:, :(Hq + Hkv) * D] = oops.rope(qk, pos, 1e6).reshape(M, -1)
+    assert_close_rel(f64_of_bf16(Y), ref, f"linear + rope M={M}")
