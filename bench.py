@@ -771,7 +771,7 @@ def run_profile_case(args):
     """Small, self-contained launches of one hot kernel for an ncu capture (no timing).
 
     round: one full verify round of the benchmark workload (for the launch list);
-    attention: one layer of B=16 ragged sequences (KV ~0.6 GB, above L2);
+    attention: one layer of --batch (16) ragged sequences (KV ~0.6 GB at 16, above L2);
     linear: one gate|up projection (201 MB of weights) at --rows rows;
     swiglu: the same projection with the SwiGLU epilogue (--n interleaved gate|up rows);
     lmhead: the LM head + softmax at --rows rows.
@@ -797,9 +797,10 @@ def run_profile_case(args):
         st["step"]()
         torch.cuda.nvtx.range_pop()
     elif args.profile == "attention":
-        batch = synth.ragged_batch(SEED, 16, G_LO, G_HI, CTX_LO, CTX_HI)
+        nb = args.batch
+        batch = synth.ragged_batch(SEED, nb, G_LO, G_HI, CTX_LO, CTX_HI)
         cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
-        kc = torch.empty((16, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        kc = torch.empty((nb, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
         vc = torch.empty_like(kc).normal_(0, 1, generator=g)
         qkv = torch.empty((batch.M, dims.qkv), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
         cu = torch.from_numpy(batch.cu_rows).to(dev)
@@ -841,6 +842,7 @@ def main():
     ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead"], default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
+    ap.add_argument("--batch", type=int, default=16, help="sequences for --profile attention")
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")
     ap.add_argument("--k", type=int, default=4096, help="reduction length for --profile linear")

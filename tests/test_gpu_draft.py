@@ -57,7 +57,8 @@ def test_sample_rows_matches_oracle(lib, V):
 def tiny_draft_stack(seed, L=2, d=256, Hq=2, Hkv=1, I=256, V=512, std=0.08):
     from speculative_decoding_verify_05_gb300 import engine as E
     dims = E.Dims(d=d, Hq=Hq, Hkv=Hkv, D=128, I=I, V=V, layers=L)
-    od = ostack.Dims(d=d, Hq=Hq, Hkv=Hkv, D=128, I=I, V=V, layers=L)
+    # (this stack's QKV projection, 4 tiles at 8 rows, takes the two-step path: rounded, then rotated)
+    od = ostack.Dims(d=d, Hq=Hq, Hkv=Hkv, D=128, I=I, V=V, layers=L, qkv_bf16_before_rope=True)
     ones = synth.f32_to_bf16_bits(np.ones(d, np.float32))
     olayers, glayers = [], []
     for li in range(L):

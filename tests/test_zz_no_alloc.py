@@ -52,8 +52,16 @@ def test_noalloc_back_to_back_different_shapes(lib):
 
 def test_noalloc_rejects_scratch_beyond_the_limit(lib):
     M, N, K = 368, 24576, 4096                         # 192 tiles of 368 rows, stream-K split
-    need = lib.spec_linear_workspace_bytes(M, N, K)
-    assert need > 16 << 20
+    lib.spec_set_option("linear_cluster", 0)           # (else whole tiles + a cluster remainder: no scratch)
+    try:
+        need = lib.spec_linear_workspace_bytes(M, N, K)
+        assert need > 16 << 20
+        _noalloc_over_limit(lib, M, N, K)
+    finally:
+        lib.spec_set_option("linear_cluster", 1)
+
+
+def _noalloc_over_limit(lib, M, N, K):
     big_x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     big_w = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     Y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
