@@ -314,14 +314,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv, G = a.G;
-  pdl_wait();
-  pdl_trigger();
-
-  // ---- per-sequence metadata: one parallel load, then a warp-0 scan of the tile counts
-  for (int b = tid; b <= B; b += THREADS) {
-    s_cu[b] = a.cu_rows[b];
-    if (b < B) s_ctx[b] = a.ctx_len[b];
-  }
   if (tid == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -347,6 +339,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TMEM_COLS);
+  // the shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
+  pdl_wait();
+  pdl_trigger();
+
+  // ---- per-sequence metadata: one parallel load, then a warp-0 scan of the tile counts
+  for (int b = tid; b <= B; b += THREADS) {
+    s_cu[b] = a.cu_rows[b];
+    if (b < B) s_ctx[b] = a.ctx_len[b];
+  }
   __syncthreads();
   if (warp == 0) {
     int carry = 0;

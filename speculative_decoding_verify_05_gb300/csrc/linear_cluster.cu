@@ -39,13 +39,16 @@ __device__ __forceinline__ void dsmem_st_f4(uint32_t addr, float a, float b, flo
 }
 
 constexpr int MAX_S = 8;
+// warps 0 (TMA) and 1 (MMA) run the main loop; after it all 8 warps move the accumulator: warp w
+// reads TMEM lane quarter w % 4, half w / 4 of the columns (the exchange is store-issue bound)
+constexpr int CL_THREADS = 256;
 
 // Slot row of weight row r: rows are XOR-swizzled inside each group of 8 so that threads
 // reading 8 consecutive rows each (rows 8t + i, t = 0..7) hit 8 different bank groups.
 __device__ __forceinline__ int slot_row(int r) { return r ^ ((r >> 3) & 7); }
 
 template <int BN, int NSUB>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(CL_THREADS, 1)
 linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                       const LinearArgs args, int S, int cpr) {
   using Cfg = LinearCfg<BN, NSUB>;
@@ -130,22 +133,22 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   // every CTA of the cluster is past its main loop: the rings are free
   const int q = warp & 3;
   const int row = q * 32 + lane;
-  bool ok = true;
-  if (warp >= 2) {
-    ok = mbar_wait(acc_full, 0u, args.status, 0x143u);
-    tc_fence_after();
-  }
+  const bool ok = mbar_wait(acc_full, 0u, args.status, 0x143u);
+  tc_fence_after();
   cluster_sync_all();
-  if (warp >= 2) {
-    // ---------------- warps 2..5 (TMEM lane quarter warp % 4): push each 4-column chunk to its rank
+  {
+    // ---------------- every warp (TMEM lane quarter warp % 4, column half warp / 4): push each
+    // 4-column chunk to its rank
     const uint32_t t_row = tmem + (uint32_t(q * 32) << 16);
     const uint32_t base = smem_u32(slots);
-    // 64 columns per TMEM wait (16, 32 or 48 at the tail: TN is a multiple of 16), then their
-    // remote stores back to back
+    constexpr int C_MID = TN / 32 * 16;
+    const int c_lo = warp < 4 ? 0 : C_MID, c_hi = warp < 4 ? C_MID : TN;
+    // 64 columns per TMEM wait (16, 32 or 48 at the ends: both halves are multiples of 16), then
+    // their remote stores back to back
 #pragma unroll 1
-    for (int c = 0; c < TN; c += 64) {
+    for (int c = c_lo; c < c_hi; c += 64) {
       float v[64];
-      const int cols = TN - c < 64 ? TN - c : 64;
+      const int cols = c_hi - c < 64 ? c_hi - c : 64;
       if (k1 > k0 && ok) {
         if (cols == 64) tmem_ld_cols<64>(t_row + c, v);
         else if (cols == 48) tmem_ld_cols<48>(t_row + c, v);
@@ -177,7 +180,7 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
     // gate and up rows interleaved per 16: item = (chunk, 8 gate rows r8..r8+7 with r8 % 32 < 16);
     // the matching up rows are r8+16..; 8 outputs per token at column n_t 64 + (r8 / 32) 16 + r8 % 32
     const int sitems = (n_chunks > 0 ? n_chunks : 0) * 8;
-    for (int it = threadIdx.x; it < sitems; it += 192) {
+    for (int it = threadIdx.x; it < sitems; it += CL_THREADS) {
       const int kk = it >> 3, q8 = it & 7, r8 = (q8 >> 1) * 32 + (q8 & 1) * 8;
       float g[8][4], u[8][4];
 #pragma unroll
@@ -214,7 +217,7 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   const bool rope = args.epi == EPI_ROPE && n_t < args.rope_tiles;
   if (rope) {
     const int ritems = (n_chunks > 0 ? n_chunks : 0) * 8;
-    for (int it = threadIdx.x; it < ritems; it += 192) {
+    for (int it = threadIdx.x; it < ritems; it += CL_THREADS) {
       const int kk = it >> 3, r8 = (it & 7) * 8;
       float a[8][4], b[8][4];
 #pragma unroll
@@ -254,7 +257,7 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
     }
   }
   const int items = (args.epi == EPI_SWIGLU || rope || n_chunks <= 0) ? 0 : n_chunks * 16;
-  for (int it = threadIdx.x; it < items; it += 192) {
+  for (int it = threadIdx.x; it < items; it += CL_THREADS) {
     const int kk = it >> 4, r8 = (it & 15) * 8;
     float acc[8][4];
 #pragma unroll
@@ -318,7 +321,7 @@ struct ClusterLaunch {
   static cudaLaunchConfig_t config(int grid, int S, cudaStream_t st, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(CL_THREADS);
     cfg.dynamicSmemBytes = smem();
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
