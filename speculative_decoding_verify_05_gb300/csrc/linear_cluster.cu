@@ -37,6 +37,9 @@ __device__ __forceinline__ void dsmem_st_f4(uint32_t addr, float a, float b, flo
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+__device__ __forceinline__ void smem_st_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 
 constexpr int MAX_S = 8;
 // warps 0 (TMA) and 1 (MMA) run the main loop; after it all 8 warps move the accumulator: warp w
@@ -164,7 +167,10 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
         const int chunk = c / 4 + e;
         const int owner = chunk / cpr, kk = chunk - owner * cpr;
         const uint32_t off = (uint32_t)(((rank * cpr + kk) * 128 + slot_row(row)) * 16);
-        dsmem_st_f4(dsmem_map(base + off, (uint32_t)owner), v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        // (this rank's own chunks take the plain shared-memory store: the cluster path is as slow
+        // for a local address as for a peer's)
+        if (owner == (int)rank) smem_st_f4(base + off, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        else dsmem_st_f4(dsmem_map(base + off, (uint32_t)owner), v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
       }
     }
     tc_fence_before();
