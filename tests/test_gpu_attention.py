@@ -158,3 +158,45 @@ def test_attention_pair_cost_partitions(lib, pair_cost, grid):
     finally:
         lib.spec_set_option("attention_pair_cost", 12)
         lib.spec_set_option("persistent_grid", 0)
+
+
+def test_attention_full_ragged_round_sampled(lib):
+    """The benchmark's attention launch at full size: B = 64, gamma_b ~ U{1..10}, ctx_b ~ U[128, 8192],
+    GQA 32/8, D = 128, the default persistent grid and pair cost.  Outputs and the cache append are
+    checked against the oracle on a sample of sequences (the shortest and longest contexts, the
+    longest block and four seeded picks); the oracle sees host copies taken before the launch."""
+    batch = synth.ragged_batch(0, 64, 1, 10, 128, 8192)
+    Hq, Hkv, B, M = 32, 8, batch.B, batch.M
+    cap = int((batch.ctx_len + batch.gammas + 1).max() + 15) // 16 * 16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2024)
+    kc = torch.empty((B, Hkv, cap, D), dtype=torch.bfloat16, device="cuda").normal_(0, 1, generator=g)
+    vc = torch.empty_like(kc).normal_(0, 1, generator=g)
+    qkv = torch.empty((M, (Hq + 2 * Hkv) * D), dtype=torch.bfloat16, device="cuda").normal_(0, 1, generator=g)
+    rng = np.random.default_rng(5)
+    picks = {int(np.argmin(batch.ctx_len)), int(np.argmax(batch.ctx_len)), int(np.argmax(batch.gammas))}
+    picks |= {int(b) for b in rng.choice(B, 4, replace=False)}
+    picks = sorted(picks)
+    qkv_h = bits_of(qkv)
+    kc_h = {b: bits_of(kc[b]) for b in picks}
+    vc_h = {b: bits_of(vc[b]) for b in picks}
+    hq, hk = Hq * D, Hkv * D
+    scale = 1.0 / math.sqrt(D)
+    O = lib.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:], dev(batch.cu_rows),
+                                  dev(batch.ctx_len), kc, vc, batch.max_rows, scale=scale)
+    lib.spec_device_status()
+    for b in picks:
+        r0, r1 = int(batch.cu_rows[b]), int(batch.cu_rows[b + 1])
+        mb = r1 - r0
+        rows = qkv_h[r0:r1]
+        q = obf.decode(rows[:, :hq]).reshape(mb, Hq, D)
+        k = obf.decode(rows[:, hq:hq + hk]).reshape(mb, Hkv, D)
+        v = obf.decode(rows[:, hq + hk:]).reshape(mb, Hkv, D)
+        cu1, ctx1 = np.array([0, mb]), np.array([int(batch.ctx_len[b])])
+        kc1, vc1 = obf.decode(kc_h[b])[None], obf.decode(vc_h[b])[None]
+        Oref, Kref, Vref = oops.verify_attention(q, k, v, cu1, kc1, vc1, ctx1, scale)
+        Omag, _, _ = oops.verify_attention(q, k, np.abs(v), cu1, kc1, np.abs(vc1), ctx1, scale)
+        assert_close_attn(f64_of_bf16(O[r0:r1]).reshape(mb, Hq, D), Oref, Omag,
+                          f"full round: sequence {b} (ctx {ctx1[0]}, {mb} rows)")
+        assert np.array_equal(obf.decode(bits_of(kc[b])), Kref[0])
+        assert np.array_equal(obf.decode(bits_of(vc[b])), Vref[0])

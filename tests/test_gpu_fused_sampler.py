@@ -12,7 +12,7 @@ import torch
 import synth
 from oracle import bf16 as obf, ops as oops, sampler as osamp
 
-from gpu_util import bf16_dev, dev
+from gpu_util import bf16_dev, bits_of, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -113,3 +113,64 @@ def test_fused_rows_outside_the_pass_are_flagged(lib):
     with pytest.raises(lib.SpecError):
         lib.spec_device_status()
     lib.spec_device_status()                      # cleared
+
+
+def test_fused_full_round_sampled(lib):
+    """The benchmark's LM head -> sampler call at full size: B = 64, gamma_b ~ U{1..10} (M = 368 rows),
+    K = 4096, V = 151936, T = 0.7.  For every sequence the fused call equals softmax + sampler bit for
+    bit.  For a sample of sequences the oracle chain agrees wherever neither side flags a near tie:
+    fp64 logits of their rows, fp64 softmax, then the oracle sampler.
+    The inputs are synthesised on the device from a seeded generator, as the benchmark does: hidden
+    rows, weights (logit spread ~4.5), q = softmax(z / T + noise) from fp32 logits, drafts drawn from
+    q, and uniforms.  The oracle gets host copies of the sampled rows."""
+    T, K, V = 0.7, 4096, 151936
+    gammas = synth.ragged_batch(0, 64, 1, 10, 128, 8192).gammas
+    batch = synth.RaggedBatch(gammas, np.zeros(len(gammas), np.int32))
+    B, M = batch.B, batch.M
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    Hd = torch.empty((M, K), dtype=torch.bfloat16, device="cuda").normal_(0, 1, generator=g)
+    Wd = torch.empty((V, K), dtype=torch.bfloat16, device="cuda").normal_(0, 0.07, generator=g)
+    qrows = np.concatenate([np.arange(batch.cu_rows[b], batch.cu_rows[b] + batch.gammas[b]) for b in range(B)])
+    z = (Hd[torch.from_numpy(qrows).cuda()].float() @ Wd.float().t()) / T
+    z += torch.empty_like(z).normal_(0, 1, generator=g)
+    Qd = torch.softmax(z, dim=1)
+    Dd = torch.multinomial(Qd, 1, generator=g).reshape(-1).to(torch.int32)
+    Ud = torch.rand(M, generator=g, device="cuda", dtype=torch.float32)
+    cu = dev(batch.cu_rows)
+    del z
+    n, t, near = lib.spec_lmhead_reject_sample(Hd, Wd, T, Qd, Dd, Ud, cu)
+    P = lib.spec_lmhead_softmax(Hd, Wd, T)
+    n2, t2, near2 = lib.spec_reject_sample(P, Qd, Dd, Ud, cu)
+    lib.spec_device_status()
+    n, t, near = n.cpu().numpy(), t.cpu().numpy(), near.cpu().numpy()
+    assert np.array_equal(n, n2.cpu().numpy()) and np.array_equal(t, t2.cpu().numpy())
+    assert np.array_equal(near, near2.cpu().numpy())
+    del P
+    # the oracle on a sample of sequences
+    rng = np.random.default_rng(11)
+    picks = sorted({int(np.argmax(batch.gammas)), int(np.argmin(batch.gammas))} |
+                   {int(b) for b in rng.choice(B, 6, replace=False)})
+    rows = np.concatenate([np.arange(batch.cu_rows[b], batch.cu_rows[b + 1]) for b in picks])
+    Hs = obf.decode(bits_of(Hd)[rows])
+    Wb = bits_of(Wd)
+    logits = np.concatenate([Hs @ obf.decode(Wb[v0:v0 + 8192]).T for v0 in range(0, V, 8192)], axis=1)
+    del Wb
+    p_all = oops.target_probs(logits, T)
+    Qh, Dh, Uh = Qd.cpu().numpy(), Dd.cpu().numpy(), Ud.cpu().numpy()
+    at = 0
+    checked = 0
+    for b in picks:
+        r0, r1 = int(batch.cu_rows[b]), int(batch.cu_rows[b + 1])
+        mb, gb = r1 - r0, int(batch.gammas[b])
+        d0 = r0 - b                       # sequence b's draft rows in Q / drafts
+        n_ref, t_ref, near_ref = osamp.reject_sample(p_all[at:at + mb], Qh[d0:d0 + gb].astype(np.float64),
+                                                     Dh[d0:d0 + gb], Uh[r0:r1], np.array([0, mb]))
+        at += mb
+        if near[b] or near_ref[0]:
+            continue
+        checked += 1
+        assert n[b] == n_ref[0], b
+        assert np.array_equal(t[r0:r0 + n[b] + 1], t_ref[:n[b] + 1]), b
+        assert np.all(t[r0 + n[b] + 1:r1] == -1), b
+    assert checked >= len(picks) // 2, (checked, picks)
