@@ -372,7 +372,8 @@ struct ClusterLaunch {
 
 // Tile shapes with a cluster build: the accumulator (TN x 128 fp32) must fit in the ring.
 #define SPEC_CLUSTER_SHAPES(X) \
-  X(1, 64) X(1, 80) X(1, 96) X(1, 112) X(1, 128) X(1, 144) X(1, 160) X(1, 176) X(1, 192) \
+  X(1, 16) X(1, 32) X(1, 48) X(1, 64) X(1, 80) X(1, 96) X(1, 112) X(1, 128) X(1, 144) X(1, 160) X(1, 176) \
+  X(1, 192) \
   X(1, 208) X(1, 224) X(1, 240) X(1, 256) X(2, 144) X(2, 160) X(2, 176) X(2, 192)
 
 int linear_cluster_capacity(int BN, int NSUB, int S) {

@@ -116,7 +116,8 @@ def test_linear_launch_accounting(lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(368, 4096, 4096), (300, 4096, 1000), (200, 4096, 520), (17, 6144, 4096),
-                                   (513, 4096, 4096), (64, 2048, 12288)])
+                                   (513, 4096, 4096), (64, 2048, 12288), (5, 512, 4096), (8, 256, 256),
+                                   (33, 1024, 4096), (48, 384, 264)])
 def test_linear_cluster_split_k(lib, M, N, K):
     """Few weight tiles: the cluster split-K kernel (pieces summed over distributed shared
     memory) and the stream-K path both match the oracle."""
