@@ -576,8 +576,8 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
     wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
-    for M, tag in ((1, "1"), (5, "5"), (1, "1_tc")):
-        S.spec_set_option("gemv_max_m", 0 if tag == "1_tc" else 4)
+    for M, tag in ((1, "1"), (5, "5"), (1, "1_gemv")):
+        S.spec_set_option("gemv_max_m", 4 if tag == "1_gemv" else 0)
         def run():
             for lw in eng.w.layers:
                 S.spec_verify_linear(eng.h[:M], lw.w_qkv, Y=eng.qkv[:M], ws=eng.ws)
@@ -608,13 +608,121 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
         out[f"m{tag}_us"] = t * 1e3
         out[f"m{tag}_hbm_gbs"] = gbs
         out[f"m{tag}_hbm_frac"] = gbs / hbm_peak
-    S.spec_set_option("gemv_max_m", 4)
+    S.spec_set_option("gemv_max_m", 0)
     out["clocks"] = clk.stop()
     out["ratio_m5_over_m1"] = out["m5_us"] / out["m1_us"]
     out["weights_gb"] = wbytes / 1e9
     out["note"] = ("36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph "
-                   "per M; m1 = CUDA-core path, m1_tc = tensor-core path at M=1; peak " + peak_src)
+                   "per M; m1 = the library's default (tensor-core) path at M=1, m1_gemv = the optional CUDA-core "
+                   "path; peak " + peak_src)
     return out
+
+
+SWEEP_B = (1, 8, 64, 256, 1024)
+SWEEP_GAMMA = (1, 4, 10)
+SWEEP_CTX = 2048
+
+
+def run_sweep(args):
+    """Batch/depth sweep on the Qwen3-8B shapes (B x gamma, M = B (gamma + 1) from 2 to 11264 rows,
+    context 2048): per point the 36-layer linear stack (one CUDA graph; % of the measured HBM copy
+    peak and of the sustained bf16 tensor peak) and one layer's verify attention over a B-sequence
+    cache of 2048 keys each (the cache is one layer's, reused: 36 layers at B = 1024 would not fit).
+    Prints one JSON line."""
+    import torch
+    from speculative_decoding_verify_05_gb300 import binding as S
+    from speculative_decoding_verify_05_gb300 import engine as E
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, tc_sust, peak_src = peaks()
+    dims = E.Dims()
+    sw = E.random_stack(dims, seed=1000, device=dev, with_head=False)
+    for lw in sw.layers:
+        E.set_gu_layout(lw, "interleaved")
+    m_max = max(b * (g + 1) for b in SWEEP_B for g in SWEEP_GAMMA)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
+    x = torch.empty((m_max, dims.d), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    h = torch.empty_like(x).normal_(0, 1, generator=gen)
+    qkv = torch.empty((m_max, dims.qkv), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    o = torch.empty((m_max, dims.Hq * dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    a = torch.empty((m_max, dims.I), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    shapes = ((dims.qkv, dims.d), (dims.d, dims.Hq * dims.D), (dims.d, dims.I))
+    need = max(max(S.spec_linear_workspace_bytes(b * (g + 1), n, k) for n, k in shapes) +
+               S.spec_swiglu_linear_workspace_bytes(b * (g + 1), dims.I, dims.d)
+               for b in SWEEP_B for g in SWEEP_GAMMA)
+    ws = S.Workspace(dev, max(need, 1 << 20))
+    wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    flops_row = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    cur = torch.cuda.current_stream()
+    clk = ClockSampler(0)
+    clk.start()
+    points = []
+    for nb in SWEEP_B:
+        for gm in SWEEP_GAMMA:
+            M = nb * (gm + 1)
+
+            def run():
+                for lw in sw.layers:
+                    S.spec_verify_linear(h[:M], lw.w_qkv, Y=qkv[:M], ws=ws)
+                    S.spec_verify_linear(o[:M], lw.w_o, Y=x[:M], residual=x[:M], ws=ws)
+                    S.spec_verify_linear_swiglu(h[:M], lw.w_gu, A=a[:M], ws=ws)
+                    S.spec_verify_linear(a[:M], lw.w_down, Y=x[:M], residual=x[:M], ws=ws)
+            g = torch.cuda.CUDAGraph()
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                run()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=st):
+                run()
+            reps = 3 if M > 2000 else 5
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            for _ in range(reps):
+                g.replay()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            t_lin = e0.elapsed_time(e1) / reps / 1e3
+            del g
+            # one layer's attention over nb sequences of SWEEP_CTX keys, gm + 1 new rows each
+            batch = synth.RaggedBatch(np.full(nb, gm), np.full(nb, SWEEP_CTX))
+            cap = (SWEEP_CTX + gm + 1 + 15) // 16 * 16
+            kc = torch.empty((nb, dims.Hkv, cap, dims.D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+            vc = torch.empty_like(kc).normal_(0, 1, generator=gen)
+            cu = torch.from_numpy(batch.cu_rows).to(dev)
+            ctx = torch.from_numpy(batch.ctx_len).to(dev)
+            hq, hk = dims.Hq * dims.D, dims.Hkv * dims.D
+            attn_ws = S.Workspace(dev, S.spec_attention_workspace_bytes(nb, gm + 1, dims.Hq, dims.Hkv, dims.D, cap))
+
+            def attn():
+                S.spec_verify_attention(qkv[:M, :hq], qkv[:M, hq:hq + hk], qkv[:M, hq + hk:], cu, ctx, kc, vc,
+                                        gm + 1, O=o[:M], ws=attn_ws)
+            for _ in range(3):
+                attn()
+            torch.cuda.synchronize()
+            e0.record(cur)
+            for _ in range(10):
+                attn()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            t_att = e0.elapsed_time(e1) / 10 / 1e3
+            ab = attention_bytes(batch, dims)
+            S.spec_device_status()
+            points.append({"B": nb, "gamma": gm, "M": M,
+                           "linear_stack_us": t_lin * 1e6,
+                           "linear_hbm_frac": wbytes / t_lin / 1e9 / hbm_peak,
+                           "linear_tensor_frac": flops_row * M / t_lin / 1e12 / tc_sust,
+                           "attention_us": t_att * 1e6,
+                           "attention_hbm_frac": ab / t_att / 1e9 / hbm_peak})
+            del kc, vc, attn_ws
+            torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "batch x depth on the Qwen3-8B shapes, context %d" % SWEEP_CTX,
+                      "peaks": {"hbm_gbs": hbm_peak, "bf16_tflops_sustained": tc_sust, "source": peak_src},
+                      "weights_gb": wbytes / 1e9, "points": points, "clocks": clk.stop()}))
 
 
 def end_to_end(args, eng, batch, dims, q, drafts, x0, S, torch, dev, steps=None):
@@ -852,6 +960,8 @@ def main():
                     help="LM head -> sampler in one call without materialising p (fused), or softmax + sampler")
     ap.add_argument("--swiglu", choices=["fused", "split"], default="fused",
                     help="SwiGLU in the gate|up GEMM epilogue (fused) or as its own kernel (split)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batch x depth sweep (B in 1..1024, gamma in 1/4/10): linear stack and attention rooflines")
     ap.add_argument("--nsub", type=int, default=0, help="linear_nsub knob for --profile linear/lmhead (0: library default)")
     args = ap.parse_args()
     if args.set and args.impl == "ours":
@@ -862,6 +972,9 @@ def main():
                 ap.error(f"--set {kv}: {S._lib.spec_last_error().decode()}")
     if args.profile:
         run_profile_case(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -81,8 +81,9 @@ SPEC_API int spec_launches(void);
 /* Library ABI version (increments on any signature change). */
 SPEC_API int spec_version(void);
 
-/* Tuning knobs (process-wide): "gemv_max_m" (0..4, default 4): largest M
- * that takes the CUDA-core path of spec_verify_linear; "persistent_grid" (0..4096,
+/* Tuning knobs (process-wide): "gemv_max_m" (0..4, default 0): largest M
+ * that takes the CUDA-core path of spec_verify_linear (by default every M runs
+ * on the tensor cores, which stream the weights faster even at M = 1); "persistent_grid" (0..4096,
  * default 0 = one CTA per SM): CTAs of the persistent tensor-core GEMM and
  * attention kernels;
  * "attention_impl" (1 = tcgen05 kernel, default; 0 = mma.sync kernel);
@@ -122,9 +123,9 @@ SPEC_API int spec_device_status(spec_stream stream, int* detail);
  *   Y        [M x N] bf16, leading dim ldy           (output, fp32 accumulate)
  *   residual [M x N] bf16, leading dim ldr, or NULL  (added before rounding;
  *            may alias Y exactly: same pointer and leading dimension)
- * Requires N >= 1, K % 8 == 0; M = 0 is a no-op.  M <= 4 runs on CUDA cores
- * (a pure weight stream), larger M on tcgen05 tensor cores with TMA-staged
- * 128 x 64 weight tiles.  Workspace: spec_linear_workspace_bytes (0 when no
+ * Requires N >= 1, K % 8 == 0; M = 0 is a no-op.  Runs on tcgen05 tensor
+ * cores with TMA-staged 128 x 64 weight tiles (M <= "gemv_max_m", off by
+ * default, takes a CUDA-core weight stream instead).  Workspace: spec_linear_workspace_bytes (0 when no
  * K split is needed; the pointer may then be NULL). */
 SPEC_API size_t spec_linear_workspace_bytes(int M, int N, int K);
 SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,

@@ -135,7 +135,7 @@ constexpr size_t kCounterBytes = 64 * 1024;
 constexpr size_t kMaxCounters = kCounterBytes / 4;
 
 // --------------------------------------------------------------------------- linear plan
-int g_gemv_max_m = 4;    // tunable: largest M that takes the CUDA-core path
+int g_gemv_max_m = 0;    // tunable: largest M that takes the CUDA-core path (0: tensor cores for every M)
 int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
@@ -181,8 +181,10 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
     p.bytes = p.splits > 1 ? kCounterBytes + round_up(size_t(p.splits) * M * N * 4, 256) : 0;
     return p;
   }
-  // up to 256 rows: one MMA of N = BN per k-substep; more rows: tiles of up to 512 rows as
-  // two MMAs of N = BN sharing each weight tile (every weight byte still read once per tile)
+  // up to 256 rows: one MMA of N = BN per k-substep; more rows: tiles of up to 384 rows as
+  // two MMAs of N = BN sharing each weight tile (every weight byte still read once per tile).
+  // 384 and not 512: a 512-row tile's 80 KB stage leaves room for two stages only, which
+  // measured 32 % of the tensor peak at 512 rows against ~50 % with three 64 KB stages
   if (M <= kMaxBN) {
     p.tiles_m = 1;
     p.NSUB = 1;
@@ -195,7 +197,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
     p.NSUB = 1;
     p.BN = std::max(16, (per + 15) / 16 * 16);
   } else {
-    p.tiles_m = (M + 2 * kMaxBN - 1) / (2 * kMaxBN);
+    p.tiles_m = (M + kMaxTN - 1) / kMaxTN;
     const int per = (M + p.tiles_m - 1) / p.tiles_m;
     p.NSUB = 2;
     p.BN = std::max(144, ((per + 1) / 2 + 15) / 16 * 16);

@@ -60,6 +60,7 @@ cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 // ---- tcgen05 GEMM: NSUB sub-tiles of BN verify rows per CTA tile
 //      (NSUB = 1: BN = 16..256 step 16; NSUB = 2: BN = 144..256 step 16)
 constexpr int kMaxBN = 256;
+constexpr int kMaxTN = 384;   // rows of a two-MMA token tile (three 64 KB ring stages)
 int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
 // Clusters of cl CTAs of the persistent GEMM that fit on the device at once (0: none / unknown).

@@ -29,7 +29,7 @@ def run_case(lib, M, N, K, residual, seed, gemv_max_m=4, grid=0, std=0.05):
         Y = lib.spec_verify_linear(bf16_dev(X), bf16_dev(W), residual=bf16_dev(R) if residual else None)
         lib.spec_device_status()
     finally:
-        lib.spec_set_option("gemv_max_m", 4)
+        lib.spec_set_option("gemv_max_m", 0)
         lib.spec_set_option("persistent_grid", 0)
     ref = oops.linear(obf.decode(X), obf.decode(W), obf.decode(R) if residual else None)
     assert_close_rel(f64_of_bf16(Y), ref, f"linear M={M} N={N} K={K}")
@@ -79,7 +79,7 @@ def test_linear_repeat_reuses_workspace(lib):
             Y = lib.spec_verify_linear(Xd, Wd, ws=ws)
             assert_close_rel(f64_of_bf16(Y), ref, "repeat")
     finally:
-        lib.spec_set_option("gemv_max_m", 4)
+        lib.spec_set_option("gemv_max_m", 0)
     lib.spec_device_status()
 
 
@@ -143,7 +143,7 @@ def run_swiglu(lib, M, I, K, seed, gemv_max_m=4, grid=0, std=0.05):
         A = lib.spec_verify_linear_swiglu(bf16_dev(X), Wgu)
         lib.spec_device_status()
     finally:
-        lib.spec_set_option("gemv_max_m", 4)
+        lib.spec_set_option("gemv_max_m", 0)
         lib.spec_set_option("persistent_grid", 0)
     x = obf.decode(X)
     ref = oops.silu_mul(oops.linear(x, obf.decode(Wg)), oops.linear(x, obf.decode(Wu)))

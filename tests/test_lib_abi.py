@@ -115,6 +115,7 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"no_such_knob", 1) == E
     assert L.spec_set_option(b"gemv_max_m", 9) == E
     assert L.spec_set_option(b"gemv_max_m", 4) == 0
+    assert L.spec_set_option(b"gemv_max_m", 0) == 0
     assert L.spec_set_option(b"attention_pair_cost", 65) == E
     assert L.spec_set_option(b"attention_pair_cost", -1) == E
     assert L.spec_set_option(b"attention_pair_cost", 8) == 0
