@@ -149,6 +149,7 @@ class VerifyEngine:
             if fused_sampler:
                 need = max(need, S.spec_lmhead_sample_workspace_bytes(max_M, dims.d, dims.V, 1.0))
         self.ws = S.Workspace(dev, need)
+        self._graphs = []          # captured rounds (kept alive with the engine)
 
     # ------------------------------------------------------------------ one layer
     def layer(self, li: int, M: int, cu_rows, ctx_len, B: int, max_rows: int):
@@ -210,6 +211,27 @@ class VerifyEngine:
         M = self._stack(x0, cu_rows, ctx_len, max_rows, None)
         return S.spec_lmhead_reject_sample(self.h[:M], self.w.w_lm, temperature, q, drafts, U, cu_rows, tie_eps,
                                            out=out, ws=self.ws)
+
+    def capture_round(self, x0, cu_rows, ctx_len, q, drafts, U, temperature: float, out,
+                      tie_eps: float = 1e-5, max_rows: int | None = None):
+        """verify_round on these device buffers, captured once in a CUDA graph; returns the replay
+        function.  A serving loop writes each round's inputs into the same buffers and replays:
+        every launch of the round is re-issued with no per-launch host work.  M and B stay those
+        of the capture; cu_rows, ctx_len, the tokens, q and U may change between rounds (the
+        kernels read them from device memory).  The buffers must hold a valid round when this is
+        called: the capture runs it twice."""
+        dev = self.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self.verify_round(x0, cu_rows, ctx_len, q, drafts, U, temperature, tie_eps, max_rows, out)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            self.verify_round(x0, cu_rows, ctx_len, q, drafts, U, temperature, tie_eps, max_rows, out)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self._graphs.append(graph)
+        return graph.replay
 
 
 class DraftEngine:

@@ -207,3 +207,45 @@ def test_linear_rope_fused(lib, M, Hq, Hkv, K):
     qk = y[:, :(Hq + Hkv) * D].reshape(M, Hq + Hkv, D)
     ref[:, :(Hq + Hkv) * D] = oops.rope(qk, pos, 1e6).reshape(M, -1)
     assert_close_rel(f64_of_bf16(Y), ref, f"linear + rope M={M}")
+
+
+def test_captured_round_replays_the_eager_round(lib):
+    """VerifyEngine.capture_round: after new inputs are written into the captured buffers (same M
+    and B, different ragged split, contexts, draft tokens and uniforms) a replay returns exactly
+    what the eager verify_round returns on those inputs, cache writes included."""
+    from speculative_decoding_verify_05_gb300 import engine as E
+    L = 2
+    dims, od, osw, gsw = _tiny_stack(L, 70)
+    V = dims.V
+
+    def inputs(seed, gammas, ctx):
+        batch = synth.RaggedBatch(gammas, ctx, cap=200)
+        rng = np.random.default_rng(seed)
+        x0 = synth.normal_bf16_bits(seed, (batch.M, dims.d), 1.0)
+        q = rng.dirichlet(np.full(V, 0.5), size=batch.M - batch.B).astype(np.float32)
+        drafts = np.array([rng.choice(V, p=r.astype(np.float64) / r.astype(np.float64).sum()) for r in q], np.int32)
+        U = synth.uniforms_f32(seed + 1, batch.M)
+        return batch, x0, q, drafts, U
+
+    bA, xA, qA, dA, uA = inputs(5, [3, 0, 5], [40, 9, 0])        # M = 11
+    bB, xB, qB, dB, uB = inputs(6, [1, 6, 1], [100, 3, 57])      # M = 11, another split
+    assert bA.M == bB.M and bA.B == bB.B
+    kc = [synth.normal_bf16_bits(200 + i, (bA.B, dims.Hkv, 200, 128), 1.0) for i in range(L)]
+    vc = [synth.normal_bf16_bits(300 + i, (bA.B, dims.Hkv, 200, 128), 1.0) for i in range(L)]
+    eng = E.VerifyEngine(dims, gsw, [bf16_dev(k) for k in kc], [bf16_dev(v) for v in vc], max_M=bA.M, max_rows=7)
+    bufs = [bf16_dev(xA), dev(bA.cu_rows), dev(bA.ctx_len), dev(qA), dev(dA), dev(uA)]
+    out = (torch.empty(bA.B, dtype=torch.int32, device="cuda"), torch.empty(bA.M, dtype=torch.int32, device="cuda"),
+           torch.empty(bA.B, dtype=torch.int32, device="cuda"))
+    replay = eng.capture_round(*bufs, 0.8, out)
+    lib.spec_device_status()
+    # eager round on inputs B (fresh tensors), then the same inputs copied into the captured buffers
+    n1, t1, z1 = eng.verify_round(bf16_dev(xB), dev(bB.cu_rows), dev(bB.ctx_len), dev(qB), dev(dB), dev(uB), 0.8)
+    n1, t1, z1 = n1.cpu(), t1.cpu(), z1.cpu()
+    cache1 = [bits_of(k) for k in eng.kc]
+    for buf, host in zip(bufs, (bf16_dev(xB), dev(bB.cu_rows), dev(bB.ctx_len), dev(qB), dev(dB), dev(uB))):
+        buf.copy_(host)
+    replay()
+    lib.spec_device_status()
+    assert torch.equal(out[0].cpu(), n1) and torch.equal(out[1].cpu(), t1) and torch.equal(out[2].cpu(), z1)
+    for k_after, k_eager in zip(eng.kc, cache1):
+        assert np.array_equal(bits_of(k_after), k_eager)
