@@ -43,7 +43,8 @@ __device__ __forceinline__ void smem_st_f4(uint32_t addr, float a, float b, floa
 
 constexpr int MAX_S = 8;
 // warps 0 (TMA) and 1 (MMA) run the main loop; after it all 8 warps move the accumulator: warp w
-// reads TMEM lane quarter w % 4, half w / 4 of the columns (the exchange is store-issue bound)
+// reads TMEM lane quarter w % 4, half w / 4 of the columns (more warps issue the
+// distributed-shared-memory stores faster; the exchange is bound by those stores)
 constexpr int CL_THREADS = 256;
 
 // Slot row of weight row r: rows are XOR-swizzled inside each group of 8 so that threads
