@@ -90,11 +90,11 @@ SPEC_API int spec_version(void);
  * "attention_pair_cost" (0..64, default 12): work the tcgen05 attention kernel
  * charges for starting a (sequence, kv head) pair, in quarters of a 128-key
  * tile, when it splits the key tiles evenly between CTAs;
- * "linear_nsub" (2, default: one tensor-core tile covers up to 512 rows; 1: up
+ * "linear_nsub" (2, default: one tensor-core tile covers up to 384 rows; 1: up
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
- * and sum the pieces on chip; "lmhead_nsub" (1 default, or 2): the LM head's
- * tensor-core tiles cover up to 256 or 512 rows; "linear_multicast" (1 =
+ * and sum the pieces on chip; "lmhead_nsub" (2 default, or 1): the LM head's
+ * tensor-core tiles cover up to 384 or 256 rows; "linear_multicast" (1 =
  * off, default; 2 or 4): the persistent tensor-core GEMM runs clusters of up
  * to that many CTAs on adjacent weight tiles, each token tile loaded once per
  * cluster (TMA multicast); "pdl" (1 default, 0 off):

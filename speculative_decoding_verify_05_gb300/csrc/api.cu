@@ -140,8 +140,8 @@ int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
-int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 512 verify rows
-int g_lmhead_nsub = 1;   // tunable: the LM head's tiles cover up to 256 (1) or 512 (2) rows
+int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 384 verify rows
+int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 384 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
 int g_linear_mc = 1;     // tunable: largest cluster that shares token tiles by TMA multicast
 
@@ -190,8 +190,10 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
     p.NSUB = 1;
     p.BN = std::max(16, (M + 15) / 16 * 16);
   } else if (lmhead ? g_lmhead_nsub == 1 : g_nsub_max == 1) {
-    // (by default the LM head keeps two accumulator buffers so each tile's epilogue overlaps
-    // the next tile's MMAs: it has ~1200 tiles, each with a long softmax-statistics epilogue)
+    // (one MMA per k-substep; with up to 256 rows two accumulator buffers fit in TMEM, so each
+    // tile's epilogue overlaps the next tile's MMAs.  The LM head takes the two-MMA tiles below by
+    // default: their one accumulator leaves the epilogue exposed, but at 368 rows they read the
+    // weights and tokens once per tile, and the short epilogue costs less than the second read)
     p.tiles_m = (M + kMaxBN - 1) / kMaxBN;
     const int per = (M + p.tiles_m - 1) / p.tiles_m;
     p.NSUB = 1;

@@ -74,7 +74,7 @@ __device__ __forceinline__ uint64_t umma_desc_lin(uint32_t smem_addr) {
 }
 
 // A CTA tile is 128 weight rows x TN = NSUB * BN verify rows: NSUB MMAs of N = BN per
-// k-substep share one weight tile, so with up to 512 verify rows every weight byte is
+// k-substep share one weight tile, so with up to 384 verify rows (kMaxTN) every weight byte is
 // read from HBM once.
 template <int BN, int NSUB>
 struct LinearCfg {

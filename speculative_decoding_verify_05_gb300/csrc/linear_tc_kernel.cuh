@@ -355,31 +355,55 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
       } else {
-        // LM-head epilogues (ranges are tile-aligned, so every segment is whole):
-        // per token column j reduce over the tile's 128 vocabulary rows
+        // LM-head epilogues (ranges are tile-aligned, so every segment is whole): per token column
+        // reduce over the tile's 128 vocabulary rows.  Each 16-column TMEM load goes through the
+        // warp's transpose block, so lanes 2j and 2j + 1 scan column j's 32 rows (16 each) and meet
+        // in one shuffle: two shuffles per 16 columns instead of five per column per reduction
+        // (the butterfly version took 22 us per 192-column tile, 40 us per 384-column tile).
+        float* eb = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
+        const int jc = lane >> 1, r0 = (lane & 1) * 16;
+        const int nr = n0 + q * 32 + r0;        // vocabulary row of this lane's first scanned entry
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
+          if constexpr (EPI == EPI_LOGITS) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = m0 + c + j;
-            const bool valid = (n < args.N);
-            if constexpr (EPI == EPI_LOGITS) {
+            for (int j = 0; j < 16; ++j) {
               const float z = v[j] * args.inv_temp;
-              if (m < args.M && valid) args.P[(size_t)m * args.ldp + n] = z;
-              const float zm = valid ? z : -INFINITY;
-              const float mx = warp_max(zm);
-              const float e = valid ? expf(z - mx) : 0.f;
-              const float sm = warp_sum(e);
-              if (lane == 0) red[q * TN + c + j] = make_float2(mx, sm);
-            } else {
-              float zv = valid ? v[j] : -INFINITY;
-              int idx = valid ? n : 0x7fffffff;
-              warp_argmax(zv, idx);
-              if (lane == 0) red[q * TN + c + j] = make_float2(zv, __int_as_float(idx));
+              const int m = m0 + c + j;
+              if (m < args.M && n < args.N) args.P[(size_t)m * args.ldp + n] = z;
+              eb[j * 33 + lane] = z;
             }
+            __syncwarp();
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (nr + i < args.N) mx = fmaxf(mx, eb[jc * 33 + r0 + i]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            float sm = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (nr + i < args.N) sm += expf(eb[jc * 33 + r0 + i] - mx);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) eb[j * 33 + lane] = v[j];
+            __syncwarp();
+            float zv = -INFINITY;
+            int idx = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {          // strict > keeps the lowest row on ties
+              const float z = eb[jc * 33 + r0 + i];
+              if (nr + i < args.N && (z > zv || idx == 0x7fffffff)) { zv = z; idx = nr + i; }
+            }
+            const float ov = __shfl_xor_sync(0xffffffffu, zv, 1);
+            const int oi = __shfl_xor_sync(0xffffffffu, idx, 1);
+            if (ov > zv || (ov == zv && oi < idx)) { zv = ov; idx = oi; }
+            if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(zv, __int_as_float(idx));
           }
+          __syncwarp();                          // eb is rewritten by the next block
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
