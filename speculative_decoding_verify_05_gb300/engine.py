@@ -219,7 +219,9 @@ class VerifyEngine:
         every launch of the round is re-issued with no per-launch host work.  M and B stay those
         of the capture; cu_rows, ctx_len, the tokens, q and U may change between rounds (the
         kernels read them from device memory).  The buffers must hold a valid round when this is
-        called: the capture runs it twice."""
+        called: the capture runs it twice.  The graph keeps the engine's workspace pointer, so that
+        workspace must not be regrown afterwards (it is sized for every call the engine makes; give
+        other calls their own)."""
         dev = self.device
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
