@@ -40,6 +40,16 @@ __device__ __forceinline__ float silu(float g) {
   return g * r;
 }
 
+// e^x for the softmax chain (LM-head statistics, normaliser, sampler): 2^(x log2 e) on the
+// hardware base-2 exponential.  Relative error ~2^-22 plus |x| 2^-24 from rounding the product,
+// under 1e-6 for the x > -20 that carry any probability.  Every step of the chain uses this one
+// function, so the fused and unfused paths stay bit-identical.
+__device__ __forceinline__ float exp_sm(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+  return e;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

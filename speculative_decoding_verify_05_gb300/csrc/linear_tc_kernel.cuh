@@ -384,7 +384,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             float sm = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (nr + i < args.N) sm += expf(eb[jc * 33 + r0 + i] - mx);
+              if (nr + i < args.N) sm += exp_sm(eb[jc * 33 + r0 + i] - mx);
             sm += __shfl_xor_sync(0xffffffffu, sm, 1);
             if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
           } else {
@@ -416,8 +416,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const float2 o = red[w * TN + j];
             if constexpr (EPI == EPI_LOGITS) {
               const float mx = fmaxf(accv.x, o.x);
-              const float s = (accv.x == -INFINITY ? 0.f : accv.y * expf(accv.x - mx)) +
-                              (o.x == -INFINITY ? 0.f : o.y * expf(o.x - mx));
+              const float s = (accv.x == -INFINITY ? 0.f : accv.y * exp_sm(accv.x - mx)) +
+                              (o.x == -INFINITY ? 0.f : o.y * exp_sm(o.x - mx));
               accv = make_float2(mx, s);
             } else {
               const int ai = __float_as_int(accv.y), oi = __float_as_int(o.y);

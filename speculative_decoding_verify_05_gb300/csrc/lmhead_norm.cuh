@@ -15,12 +15,12 @@ namespace spec {
 __device__ __forceinline__ void lm_merge(float& m, float& s, float om, float os) {
   const float mm = fmaxf(m, om);
   if (mm == -INFINITY) return;        // both empty
-  s = s * expf(m - mm) + os * expf(om - mm);
+  s = s * exp_sm(m - mm) + os * exp_sm(om - mm);
   m = mm;
 }
 
 // Called by all 32 lanes of a warp: max over the row and inv = 1 / sum_x e^(z_x - max), so that
-// p_x = expf(z_x - mx) * inv.  Lane l takes tiles l, l + 32, ... in order, then the lanes merge
+// p_x = exp_sm(z_x - mx) * inv.  Lane l takes tiles l, l + 32, ... in order, then the lanes merge
 // in a fixed butterfly order.
 __device__ __forceinline__ void lm_row_norm_warp(const float2* __restrict__ st, int n_tiles, float& mx_out,
                                                  float& inv_out) {

@@ -19,7 +19,7 @@
 //
 // The probabilities come either as a materialised p [M x V] (spec_reject_sample) or, for the
 // fused LM-head -> sampler path (spec_lmhead_reject_sample), as the LM head's logits z / T and
-// per-tile statistics: p_x = expf(z_x - max) * inv with the row's normaliser computed here by
+// per-tile statistics: p_x = exp_sm(z_x - max) * inv with the row's normaliser computed here by
 // the same code as the normalisation kernel (bit-identical p; one warp per row, 16 rows at a
 // time), or a one-hot row at the argmax when the temperature is 0.  Only the rows the sampler
 // reads are ever evaluated.
@@ -41,13 +41,13 @@ constexpr int MAX_TILES = 256;                             // V <= 1,048,576
 enum { P_GIVEN = 0, P_LOGITS = 1, P_ARGMAX = 2 };
 struct RowP {
   const float* v;   // P_GIVEN: the p row; P_LOGITS: the z / T row
-  float mx, inv;    // P_LOGITS: p_x = expf(z_x - mx) * inv
+  float mx, inv;    // P_LOGITS: p_x = exp_sm(z_x - mx) * inv
   int am;           // P_ARGMAX: p_x = (x == am)
 };
 template <int MODE>
 __device__ __forceinline__ float p_at(const RowP& r, int x) {
   if constexpr (MODE == P_GIVEN) return r.v[x];
-  else if constexpr (MODE == P_LOGITS) return expf(r.v[x] - r.mx) * r.inv;
+  else if constexpr (MODE == P_LOGITS) return exp_sm(r.v[x] - r.mx) * r.inv;
   else return x == r.am ? 1.f : 0.f;
 }
 
@@ -67,7 +67,7 @@ __device__ __forceinline__ void load_weights(const RowP& pr, const float* qrow, 
       w[0] = p0.x; w[1] = p0.y; w[2] = p0.z; w[3] = p0.w; w[4] = p1.x; w[5] = p1.y; w[6] = p1.z; w[7] = p1.w;
       if constexpr (MODE == P_LOGITS) {
 #pragma unroll
-        for (int e = 0; e < PER_THREAD; ++e) w[e] = expf(w[e] - pr.mx) * pr.inv;
+        for (int e = 0; e < PER_THREAD; ++e) w[e] = exp_sm(w[e] - pr.mx) * pr.inv;
       }
     }
     if (!use_p) {

@@ -56,13 +56,13 @@ lmhead_normalize_kernel(float* __restrict__ P, long long ldp, const float2* __re
   for (int x = x0 + tid * 4; x < x1; x += NORM_THREADS * 4) {
     if (x + 3 < x1) {
       float4 v = *reinterpret_cast<float4*>(row + x);
-      v.x = expf(v.x - mx) * inv;
-      v.y = expf(v.y - mx) * inv;
-      v.z = expf(v.z - mx) * inv;
-      v.w = expf(v.w - mx) * inv;
+      v.x = exp_sm(v.x - mx) * inv;
+      v.y = exp_sm(v.y - mx) * inv;
+      v.z = exp_sm(v.z - mx) * inv;
+      v.w = exp_sm(v.w - mx) * inv;
       *reinterpret_cast<float4*>(row + x) = v;
     } else {
-      for (int k = x; k < x1; ++k) row[k] = expf(row[k] - mx) * inv;
+      for (int k = x; k < x1; ++k) row[k] = exp_sm(row[k] - mx) * inv;
     }
   }
 }
