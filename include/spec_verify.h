@@ -125,8 +125,9 @@ SPEC_API int spec_device_status(spec_stream stream, int* detail);
  *            may alias Y exactly: same pointer and leading dimension)
  * Requires N >= 1, K % 8 == 0; M = 0 is a no-op.  Runs on tcgen05 tensor
  * cores with TMA-staged 128 x 64 weight tiles (M <= "gemv_max_m", off by
- * default, takes a CUDA-core weight stream instead).  Workspace: spec_linear_workspace_bytes (0 when no
- * K split is needed; the pointer may then be NULL). */
+ * default, takes a CUDA-core weight stream instead).  Workspace:
+ * spec_linear_workspace_bytes (0 when no K split is needed; the pointer may
+ * then be NULL). */
 SPEC_API size_t spec_linear_workspace_bytes(int M, int N, int K);
 SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,
                        const spec_bf16* W, int N, int ldw,
