@@ -177,3 +177,31 @@ def test_sampler_empty_batch_and_bad_token_flag(lib):
     empty = torch.zeros(1, dtype=torch.int32, device="cuda")
     n, t, near = lib.spec_reject_sample(Pd, Qd, dev(drafts), dev(U), empty)
     assert n.numel() == 0 and near.numel() == 0
+
+
+@pytest.mark.parametrize("M,T", [(368, 0.7), (300, 0.0), (260, 1.0)])
+def test_lmhead_token_tiling_does_not_change_results(lib, M, T):
+    """One 384-row token tile (lmhead_nsub 2, the default above 256 rows) or two 192-row tiles
+    (lmhead_nsub 1): every logit is the same k-ordered sum and every statistic covers the same 128
+    vocabulary rows, so the probabilities come out bit for bit the same; both match the oracle."""
+    K, V = 512, 8200
+    H = bf16_dev(synth.normal_bf16_bits(M, (M, K), 1.0))
+    W = bf16_dev(synth.normal_bf16_bits(M + 1, (V, K), 0.05))
+    out = {}
+    for nsub in (1, 2):
+        lib.spec_set_option("lmhead_nsub", nsub)
+        try:
+            out[nsub] = lib.spec_lmhead_softmax(H, W, T)
+            lib.spec_device_status()
+        finally:
+            lib.spec_set_option("lmhead_nsub", 2)
+    assert torch.equal(out[1], out[2])
+    logits = oops.linear(obf.decode(synth.normal_bf16_bits(M, (M, K), 1.0)),
+                         obf.decode(synth.normal_bf16_bits(M + 1, (V, K), 0.05)))
+    ref = oops.target_probs(logits, T)
+    if T > 0:
+        assert np.abs(out[2].cpu().numpy().astype(np.float64) - ref).max() < PROB_ATOL
+    else:
+        top2 = np.sort(logits, axis=1)
+        clear = (top2[:, -1] - top2[:, -2]) > 1e-3
+        assert np.array_equal(out[2].cpu().numpy().argmax(1)[clear], logits.argmax(1)[clear])
