@@ -94,10 +94,7 @@ SPEC_API int spec_version(void);
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
  * and sum the pieces on chip; "lmhead_nsub" (2 default, or 1): the LM head's
- * tensor-core tiles cover up to 384 or 256 rows; "linear_multicast" (1 =
- * off, default; 2 or 4): the persistent tensor-core GEMM runs clusters of up
- * to that many CTAs on adjacent weight tiles, each token tile loaded once per
- * cluster (TMA multicast); "pdl" (1 default, 0 off):
+ * tensor-core tiles cover up to 384 or 256 rows; "pdl" (1 default, 0 off):
  * kernels are launched with programmatic dependent launch, so each one's
  * launch and on-chip setup overlap the end of the kernel before it on the
  * stream (every kernel still waits for that kernel before touching memory).
@@ -112,6 +109,19 @@ SPEC_API int spec_set_option(const char* name, int value);
  * cache capacity, draft tokens outside the vocabulary); or SPEC_ECUDA.
  * *detail (may be NULL) gets the kernel's site code. */
 SPEC_API int spec_device_status(spec_stream stream, int* detail);
+
+/* Failure-detection probe of the bounded device wait that every TMA / MMA
+ * pipeline of the library waits with (no counterpart on the pages: it tests
+ * the library's own error path, the way a failing wait would surface).  One
+ * CTA waits on an mbarrier that expects one arrival.  arrive = 0: nothing
+ * arrives, the wait gives up after limit_us microseconds (1..2000000) and
+ * records site SPEC_PROBE_WAIT_SITE, so the next spec_device_status returns
+ * SPEC_ETIMEOUT with that detail and clears it; the kernel returns and the
+ * context stays usable.  arrive = 1: a second warp arrives after about
+ * limit_us / 4 and the wait succeeds (status stays clear).  Asynchronous on
+ * `stream`; no workspace. */
+#define SPEC_PROBE_WAIT_SITE 0x1E1
+SPEC_API int spec_probe_bounded_wait(int limit_us, int arrive, spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Verify linear: Y = X W^T (+ residual)                                     */
@@ -145,8 +155,11 @@ SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,
  * holds until the process exits.  Calls whose K split needs more scratch than
  * that return SPEC_EUNSUPPORTED and launch nothing (use spec_verify_linear with
  * a workspace instead; small verify passes need none or a few MiB).
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call outside any stream capture.
+ * The first call in each CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it for that context (a device reset gives
+ * a new context, so the next call looks it up again); make that first call
+ * outside any stream capture.  All argument checks run before the stream or
+ * the array is touched: a rejected call enqueues nothing.
  * Each call clears the counters it needs (an async memset on `stream`); all
  * calls share the array, so calls that may overlap on the GPU (other streams,
  * other host threads) race.  No cudaMalloc, cudaFree or other allocating call

@@ -27,6 +27,7 @@ _SIGS = {
     "spec_launches": (_i, []),
     "spec_set_option": (_i, [ctypes.c_char_p, _i]),
     "spec_device_status": (_i, [_vp, ctypes.POINTER(_i)]),
+    "spec_probe_bounded_wait": (_i, [_i, _i, _vp]),
     "spec_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
@@ -137,6 +138,24 @@ def spec_device_status(stream=None) -> int:
     detail = ctypes.c_int(0)
     _check(_lib.spec_device_status(_stream(stream), ctypes.byref(detail)))
     return detail.value
+
+
+def spec_device_status_code(stream=None) -> tuple[int, int]:
+    """Like spec_device_status, but returns (status code, site detail) instead of raising on a
+    device-side status (SPEC_ETIMEOUT / SPEC_EINVAL)."""
+    detail = ctypes.c_int(0)
+    rc = _lib.spec_device_status(_stream(stream), ctypes.byref(detail))
+    if rc not in (SPEC_OK, SPEC_ETIMEOUT, SPEC_EINVAL):
+        _check(rc)
+    return rc, detail.value
+
+
+PROBE_WAIT_SITE = 0x1E1
+
+
+def spec_probe_bounded_wait(limit_us: int, arrive: bool = False, stream=None) -> None:
+    """One bounded device wait that runs out after limit_us (arrive False) or completes."""
+    _check(_lib.spec_probe_bounded_wait(int(limit_us), 1 if arrive else 0, _stream(stream)), compute=True)
 
 
 class Workspace:

@@ -48,8 +48,50 @@ int cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The current thread's CUDA context (the driver's handle).  Device addresses of the library's
+// __device__ variables are cached per context: a device reset (cudaDeviceReset) destroys the
+// context and reloads the module, so its next context gets the addresses looked up afresh.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+
+// *ctx = the current context, or NULL when the runtime has not made one current yet.
+int current_context(CUcontext* ctx) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+  });
+  if (!g_ctx_get) return fail(SPEC_ECUDA, "cuCtxGetCurrent entry point unavailable");
+  *ctx = nullptr;
+  if (g_ctx_get(ctx) != CUDA_SUCCESS) return fail(SPEC_ECUDA, "cuCtxGetCurrent failed");
+  return SPEC_OK;
+}
+
+// Device address of one of the library's __device__ variables in the current context, cached in
+// (*cached_ctx, *cached_ptr).  cudaGetSymbolAddress makes the device's primary context current when
+// none is yet, so the context is read again after it.
+template <typename T>
+int symbol_address(const T& symbol, const char* what, CUcontext* cached_ctx, void** cached_ptr) {
+  CUcontext ctx = nullptr;
+  if (int rc = current_context(&ctx)) return rc;
+  if (ctx && ctx == *cached_ctx && *cached_ptr) return SPEC_OK;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, symbol);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  if (int rc = current_context(&ctx)) return rc;
+  if (!ctx) return fail(SPEC_ECUDA, "no current CUDA context after %s", what);
+  *cached_ctx = ctx;
+  *cached_ptr = p;
+  return SPEC_OK;
+}
+
 struct DevInfo {
   int sms = 0;
+  CUcontext ctx = nullptr;     // the context `status` belongs to
+  void* status_ptr = nullptr;
   unsigned* status = nullptr;
 };
 DevInfo g_dev[64];
@@ -65,11 +107,9 @@ int dev_info(DevInfo** out) {
   if (d.sms == 0) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_spec_status);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
-    d.status = static_cast<unsigned*>(p);
   }
+  if (int rc = symbol_address(g_spec_status, "cudaGetSymbolAddress(status)", &d.ctx, &d.status_ptr)) return rc;
+  d.status = static_cast<unsigned*>(d.status_ptr);
   *out = &d;
   return SPEC_OK;
 }
@@ -143,17 +183,15 @@ int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 384 verify rows
 int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 384 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
-int g_linear_mc = 1;     // tunable: largest cluster that shares token tiles by TMA multicast
 
 struct LinPlan {
   bool gemv = false;
   int BN = 16, NSUB = 1, tiles_m = 1, tiles_n = 1, k_tiles = 1, splits = 1;
-  int grid = 1;                 // persistent work groups of the tensor-core path (clusters of cl CTAs)
-  int cl = 1;                   // CTAs per cluster sharing each token tile (TMA multicast)
+  int grid = 1;                 // persistent CTAs of the tensor-core path
   int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
   int rem_S = 0;                // > 0: whole tiles on the persistent kernel, then the remaining
   long long rem_tiles = 0;      //      rem_tiles on the cluster split-K kernel (S = rem_S)
-  int x_box_rows() const { return cl > 1 ? BN * NSUB / cl : BN; }   // token rows per TMA load
+  int x_box_rows() const { return BN; }   // token rows per TMA load
   bool aligned = false;         // whole tiles only (no stream-K region)
   long long dp_tiles = 0, sk_units = 0;
   long long units = 0;
@@ -234,25 +272,11 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
       return p;
     }
   }
-  // token tiles of 64+ rows (as many bytes per k-step as half a weight tile or more): clusters
-  // of cl CTAs take cl adjacent weight tiles in lockstep and load each token tile once for all
-  // of them (TMA multicast), which cuts the L2 -> SM traffic that otherwise dominates
-  int cl_cap = 0;
-  if (TN >= 64)
-    for (int c = g_linear_mc; c >= 2; c /= 2) {
-      if (TN % (8 * c) != 0 || p.tiles_n < c) continue;
-      const int cap = linear_tc_cluster_capacity(p.BN, p.NSUB, c);
-      if (cap < 1) continue;
-      p.cl = c;
-      cl_cap = cap;
-      break;
-    }
-  const long long ctiles = (long long)p.tiles_m * ((p.tiles_n + p.cl - 1) / p.cl);
-  p.units = ctiles * p.k_tiles;
+  const long long ctiles = tiles;
   // many tiles, not a multiple of the SM count: the whole tiles one per CTA (none split) on the
   // persistent kernel, then the remainder on the cluster split-K kernel (on-chip sums: no fp32
   // pieces through L2, no reduce kernel), when that costs fewer k-steps than stream-K
-  if (!lmhead && g_linear_cluster && g_force_grid == 0 && p.cl == 1 && tiles > sms && tiles % sms != 0 &&
+  if (!lmhead && g_linear_cluster && g_force_grid == 0 && tiles > sms && tiles % sms != 0 &&
       !p.aligned) {
     const long long rem = tiles % sms;
     int best = 0;
@@ -274,11 +298,11 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
       return p;
     }
   }
-  int grid = g_force_grid > 0 ? g_force_grid : (p.cl > 1 ? std::min(cl_cap, sms / p.cl) : sms);
+  int grid = g_force_grid > 0 ? g_force_grid : sms;
   const long long cap_units = p.aligned ? ctiles : p.units;
   if (grid > cap_units) grid = (int)cap_units;
   p.grid = std::max(1, grid);
-  // data-parallel tiles first (every group gets as many whole cluster tiles as all can), stream-K
+  // data-parallel tiles first (every CTA gets as many whole tiles as all can), stream-K
   // for the rest
   if (p.aligned) {
     p.dp_tiles = ctiles;
@@ -293,7 +317,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   }
   bool split = false;
   for (int c = 1; c < p.grid && !split && p.sk_units > 0; ++c) split = ((p.sk_units * c / p.grid) % p.k_tiles) != 0;
-  p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * p.cl * 2 * TN * 128 * 4, 256) : 0;
+  p.bytes = split ? kCounterBytes + round_up(size_t(p.grid) * 2 * TN * 128 * 4, 256) : 0;
   return p;
 }
 
@@ -356,11 +380,6 @@ int spec_set_option(const char* name, int value) {
     g_w_promotion = value;
     return ok();
   }
-  if (!strcmp(name, "linear_multicast")) {
-    if (value != 1 && value != 2 && value != 4) return fail(SPEC_EINVAL, "linear_multicast must be 1, 2 or 4");
-    g_linear_mc = value;
-    return ok();
-  }
   if (!strcmp(name, "lmhead_nsub")) {
     if (value < 1 || value > 2) return fail(SPEC_EINVAL, "lmhead_nsub must be 1 or 2");
     g_lmhead_nsub = value;
@@ -414,17 +433,28 @@ int spec_device_status(spec_stream stream, int* detail) {
   return ok();
 }
 
+int spec_probe_bounded_wait(int limit_us, int arrive, spec_stream stream) {
+  if (limit_us < 1 || limit_us > 2000000) return fail(SPEC_EINVAL, "limit_us=%d must be in [1, 2000000]", limit_us);
+  if (arrive != 0 && arrive != 1) return fail(SPEC_EINVAL, "arrive must be 0 or 1");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaError_t e = launch_wait_probe(d->status, SPEC_PROBE_WAIT_SITE, (unsigned long long)limit_us * 1000ull, arrive,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+  return ok(1);
+}
+
 // --------------------------------------------------------------------------- linear
 size_t spec_linear_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   return plan_linear(M, N, K, false).bytes;
 }
 
-int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
-                       int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
-                       void* workspace, size_t workspace_bytes, spec_stream stream) {
-  if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
-  if (M == 0) return ok();
+}  // extern "C"
+
+// Host-side checks of a verify-linear call with M >= 1 (everything but the workspace).
+static int check_linear_args(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                             const spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr) {
   if (!X || !W || !Y) return fail(SPEC_EINVAL, "X, W and Y must be non-NULL");
   if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
   if (ldx < K || ldw < K || ldy < N || (residual && ldr < N))
@@ -441,6 +471,17 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     if (r0 < y1 && y0 < r1) return fail(SPEC_EINVAL, "residual overlaps Y without being Y");
   }
   if (residual == Y && ldr != ldy) return fail(SPEC_EINVAL, "residual aliases Y with another ldr");
+  return SPEC_OK;
+}
+
+extern "C" {
+
+int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                       int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
+                       void* workspace, size_t workspace_bytes, spec_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
+  if (M == 0) return ok();
+  if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr)) return rc;
   LinPlan p = plan_linear(M, N, K, false);
   if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes))
     return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
@@ -474,7 +515,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
@@ -485,7 +526,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
     if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch");
     return ok(1);
   }
-  dim3 grid(p.grid * p.cl);
+  dim3 grid(p.grid);
   cudaError_t e = launch_linear_tc_bf16(p.BN, p.NSUB, tw, tx, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 linear launch");
   if (p.rem_S > 0) {   // the tiles after a.dp_tiles: cluster split-K
@@ -550,7 +591,7 @@ int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spe
     }
     LinearArgs a{};
     a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-    a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+    a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
     a.Y = Y; a.ldy = ldy; a.residual = nullptr; a.ldr = 0;
     a.status = d->status;
     a.tn = p.BN * p.NSUB;
@@ -636,7 +677,7 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   }
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.Y = A; a.ldy = lda; a.residual = nullptr; a.ldr = 0;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
@@ -647,7 +688,7 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
     if (e != cudaSuccess) return cuda_fail(e, "cluster swiglu linear launch");
     return ok(1);
   }
-  cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid * p.cl), s);
+  cudaError_t e = launch_linear_tc_swiglu(p.BN, p.NSUB, tw, tx, a, dim3(p.grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 swiglu linear launch");
   if (p.rem_S > 0) {
     e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.rem_S, (int)p.rem_tiles, s);
@@ -687,13 +728,13 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
   const bool greedy = temperature == 0.f;
   LinearArgs a{};
   a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
-  a.units = p.units; a.grid = p.grid; a.cl = p.cl; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
+  a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.status = d->status;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = Z;
   a.ldp = ldz;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
-  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid * p.cl), s);
+  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   *stats_out = a.stats;
   return SPEC_OK;
@@ -1010,7 +1051,11 @@ int spec_silu_mul(const spec_bf16* GU, int M, int I, int ldgu, spec_bf16* A, int
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-void* g_noalloc_ptr[64] = {};
+struct NoallocSlot {
+  CUcontext ctx = nullptr;
+  void* ptr = nullptr;
+};
+NoallocSlot g_noalloc[64];
 std::mutex g_noalloc_mu;
 
 int noalloc_scratch(void** out) {
@@ -1019,13 +1064,10 @@ int noalloc_scratch(void** out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(SPEC_EUNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  NoallocSlot& sl = g_noalloc[dev];
+  if (int rc = symbol_address(g_noalloc_scratch, "cudaGetSymbolAddress(static scratch)", &sl.ctx, &sl.ptr))
+    return rc;
+  *out = sl.ptr;
   return SPEC_OK;
 }
 }  // namespace
@@ -1036,6 +1078,8 @@ extern "C" int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int 
                                           spec_stream stream) {
   if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
   if (M == 0) return ok();
+  // every argument check runs before anything touches the stream or the scratch
+  if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr)) return rc;
   const size_t need = spec_linear_workspace_bytes(M, N, K);
   if (need > SPEC_NOALLOC_SCRATCH_BYTES)
     return fail(SPEC_EUNSUPPORTED,

@@ -99,15 +99,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: true when the phase with `parity` completed, false on timeout
-// (status word set to `site`).
+// Bounded wait: true when the phase with `parity` completed, false once `limit_ns` of wall time
+// has passed without it (status word set to `site`).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status,
-                                          unsigned site) {
+                                          unsigned site, uint64_t limit_ns = SPEC_WAIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && globaltimer() - t0 > SPEC_WAIT_NS) {
+    if ((it & 255u) == 255u && globaltimer() - t0 > limit_ns) {
       set_status(status, site);
       return false;
     }
@@ -132,16 +132,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-// The same load delivered to the same shared-memory offset (and mbarrier offset) of every CTA
-// of the cluster named in `mask` (one bit per rank).
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
 }
 // Rank of this CTA in its cluster, and a barrier over every thread of every CTA of the cluster
@@ -218,14 +208,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-// Arrive on the mbarrier at `bar`'s offset in every CTA of the cluster named in `mask` once all
-// previously issued MMAs of this thread complete.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)), "h"(mask)
       : "memory");
 }
 // 16 consecutive TMEM columns of this thread's lane, loaded and waited for in one asm

@@ -266,7 +266,35 @@ rope_apply_kernel(uint16_t* __restrict__ Y, int ldy, int heads, int D, const flo
   }
 }
 
+// Failure-detection probe of the bounded wait every pipeline uses: thread 0 waits on an mbarrier
+// that expects one arrival.  With arrive = 0 nothing arrives, so the wait runs out after limit_ns
+// and records `site`; with arrive = 1 warp 1 arrives after about limit_ns / 4 and the wait succeeds.
+// Both ends are bounded: the waiting side by the wait's limit, the arriving side by its own delay.
+__global__ void wait_probe_kernel(unsigned* status, unsigned site, unsigned long long limit_ns, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait(&bar, 0u, status, site, limit_ns);
+  } else if (threadIdx.x == 32 && arrive) {
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < limit_ns / 4) {
+    }
+    mbar_arrive(&bar);
+  }
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned* status, unsigned site, unsigned long long limit_ns, int arrive,
+                              cudaStream_t s) {
+  cudaError_t e = launch_k(wait_probe_kernel, dim3(1), dim3(64), 0, s, status, site, limit_ns, arrive);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
                            uint16_t* Y, int ldy, cudaStream_t s) {

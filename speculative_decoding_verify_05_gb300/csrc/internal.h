@@ -63,8 +63,6 @@ constexpr int kMaxBN = 256;
 constexpr int kMaxTN = 384;   // rows of a two-MMA token tile (three 64 KB ring stages)
 int linear_tc_smem_bytes(int BN, int NSUB);
 bool linear_tc_supported(int BN, int NSUB);
-// Clusters of cl CTAs of the persistent GEMM that fit on the device at once (0: none / unknown).
-int linear_tc_cluster_capacity(int BN, int NSUB, int cl);
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_linear_tc_swiglu(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
@@ -156,6 +154,11 @@ cudaError_t launch_typical_sample(const float* P, const int32_t* draft, const fl
 constexpr int NGRAM_MAX_WINDOW = 64;
 cudaError_t launch_ngram_propose(const int32_t* tokens, const int32_t* cu_len, int B, int k, int n_min, int n_max,
                                  int32_t* drafts, int32_t* n_drafts, unsigned* status, cudaStream_t s);
+
+// ---- failure-detection probe: one bounded mbarrier wait that nothing (arrive = 0) or a second
+//      warp (arrive = 1) completes
+cudaError_t launch_wait_probe(unsigned* status, unsigned site, unsigned long long limit_ns, int arrive,
+                              cudaStream_t s);
 
 // ---- glue
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,

@@ -41,16 +41,14 @@ struct LinearArgs {
   int k_tiles;          // 64-wide k-steps per tile
   int tiles_m, tiles_n;
   long long units;      // work units: cluster tiles * k_tiles
-  int grid;             // persistent work groups (clusters of cl CTAs)
-  int cl;               // CTAs per cluster: they take cl adjacent weight tiles of one cluster tile
-                        // in lockstep and share each token tile by TMA multicast (1: no cluster)
-  long long dp_tiles;   // cluster tiles 0 .. dp_tiles - 1 go whole to groups c, c + grid, ...
+  int grid;             // persistent CTAs
+  long long dp_tiles;   // tiles 0 .. dp_tiles - 1 go whole to CTAs c, c + grid, ...
   long long sk_units;   // the k-steps of the other tiles, split evenly between the CTAs (stream-K)
   uint16_t* Y;
   int ldy;
   const uint16_t* residual;
   int ldr;
-  float* partial;       // [grid * cl][2][TN][128] fp32 (split tiles only)
+  float* partial;       // [grid][2][TN][128] fp32 (split tiles only)
   int tn;               // token columns per tile (BN * NSUB)
   int epi;              // the reduce kernel's epilogue: EPI_BF16 (+ residual) or EPI_SWIGLU
   unsigned* status;     // library status word (bounded-wait timeouts)

@@ -36,27 +36,6 @@ int linear_tc_smem_bytes(int BN, int NSUB) {
 
 bool linear_tc_supported(int BN, int NSUB) { return linear_tc_smem_bytes(BN, NSUB) > 0; }
 
-int linear_tc_cluster_capacity(int BN, int NSUB, int cl) {
-  if (cl < 2 || cl > 8 || BN % 16 || BN < 16 || BN > 256 || NSUB < 1 || NSUB > 2) return 0;
-  static int cache[64][3][17][9];   // [device][NSUB][BN / 16][cl]: clusters + 1, 0 = not asked yet
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const bool cacheable = dev >= 0 && dev < 64;
-  if (cacheable && cache[dev][NSUB][BN / 16][cl] != 0) return cache[dev][NSUB][BN / 16][cl] - 1;
-  int n = 0;
-  switch (NSUB * 1000 + BN) {
-#define X(ns, bn) \
-  case ns * 1000 + bn: n = linear_tc_clusters_resident<bn, ns, EPI_BF16>(cl); break;
-    X(1, 16) X(1, 32) X(1, 48) X(1, 64) X(1, 80) X(1, 96) X(1, 112) X(1, 128) X(1, 144) X(1, 160)
-    X(1, 176) X(1, 192) X(1, 208) X(1, 224) X(1, 240) X(1, 256)
-    X(2, 144) X(2, 160) X(2, 176) X(2, 192) X(2, 208) X(2, 224) X(2, 240) X(2, 256)
-#undef X
-    default: n = 0;
-  }
-  if (cacheable) cache[dev][NSUB][BN / 16][cl] = n + 1;
-  return n;
-}
-
 cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, dim3 grid, cudaStream_t s) {
   switch (NSUB * 1000 + BN) {
@@ -118,21 +97,18 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
     s_hi[c] = hi;
   }
   __syncthreads();
-  const int CL = a.cl > 1 ? a.cl : 1;
   const int cols8 = (TN + 7) / 8;
-  const long long items = (long long)G * CL * cols8;
+  const long long items = (long long)G * cols8;
   const int lane = threadIdx.x & 31;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
-    const int cr = (int)(it / cols8);
-    const int c = cr / CL, r = cr - c * CL;
+    const int c = (int)(it / cols8);
     const int hi = s_hi[c];
     if (hi < 0) continue;
-    const int j0 = (int)(it - (long long)cr * cols8) * 8;
+    const int j0 = (int)(it - (long long)c * cols8) * 8;
     const long long t0 = s_beg[c] / kt * kt;
     const long long ctile = a.dp_tiles + t0 / kt;
-    const int n_t = (int)(ctile / a.tiles_m) * CL + r;
-    if (n_t >= a.tiles_n) continue;
+    const int n_t = (int)(ctile / a.tiles_m);
     const int m0 = (int)(ctile % a.tiles_m) * TN + j0;
     const int n4 = n_t * 128 + lane * 4;
     float4 acc[8];
@@ -146,7 +122,7 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
         // slot 0 holds the piece that opens a CTA's stream-K range: the tile's iff the range starts
         // inside it; a CTA with an empty range (fewer stream-K units than CTAs) left nothing
         const float* base = (cc <= hi && s_beg[cc] < s_beg[cc + 1])
-                                ? a.partial + ((size_t)(cc * CL + r) * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
+                                ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
                                 : nullptr;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
@@ -213,7 +189,7 @@ cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   // one wave: two 256-thread blocks per SM (register budget), grid-stride over the items
-  const long long warps = (long long)a.grid * (a.cl > 1 ? a.cl : 1) * ((a.tn + 7) / 8);
+  const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
   long long blocks = (warps + 7) / 8;
   if (blocks > 2LL * sms) blocks = 2LL * sms;
   cudaError_t e = launch_k(linear_reduce_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), smem, s, a);

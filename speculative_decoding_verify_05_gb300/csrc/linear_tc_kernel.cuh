@@ -69,10 +69,9 @@ __device__ __forceinline__ bool bar_epi_and(bool v) {
   return r != 0;
 }
 
-// Work of persistent group c (a cluster of cl CTAs, or one CTA): its data-parallel cluster tiles
-// c, c + grid, ... below dp_tiles, then its share [sk_begin, sk_end) of the stream-K units (unit u
-// is k-step u % kt of cluster tile dp_tiles + u / kt).  Cluster tile t covers token tile
-// t % tiles_m and weight tiles (t / tiles_m) cl .. + cl - 1, one per rank of the cluster.
+// Work of persistent CTA c: its data-parallel tiles c, c + grid, ... below dp_tiles, then its
+// share [sk_begin, sk_end) of the stream-K units (unit u is k-step u % kt of tile dp_tiles + u / kt).
+// Tile t covers token tile t % tiles_m and weight tile t / tiles_m.
 struct CtaWork {
   int n_dp;
   long long sk_begin, sk_end;
@@ -141,10 +140,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;                       // partial-sum slots are per CTA
-  const int CL = args.cl > 1 ? args.cl : 1;         // CTAs sharing each token tile
-  const int rank = CL > 1 ? (int)cta_rank_in_cluster() : 0;
-  const uint16_t mc_mask = (uint16_t)((1u << CL) - 1u);
-  const int wg = cta / CL;                           // work group (cluster)
+  const int wg = cta;                                // work group
   const CtaWork work = cta_work(args, wg);
 
   if (threadIdx.x == 0) {
@@ -152,7 +148,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     tma_prefetch_desc(&tm_x);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);   // one MMA commit from every CTA of the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -163,8 +159,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  // peers multicast into this CTA's stages and arrive on its barriers: all initialised first
-  if (CL > 1) cluster_barrier();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
@@ -172,11 +166,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   pdl_trigger();
 
   if (warp == 0) {
-    // ---------------- TMA producer: one continuous stream over this CTA's units.  In a cluster,
-    // rank r loads rows [r TN / CL, (r + 1) TN / CL) of the token tile into every CTA's stage, so
-    // a stage is refilled only once every CTA has consumed it (empty counts CL commits).
+    // ---------------- TMA producer: one continuous stream over this CTA's units
     if (lane == 0) {
-      long long issued = 0;
       for (long long i = 0; i < work.n; ++i) {
         const int s = (int)(i % STAGES);
         const long long r = i / STAGES;
@@ -184,25 +175,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const Seg g = seg_at(args, work, wg, i);
         const int k = g.k;
         const int m_t = (int)(g.tile % args.tiles_m);
-        const int n_t = (int)(g.tile / args.tiles_m) * CL + rank;   // past the last tile: zero fill
+        const int n_t = (int)(g.tile / args.tiles_m);
         mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
         tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
-        if (CL == 1) {
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);
-        } else {
-          const int rows = TN / CL;
-          tma_load_2d_mc(sB + s * Cfg::B_BYTES + rank * rows * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK,
-                         m_t * TN + rank * rows, mc_mask);
-        }
-        issued = i + 1;
+        for (int sub = 0; sub < NSUB; ++sub)
+          tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);
       }
-      // every CTA of the cluster has consumed (and signalled) the last use of each stage before
-      // this CTA may leave: no remote arrival is still on its way to these barriers
-      if (CL > 1)
-        for (long long i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
-          if (!mbar_wait(&empty[i % STAGES], (uint32_t)((i / STAGES) & 1), args.status, 0x105u)) break;
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -231,8 +210,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             for (int sub = 0; sub < NSUB; ++sub)
               umma_bf16(d + sub * BN, umma_desc_lin(a + kk * 32), umma_desc_lin(b + sub * BN * LIN_ROW_BYTES + kk * 32),
                         idesc, (uu > u || kk > 0) ? 1u : 0u);
-          if (CL > 1) umma_commit_mc(&empty[s], mc_mask);
-          else umma_commit(&empty[s]);
+          umma_commit(&empty[s]);
         }
         if (!ok) break;
         umma_commit(&acc_full[acc]);
@@ -258,19 +236,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       const bool whole = g.whole;
       const int acc = seg % NBUF;
       const int m0 = (int)(tile % args.tiles_m) * TN;
-      const int n_t = (int)(tile / args.tiles_m) * CL + rank;
+      const int n_t = (int)(tile / args.tiles_m);
       const int n0 = n_t * 128;
       const int n = n0 + row;
       ok = ok && mbar_wait(&acc_full[acc], (uint32_t)((seg / NBUF) & 1), args.status, 0x104u);
       ok = bar_epi_and(ok);
       if (!ok) break;
       tc_fence_after();
-      if (n_t >= args.tiles_n) {   // a cluster's spare rank past the last weight tile
-        tc_fence_before();
-        mbar_arrive(&acc_empty[acc]);
-        u = seg_end;
-        continue;
-      }
       const uint32_t t_row = tmem + acc * Cfg::ACC_COLS + (uint32_t(q * 32) << 16);
 
       if constexpr (EPI == EPI_BF16 || EPI == EPI_SWIGLU) {
@@ -434,12 +406,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_barrier();
   if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
-// Host side: one instantiation's launch (a cluster of a.cl CTAs when a.cl > 1) and the number of
-// its clusters of `cl` CTAs that can be resident at once.
+// Host side: one instantiation's launch.
 template <int BN, int NSUB, int EPI>
 static bool linear_tc_configure() {
   static bool configured[64] = {};   // per device
@@ -458,35 +428,9 @@ static cudaError_t launch_linear_tc_one(const CUtensorMap& tw, const CUtensorMap
                                         dim3 grid, cudaStream_t st) {
   using Cfg = LinearCfg<BN, NSUB>;
   if (!linear_tc_configure<BN, NSUB, EPI>()) return cudaGetLastError();
-  cudaError_t e = launch_kc(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, st,
-                            a.cl > 1 ? a.cl : 1, tw, tx, a);
+  cudaError_t e = launch_k(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, st,
+                           tw, tx, a);
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-template <int BN, int NSUB, int EPI>
-static int linear_tc_clusters_resident(int cl) {
-  using Cfg = LinearCfg<BN, NSUB>;
-  if (!linear_tc_configure<BN, NSUB, EPI>()) {
-    cudaGetLastError();
-    return 0;
-  }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(cl * 64);
-  cfg.blockDim = dim3(Cfg::THREADS);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)linear_tc_kernel<BN, NSUB, EPI>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
 }
 
 }  // namespace spec

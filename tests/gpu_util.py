@@ -71,10 +71,33 @@ def assert_close_attn(got, ref, mag, what: str, rel=REL, abs_frac=ATTN_ABS):
                              f"got {got[i]!r} ref {ref[i]!r} magnitude {mag[i]!r}")
 
 
-def assert_rows_close_l2(got, ref, what: str, rel=REL):
-    """Row-wise ||gpu - ref|| / ||ref|| <= rel: the bar for chains of several bf16 ops."""
-    got = np.asarray(got, np.float64).reshape(len(got), -1)
-    ref = np.asarray(ref, np.float64).reshape(len(ref), -1)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    r = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
-    assert r.max() <= rel, f"{what}: worst row relative L2 error {r.max():.3g} (row {int(r.argmax())})"
+# Chains of L layers (hidden state, caches): every bf16 rounding point moves a tensor by up to 2^-9
+# of each element; once that tensor has gone through a linear map and the residual add, the
+# differences are absolute errors of the order of 2^-9 rms per element, and independent rounding
+# differences add up like sqrt(L).  The floor CHAIN_FLOOR sqrt(L) rms(ref) is derived and pinned on
+# the CPU (tests/test_oracle_chain_tolerance.py): correct plans of the arithmetic (fp32 sums,
+# bf16 softmax weights in P.V, other rounding points) stay below it with margin >= 1.5, and planted
+# mistakes exceed it at least 5-fold.
+CHAIN_FLOOR = 0.03
+
+
+def chain_floor(L: int) -> float:
+    return CHAIN_FLOOR * float(np.sqrt(max(L, 1)))
+
+
+def assert_close_chain(got, ref, L: int, what: str):
+    """Element-wise |gpu - ref| <= 2e-2 |ref| + CHAIN_FLOOR sqrt(L) rms(ref)."""
+    assert_close_rel(got, ref, what, rel=REL, floor=chain_floor(L))
+
+
+# The draft engine's q rows after two layers of a peaked draft stack (tied table of std 0.2:
+# p up to ~0.9): the oracle's own perturbation to GPU-like arithmetic moves q by up to 0.025
+# (tests/test_oracle_chain_tolerance.py), so the GPU is held to 1.6 times that.
+DRAFT_PROB_BOUND = 4e-2
+
+
+# Probabilities at the end of a stack of up to 2 layers (the tiny GPU stacks, T > 0): correct plans
+# move them by up to 1.1e-3 on the oracle itself, about half of this bound (pinned in
+# test_oracle_chain_tolerance.py); the 1e-5 bar applies to the LM-head softmax on identical logits,
+# which the op tests check.
+STACK_PROB_BOUND = 2e-3

@@ -224,34 +224,27 @@ def test_linear_swiglu_leaves_counter_region_zero(lib, M, I, K):
     assert torch.count_nonzero(ws.buf[:1 << 16]).item() == 0
 
 
-@pytest.mark.parametrize("mc", [1, 2, 4])
 @pytest.mark.parametrize("M,N,K,grid", [
-    (368, 6144, 1024, 0),    # 48 weight tiles, cluster tiles of 2 / 4, stream-K remainder
-    (300, 1152, 1000, 0),    # 9 weight tiles: spare ranks in the last cluster tile
+    (368, 6144, 1024, 0),    # 48 weight tiles on the persistent kernel, stream-K remainder
+    (300, 1152, 1000, 0),    # 9 weight tiles
     (513, 640, 256, 0),      # two token tiles, 5 weight tiles
-    (100, 1000, 520, 7),     # ragged N, forced grid of 7 groups
-    (368, 2048, 512, 3),     # 3 groups: every cluster tile split between groups
+    (100, 1000, 520, 7),     # ragged N, forced grid of 7 CTAs
+    (368, 2048, 512, 3),     # 3 CTAs: every tile split between CTAs
     (64, 384, 264, 0),
 ])
-def test_linear_token_multicast(lib, mc, M, N, K, grid):
-    """Persistent GEMM with clusters sharing each token tile by TMA multicast (1 = no cluster)."""
-    lib.spec_set_option("linear_multicast", mc)
+def test_linear_persistent_stream_k(lib, M, N, K, grid):
+    """Persistent GEMM with the cluster split-K plan switched off: whole tiles, stream-K pieces
+    and the reduce kernel on every shape."""
     lib.spec_set_option("linear_cluster", 0)
     try:
-        run_case(lib, M, N, K, True, seed=M + N + K + mc, gemv_max_m=0, grid=grid)
+        run_case(lib, M, N, K, True, seed=M + N + K, gemv_max_m=0, grid=grid)
     finally:
-        lib.spec_set_option("linear_multicast", 1)
         lib.spec_set_option("linear_cluster", 1)
 
 
-@pytest.mark.parametrize("mc", [1, 2, 4])
 @pytest.mark.parametrize("grid", [0, 5])
-def test_linear_swiglu_token_multicast(lib, mc, grid):
-    lib.spec_set_option("linear_multicast", mc)
-    try:
-        run_swiglu(lib, 368, 1216, 1024, seed=500 + mc + grid, gemv_max_m=0, grid=grid)
-    finally:
-        lib.spec_set_option("linear_multicast", 1)
+def test_linear_swiglu_persistent(lib, grid):
+    run_swiglu(lib, 368, 1216, 1024, seed=500 + grid, gemv_max_m=0, grid=grid)
 
 
 @pytest.mark.parametrize("M,N,K", [(368, 24576, 4096), (200, 20480, 136), (300, 19584, 520)])

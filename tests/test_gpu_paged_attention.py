@@ -11,7 +11,7 @@ import torch
 import synth
 from oracle import bf16 as obf, ops as oops
 
-from gpu_util import assert_rows_close_l2, bf16_dev, bits_of, dev
+from gpu_util import assert_close_attn, bf16_dev, bits_of, dev
 
 pytestmark = pytest.mark.gpu
 PAGE = 128
@@ -71,8 +71,11 @@ def test_paged_equals_contiguous_and_oracle(lib, gammas, ctx):
     v = obf.decode(qkv[:, hq + hk:]).reshape(batch.M, Hkv, D)
     ref, _, _ = oops.verify_attention(q, k, v, batch.cu_rows, obf.decode(kc), obf.decode(vc), batch.ctx_len,
                                       1.0 / np.sqrt(D))
+    # magnitude of the summed terms: the same weights applied to |v| (the attention bar)
+    mag, _, _ = oops.verify_attention(q, k, np.abs(v), batch.cu_rows, obf.decode(kc), np.abs(obf.decode(vc)),
+                                      batch.ctx_len, 1.0 / np.sqrt(D))
     got = obf.decode(bits_of(O2)).reshape(batch.M, Hq, D)
-    assert_rows_close_l2(got.reshape(-1, D), ref.reshape(-1, D), "paged attention")
+    assert_close_attn(got, ref, mag, "paged attention")
 
 
 def test_paged_bad_page_id_is_flagged(lib):

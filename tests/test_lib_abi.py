@@ -119,8 +119,15 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"attention_pair_cost", 65) == E
     assert L.spec_set_option(b"attention_pair_cost", -1) == E
     assert L.spec_set_option(b"attention_pair_cost", 8) == 0
-    assert L.spec_set_option(b"linear_multicast", 3) == E
-    assert L.spec_set_option(b"linear_multicast", 4) == 0
+    assert L.spec_set_option(b"linear_multicast", 1) == E      # removed knob
+    # the bounded-wait probe checks its limit before touching the device
+    assert L.spec_probe_bounded_wait(0, 0, None) == E
+    assert L.spec_probe_bounded_wait(2000001, 0, None) == E
+    assert L.spec_probe_bounded_wait(100, 2, None) == E
+    # the allocation-free linear rejects bad arguments before any CUDA call
+    assert L.spec_verify_linear_noalloc(None, 4, 64, 64, fake, 128, 64, fake, 128, None, 0, None) == E
+    assert L.spec_verify_linear_noalloc(fake, 4, 64, 64, fake, 128, 64, fake, 128, odd, 128, None) == E
+    assert L.spec_launches() == 0
 
 
 def test_workspace_queries_are_host_only(built):
