@@ -612,24 +612,51 @@ def ngram_timing(S, hbm_peak, peak_src, dev, reps=5):
                          "traffic": None, "algorithmic_bytes": hb, "peak_source": f"{peak_src} hbm_gbs"}}
 
 
+def stack_chain_ops(S, eng, M, interleaved=True):
+    """The 36-layer linear stack as one chain of products for spec_verify_linear_chain: per layer
+    QKV (h -> qkv), O (o -> x, residual x), gate|up with SwiGLU (h -> a), down (a -> x, residual x).
+    With `interleaved`, layer l+1's QKV projection (independent of layer l) sits between layer l's
+    gate|up and its down projection, which waits for gate|up's output."""
+    per = []
+    for lw in eng.w.layers:
+        per.append([S.linear_op(eng.h[:M], lw.w_qkv, eng.qkv[:M]),
+                    S.linear_op(eng.o[:M], lw.w_o, eng.x[:M], residual=eng.x[:M]),
+                    S.linear_op(eng.h[:M], lw.w_gu, eng.a[:M], swiglu=True),
+                    S.linear_op(eng.a[:M], lw.w_down, eng.x[:M], residual=eng.x[:M])])
+    if not interleaved:
+        return [op for layer in per for op in layer]
+    ops = [per[0][0]]
+    for l, (q, o, gu, dn) in enumerate(per):
+        ops += [o, gu] + ([per[l + 1][0]] if l + 1 < len(per) else []) + [dn]
+    return ops
+
+
 def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
-    """36-layer linear stack (QKV, O, gate/up, down) at M = 5 and M = 1 rows."""
+    """36-layer linear stack (QKV, O, gate|up + SwiGLU, down) at M = 5 and M = 1 rows: the library's
+    small-M path (one weight-streaming chain, spec_verify_linear_chain) and, for comparison, one
+    call per product (and the optional CUDA-core path at M = 1)."""
     import torch
     cur = torch.cuda.current_stream()
-    out = {}
+    out = {"per_call": {}}
     wbytes = dims.layers * 2.0 * (dims.qkv * dims.d + dims.d * dims.Hq * dims.D + 2 * dims.I * dims.d + dims.d * dims.I)
+    assert eng.fused_swiglu
+    chain_ws = S.Workspace(eng.device, max(S.spec_linear_chain_workspace_bytes(stack_chain_ops(S, eng, M), M)
+                                           for M in (1, 5)))
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
-    for M, tag in ((1, "1"), (5, "5"), (1, "1_gemv")):
+    for M, tag in ((1, "1"), (5, "5"), (1, "1_gemv"), (1, "1_chain"), (5, "5_chain")):
         S.spec_set_option("gemv_max_m", 4 if tag == "1_gemv" else 0)
+        chain = tag.endswith("_chain")
+        ops = stack_chain_ops(S, eng, M) if chain else None
+
         def run():
+            if chain:
+                S.spec_verify_linear_chain(ops, M, ws=chain_ws)
+                return
             for lw in eng.w.layers:
                 S.spec_verify_linear(eng.h[:M], lw.w_qkv, Y=eng.qkv[:M], ws=eng.ws)
                 S.spec_verify_linear(eng.o[:M], lw.w_o, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
-                if eng.fused_swiglu:
-                    S.spec_verify_linear_swiglu(eng.h[:M], lw.w_gu, A=eng.a[:M], ws=eng.ws)
-                else:
-                    S.spec_verify_linear(eng.h[:M], lw.w_gu, Y=eng.gu[:M], ws=eng.ws)
+                S.spec_verify_linear_swiglu(eng.h[:M], lw.w_gu, A=eng.a[:M], ws=eng.ws)
                 S.spec_verify_linear(eng.a[:M], lw.w_down, Y=eng.x[:M], residual=eng.x[:M], ws=eng.ws)
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
@@ -649,16 +676,21 @@ def linear_stack_ratio(eng, dims, S, hbm_peak, peak_src, reps=5):
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / reps
         gbs = wbytes / (t / 1e3) / 1e9
-        out[f"m{tag}_us"] = t * 1e3
-        out[f"m{tag}_hbm_gbs"] = gbs
-        out[f"m{tag}_hbm_frac"] = gbs / hbm_peak
+        key = tag.replace("_chain", "")
+        dst = out if chain else out["per_call"]
+        dst[f"m{key}_us"] = t * 1e3
+        dst[f"m{key}_hbm_gbs"] = gbs
+        dst[f"m{key}_hbm_frac"] = gbs / hbm_peak
     S.spec_set_option("gemv_max_m", 0)
+    S.spec_device_status()
     out["clocks"] = clk.stop()
     out["ratio_m5_over_m1"] = out["m5_us"] / out["m1_us"]
+    out["per_call"]["ratio_m5_over_m1"] = out["per_call"]["m5_us"] / out["per_call"]["m1_us"]
     out["weights_gb"] = wbytes / 1e9
-    out["note"] = ("36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096, down 4096x12288}, one CUDA graph "
-                   "per M; m1 = the library's default (tensor-core) path at M=1, m1_gemv = the optional CUDA-core "
-                   "path; peak " + peak_src)
+    out["note"] = ("36 layers x {QKV 6144x4096, O 4096x4096, gate|up 24576x4096 + SwiGLU, down 4096x12288}, one "
+                   "CUDA graph per M; m1/m5 = the small-M path (spec_verify_linear_chain: the 144 products in "
+                   "weight-streaming launches of up to 48, the next layer's QKV between gate|up and down); "
+                   "per_call = one library call per product (m1_gemv: the optional CUDA-core path); peak " + peak_src)
     return out
 
 
@@ -1112,6 +1144,7 @@ def run_profile_case(args):
     round: one full verify round of the benchmark workload (for the launch list);
     attention: one layer of --batch (16) ragged sequences (KV ~0.6 GB at 16, above L2);
     linear: one gate|up projection (201 MB of weights) at --rows rows;
+    chain: the weight-streaming chain of --layers layers' linears at --rows rows;
     swiglu: the same projection with the SwiGLU epilogue (--n interleaved gate|up rows);
     lmhead: the LM head + softmax at --rows rows.
     """
@@ -1135,6 +1168,16 @@ def run_profile_case(args):
         torch.cuda.nvtx.range_push("round")
         st["step"]()
         torch.cuda.nvtx.range_pop()
+    elif args.profile == "chain":
+        # the small-M weight-streaming chain on --layers layers of the stack at --rows rows (4 layers:
+        # 1.5 GB of weights, above L2), interleaved as the benchmark's linear stack
+        dims_c = E.Dims(layers=args.layers)
+        sw = E.random_stack(dims_c, seed=1000, device=dev, with_head=False)
+        eng = E.VerifyEngine(dims_c, sw, [], [], max_M=args.rows, max_rows=1, device=dev)
+        ops = stack_chain_ops(S, eng, args.rows)
+        cws = S.Workspace(dev, S.spec_linear_chain_workspace_bytes(ops, args.rows))
+        for _ in range(args.reps):
+            S.spec_verify_linear_chain(ops, args.rows, ws=cws)
     elif args.profile == "attention":
         nb = args.batch
         batch = synth.ragged_batch(SEED, nb, G_LO, G_HI, CTX_LO, CTX_HI)
@@ -1179,9 +1222,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-draft", action="store_true", help="skip the draft-phase measurement")
     ap.add_argument("--no-extra", action="store_true", help="skip the sweep points and configuration 3")
-    ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead"], default=None,
+    ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead", "chain"], default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
-    ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead")
+    ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead/chain")
+    ap.add_argument("--layers", type=int, default=4, help="stack layers for --profile chain")
     ap.add_argument("--batch", type=int, default=16, help="sequences for --profile attention")
     ap.add_argument("--reps", type=int, default=3, help="launches for --profile")
     ap.add_argument("--n", type=int, default=24576, help="weight rows for --profile linear")

@@ -170,6 +170,45 @@ SPEC_API int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ld
                                         spec_bf16* Y, int ldy,
                                         const spec_bf16* residual, int ldr, spec_stream stream);
 
+/* ------------------------------------------------------------------------ */
+/* Chain of verify linears for a handful of rows (weight-streaming path)     */
+/* ------------------------------------------------------------------------ */
+/* One product of a chain: Y = X W^T (+ residual), or with swiglu = 1 the
+ * fused SwiGLU form of spec_verify_linear_swiglu (W = [2I x K] gate|up rows
+ * interleaved in blocks of 16, N = 2I, Y = A [M x I], no residual).  Same
+ * layouts and alignment rules as spec_verify_linear. */
+typedef struct {
+  const spec_bf16* X; int ldx;
+  const spec_bf16* W; int ldw;
+  spec_bf16* Y; int ldy;
+  const spec_bf16* residual; int ldr;   /* NULL or [M x N]; may alias Y exactly */
+  int N, K;
+  int swiglu;
+} spec_linear_op;
+
+/* Runs n_ops products over the same M (1..32) verify rows, in order: the
+ * result is that of calling spec_verify_linear / spec_verify_linear_swiglu
+ * for each in turn.  At small M the verify pass is a weight stream ([P1] "The
+ * speedup is borrowed, and there is a lender": one weight read serves all
+ * rows; [P3] "Prefill and Decode": bound by memory bandwidth), and one launch
+ * per product pays a pipeline fill and drain each time.  Here one persistent
+ * launch (up to 48 products; longer chains take several) streams the weights
+ * of product j+1 while product j drains: weights never depend on
+ * activations.  Token loads, residual reads and output writes wait on device
+ * flags of the products they depend on, which the library derives from the
+ * buffers' address ranges (read-after-write per 128-column tile where the
+ * regions line up, whole products otherwise).  Putting independent products
+ * between a producer and its consumer (e.g. the next layer's QKV projection
+ * between gate|up and down) hides the wait.  Per 128 x 64 weight tile, the
+ * k-steps are split evenly between CTAs and the pieces summed on chip in CTA
+ * order (deterministic).  X of a product must not overlap its own Y.
+ * Workspace: spec_linear_chain_workspace_bytes (the first 64 KiB are the
+ * shared counter region and are left untouched; the call clears its own
+ * flags after it with an async memset). */
+SPEC_API size_t spec_linear_chain_workspace_bytes(const spec_linear_op* ops, int n_ops, int M);
+SPEC_API int spec_verify_linear_chain(const spec_linear_op* ops, int n_ops, int M,
+                                      void* workspace, size_t workspace_bytes, spec_stream stream);
+
 /* Fused QKV projection and rotary embedding: Y = X W^T, then the first
  * rope_heads 128-column heads of Y (the query and key heads of a fused QKV
  * output) rotated as spec_rope does (rotate-half pairs (i, i + 64)), with the

@@ -32,6 +32,8 @@ _SIGS = {
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
     "spec_verify_linear_rope": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
+    "spec_linear_chain_workspace_bytes": (_sz, [_vp, _i, _i]),
+    "spec_verify_linear_chain": (_i, [_vp, _i, _i, _vp, _sz, _vp]),
     "spec_rope_table": (_i, [_vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "spec_swiglu_linear_workspace_bytes": (_sz, [_i, _i, _i]),
     "spec_verify_linear_swiglu": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _sz, _vp]),
@@ -232,6 +234,47 @@ def spec_verify_linear_noalloc(X, W, Y, residual=None, stream=None):
         _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
         _stream(stream)), True)
     return Y
+
+
+class LinearOp(ctypes.Structure):
+    """One product of spec_verify_linear_chain (the C struct spec_linear_op)."""
+    _fields_ = [("X", _vp), ("ldx", _i), ("W", _vp), ("ldw", _i), ("Y", _vp), ("ldy", _i),
+                ("residual", _vp), ("ldr", _i), ("N", _i), ("K", _i), ("swiglu", _i)]
+
+
+def linear_op(X, W, Y, residual=None, swiglu: bool = False) -> "LinearOp":
+    """Describe Y = X W^T (+ residual), or the fused SwiGLU form (W gate|up interleaved, Y = A)."""
+    for t, name in ((X, "X"), (W, "W"), (Y, "Y")):
+        _need(t, torch.bfloat16, name)
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual")
+    N, K = W.shape
+    if X.shape[1] != K or Y.shape[0] != X.shape[0] or Y.shape[1] != (N // 2 if swiglu else N):
+        raise ValueError("shapes of X, W and Y do not match")
+    op = LinearOp(X.data_ptr(), _rowmajor(X, "X"), W.data_ptr(), _rowmajor(W, "W"), Y.data_ptr(),
+                  _rowmajor(Y, "Y"), residual.data_ptr() if residual is not None else None,
+                  _rowmajor(residual, "residual") if residual is not None else 0, N, K, 1 if swiglu else 0)
+    op.tensors = (X, W, Y, residual)    # the struct holds raw pointers: keep their memory alive with it
+    return op
+
+
+def _op_array(ops):
+    arr = (LinearOp * len(ops))()
+    for i, o in enumerate(ops):
+        arr[i] = o
+    return arr
+
+
+def spec_linear_chain_workspace_bytes(ops, M: int) -> int:
+    return int(_lib.spec_linear_chain_workspace_bytes(_op_array(ops), len(ops), int(M)))
+
+
+def spec_verify_linear_chain(ops, M: int, ws=None, stream=None, device=None) -> None:
+    """Run the products `ops` (a list of linear_op(...)) over M rows in one weight stream."""
+    arr = _op_array(ops)
+    need = int(_lib.spec_linear_chain_workspace_bytes(arr, len(ops), int(M)))
+    wp, wn = _ws_args(ws, need, device if device is not None else torch.cuda.current_device())
+    _check(_lib.spec_verify_linear_chain(arr, len(ops), int(M), wp, wn, _stream(stream)), True)
 
 
 def spec_rope_table(cu_rows, ctx_len, M: int, D: int, theta: float = 1e6, cs=None, stream=None):

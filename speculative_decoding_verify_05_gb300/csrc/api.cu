@@ -10,6 +10,8 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
+#include <algorithm>
 
 #include "../../include/spec_verify.h"
 #include "common.cuh"
@@ -540,6 +542,259 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
   return ok(2);
 }
+
+}  // extern "C"
+
+// --------------------------------------------------------------------------- linear chain (small M)
+namespace {
+
+// An [M x cols] bf16 matrix with leading dimension ld, for dependency analysis.
+struct Region {
+  const char* base = nullptr;
+  long long ld = 0, cols = 0;
+  bool valid() const { return base != nullptr; }
+};
+
+Region region_of(const void* p, int ld, long long cols) {
+  Region r;
+  r.base = static_cast<const char*>(p);
+  r.ld = ld;
+  r.cols = cols;
+  return r;
+}
+
+// Do a and b share an element?  Exact for matrices of the same leading dimension in one row frame,
+// a byte-interval test otherwise (conservative).
+bool overlaps(const Region& a, const Region& b, int M) {
+  if (!a.valid() || !b.valid()) return false;
+  if (a.ld == b.ld) {
+    const long long d = (a.base - b.base) / 2;
+    if ((a.base - b.base) % 2 == 0) {
+      if (d >= 0 && d + a.cols <= a.ld) return d < b.cols;              // a's columns [d, d + cols) in b's frame
+      if (d < 0 && -d + b.cols <= b.ld) return -d < a.cols;
+    }
+  }
+  const char* a1 = a.base + ((long long)(M - 1) * a.ld + a.cols) * 2;
+  const char* b1 = b.base + ((long long)(M - 1) * b.ld + b.cols) * 2;
+  return a.base < b1 && b.base < a1;
+}
+
+// Is every element of reader r inside writer w, column c of r at column c + shift of w?
+bool contains(const Region& w, const Region& r, long long* shift) {
+  if (!w.valid() || !r.valid() || w.ld != r.ld || (r.base - w.base) % 2) return false;
+  const long long d = (r.base - w.base) / 2;
+  if (d < 0 || d + r.cols > w.cols) return false;
+  *shift = d;
+  return true;
+}
+
+struct ChainOpHost {
+  Region x, r, y;
+  const spec_linear_op* op;
+};
+
+// Dependencies of product j on the products [first, j) of its launch (products of earlier launches
+// are complete when it starts).  Returns false when they need more than CH_MAX_DEPS entries.
+bool chain_deps(const std::vector<ChainOpHost>& h, int first, int j, int M, ChainOp* o) {
+  o->n_deps = 0;
+  auto add = [&](int op, int kind, long long shift) {
+    for (int i = 0; i < o->n_deps; ++i)
+      if (o->dep[i].op == op - first && o->dep[i].kind == kind) {
+        if (o->dep[i].shift != (int)shift) o->dep[i].shift = -1;
+        return true;
+      }
+    if (o->n_deps >= CH_MAX_DEPS) return false;
+    o->dep[o->n_deps++] = ChainDep{op - first, kind, (int)shift};
+    return true;
+  };
+  // read-after-write: the latest writer of each read region; when it covers the region, earlier
+  // writers are ordered before it (its own write waited for them)
+  for (int kind : {CH_DEP_X, CH_DEP_RES}) {
+    const Region& rd = kind == CH_DEP_X ? h[j].x : h[j].r;
+    if (!rd.valid()) continue;
+    if (kind == CH_DEP_RES && rd.base == h[j].y.base && rd.ld == h[j].y.ld) {
+      // in place: the residual is this product's own output region; the writers of that region
+      // are found below as well
+    }
+    for (int i = j - 1; i >= first; --i) {
+      if (!overlaps(h[i].y, rd, M)) continue;
+      long long shift = -1;
+      const bool covered = contains(h[i].y, rd, &shift);
+      if (!add(i, kind, covered ? shift : -1)) return false;
+      if (covered) break;
+    }
+  }
+  // write-after-read / write-after-write on Y's region: the latest writer (when it covers the
+  // region, nothing before it matters) and every reader after it
+  int w = first - 1;
+  for (int i = j - 1; i >= first; --i) {
+    if (!overlaps(h[i].y, h[j].y, M)) continue;
+    long long sh;
+    if (contains(h[i].y, h[j].y, &sh)) { w = i; break; }
+  }
+  for (int i = j - 1; i >= first && i >= (w < first ? first : w); --i) {
+    const bool reads = overlaps(h[i].x, h[j].y, M) || overlaps(h[i].r, h[j].y, M);
+    const bool writes = overlaps(h[i].y, h[j].y, M);
+    if (!reads && !writes) continue;
+    // in-place residual stream: product i wrote (and read as its own residual) exactly this
+    // region, and product j waits for i's tile t before reading its residual tile t; its write of
+    // tile t comes after that
+    bool per_tile = false;
+    for (int d = 0; d < o->n_deps; ++d)
+      per_tile = per_tile || (o->dep[d].op == i - first && o->dep[d].kind == CH_DEP_RES && o->dep[d].shift == 0);
+    const bool same_y = h[i].y.base == h[j].y.base && h[i].y.ld == h[j].y.ld && h[i].y.cols == h[j].y.cols &&
+                        h[i].op->swiglu == h[j].op->swiglu;
+    const bool i_in_place = !h[i].r.valid() || (h[i].r.base == h[i].y.base && h[i].r.ld == h[i].y.ld);
+    const bool j_in_place = h[j].r.valid() && h[j].r.base == h[j].y.base && h[j].r.ld == h[j].y.ld;
+    if (per_tile && same_y && i_in_place && j_in_place && !overlaps(h[i].x, h[j].y, M)) continue;
+    if (!add(i, CH_DEP_WRITE, -1)) return false;
+  }
+  return true;
+}
+
+int check_chain_op(const spec_linear_op& op, int M, int k) {
+  if (op.N <= 0 || op.K <= 0) return fail(SPEC_EINVAL, "op %d: bad sizes N=%d K=%d", k, op.N, op.K);
+  if (op.swiglu) {
+    if (op.N % 128) return fail(SPEC_EINVAL, "op %d: SwiGLU needs N = 2I with I a multiple of 64", k);
+    if (op.residual) return fail(SPEC_EINVAL, "op %d: SwiGLU takes no residual", k);
+    if (!op.X || !op.W || !op.Y) return fail(SPEC_EINVAL, "op %d: X, W and Y must be non-NULL", k);
+    if (op.K % 8 || op.ldx < op.K || op.ldw < op.K || op.ldy < op.N / 2 || op.ldx % 8 || op.ldw % 8 || op.ldy % 8)
+      return fail(SPEC_EINVAL, "op %d: K and the leading dimensions must be multiples of 8, ld >= width", k);
+    if (!aligned16(op.X) || !aligned16(op.W) || !aligned16(op.Y))
+      return fail(SPEC_EINVAL, "op %d: X, W, Y must be 16-byte aligned", k);
+    return SPEC_OK;
+  }
+  return check_linear_args(op.X, M, op.K, op.ldx, op.W, op.N, op.ldw, op.Y, op.ldy, op.residual, op.ldr);
+}
+
+// Launches of one chain: products [first, last) each (at most CH_MAX_OPS, and a new launch where a
+// product's dependencies do not fit).
+std::vector<std::pair<int, int>> chain_launches(const std::vector<ChainOpHost>& h, int M) {
+  std::vector<std::pair<int, int>> out;
+  int first = 0;
+  const int n = (int)h.size();
+  while (first < n) {
+    int last = first + 1;
+    ChainOp tmp;
+    while (last < n && last - first < CH_MAX_OPS && chain_deps(h, first, last, M, &tmp)) ++last;
+    out.emplace_back(first, last);
+    first = last;
+  }
+  return out;
+}
+
+size_t chain_flags_bytes(const std::vector<ChainOpHost>& h, int first, int last) {
+  long long tiles = 0;
+  for (int j = first; j < last; ++j) tiles += (h[j].op->N + 127) / 128;
+  return round_up(size_t(2 * tiles + (last - first)) * 4, 256);
+}
+
+size_t chain_pieces_bytes(int n_ops, int M) {
+  return size_t(n_ops) * plan_sms() * chain_bn(M) * 128 * 4;
+}
+
+std::vector<ChainOpHost> chain_host(const spec_linear_op* ops, int n_ops) {
+  std::vector<ChainOpHost> h(n_ops);
+  for (int j = 0; j < n_ops; ++j) {
+    const spec_linear_op& op = ops[j];
+    h[j].op = &op;
+    h[j].x = region_of(op.X, op.ldx, op.K);
+    h[j].y = region_of(op.Y, op.ldy, op.swiglu ? op.N / 2 : op.N);
+    if (op.residual) h[j].r = region_of(op.residual, op.ldr, op.N);
+  }
+  return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_linear_chain_workspace_bytes(const spec_linear_op* ops, int n_ops, int M) {
+  if (!ops || n_ops <= 0 || M <= 0 || M > CH_MAX_M) return 0;
+  const std::vector<ChainOpHost> h = chain_host(ops, n_ops);
+  size_t need = 0;
+  for (const auto& l : chain_launches(h, M))
+    need = std::max(need, kCounterBytes + chain_flags_bytes(h, l.first, l.second) +
+                              chain_pieces_bytes(l.second - l.first, M));
+  return need;
+}
+
+int spec_verify_linear_chain(const spec_linear_op* ops, int n_ops, int M, void* workspace, size_t workspace_bytes,
+                             spec_stream stream) {
+  if (n_ops < 0 || M < 0) return fail(SPEC_EINVAL, "bad sizes n_ops=%d M=%d", n_ops, M);
+  if (n_ops == 0 || M == 0) return ok();
+  if (!ops) return fail(SPEC_EINVAL, "ops must be non-NULL");
+  if (M > CH_MAX_M) return fail(SPEC_EUNSUPPORTED, "M=%d > %d rows (use spec_verify_linear per product)", M, CH_MAX_M);
+  for (int j = 0; j < n_ops; ++j)
+    if (int rc = check_chain_op(ops[j], M, j)) return rc;
+  const std::vector<ChainOpHost> h = chain_host(ops, n_ops);
+  for (int j = 0; j < n_ops; ++j)
+    if (overlaps(h[j].x, h[j].y, M)) return fail(SPEC_EINVAL, "op %d: X overlaps its own Y", j);
+  const auto launches = chain_launches(h, M);
+  size_t need = 0;
+  for (const auto& l : launches)
+    need = std::max(need, kCounterBytes + chain_flags_bytes(h, l.first, l.second) + chain_pieces_bytes(l.second - l.first, M));
+  if (!workspace || workspace_bytes < need) return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int BN = chain_bn(M);
+  int launched = 0;
+  for (const auto& l : launches) {
+    static thread_local ChainParams P;   // ~19 KB: kept off the stack
+    memset(&P, 0, sizeof(P));
+    P.n_ops = l.second - l.first;
+    P.M = M;
+    P.grid = d->sms;
+    const size_t flags = chain_flags_bytes(h, l.first, l.second);
+    unsigned* fl = reinterpret_cast<unsigned*>(ws + kCounterBytes);
+    long long tiles = 0;
+    for (int j = l.first; j < l.second; ++j) tiles += (ops[j].N + 127) / 128;
+    P.arrive = fl;
+    P.done = fl + tiles;
+    P.op_done = fl + 2 * tiles;
+    P.pieces = reinterpret_cast<float*>(ws + kCounterBytes + flags);
+    P.status = d->status;
+    int flag_base = 0;
+    for (int j = l.first; j < l.second; ++j) {
+      const spec_linear_op& op = ops[j];
+      ChainOp& o = P.op[j - l.first];
+      o.Y = op.Y;
+      o.residual = op.residual;
+      o.ldy = op.ldy;
+      o.ldr = op.ldr;
+      o.N = op.N;
+      o.K = op.K;
+      o.k_tiles = (op.K + LIN_BK - 1) / LIN_BK;
+      o.tiles_n = (op.N + 127) / 128;
+      o.units = o.k_tiles * o.tiles_n;
+      o.epi = op.swiglu ? EPI_SWIGLU : EPI_BF16;
+      o.ycols = op.swiglu ? 64 : 128;
+      o.flag_base = flag_base;
+      flag_base += o.tiles_n;
+      if (!chain_deps(h, l.first, j, M, &o)) return fail(SPEC_ECUDA, "internal: chain dependencies overflow");
+      cuuint64_t wd[2] = {(cuuint64_t)op.K, (cuuint64_t)op.N};
+      cuuint64_t wst[1] = {(cuuint64_t)op.ldw * 2};
+      cuuint32_t wbox[2] = {LIN_BK, 128};
+      if (int rc = encode_bf16(&P.tw[j - l.first], op.W, 2, wd, wst, wbox, "W", g_w_promotion, kLinSwizzle)) return rc;
+      cuuint64_t xd[2] = {(cuuint64_t)op.K, (cuuint64_t)M};
+      cuuint64_t xst[1] = {(cuuint64_t)op.ldx * 2};
+      cuuint32_t xbox[2] = {LIN_BK, (cuuint32_t)BN};
+      if (int rc = encode_bf16(&P.tx[j - l.first], op.X, 2, xd, xst, xbox, "X", 3, kLinSwizzle)) return rc;
+    }
+    cudaError_t e = cudaMemsetAsync(fl, 0, flags, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear chain flags");
+    e = launch_linear_chain(P, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear chain launch");
+    ++launched;
+  }
+  return ok(launched);
+}
+
+}  // extern "C"
+
+extern "C" {
 
 // --------------------------------------------------------------------------- linear + RoPE
 int spec_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M, int D, float theta, float* cs,

@@ -80,6 +80,45 @@ cudaError_t launch_linear_tc_lmhead(int BN, int NSUB, bool greedy, const CUtenso
                                     const CUtensorMap& tx, const LinearArgs& a, dim3 grid,
                                     cudaStream_t s);
 
+// ---- weight-streaming chain of small-M GEMMs (one persistent launch for a list of products)
+constexpr int CH_MAX_OPS = 48;     // products per launch (kernel parameter space)
+constexpr int CH_MAX_DEPS = 6;
+constexpr int CH_MAX_M = 32;
+enum ChainDepKind : int {
+  CH_DEP_X = 0,       // X of the product reads Y of `op`: token loads wait (per tile when shift >= 0)
+  CH_DEP_RES = 1,     // the residual reads Y of `op`: the epilogue waits (per tile when shift >= 0)
+  CH_DEP_WRITE = 2    // Y overwrites what `op` reads or writes: the first write waits for all of `op`
+};
+struct ChainDep {
+  int op, kind;
+  int shift;          // >= 0: column c of the consumer's operand is column c + shift of Y_op; -1: whole op
+};
+struct ChainOp {
+  uint16_t* Y;
+  const uint16_t* residual;
+  int ldy, ldr;
+  int N, K, k_tiles, tiles_n;
+  int units;          // tiles_n * k_tiles
+  int epi;            // EPI_BF16 (+ residual) or EPI_SWIGLU
+  int ycols;          // Y columns per weight tile: 128, or 64 with the SwiGLU epilogue
+  int flag_base;      // first per-tile flag of this product
+  int n_deps;
+  ChainDep dep[CH_MAX_DEPS];
+};
+struct ChainParams {
+  CUtensorMap tw[CH_MAX_OPS];
+  CUtensorMap tx[CH_MAX_OPS];
+  ChainOp op[CH_MAX_OPS];
+  int n_ops, M, grid;
+  float* pieces;      // [n_ops][grid][BN][128] fp32
+  unsigned* arrive;   // per tile: pieces published
+  unsigned* done;     // per tile: 1 once Y of the tile is stored
+  unsigned* op_done;  // per product: tiles stored
+  unsigned* status;
+};
+int chain_bn(int M);   // token rows per tile for an M-row chain (-1: M too large)
+cudaError_t launch_linear_chain(const ChainParams& p, cudaStream_t s);
+
 // ---- CUDA-core skinny GEMM (M <= 4)
 struct GemvArgs {
   const uint16_t* X; int ldx;
