@@ -94,7 +94,14 @@ SPEC_API int spec_version(void);
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
  * and sum the pieces on chip; "lmhead_nsub" (2 default, or 1): the LM head's
- * tensor-core tiles cover up to 384 or 256 rows; "pdl" (1 default, 0 off):
+ * tensor-core tiles cover up to 384 or 256 rows; "linear_pair" (1 default,
+ * 0 off): verify linears of 64+ rows with more 128-row weight tiles than SMs
+ * run 256-row tiles on CTA pairs (the tcgen05 2-SM MMA: each CTA of a pair
+ * stages half of the token rows), whole pair tiles first, the rest split
+ * between the pairs of a cluster, no workspace; "linear_pair_few" (0
+ * default, 1): the pair kernel also for products with fewer tiles (split-K
+ * on pairs; measured slower than the one-SM cluster kernel at 368 rows);
+ * "pdl" (1 default, 0 off):
  * kernels are launched with programmatic dependent launch, so each one's
  * launch and on-chip setup overlap the end of the kernel before it on the
  * stream (every kernel still waits for that kernel before touching memory).

@@ -185,6 +185,8 @@ int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 384 verify rows
 int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 384 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
+int g_linear_pair = 1;   // tunable: 1 lets the planner run 256-row pair tiles on the 2-SM MMA
+int g_linear_pair_few = 0;  // tunable: 1 also for products with fewer tiles than SMs (split-K on pairs)
 
 struct LinPlan {
   bool gemv = false;
@@ -193,7 +195,12 @@ struct LinPlan {
   int cluster_S = 0;            // > 0: cluster split-K kernel, S CTAs per tile
   int rem_S = 0;                // > 0: whole tiles on the persistent kernel, then the remaining
   long long rem_tiles = 0;      //      rem_tiles on the cluster split-K kernel (S = rem_S)
-  int x_box_rows() const { return BN; }   // token rows per TMA load
+  int pair_n = 0;               // > 0: launches of the 2-SM pair kernel, launch i covering pair
+  int pair_first[2] = {0, 0};   //      tiles pair_first[i] .. + pair_count[i] - 1 with pair_S[i]
+  int pair_count[2] = {0, 0};   //      pairs per tile
+  int pair_S[2] = {0, 0};
+  // token rows per TMA load: each CTA of a pair stages half of every MMA's token rows
+  int x_box_rows() const { return pair_n > 0 ? BN / 2 : BN; }
   bool aligned = false;         // whole tiles only (no stream-K region)
   long long dp_tiles = 0, sk_units = 0;
   long long units = 0;
@@ -253,6 +260,52 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   // persistent stream-K: one CTA per SM, each streaming an equal share of (tile, k-step) units;
   // the LM-head epilogue needs whole tiles, so its ranges are tile-aligned
   p.aligned = lmhead || tiles > (long long)kMaxCounters;
+  // 2-SM pair tiles (256 weight rows on a CTA pair; each CTA stages half of the token rows, which
+  // halves the shared-memory traffic per MMA that bounds the one-SM kernels at a few hundred rows):
+  // few pair tiles -> one cluster split-K launch of S pairs per tile; more -> whole pair tiles on
+  // every pair (S = 1), then the rest split
+  if (!lmhead && g_linear_pair && g_force_grid == 0 && TN >= 64 && (g_linear_pair_few || tiles > sms)) {
+    const long long ptiles = (long long)p.tiles_m * ((p.tiles_n + 1) / 2);
+    auto best_S = [&](long long n_pt, long long* cost_out) {
+      int best = 0;
+      long long best_cost = 0;
+      for (int S = 1; S <= 4 && S <= p.k_tiles; ++S) {
+        const int cap = linear_pair_capacity(p.BN, p.NSUB, S);
+        if (cap <= 0 || n_pt * 2 * S > cap) continue;
+        const long long cost = (p.k_tiles + S - 1) / S + (S > 1 ? 6 * 64 / LIN_BK : 2);
+        if (best == 0 || cost < best_cost) { best = S; best_cost = cost; }
+      }
+      *cost_out = best_cost;
+      return best;
+    };
+    long long c1 = 0;
+    const int S1 = g_linear_pair_few ? best_S(ptiles, &c1) : 0;
+    if (S1 > 0) {
+      p.pair_n = 1;
+      p.pair_first[0] = 0;
+      p.pair_count[0] = (int)ptiles;
+      p.pair_S[0] = S1;
+      p.bytes = 0;
+      return p;
+    }
+    const int cap1 = linear_pair_capacity(p.BN, p.NSUB, 1);
+    const long long whole = cap1 / 2;
+    if (whole > 0 && ptiles > whole && ptiles - whole <= whole) {
+      long long c2 = 0;
+      const int S2 = best_S(ptiles - whole, &c2);
+      if (S2 > 0) {
+        p.pair_n = 2;
+        p.pair_first[0] = 0;
+        p.pair_count[0] = (int)whole;
+        p.pair_S[0] = 1;
+        p.pair_first[1] = (int)whole;
+        p.pair_count[1] = (int)(ptiles - whole);
+        p.pair_S[1] = S2;
+        p.bytes = 0;
+        return p;
+      }
+    }
+  }
   // few tiles: S CTAs of a cluster split each tile's k-steps and sum on chip (one wave of
   // tiles * S CTAs).  Cost model in k-steps of one tile on one SM: the cluster kernel takes
   // ceil(kt / S) plus ~6 for its on-chip reduction; stream-K takes ceil(units / SMs) plus
@@ -372,6 +425,16 @@ int spec_set_option(const char* name, int value) {
     g_gemv_max_m = value;
     return ok();
   }
+  if (!strcmp(name, "linear_pair")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_pair must be 0 or 1");
+    g_linear_pair = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_pair_few")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_pair_few must be 0 or 1");
+    g_linear_pair_few = value;
+    return ok();
+  }
   if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "pdl must be 0 or 1");
     g_pdl = value;
@@ -476,6 +539,18 @@ static int check_linear_args(const spec_bf16* X, int M, int K, int ldx, const sp
   return SPEC_OK;
 }
 
+// The launches of a pair plan (epilogue already set in a).  Returns the number of launches (0 on
+// error, *err set).
+static int launch_pair_plan(const LinPlan& p, const CUtensorMap& tw, const CUtensorMap& tx, LinearArgs a,
+                            cudaStream_t s, cudaError_t* err) {
+  for (int i = 0; i < p.pair_n; ++i) {
+    a.dp_tiles = p.pair_first[i];
+    *err = launch_linear_pair(p.BN, p.NSUB, tw, tx, a, p.pair_S[i], p.pair_count[i], s);
+    if (*err != cudaSuccess) return 0;
+  }
+  return p.pair_n;
+}
+
 extern "C" {
 
 int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
@@ -523,6 +598,12 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_BF16;
+  if (p.pair_n > 0) {
+    cudaError_t e = cudaSuccess;
+    const int n = launch_pair_plan(p, tw, tx, a, s, &e);
+    if (!n) return cuda_fail(e, "pair linear launch");
+    return ok(n);
+  }
   if (p.cluster_S > 0) {
     cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster linear launch");
@@ -822,8 +903,8 @@ int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spe
   if (rope_heads > 0 && !cs) return fail(SPEC_EINVAL, "cs must be non-NULL");
   if (rope_heads > 0 && !aligned16(cs)) return fail(SPEC_EINVAL, "cs must be 16-byte aligned");
   const LinPlan p = plan_linear(M, N, K, false);
-  if (rope_heads > 0 && p.cluster_S > 0 && !p.gemv) {
-    // few weight tiles: the cluster split-K kernel rotates the q / k heads in its epilogue
+  if (rope_heads > 0 && (p.cluster_S > 0 || p.pair_n > 0) && !p.gemv) {
+    // few weight tiles: the cluster (or pair) split-K kernel rotates the q / k heads in its epilogue
     if (!X || !W || !Y) return fail(SPEC_EINVAL, "X, W and Y must be non-NULL");
     if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
     if (ldx < K || ldw < K || ldy < N || ldx % 8 || ldw % 8 || ldy % 8)
@@ -853,6 +934,12 @@ int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spe
     a.epi = EPI_ROPE;
     a.rope_cs = reinterpret_cast<const float2*>(cs);
     a.rope_tiles = rope_heads;
+    if (p.pair_n > 0) {
+      cudaError_t e = cudaSuccess;
+      const int n = launch_pair_plan(p, tw, tx, a, static_cast<cudaStream_t>(stream), &e);
+      if (!n) return cuda_fail(e, "pair linear + rope launch");
+      return ok(n);
+    }
     cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cluster linear + rope launch");
@@ -938,6 +1025,12 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
+  if (p.pair_n > 0) {
+    cudaError_t e = cudaSuccess;
+    const int n = launch_pair_plan(p, tw, tx, a, s, &e);
+    if (!n) return cuda_fail(e, "pair swiglu linear launch");
+    return ok(n);
+  }
   if (p.cluster_S > 0) {
     cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, s);
     if (e != cudaSuccess) return cuda_fail(e, "cluster swiglu linear launch");

@@ -73,6 +73,12 @@ cudaError_t launch_linear_tc_swiglu(int BN, int NSUB, const CUtensorMap& tw, con
 int linear_cluster_capacity(int BN, int NSUB, int S);
 cudaError_t launch_linear_cluster(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx,
                                   const LinearArgs& a, int S, int tiles, cudaStream_t s);
+// Split-K GEMM on CTA pairs (tcgen05 2-SM MMA, 256-row pair tiles): CTAs resident at once in
+// clusters of S pairs (0: no pair build for the tile shape, or S out of range), and the launch of
+// pair tiles a.dp_tiles .. + pair_tiles - 1 (2 S CTAs each; no workspace).
+int linear_pair_capacity(int BN, int NSUB, int S);
+cudaError_t launch_linear_pair(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a,
+                               int S, int pair_tiles, cudaStream_t s);
 // Second pass of a split GEMM: sums the fp32 pieces of every split tile (in CTA order), adds the
 // residual and writes bf16 Y.  `sms` sizes its grid.
 cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s);
