@@ -178,6 +178,50 @@ SPEC_API int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int ld
                                         const spec_bf16* residual, int ldr, spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm folded into the verify linears                                    */
+/* ------------------------------------------------------------------------ */
+/* A pre-norm layer computes h = RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w and
+ * then h W^T.  With w folded into W once (W' = W diag(w)), that is
+ * (x W'^T) / rms(x): the product can take x itself and scale its rows in the
+ * epilogue, and the product that stores x can leave the sums of squares of the
+ * values it stored, so no separate normalisation pass over x is needed.
+ *   in_ssq   [M x in_tiles] fp32 or NULL: partial sums of squares of X's
+ *            rows (their sum over the in_tiles entries, in order, is
+ *            sum_k X[m][k]^2); row m of the product is scaled by
+ *            1 / sqrt(sum / K + eps)
+ *   out_ssq  [M x ceil(Nout / 128)] fp32 or NULL: per row and 128-column tile
+ *            of the output (Nout = N; I for SwiGLU), the sum of squares of
+ *            the bf16 values stored
+ * Plans whose epilogue cannot do this (tiles not split between CTAs) run a
+ * small normalisation / sum-of-squares kernel instead (same results within
+ * the chain tolerance); the _norm workspace query covers that case. */
+typedef struct {
+  const float* in_ssq;
+  int in_tiles;
+  float eps;
+  float* out_ssq;
+} spec_rownorm;
+
+/* out[m][t] = sum of squares of X[m][128 t .. 128 t + 127] (bf16 values): the
+ * partial sums of a tensor no product stored (e.g. the first layer's input). */
+SPEC_API int spec_row_ssq(const spec_bf16* X, int M, int N, int ldx, float* out, spec_stream stream);
+
+/* spec_verify_linear / _swiglu / _rope with a folded RMSNorm (norm may be NULL). */
+SPEC_API size_t spec_linear_norm_workspace_bytes(int M, int N, int K, int swiglu);
+SPEC_API int spec_verify_linear_norm(const spec_bf16* X, int M, int K, int ldx,
+                                     const spec_bf16* W, int N, int ldw, spec_bf16* Y, int ldy,
+                                     const spec_bf16* residual, int ldr, const spec_rownorm* norm,
+                                     void* workspace, size_t workspace_bytes, spec_stream stream);
+SPEC_API int spec_verify_linear_swiglu_norm(const spec_bf16* X, int M, int K, int ldx,
+                                            const spec_bf16* Wgu, int ldw, int I, spec_bf16* A, int lda,
+                                            const spec_rownorm* norm, void* workspace,
+                                            size_t workspace_bytes, spec_stream stream);
+SPEC_API int spec_verify_linear_rope_norm(const spec_bf16* X, int M, int K, int ldx,
+                                          const spec_bf16* W, int N, int ldw, spec_bf16* Y, int ldy,
+                                          const float* cs, int rope_heads, const spec_rownorm* norm,
+                                          void* workspace, size_t workspace_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Chain of verify linears for a handful of rows (weight-streaming path)     */
 /* ------------------------------------------------------------------------ */
 /* One product of a chain: Y = X W^T (+ residual), or with swiglu = 1 the
@@ -422,6 +466,15 @@ SPEC_API int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const s
                                        const float* U, const int32_t* cu_rows, int B, float tie_eps,
                                        int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
                                        void* workspace, size_t workspace_bytes, spec_stream stream);
+/* The same with the final RMSNorm folded in: H is the residual stream x itself
+ * (W_lm carrying the norm weight) and norm->in_ssq its rows' partial sums of
+ * squares (see spec_rownorm; out_ssq unused).  Same workspace query. */
+SPEC_API int spec_lmhead_reject_sample_norm(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V,
+                                            float temperature, const float* Q, const int32_t* draft_tok,
+                                            const float* U, const int32_t* cu_rows, int B, float tie_eps,
+                                            int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                                            const spec_rownorm* norm, void* workspace, size_t workspace_bytes,
+                                            spec_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Layer glue of the decoder stack (not on the pages: the stack's layout is  */

@@ -32,6 +32,13 @@ _SIGS = {
     "spec_verify_linear": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp]),
     "spec_verify_linear_rope": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _sz, _vp]),
+    "spec_row_ssq": (_i, [_vp, _i, _i, _i, _vp, _vp]),
+    "spec_linear_norm_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "spec_verify_linear_norm": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp]),
+    "spec_verify_linear_swiglu_norm": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _vp, _sz, _vp]),
+    "spec_verify_linear_rope_norm": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp]),
+    "spec_lmhead_reject_sample_norm": (_i, [_vp, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _vp,
+                                            _vp, _vp, _sz, _vp]),
     "spec_linear_chain_workspace_bytes": (_sz, [_vp, _i, _i]),
     "spec_verify_linear_chain": (_i, [_vp, _i, _i, _vp, _sz, _vp]),
     "spec_rope_table": (_i, [_vp, _vp, _i, _i, _i, _f, _vp, _vp]),
@@ -198,8 +205,44 @@ def spec_linear_workspace_bytes(M: int, N: int, K: int) -> int:
     return _lib.spec_linear_workspace_bytes(M, N, K)
 
 
-def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None, stream=None):
-    """Y[M, N] = X[M, K] @ W[N, K]^T (+ residual), bf16 in/out, fp32 accumulate."""
+class RowNorm(ctypes.Structure):
+    """A folded RMSNorm (the C struct spec_rownorm): in_ssq [M, in_tiles] fp32 partial sums of
+    squares of X's rows (X's rows are scaled by 1 / sqrt(sum / K + eps)), out_ssq [M, ceil(N/128)]
+    fp32 filled with the sums of squares of the output as stored."""
+    _fields_ = [("in_ssq", _vp), ("in_tiles", _i), ("eps", _f), ("out_ssq", _vp)]
+
+
+def row_norm(in_ssq=None, eps: float = 1e-6, out_ssq=None) -> "RowNorm":
+    for t, name in ((in_ssq, "in_ssq"), (out_ssq, "out_ssq")):
+        if t is not None:
+            _need(t, torch.float32, name)
+            if not t.is_contiguous() or t.dim() != 2:
+                raise ValueError(f"{name} must be a contiguous [M, tiles] tensor")
+    nm = RowNorm(in_ssq.data_ptr() if in_ssq is not None else None,
+                 in_ssq.shape[1] if in_ssq is not None else 0, float(eps),
+                 out_ssq.data_ptr() if out_ssq is not None else None)
+    nm.tensors = (in_ssq, out_ssq)
+    return nm
+
+
+def spec_row_ssq(X, out=None, stream=None):
+    """out[M, ceil(N/128)] = per row and 128-column tile, the sum of squares of X's bf16 values."""
+    _need(X, torch.bfloat16, "X")
+    M, N = X.shape
+    if out is None:
+        out = torch.empty((M, (N + 127) // 128), dtype=torch.float32, device=X.device)
+    _need(out, torch.float32, "out")
+    _check(_lib.spec_row_ssq(_p(X), M, N, _rowmajor(X, "X"), _p(out), _stream(stream)), True)
+    return out
+
+
+def spec_linear_norm_workspace_bytes(M, N, K, swiglu: bool = False) -> int:
+    return _lib.spec_linear_norm_workspace_bytes(M, N, K, 1 if swiglu else 0)
+
+
+def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None, stream=None, norm=None):
+    """Y[M, N] = X[M, K] @ W[N, K]^T (+ residual), bf16 in/out, fp32 accumulate (norm: a folded
+    RMSNorm, see row_norm)."""
     _need(X, torch.bfloat16, "X"); _need(W, torch.bfloat16, "W")
     M, K = X.shape
     N = W.shape[0]
@@ -210,6 +253,13 @@ def spec_verify_linear(X, W, Y=None, residual=None, ws: Workspace | None = None,
     _need(Y, torch.bfloat16, "Y")
     if residual is not None:
         _need(residual, torch.bfloat16, "residual")
+    if norm is not None:
+        wp, wn = _ws_args(ws, spec_linear_norm_workspace_bytes(M, N, K), X.device)
+        _check(_lib.spec_verify_linear_norm(
+            _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
+            _p(residual), _rowmajor(residual, "residual") if residual is not None else 0,
+            ctypes.byref(norm), wp, wn, _stream(stream)), True)
+        return Y
     wp, wn = _ws_args(ws, spec_linear_workspace_bytes(M, N, K), X.device)
     _check(_lib.spec_verify_linear(
         _p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y), _rowmajor(Y, "Y"),
@@ -290,7 +340,8 @@ def spec_rope_table(cu_rows, ctx_len, M: int, D: int, theta: float = 1e6, cs=Non
     return cs
 
 
-def spec_verify_linear_rope(X, W, cs, rope_heads: int, Y=None, ws: Workspace | None = None, stream=None):
+def spec_verify_linear_rope(X, W, cs, rope_heads: int, Y=None, ws: Workspace | None = None, stream=None,
+                            norm=None):
     """Y = X W^T with the first rope_heads 128-column heads rotated by the table cs [M, 64, 2]."""
     _need(X, torch.bfloat16, "X"); _need(W, torch.bfloat16, "W"); _need(cs, torch.float32, "cs")
     M, K = X.shape
@@ -302,6 +353,12 @@ def spec_verify_linear_rope(X, W, cs, rope_heads: int, Y=None, ws: Workspace | N
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _need(Y, torch.bfloat16, "Y")
+    if norm is not None:
+        wp, wn = _ws_args(ws, spec_linear_norm_workspace_bytes(M, N, K), X.device)
+        _check(_lib.spec_verify_linear_rope_norm(_p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y),
+                                                 _rowmajor(Y, "Y"), _p(cs), int(rope_heads), ctypes.byref(norm), wp,
+                                                 wn, _stream(stream)), True)
+        return Y
     wp, wn = _ws_args(ws, spec_linear_workspace_bytes(M, N, K), X.device)
     _check(_lib.spec_verify_linear_rope(_p(X), M, K, _rowmajor(X, "X"), _p(W), N, _rowmajor(W, "W"), _p(Y),
                                         _rowmajor(Y, "Y"), _p(cs), int(rope_heads), wp, wn, _stream(stream)), True)
@@ -327,7 +384,7 @@ def interleave_gate_up(Wg, Wu):
     return torch.stack((Wg.reshape(I // b, b, K), Wu.reshape(I // b, b, K)), dim=1).reshape(2 * I, K).contiguous()
 
 
-def spec_verify_linear_swiglu(X, Wgu, A=None, ws: Workspace | None = None, stream=None):
+def spec_verify_linear_swiglu(X, Wgu, A=None, ws: Workspace | None = None, stream=None, norm=None):
     """A[M, I] = silu(X Wg^T) * (X Wu^T), Wgu = interleave_gate_up(Wg, Wu) of shape [2I, K]."""
     _need(X, torch.bfloat16, "X"); _need(Wgu, torch.bfloat16, "Wgu")
     M, K = X.shape
@@ -338,6 +395,12 @@ def spec_verify_linear_swiglu(X, Wgu, A=None, ws: Workspace | None = None, strea
     if A is None:
         A = torch.empty((M, inter), dtype=torch.bfloat16, device=X.device)
     _need(A, torch.bfloat16, "A")
+    if norm is not None:
+        wp, wn = _ws_args(ws, spec_linear_norm_workspace_bytes(M, inter, K, swiglu=True), X.device)
+        _check(_lib.spec_verify_linear_swiglu_norm(
+            _p(X), M, K, _rowmajor(X, "X"), _p(Wgu), _rowmajor(Wgu, "Wgu"), inter,
+            _p(A), _rowmajor(A, "A"), ctypes.byref(norm), wp, wn, _stream(stream)), True)
+        return A
     wp, wn = _ws_args(ws, spec_swiglu_linear_workspace_bytes(M, inter, K), X.device)
     _check(_lib.spec_verify_linear_swiglu(
         _p(X), M, K, _rowmajor(X, "X"), _p(Wgu), _rowmajor(Wgu, "Wgu"), inter,
@@ -528,7 +591,7 @@ def spec_lmhead_sample_workspace_bytes(M, K, V, temperature) -> int:
 
 
 def spec_lmhead_reject_sample(H, W_lm, temperature: float, Q, draft_tok, U, cu_rows, tie_eps: float = 1e-5,
-                              out=None, ws: Workspace | None = None, stream=None):
+                              out=None, ws: Workspace | None = None, stream=None, norm=None):
     """Fused LM head -> sampler; returns (n_acc [B], out_tok [M], near_tie [B]) int32 device tensors."""
     _need(H, torch.bfloat16, "H"); _need(W_lm, torch.bfloat16, "W_lm")
     _need(Q, torch.float32, "Q"); _need(U, torch.float32, "U")
@@ -547,6 +610,12 @@ def spec_lmhead_reject_sample(H, W_lm, temperature: float, Q, draft_tok, U, cu_r
                torch.empty(B, dtype=torch.int32, device=dev))
     n_acc, out_tok, near = out
     wp, wn = _ws_args(ws, spec_lmhead_sample_workspace_bytes(M, K, V, temperature), H.device)
+    if norm is not None:
+        _check(_lib.spec_lmhead_reject_sample_norm(_p(H), M, K, _p(W_lm), V, float(temperature), _p(Q),
+                                                   _p(draft_tok), _p(U), _p(cu_rows), B, float(tie_eps), _p(n_acc),
+                                                   _p(out_tok), _p(near), ctypes.byref(norm), wp, wn,
+                                                   _stream(stream)), True)
+        return n_acc, out_tok, near
     _check(_lib.spec_lmhead_reject_sample(_p(H), M, K, _p(W_lm), V, float(temperature), _p(Q), _p(draft_tok),
                                           _p(U), _p(cu_rows), B, float(tie_eps), _p(n_acc), _p(out_tok),
                                           _p(near), wp, wn, _stream(stream)), True)

@@ -553,19 +553,118 @@ static int launch_pair_plan(const LinPlan& p, const CUtensorMap& tw, const CUten
 
 extern "C" {
 
-int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
-                       int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
-                       void* workspace, size_t workspace_bytes, spec_stream stream) {
+}  // extern "C"
+
+static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                              int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
+                              const spec_rownorm* norm, char* ws, DevInfo* d, cudaStream_t s);
+static int swiglu_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
+                       int I, spec_bf16* A, int lda, const spec_rownorm* norm, char* ws, DevInfo* d, cudaStream_t s);
+
+// A folded RMSNorm on a plan: the split-K epilogues (cluster and pair kernels) scale rows and sum
+// squares themselves; other plans take the normalised copy of X / a sum-of-squares pass over Y.
+static bool plan_fuses_norm(const LinPlan& p) { return !p.gemv && (p.cluster_S > 0 || p.pair_n > 0); }
+static bool norm_in(const spec_rownorm* nm) { return nm && nm->in_ssq; }
+static bool norm_out(const spec_rownorm* nm) { return nm && nm->out_ssq; }
+static int check_norm(const spec_rownorm* nm) {
+  if (!nm) return SPEC_OK;
+  if (nm->in_ssq && (nm->in_tiles <= 0 || !(nm->eps >= 0.f) || std::isinf(nm->eps)))
+    return fail(SPEC_EINVAL, "norm: in_tiles must be >= 1 and eps finite and >= 0");
+  return SPEC_OK;
+}
+// Offset of the normalised copy of X in the workspace: after the plan's own scratch, never inside
+// the counter region.
+static size_t norm_copy_off(size_t plan_bytes) { return std::max(round_up(plan_bytes, 256), kCounterBytes); }
+// (out_ssq only with the plain bf16 epilogue, the one that sums the squares of what it stores)
+static void set_norm_args(LinearArgs& a, const spec_rownorm* nm, int K, bool fused) {
+  if (!fused || !nm) return;
+  if (nm->in_ssq) {
+    a.norm_ssq = nm->in_ssq;
+    a.norm_tiles = nm->in_tiles;
+    a.norm_k = (float)K;
+    a.norm_eps = nm->eps;
+  }
+  if (a.epi == EPI_BF16) a.out_ssq = nm->out_ssq;
+}
+
+static int verify_linear_impl(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                              spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr, const spec_rownorm* norm,
+                              void* workspace, size_t workspace_bytes, spec_stream stream) {
   if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
   if (M == 0) return ok();
   if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr)) return rc;
+  if (int rc = check_norm(norm)) return rc;
   LinPlan p = plan_linear(M, N, K, false);
-  if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes))
-    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", p.bytes);
+  const bool fused = plan_fuses_norm(p);
+  const bool copy_x = norm_in(norm) && !fused;
+  const size_t need = copy_x ? norm_copy_off(p.bytes) + round_up(size_t(M) * K * 2, 256) : p.bytes;
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
   DevInfo* d = nullptr;
   if (int rc = dev_info(&d)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  int extra = 0;
+  if (copy_x) {
+    // the RMSNorm of X from its sums of squares, into the workspace; the product reads that copy
+    spec_bf16* Xn = reinterpret_cast<spec_bf16*>(ws + norm_copy_off(p.bytes));
+    cudaError_t e = launch_rownorm_ssq(X, M, K, ldx, norm->in_ssq, norm->in_tiles, norm->eps, Xn, K, s);
+    if (e != cudaSuccess) return cuda_fail(e, "row normalisation launch");
+    X = Xn;
+    ldx = K;
+    extra = 1;
+  }
+  const int rc = verify_linear_plan(p, X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr,
+                                    fused ? norm : nullptr, ws, d, s);
+  if (rc) return rc;
+  int n = t_launches + extra;
+  if (norm_out(norm) && !fused) {
+    cudaError_t e = launch_row_ssq(Y, M, N, ldy, norm->out_ssq, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
+    ++n;
+  }
+  return ok(n);
+}
+
+extern "C" {
+
+int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                       int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
+                       void* workspace, size_t workspace_bytes, spec_stream stream) {
+  return verify_linear_impl(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, nullptr, workspace, workspace_bytes,
+                            stream);
+}
+
+int spec_verify_linear_norm(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                            spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr, const spec_rownorm* norm,
+                            void* workspace, size_t workspace_bytes, spec_stream stream) {
+  return verify_linear_impl(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, norm, workspace, workspace_bytes,
+                            stream);
+}
+
+size_t spec_linear_norm_workspace_bytes(int M, int N, int K, int swiglu) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const LinPlan p = plan_linear(M, swiglu ? 2 * N : N, K, false, swiglu != 0);
+  const size_t own = swiglu ? spec_swiglu_linear_workspace_bytes(M, N, K) : p.bytes;
+  return plan_fuses_norm(p) ? own : norm_copy_off(own) + round_up(size_t(M) * K * 2, 256);
+}
+
+int spec_row_ssq(const spec_bf16* X, int M, int N, int ldx, float* out, spec_stream stream) {
+  if (M < 0 || N <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d", M, N);
+  if (M == 0) return ok();
+  if (!X || !out) return fail(SPEC_EINVAL, "NULL argument");
+  if (ldx < N) return fail(SPEC_EINVAL, "ldx=%d < N=%d", ldx, N);
+  cudaError_t e = launch_row_ssq(X, M, N, ldx, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
+  return ok(1);
+}
+
+}  // extern "C"
+
+// The launches of one linear plan (arguments already checked; the workspace holds p.bytes).
+static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
+                              int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
+                              const spec_rownorm* norm, char* ws, DevInfo* d, cudaStream_t s) {
   if (p.gemv) {
     GemvArgs a;
     a.X = X; a.ldx = ldx; a.W = W; a.ldw = ldw; a.Y = Y; a.ldy = ldy;
@@ -598,6 +697,7 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_BF16;
+  set_norm_args(a, norm, K, plan_fuses_norm(p));
   if (p.pair_n > 0) {
     cudaError_t e = cudaSuccess;
     const int n = launch_pair_plan(p, tw, tx, a, s, &e);
@@ -623,8 +723,6 @@ int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx, const spec_bf1
   if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
   return ok(2);
 }
-
-}  // extern "C"
 
 // --------------------------------------------------------------------------- linear chain (small M)
 namespace {
@@ -892,9 +990,11 @@ int spec_rope_table(const int32_t* cu_rows, const int32_t* ctx_len, int B, int M
   return ok(1);
 }
 
-int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
-                            spec_bf16* Y, int ldy, const float* cs, int rope_heads, void* workspace,
-                            size_t workspace_bytes, spec_stream stream) {
+}  // extern "C"
+
+static int verify_linear_rope_impl(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                                   spec_bf16* Y, int ldy, const float* cs, int rope_heads, const spec_rownorm* norm,
+                                   void* workspace, size_t workspace_bytes, spec_stream stream) {
   constexpr int HD = 128;   // head size: one weight tile of the GEMM is one head
   if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
   if (M == 0) return ok();
@@ -902,14 +1002,12 @@ int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spe
     return fail(SPEC_EINVAL, "rope_heads=%d heads of 128 do not fit in N=%d", rope_heads, N);
   if (rope_heads > 0 && !cs) return fail(SPEC_EINVAL, "cs must be non-NULL");
   if (rope_heads > 0 && !aligned16(cs)) return fail(SPEC_EINVAL, "cs must be 16-byte aligned");
+  if (int rc = check_norm(norm)) return rc;
   const LinPlan p = plan_linear(M, N, K, false);
   if (rope_heads > 0 && (p.cluster_S > 0 || p.pair_n > 0) && !p.gemv) {
     // few weight tiles: the cluster (or pair) split-K kernel rotates the q / k heads in its epilogue
-    if (!X || !W || !Y) return fail(SPEC_EINVAL, "X, W and Y must be non-NULL");
-    if (K % 8) return fail(SPEC_EINVAL, "K=%d must be a multiple of 8", K);
-    if (ldx < K || ldw < K || ldy < N || ldx % 8 || ldw % 8 || ldy % 8)
-      return fail(SPEC_EINVAL, "bad leading dimensions");
-    if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return fail(SPEC_EINVAL, "X, W, Y must be 16-byte aligned");
+    // (and applies a folded RMSNorm's row scales before the rotation)
+    if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, nullptr, 0)) return rc;
     DevInfo* d = nullptr;
     if (int rc = dev_info(&d)) return rc;
     CUtensorMap tw, tx;
@@ -934,26 +1032,55 @@ int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spe
     a.epi = EPI_ROPE;
     a.rope_cs = reinterpret_cast<const float2*>(cs);
     a.rope_tiles = rope_heads;
+    set_norm_args(a, norm, K, true);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int n = 1;
     if (p.pair_n > 0) {
       cudaError_t e = cudaSuccess;
-      const int n = launch_pair_plan(p, tw, tx, a, static_cast<cudaStream_t>(stream), &e);
+      n = launch_pair_plan(p, tw, tx, a, st, &e);
       if (!n) return cuda_fail(e, "pair linear + rope launch");
-      return ok(n);
+    } else {
+      cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S, st);
+      if (e != cudaSuccess) return cuda_fail(e, "cluster linear + rope launch");
     }
-    cudaError_t e = launch_linear_cluster(p.BN, p.NSUB, tw, tx, a, p.cluster_S, p.grid / p.cluster_S,
-                                          static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cluster linear + rope launch");
-    return ok(1);
+    if (norm_out(norm)) {   // (the rope epilogue does not sum squares)
+      cudaError_t e = launch_row_ssq(Y, M, N, ldy, norm->out_ssq, st);
+      if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
+      ++n;
+    }
+    return ok(n);
   }
   // otherwise the plain product, then the rotation from the table
-  if (int rc = spec_verify_linear(X, M, K, ldx, W, N, ldw, Y, ldy, nullptr, 0, workspace, workspace_bytes, stream))
+  if (int rc = verify_linear_impl(X, M, K, ldx, W, N, ldw, Y, ldy, nullptr, 0, norm, workspace, workspace_bytes,
+                                  stream))
     return rc;
   const int n_lin = t_launches;
   if (rope_heads == 0) return ok(n_lin);
   cudaError_t e = launch_rope_apply(Y, ldy, rope_heads, HD, reinterpret_cast<const float2*>(cs), M,
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rope_apply launch");
+  if (norm_out(norm)) {   // the rotation changed Y after its sums of squares: take them again
+    e = launch_row_ssq(Y, M, N, ldy, norm->out_ssq, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
+    return ok(n_lin + 2);
+  }
   return ok(n_lin + 1);
+}
+
+extern "C" {
+
+int spec_verify_linear_rope(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                            spec_bf16* Y, int ldy, const float* cs, int rope_heads, void* workspace,
+                            size_t workspace_bytes, spec_stream stream) {
+  return verify_linear_rope_impl(X, M, K, ldx, W, N, ldw, Y, ldy, cs, rope_heads, nullptr, workspace,
+                                 workspace_bytes, stream);
+}
+
+int spec_verify_linear_rope_norm(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
+                                 spec_bf16* Y, int ldy, const float* cs, int rope_heads, const spec_rownorm* norm,
+                                 void* workspace, size_t workspace_bytes, spec_stream stream) {
+  return verify_linear_rope_impl(X, M, K, ldx, W, N, ldw, Y, ldy, cs, rope_heads, norm, workspace,
+                                 workspace_bytes, stream);
 }
 
 // --------------------------------------------------------------------------- fused SwiGLU linear
@@ -970,9 +1097,11 @@ size_t spec_swiglu_linear_workspace_bytes(int M, int I, int K) {
   return p.gemv ? swiglu_gemv_scratch_off(p) + round_up(size_t(M) * 2 * I * 2, 256) : p.bytes;
 }
 
-int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
-                              int I, spec_bf16* A, int lda, void* workspace, size_t workspace_bytes,
-                              spec_stream stream) {
+}  // extern "C"
+
+static int verify_linear_swiglu_impl(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw, int I,
+                                     spec_bf16* A, int lda, const spec_rownorm* norm, void* workspace,
+                                     size_t workspace_bytes, spec_stream stream) {
   if (M < 0 || I <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d I=%d K=%d", M, I, K);
   if (M == 0) return ok();
   if (!X || !Wgu || !A) return fail(SPEC_EINVAL, "X, Wgu and A must be non-NULL");
@@ -981,15 +1110,42 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   if (ldx < K || ldw < K || lda < I) return fail(SPEC_EINVAL, "leading dimensions too small");
   if (ldx % 8 || ldw % 8 || lda % 8) return fail(SPEC_EINVAL, "leading dimensions must be multiples of 8");
   if (!aligned16(X) || !aligned16(Wgu) || !aligned16(A)) return fail(SPEC_EINVAL, "X, Wgu, A must be 16-byte aligned");
+  if (int rc = check_norm(norm)) return rc;
   const int N = 2 * I;
   LinPlan p = plan_linear(M, N, K, false, true);
-  const size_t need = spec_swiglu_linear_workspace_bytes(M, I, K);
+  const bool fused = plan_fuses_norm(p);
+  const bool copy_x = norm_in(norm) && !fused;
+  const size_t own = spec_swiglu_linear_workspace_bytes(M, I, K);
+  const size_t need = copy_x ? norm_copy_off(own) + round_up(size_t(M) * K * 2, 256) : own;
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
   DevInfo* d = nullptr;
   if (int rc = dev_info(&d)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  int extra = 0;
+  if (copy_x) {
+    spec_bf16* Xn = reinterpret_cast<spec_bf16*>(ws + norm_copy_off(own));
+    cudaError_t e = launch_rownorm_ssq(X, M, K, ldx, norm->in_ssq, norm->in_tiles, norm->eps, Xn, K, s);
+    if (e != cudaSuccess) return cuda_fail(e, "row normalisation launch");
+    X = Xn;
+    ldx = K;
+    extra = 1;
+  }
+  const int rc = swiglu_plan(p, X, M, K, ldx, Wgu, ldw, I, A, lda, fused ? norm : nullptr, ws, d, s);
+  if (rc) return rc;
+  int n = t_launches + extra;
+  if (norm_out(norm)) {
+    cudaError_t e = launch_row_ssq(A, M, I, lda, norm->out_ssq, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
+    ++n;
+  }
+  return ok(n);
+}
+
+static int swiglu_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
+                       int I, spec_bf16* A, int lda, const spec_rownorm* norm, char* ws, DevInfo* d, cudaStream_t s) {
+  const int N = 2 * I;
   if (p.gemv) {
     spec_bf16* gu = reinterpret_cast<spec_bf16*>(ws + swiglu_gemv_scratch_off(p));
     GemvArgs g;
@@ -1025,6 +1181,7 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
+  set_norm_args(a, norm, K, plan_fuses_norm(p));
   if (p.pair_n > 0) {
     cudaError_t e = cudaSuccess;
     const int n = launch_pair_plan(p, tw, tx, a, s, &e);
@@ -1049,6 +1206,20 @@ int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const s
   return ok(2);
 }
 
+extern "C" {
+
+int spec_verify_linear_swiglu(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
+                              int I, spec_bf16* A, int lda, void* workspace, size_t workspace_bytes,
+                              spec_stream stream) {
+  return verify_linear_swiglu_impl(X, M, K, ldx, Wgu, ldw, I, A, lda, nullptr, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_linear_swiglu_norm(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw, int I,
+                                   spec_bf16* A, int lda, const spec_rownorm* norm, void* workspace,
+                                   size_t workspace_bytes, spec_stream stream) {
+  return verify_linear_swiglu_impl(X, M, K, ldx, Wgu, ldw, I, A, lda, norm, workspace, workspace_bytes, stream);
+}
+
 // --------------------------------------------------------------------------- LM head
 size_t spec_lmhead_workspace_bytes(int M, int K, int V) {
   if (M <= 0 || K <= 0 || V <= 0) return 0;
@@ -1059,7 +1230,7 @@ size_t spec_lmhead_workspace_bytes(int M, int K, int V) {
 // sum of exp; or max, argmax when T = 0) into the workspace after its counter region.
 static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
                               float* Z, long long ldz, void* workspace, const LinPlan& p, DevInfo* d, cudaStream_t s,
-                              float2** stats_out) {
+                              float2** stats_out, const spec_rownorm* norm = nullptr) {
   CUtensorMap tw, tx;
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)V};
@@ -1082,6 +1253,13 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
   a.P = Z;
   a.ldp = ldz;
   a.stats = reinterpret_cast<float2*>(static_cast<char*>(workspace) + p.partial_off);
+  // a folded final RMSNorm scales each row's logits (the argmax of a row does not change)
+  if (norm_in(norm)) {
+    a.norm_ssq = norm->in_ssq;
+    a.norm_tiles = norm->in_tiles;
+    a.norm_k = (float)K;
+    a.norm_eps = norm->eps;
+  }
   cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   *stats_out = a.stats;
@@ -1136,10 +1314,12 @@ size_t spec_lmhead_sample_workspace_bytes(int M, int K, int V, float temperature
   return temperature == 0.f ? p.bytes : fused_logits_off(p) + round_up(size_t(M) * V * 4, 256);
 }
 
-int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+}  // extern "C"
+
+static int lmhead_reject_sample_impl(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
                               const float* Q, const int32_t* draft_tok, const float* U, const int32_t* cu_rows,
                               int B, float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
-                              void* workspace, size_t workspace_bytes, spec_stream stream) {
+                              const spec_rownorm* norm, void* workspace, size_t workspace_bytes, spec_stream stream) {
   if (M < 0 || K <= 0 || V <= 0 || B < 0) return fail(SPEC_EINVAL, "bad sizes M=%d K=%d V=%d B=%d", M, K, V, B);
   if (B == 0) return ok();
   if (M < B) return fail(SPEC_EINVAL, "M=%d verify rows cannot hold B=%d sequences", M, B);
@@ -1148,6 +1328,7 @@ int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16*
     return fail(SPEC_EINVAL, "NULL argument");
   if (!(tie_eps >= 0.f)) return fail(SPEC_EINVAL, "tie_eps must be >= 0");
   if (V > (1 << 20)) return fail(SPEC_EUNSUPPORTED, "V=%d > 1048576", V);
+  if (int rc = check_norm(norm)) return rc;
   const LinPlan p = plan_linear(M, V, K, true);
   const size_t need = spec_lmhead_sample_workspace_bytes(M, K, V, temperature);
   if (!workspace || workspace_bytes < need) return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
@@ -1157,11 +1338,30 @@ int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16*
   const bool greedy = temperature == 0.f;
   float* Z = greedy ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + fused_logits_off(p));
   float2* stats = nullptr;
-  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, Z, V, workspace, p, d, s, &stats)) return rc;
+  if (int rc = launch_lmhead_gemm(H, M, K, Wlm, V, temperature, Z, V, workspace, p, d, s, &stats, norm)) return rc;
   cudaError_t e = launch_reject_sample_logits(Z, stats, p.tiles_n, greedy, Q, draft_tok, U, cu_rows, B, M, V,
                                               tie_eps, n_acc, out_tok, near_tie, d->status, s);
   if (e != cudaSuccess) return cuda_fail(e, "fused sampler launch");
   return ok(2);
+}
+
+extern "C" {
+
+int spec_lmhead_reject_sample(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+                              const float* Q, const int32_t* draft_tok, const float* U, const int32_t* cu_rows,
+                              int B, float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                              void* workspace, size_t workspace_bytes, spec_stream stream) {
+  return lmhead_reject_sample_impl(H, M, K, Wlm, V, temperature, Q, draft_tok, U, cu_rows, B, tie_eps, n_acc, out_tok,
+                                   near_tie, nullptr, workspace, workspace_bytes, stream);
+}
+
+int spec_lmhead_reject_sample_norm(const spec_bf16* H, int M, int K, const spec_bf16* Wlm, int V, float temperature,
+                                   const float* Q, const int32_t* draft_tok, const float* U, const int32_t* cu_rows,
+                                   int B, float tie_eps, int32_t* n_acc, int32_t* out_tok, int32_t* near_tie,
+                                   const spec_rownorm* norm, void* workspace, size_t workspace_bytes,
+                                   spec_stream stream) {
+  return lmhead_reject_sample_impl(H, M, K, Wlm, V, temperature, Q, draft_tok, U, cu_rows, B, tie_eps, n_acc, out_tok,
+                                   near_tie, norm, workspace, workspace_bytes, stream);
 }
 
 // --------------------------------------------------------------------------- attention

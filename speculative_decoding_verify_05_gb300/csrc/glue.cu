@@ -288,7 +288,66 @@ __global__ void wait_probe_kernel(unsigned* status, unsigned site, unsigned long
   __syncthreads();
 }
 
+// Sums of squares of the bf16 values of X, per row and 128-column tile: one warp per (row, tile),
+// 4 columns per lane, a fixed butterfly across the warp.
+__global__ void __launch_bounds__(256) row_ssq_kernel(const uint16_t* __restrict__ X, int M, int N, int ldx,
+                                                       float* __restrict__ out, int tiles) {
+  pdl_wait();
+  pdl_trigger();
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)M * tiles) return;
+  const int m = (int)(w / tiles), t = (int)(w - (long long)m * tiles);
+  float s = 0.f;
+  const int c0 = t * 128 + lane * 4;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (c0 + e < N) {
+      const float v = bf16f(X[(size_t)m * ldx + c0 + e]);
+      s += v * v;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) out[(size_t)m * tiles + t] = s;
+}
+
+// Y = X row-scaled by 1 / sqrt(sum_t ssq[m][t] / K + eps) (t in order), rounded to bf16: the
+// RMSNorm of a row whose partial sums of squares were written by the product that stored it.
+__global__ void __launch_bounds__(256) rownorm_ssq_kernel(const uint16_t* __restrict__ X, int K, int ldx,
+                                                           const float* __restrict__ ssq, int tiles, float eps,
+                                                           uint16_t* __restrict__ Y, int ldy) {
+  pdl_wait();
+  pdl_trigger();
+  const int m = blockIdx.x;
+  __shared__ float s_r;
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int t = 0; t < tiles; ++t) s += ssq[(size_t)m * tiles + t];
+    s_r = 1.0f / sqrtf(s / (float)K + eps);
+  }
+  __syncthreads();
+  const float r = s_r;
+  for (int c = threadIdx.x; c < K; c += blockDim.x)
+    Y[(size_t)m * ldy + c] = f2bf(bf16f(X[(size_t)m * ldx + c]) * r);
+}
+
 }  // namespace
+
+cudaError_t launch_row_ssq(const uint16_t* X, int M, int N, int ldx, float* out, cudaStream_t s) {
+  const int tiles = (N + 127) / 128;
+  const long long warps = (long long)M * tiles;
+  const long long blocks = (warps + 7) / 8;
+  cudaError_t e = launch_k(row_ssq_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), 0, s, X, M, N, ldx,
+                           out, tiles);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_rownorm_ssq(const uint16_t* X, int M, int K, int ldx, const float* ssq, int tiles, float eps,
+                               uint16_t* Y, int ldy, cudaStream_t s) {
+  cudaError_t e = launch_k(rownorm_ssq_kernel, dim3(M), dim3(256), 0, s, X, K, ldx, ssq, tiles, eps, Y, ldy);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_wait_probe(unsigned* status, unsigned site, unsigned long long limit_ns, int arrive,
                               cudaStream_t s) {

@@ -205,6 +205,12 @@ cudaError_t launch_ngram_propose(const int32_t* tokens, const int32_t* cu_len, i
 cudaError_t launch_wait_probe(unsigned* status, unsigned site, unsigned long long limit_ns, int arrive,
                               cudaStream_t s);
 
+// ---- folded RMSNorm: per-row, per-128-column-tile sums of squares of a bf16 matrix; and the
+//      row normalisation from such sums (the fallback for plans whose epilogue cannot scale rows)
+cudaError_t launch_row_ssq(const uint16_t* X, int M, int N, int ldx, float* out, cudaStream_t s);
+cudaError_t launch_rownorm_ssq(const uint16_t* X, int M, int K, int ldx, const float* ssq, int tiles, float eps,
+                               uint16_t* Y, int ldy, cudaStream_t s);
+
 // ---- glue
 cudaError_t launch_rmsnorm(const uint16_t* X, int M, int N, int ldx, const uint16_t* w, float eps,
                            uint16_t* Y, int ldy, cudaStream_t s);

@@ -108,6 +108,11 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
       umma_commit(acc_full);
     }
     __syncwarp();
+  } else if (args.norm_ssq) {
+    // warps 2-7 are idle during the main loop: the row scales of a folded RMSNorm (made visible to
+    // the whole CTA by the cluster barriers below)
+    fill_row_scales(args, reinterpret_cast<float*>(smem + Cfg::RMS_OFF), split_first_row<TN>(cpr, (int)rank, m_t),
+                    split_rows<TN>(cpr, (int)rank), threadIdx.x - 64, CL_THREADS - 64);
   }
   // every CTA of the cluster is past its main loop: the rings are free
   const bool ok = mbar_wait(acc_full, 0u, args.status, 0x143u);
@@ -118,7 +123,8 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   // every piece has landed in its owner's slots
   cluster_sync_all();
 
-  split_sum_epilogue<TN, CL_THREADS>(slots, args, S, cpr, (int)rank, n_t, m_t);
+  split_sum_epilogue<TN, CL_THREADS>(slots, args, S, cpr, (int)rank, n_t, m_t,
+                                     reinterpret_cast<float*>(smem + Cfg::RMS_OFF));
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::ACC_COLS < 32 ? 32 : Cfg::ACC_COLS);

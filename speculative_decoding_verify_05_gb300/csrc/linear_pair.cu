@@ -33,7 +33,8 @@ struct PairCfg {
   static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
   static constexpr int TMEM_COLS = TN <= 32 ? 32 : TN <= 64 ? 64 : TN <= 128 ? 128 : TN <= 256 ? 256 : 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int RMS_OFF = STAGES * STAGE_BYTES + 1024;      // row scales of a folded RMSNorm
+  static constexpr int SMEM_BYTES = RMS_OFF + TN * 4 + 1024;
 };
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
@@ -160,6 +161,11 @@ linear_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
       umma_commit_pair(dsmem_map(smem_u32(acc_full), peer));
     }
     __syncwarp();
+  } else if (warp >= 2 && args.norm_ssq) {
+    // warps 2-7 are idle during the main loop: the row scales of a folded RMSNorm (made visible to
+    // the whole CTA by the cluster barriers below)
+    fill_row_scales(args, reinterpret_cast<float*>(smem + Cfg::RMS_OFF), split_first_row<TN>(cpr, pr, m_t),
+                    split_rows<TN>(cpr, pr), threadIdx.x - 64, PR_THREADS - 64);
   }
   const bool ok = mbar_wait(acc_full, 0u, args.status, 0x173u);
   tc_fence_after();
@@ -173,7 +179,8 @@ linear_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     tc_fence_after();
     tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
   }
-  if (n_t < args.tiles_n) split_sum_epilogue<TN, PR_THREADS>(slots, args, S, cpr, pr, n_t, m_t);
+  if (n_t < args.tiles_n)
+    split_sum_epilogue<TN, PR_THREADS>(slots, args, S, cpr, pr, n_t, m_t, reinterpret_cast<float*>(smem + Cfg::RMS_OFF));
 }
 
 template <int BN, int NSUB>

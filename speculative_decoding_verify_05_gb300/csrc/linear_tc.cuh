@@ -58,7 +58,41 @@ struct LinearArgs {
   float* P;             // EPI_LOGITS: [M x N] fp32, leading dimension ldp
   long long ldp;
   float2* stats;        // EPI_LOGITS / EPI_ARGMAX: [M][tiles_n] (max, sum) or (max, idx bits)
+  // RMSNorm of X folded into the product (its weight folded into W beforehand): row m of the result
+  // is scaled by 1 / sqrt(sum_t norm_ssq[m][t] / norm_k + norm_eps) (t in order), the partial sums
+  // of squares of X's row m written by the product that stored X (nullptr: no scaling)
+  const float* norm_ssq;
+  int norm_tiles;
+  float norm_k, norm_eps;
+  // the partial sums of squares of Y as stored (bf16), per row and 128-column tile: [M][tiles_n]
+  // (nullptr: none)
+  float* out_ssq;
 };
+
+// 1 / rms of row m from its partial sums of squares (t in order; the loads go out 8 at a time).
+__device__ __forceinline__ float row_inv_rms(const LinearArgs& a, int m) {
+  const float* p = a.norm_ssq + (size_t)m * a.norm_tiles;
+  float s = 0.f;
+  int t = 0;
+  for (; t + 8 <= a.norm_tiles; t += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(p + t + i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += v[i];
+  }
+  for (; t < a.norm_tiles; ++t) s += __ldg(p + t);
+  return 1.0f / sqrtf(s / a.norm_k + a.norm_eps);
+}
+// s_rms[j] = 1 / rms of row m_first + j for j < n (1 past M, or without a folded norm), by threads
+// tid .. of nthreads: run by warps that are idle during the main loop, so it overlaps the MMAs.
+__device__ __forceinline__ void fill_row_scales(const LinearArgs& a, float* s_rms, int m_first, int n, int tid,
+                                                int nthreads) {
+  for (int j = tid; j < n; j += nthreads) {
+    const int m = m_first + j;
+    s_rms[j] = (a.norm_ssq && m < a.M) ? row_inv_rms(a, m) : 1.f;
+  }
+}
 
 // k-step of the tensor-core GEMMs: LIN_BK bf16 per operand row and stage (one swizzle row of
 // LIN_ROW_BYTES): 64 with 128-byte swizzle, or 32 with 64-byte swizzle.  Half-size stages keep
@@ -93,8 +127,9 @@ struct LinearCfg {
   // 16-byte stores along the weight rows
   static constexpr int EPI_BUF_FLOATS = 16 * 33;
   // ring + barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) + epilogue
-  // transpose blocks + alignment slack
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4 + 1024;
+  // transpose blocks + row scales of a folded RMSNorm (TN floats) + alignment slack
+  static constexpr int RMS_OFF = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4;
+  static constexpr int SMEM_BYTES = RMS_OFF + TN * 4 + 1024;
 };
 
 }  // namespace spec

@@ -136,6 +136,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   float2* red = reinterpret_cast<float2*>(smem + STAGES * Cfg::STAGE_BYTES + 1024);  // [4][TN]
   float* ebuf_all = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + 1024 + 4 * TN * 8);
+  float* s_rms = reinterpret_cast<float*>(smem + Cfg::RMS_OFF);   // [TN]: folded-RMSNorm row scales
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -229,6 +230,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     const int c_end = min(TN, c_begin + per_half * 16);
     int seg = 0;
     bool ok = true;
+    int rms_m0 = -1;       // token tile whose folded-RMSNorm scales s_rms holds
     for (long long u = 0; u < work.n; ++seg) {
       const Seg g = seg_at(args, work, wg, u);
       const long long tile = g.tile;
@@ -239,6 +241,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       const int n_t = (int)(tile / args.tiles_m);
       const int n0 = n_t * 128;
       const int n = n0 + row;
+      if constexpr (EPI == EPI_LOGITS) {
+        // folded final RMSNorm: the scale of every token row of this tile, before waiting for its
+        // accumulator (so the first tile's overlaps the main loop); recomputed only when the token
+        // tile changes (the LM head has one token tile up to 384 rows)
+        if (args.norm_ssq && m0 != rms_m0) {
+          fill_row_scales(args, s_rms, m0, TN, etid, 32 * Cfg::EPI_WARPS);
+          bar_epi();
+          rms_m0 = m0;
+        }
+      }
       ok = ok && mbar_wait(&acc_full[acc], (uint32_t)((seg / NBUF) & 1), args.status, 0x104u);
       ok = bar_epi_and(ok);
       if (!ok) break;
@@ -335,6 +347,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         float* eb = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
         const int jc = lane >> 1, r0 = (lane & 1) * 16;
         const int nr = n0 + q * 32 + r0;        // vocabulary row of this lane's first scanned entry
+
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 16) {
           float v[16];
@@ -342,7 +355,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           if constexpr (EPI == EPI_LOGITS) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float z = v[j] * args.inv_temp;
+              const float z = v[j] * (args.norm_ssq ? args.inv_temp * s_rms[c + j] : args.inv_temp);
               const int m = m0 + c + j;
               if (m < args.M && n < args.N) args.P[(size_t)m * args.ldp + n] = z;
               eb[j * 33 + lane] = z;

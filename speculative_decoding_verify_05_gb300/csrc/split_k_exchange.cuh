@@ -81,15 +81,28 @@ __device__ __forceinline__ void push_accumulator(uint32_t tmem, int warp, int la
   }
 }
 
+// The token rows participant `me` stores: the first and how many (their row scales of a folded
+// RMSNorm go to s_rms before the epilogue, see fill_row_scales).
+template <int TN>
+__device__ __forceinline__ int split_first_row(int cpr, int me, int m_t) { return m_t * TN + me * cpr * 4; }
+template <int TN>
+__device__ __forceinline__ int split_rows(int cpr, int me) {
+  const int n = min(cpr, TN / 4 - me * cpr);
+  return n > 0 ? n * 4 : 0;
+}
+
 // Owner `me`'s chunks: sum the S slots in participant order and store them as weight tile n_t,
 // token tile m_t of Y with the epilogue args.epi (bf16 + residual, SwiGLU, or RoPE); NT threads.
+// With a folded RMSNorm, s_rms holds the scales of the owner's rows (filled and made visible to
+// every thread before the call).
 template <int TN, int NT>
 __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const LinearArgs& args, int S, int cpr,
-                                                   int me, int n_t, int m_t) {
+                                                   int me, int n_t, int m_t, const float* s_rms) {
   // ---------------- this rank's chunks: sum the S slots in rank order, add the residual, store.
   // Item = (chunk, 8 consecutive weight rows): 4 tokens x 8 rows, so the residual and Y move
   // in 16-byte pieces (8 bf16 of one token row).
   const int n_chunks = min(cpr, TN / 4 - me * cpr);
+  const bool scale = args.norm_ssq != nullptr;
   if (args.epi == EPI_SWIGLU) {
     // gate and up rows interleaved per 16: item = (chunk, 8 gate rows r8..r8+7 with r8 % 32 < 16);
     // the matching up rows are r8+16..; 8 outputs per token at column n_t 64 + (r8 / 32) 16 + r8 % 32
@@ -115,6 +128,14 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
       }
       const int n = n_t * 64 + (r8 >> 5) * 16 + (r8 & 31);
       const int mb = m_t * TN + (me * cpr + kk) * 4;
+      if (scale) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float rs = s_rms[kk * 4 + e];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) { g[i][e] *= rs; u[i][e] *= rs; }
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (mb + e >= args.M) break;
@@ -152,6 +173,14 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
       }
       const int n = n_t * 128 + r8;
       const int mb = m_t * TN + (me * cpr + kk) * 4;
+      if (scale) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float rs = s_rms[kk * 4 + e];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) { a[i][e] *= rs; b[i][e] *= rs; }
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = mb + e;
@@ -171,8 +200,12 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
     }
   }
   const int items = (args.epi == EPI_SWIGLU || rope || n_chunks <= 0) ? 0 : n_chunks * 16;
-  for (int it = threadIdx.x; it < items; it += NT) {
-    const int kk = it >> 4, r8 = (it & 15) * 8;
+  // (a chunk's 16 items sit in 16 consecutive lanes: the loop runs whole warps so that they can sum
+  // the squares of the chunk's stored values for out_ssq)
+  const int items_w = (items + 31) / 32 * 32;
+  for (int it = threadIdx.x; it < items_w; it += NT) {
+    const bool act = it < items;
+    const int kk = act ? it >> 4 : 0, r8 = (it & 15) * 8;
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -186,9 +219,18 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
         acc[i][0] += v.x; acc[i][1] += v.y; acc[i][2] += v.z; acc[i][3] += v.w;
       }
     }
+    if (scale) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float rs = s_rms[kk * 4 + e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i][e] *= rs;
+      }
+    }
     const int n0 = n_t * 128 + r8;
     const int mb = m_t * TN + (me * cpr + kk) * 4;
-    if (n0 + 8 <= args.N) {
+    float sq[4] = {0.f, 0.f, 0.f, 0.f};
+    if (act && n0 + 8 <= args.N) {
       uint4 res[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -201,17 +243,32 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
         const uint32_t r4[4] = {res[e].x, res[e].y, res[e].z, res[e].w};
         uint32_t o4[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+        for (int h = 0; h < 4; ++h) {
           o4[h] = pack_bf16x2(acc[2 * h][e] + bf16lo(r4[h]), acc[2 * h + 1][e] + bf16hi(r4[h]));
+          sq[e] += bf16lo(o4[h]) * bf16lo(o4[h]) + bf16hi(o4[h]) * bf16hi(o4[h]);
+        }
         *reinterpret_cast<uint4*>(args.Y + (size_t)(mb + e) * args.ldy + n0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-    } else {
+    } else if (act) {
       for (int e = 0; e < 4 && mb + e < args.M; ++e)
         for (int i = 0; i < 8 && n0 + i < args.N; ++i) {
           float o = acc[i][e];
           if (args.residual) o += bf16f(args.residual[(size_t)(mb + e) * args.ldr + n0 + i]);
-          args.Y[(size_t)(mb + e) * args.ldy + n0 + i] = f2bf(o);
+          const uint16_t ob = f2bf(o);
+          args.Y[(size_t)(mb + e) * args.ldy + n0 + i] = ob;
+          sq[e] += bf16f(ob) * bf16f(ob);
         }
+    }
+    if (args.out_ssq) {
+      // the chunk's 16 lanes (128 columns of the tile) in a fixed butterfly
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sq[e] += __shfl_xor_sync(0xffffffffu, sq[e], o);
+      if (act && (it & 15) == 0)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (mb + e < args.M) args.out_ssq[(size_t)(mb + e) * args.tiles_n + n_t] = sq[e];
     }
   }
 }

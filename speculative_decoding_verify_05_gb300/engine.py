@@ -63,6 +63,27 @@ class StackW:
     layers: list = field(default_factory=list)
     final_norm: torch.Tensor | None = None
     w_lm: torch.Tensor | None = None
+    norms_folded: bool = False   # RMSNorm weights multiplied into the products that consume them
+
+
+def fold_norm_weights(sw: StackW) -> None:
+    """Folds each RMSNorm weight into the product that reads the normed rows, once, in place:
+    W_qkv <- W_qkv diag(attn_norm), W_gu <- W_gu diag(mlp_norm), W_lm <- W_lm diag(final_norm)
+    (one bf16 rounding of W w; exact for unit weights), and sets the norm weights to 1, so a
+    product can take the raw rows and scale them by 1 / rms in its epilogue."""
+    if sw.norms_folded:
+        return
+    for lw in sw.layers:
+        lw.w_qkv.mul_(lw.attn_norm[None, :])
+        lw.w_gu.mul_(lw.mlp_norm[None, :])
+    if sw.w_lm is not None and sw.final_norm is not None:
+        sw.w_lm.mul_(sw.final_norm[None, :])
+    for lw in sw.layers:
+        lw.attn_norm.fill_(1.0)
+        lw.mlp_norm.fill_(1.0)
+    if sw.final_norm is not None:
+        sw.final_norm.fill_(1.0)
+    sw.norms_folded = True
 
 
 def random_stack(dims: Dims, seed: int, device, std: float = 0.02, with_head: bool = True) -> StackW:
@@ -108,7 +129,8 @@ class VerifyEngine:
     """Buffers + call sequence of one verify pass / round for up to ``max_M`` rows."""
 
     def __init__(self, dims: Dims, weights: StackW, kcaches, vcaches, max_M: int, max_rows: int,
-                 device=None, fused_swiglu: bool = True, fused_sampler: bool = True, fused_rope: bool = True):
+                 device=None, fused_swiglu: bool = True, fused_sampler: bool = True, fused_rope: bool = True,
+                 fold_norms: bool = True):
         self.dims = dims
         self.w = weights
         # verify_round: LM head and sampler in one call that never materialises p
@@ -119,6 +141,11 @@ class VerifyEngine:
         want = "interleaved" if self.fused_swiglu else "split"
         for lw in weights.layers:
             set_gu_layout(lw, want)
+        # RMSNorm folded into the products: the products that store the residual stream leave its
+        # per-tile sums of squares, the products that read it scale their rows (no norm launches)
+        self.fold_norms = fold_norms
+        if fold_norms:
+            fold_norm_weights(weights)
         self.kc = kcaches
         self.vc = vcaches
         self.max_M = max_M
@@ -133,6 +160,9 @@ class VerifyEngine:
         self.gu = None if self.fused_swiglu else torch.empty((max_M, 2 * dims.I), **bf)
         self.a = torch.empty((max_M, dims.I), **bf)
         self.cs = torch.empty((max_M, dims.D // 2, 2), dtype=torch.float32, device=dev)
+        self.ssq = torch.empty((max_M, (dims.d + 127) // 128), dtype=torch.float32, device=dev)
+        self.norm_in = S.row_norm(in_ssq=self.ssq, eps=dims.eps) if fold_norms else None
+        self.norm_out = S.row_norm(out_ssq=self.ssq) if fold_norms else None
         self.P = torch.empty((max_M, dims.V), dtype=torch.float32, device=dev) if weights.w_lm is not None else None
         B, cap = (kcaches[0].shape[0], kcaches[0].shape[2]) if kcaches else (1, 1)
         need = 0
@@ -142,6 +172,10 @@ class VerifyEngine:
                 need = max(need, S.spec_linear_workspace_bytes(M, n, k))
             if self.fused_swiglu:
                 need = max(need, S.spec_swiglu_linear_workspace_bytes(M, dims.I, dims.d))
+            if fold_norms:
+                need = max(need, S.spec_linear_norm_workspace_bytes(M, dims.qkv, dims.d),
+                           S.spec_linear_norm_workspace_bytes(M, 2 * dims.I, dims.d),
+                           S.spec_linear_norm_workspace_bytes(M, dims.I, dims.d, swiglu=True))
         if kcaches:
             need = max(need, S.spec_attention_workspace_bytes(B, max_rows, dims.Hq, dims.Hkv, dims.D, cap))
         if weights.w_lm is not None:
@@ -157,27 +191,34 @@ class VerifyEngine:
         x, h, qkv, o, a = (self.x[:M], self.h[:M], self.qkv[:M], self.o[:M], self.a[:M])
         hq = dm.Hq * dm.D
         hk = dm.Hkv * dm.D
-        S.spec_rmsnorm(x, lw.attn_norm, dm.eps, Y=h)
+        # the pre-norm input of the QKV and gate|up products: x itself when the norms are folded
+        # (its sums of squares in self.ssq), else the RMSNorm kernel's output h
+        nin, nout = self.norm_in, self.norm_out
+        if not self.fold_norms:
+            S.spec_rmsnorm(x, lw.attn_norm, dm.eps, Y=h)
+        hin = x if self.fold_norms else h
         if self.fused_rope:
-            S.spec_verify_linear_rope(h, lw.w_qkv, self.cs[:M], dm.Hq + dm.Hkv, Y=qkv, ws=self.ws)
+            S.spec_verify_linear_rope(hin, lw.w_qkv, self.cs[:M], dm.Hq + dm.Hkv, Y=qkv, ws=self.ws, norm=nin)
         else:
-            S.spec_verify_linear(h, lw.w_qkv, Y=qkv, ws=self.ws)
+            S.spec_verify_linear(hin, lw.w_qkv, Y=qkv, ws=self.ws, norm=nin)
         q, k, v = qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:]
         if not self.fused_rope:
             S.spec_rope(q, k, cu_rows, ctx_len, dm.D, dm.theta)
         S.spec_verify_attention(q, k, v, cu_rows, ctx_len, self.kc[li], self.vc[li], max_rows, O=o,
                                 ws=self.ws)
-        S.spec_verify_linear(o, lw.w_o, Y=x, residual=x, ws=self.ws)
-        S.spec_rmsnorm(x, lw.mlp_norm, dm.eps, Y=h)
+        S.spec_verify_linear(o, lw.w_o, Y=x, residual=x, ws=self.ws, norm=nout)
+        if not self.fold_norms:
+            S.spec_rmsnorm(x, lw.mlp_norm, dm.eps, Y=h)
         if self.fused_swiglu:
-            S.spec_verify_linear_swiglu(h, lw.w_gu, A=a, ws=self.ws)
+            S.spec_verify_linear_swiglu(hin, lw.w_gu, A=a, ws=self.ws, norm=nin)
         else:
-            S.spec_verify_linear(h, lw.w_gu, Y=self.gu[:M], ws=self.ws)
+            S.spec_verify_linear(hin, lw.w_gu, Y=self.gu[:M], ws=self.ws, norm=nin)
             S.spec_silu_mul(self.gu[:M], A=a)
-        S.spec_verify_linear(a, lw.w_down, Y=x, residual=x, ws=self.ws)
+        S.spec_verify_linear(a, lw.w_down, Y=x, residual=x, ws=self.ws, norm=nout)
 
-    def _stack(self, x0, cu_rows, ctx_len, max_rows, n_layers):
-        """All layers and the final RMSNorm over the packed rows; the normed rows are in self.h."""
+    def _stack(self, x0, cu_rows, ctx_len, max_rows, n_layers, final_norm: bool = True):
+        """All layers and (with final_norm) the final RMSNorm over the packed rows into self.h.  With
+        folded norms and final_norm False, the LM head reads self.x with the sums of squares."""
         M = x0.shape[0]
         B = cu_rows.numel() - 1
         max_rows = self.max_rows if max_rows is None else max_rows
@@ -188,9 +229,11 @@ class VerifyEngine:
         L = len(self.w.layers) if n_layers is None else n_layers
         if self.fused_rope and L > 0:
             S.spec_rope_table(cu_rows, ctx_len, M, self.dims.D, self.dims.theta, cs=self.cs[:M])
+        if self.fold_norms and L > 0:
+            S.spec_row_ssq(self.x[:M], out=self.ssq[:M])     # the first layer's input has no producer
         for li in range(L):
             self.layer(li, M, cu_rows, ctx_len, B, max_rows)
-        if self.w.w_lm is not None:
+        if self.w.w_lm is not None and (final_norm or not self.fold_norms):
             S.spec_rmsnorm(self.x[:M], self.w.final_norm, self.dims.eps, Y=self.h[:M])
         return M
 
@@ -208,7 +251,12 @@ class VerifyEngine:
         if not self.fused_sampler:
             P = self.verify_pass(x0, cu_rows, ctx_len, temperature, max_rows)
             return S.spec_reject_sample(P, q, drafts, U, cu_rows, tie_eps, out=out)
-        M = self._stack(x0, cu_rows, ctx_len, max_rows, None)
+        M = self._stack(x0, cu_rows, ctx_len, max_rows, None, final_norm=False)
+        if self.fold_norms:
+            if self.dims.layers == 0:
+                S.spec_row_ssq(self.x[:M], out=self.ssq[:M])
+            return S.spec_lmhead_reject_sample(self.x[:M], self.w.w_lm, temperature, q, drafts, U, cu_rows, tie_eps,
+                                               out=out, ws=self.ws, norm=self.norm_in)
         return S.spec_lmhead_reject_sample(self.h[:M], self.w.w_lm, temperature, q, drafts, U, cu_rows, tie_eps,
                                            out=out, ws=self.ws)
 
@@ -253,8 +301,9 @@ class DraftEngine:
         self.dims = dims
         self.B = B
         self.gamma = gamma
+        # (the LM head is the embedding table here: its rows must stay unscaled, so no folded norms)
         self.eng = VerifyEngine(dims, weights, kcaches, vcaches, max_M=B, max_rows=1, device=device,
-                                fused_sampler=False)
+                                fused_sampler=False, fold_norms=False)
         dev = self.eng.device
         self.table = weights.w_lm
         self.cu = torch.arange(B + 1, dtype=torch.int32, device=dev)

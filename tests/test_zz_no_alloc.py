@@ -46,6 +46,7 @@ class _options:
     def __exit__(self, *exc):
         self.lib.spec_set_option("gemv_max_m", 0)
         self.lib.spec_set_option("linear_cluster", 1)
+        self.lib.spec_set_option("linear_pair", 1)
         self.lib.spec_set_option("persistent_grid", 0)
 
 
@@ -109,7 +110,8 @@ def test_noalloc_back_to_back_different_plans(lib):
 
 def test_noalloc_rejects_scratch_beyond_the_limit(lib):
     M, N, K = 368, 24576, 4096                         # 192 tiles of 368 rows, stream-K split
-    with _options(lib, linear_cluster=0):              # (else whole tiles + a cluster remainder: no scratch)
+    # (the pair plan and the whole tiles + cluster remainder plan need no scratch: both off)
+    with _options(lib, linear_cluster=0, linear_pair=0):
         need = lib.spec_linear_workspace_bytes(M, N, K)
         assert need > LIMIT
         big_x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
