@@ -612,17 +612,19 @@ def ngram_timing(S, hbm_peak, peak_src, dev, reps=5):
                          "traffic": None, "algorithmic_bytes": hb, "peak_source": f"{peak_src} hbm_gbs"}}
 
 
-def stack_chain_ops(S, eng, M, interleaved=True):
+def stack_chain_ops(S, eng, M, interleaved=True, bufs=None):
     """The 36-layer linear stack as one chain of products for spec_verify_linear_chain: per layer
     QKV (h -> qkv), O (o -> x, residual x), gate|up with SwiGLU (h -> a), down (a -> x, residual x).
     With `interleaved`, layer l+1's QKV projection (independent of layer l) sits between layer l's
-    gate|up and its down projection, which waits for gate|up's output."""
+    gate|up and its down projection, which waits for gate|up's output.  `bufs` = (layers, h, o, qkv,
+    x, a) in place of the engine's."""
+    layers, h, o, qkv, x, a = bufs if bufs is not None else (eng.w.layers, eng.h, eng.o, eng.qkv, eng.x, eng.a)
     per = []
-    for lw in eng.w.layers:
-        per.append([S.linear_op(eng.h[:M], lw.w_qkv, eng.qkv[:M]),
-                    S.linear_op(eng.o[:M], lw.w_o, eng.x[:M], residual=eng.x[:M]),
-                    S.linear_op(eng.h[:M], lw.w_gu, eng.a[:M], swiglu=True),
-                    S.linear_op(eng.a[:M], lw.w_down, eng.x[:M], residual=eng.x[:M])])
+    for lw in layers:
+        per.append([S.linear_op(h[:M], lw.w_qkv, qkv[:M]),
+                    S.linear_op(o[:M], lw.w_o, x[:M], residual=x[:M]),
+                    S.linear_op(h[:M], lw.w_gu, a[:M], swiglu=True),
+                    S.linear_op(a[:M], lw.w_down, x[:M], residual=x[:M])])
     if not interleaved:
         return [op for layer in per for op in layer]
     ops = [per[0][0]]
@@ -733,8 +735,16 @@ class SweepRig:
         import synth
         M = nb * (gm + 1)
         x, h, qkv, o, a, ws = self.x, self.h, self.qkv, self.o, self.a, self.ws
+        # the small-M path (M <= 32): the weight-streaming chain; above it, one call per product
+        chain = M <= 32
+        if chain:
+            ops = stack_chain_ops(S, None, M, bufs=(self.sw.layers, h, o, qkv, x, a))
+            cws = S.Workspace(dev, S.spec_linear_chain_workspace_bytes(ops, M))
 
         def run():
+            if chain:
+                S.spec_verify_linear_chain(ops, M, ws=cws)
+                return
             for lw in self.sw.layers:
                 S.spec_verify_linear(h[:M], lw.w_qkv, Y=qkv[:M], ws=ws)
                 S.spec_verify_linear(o[:M], lw.w_o, Y=x[:M], residual=x[:M], ws=ws)
@@ -786,7 +796,7 @@ class SweepRig:
         S.spec_device_status()
         del kc, vc, attn_ws
         torch.cuda.empty_cache()
-        return {"B": nb, "gamma": gm, "M": M,
+        return {"B": nb, "gamma": gm, "M": M, "linear_path": "chain" if chain else "one call per product",
                 "linear_stack_us": t_lin * 1e6,
                 "linear_hbm_frac": self.wbytes / t_lin / 1e9 / hbm_peak,
                 "linear_tensor_frac": self.flops_row * M / t_lin / 1e12 / tc_sust,
