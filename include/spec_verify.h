@@ -94,11 +94,18 @@ SPEC_API int spec_version(void);
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
  * and sum the pieces on chip; "lmhead_nsub" (2 default, or 1): the LM head's
- * tensor-core tiles cover up to 384 or 256 rows; "linear_pair" (1 default,
- * 0 off): verify linears of 64+ rows with more 128-row weight tiles than SMs
- * run 256-row tiles on CTA pairs (the tcgen05 2-SM MMA: each CTA of a pair
- * stages half of the token rows), whole pair tiles first, the rest split
- * between the pairs of a cluster, no workspace; "linear_pair_few" (0
+ * tensor-core tiles cover up to 384 or 256 rows; "lmhead_pair" (1 default,
+ * 0 off): the LM head (64+ rows) runs 256-row vocabulary tiles on CTA pairs
+ * (the tcgen05 2-SM MMA: each CTA of a pair stages half of the token rows),
+ * a persistent kernel on every pair taking whole tiles round-robin;
+ * "linear_pair" (1 default, 0 off): verify linears of 64+ rows with more
+ * 128-row weight tiles than SMs run 256-row tiles on CTA pairs, whole pair
+ * tiles first (one launch), the rest split between the pairs of a cluster
+ * (a second launch), no workspace; "linear_pair_persistent" (0 default, 1,
+ * 2): instead the persistent pair kernel takes the whole pair tiles, then
+ * with 1 cuts the rest into stream-K pieces that a second kernel sums
+ * (workspace: 4 fp32 token tiles per pair), with 2 runs the rest split
+ * between the pairs of a cluster; "linear_pair_few" (0
  * default, 1): the pair kernel also for products with fewer tiles (split-K
  * on pairs; measured slower than the one-SM cluster kernel at 368 rows);
  * "pdl" (1 default, 0 off):

@@ -187,6 +187,12 @@ int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
 int g_linear_pair = 1;   // tunable: 1 lets the planner run 256-row pair tiles on the 2-SM MMA
 int g_linear_pair_few = 0;  // tunable: 1 also for products with fewer tiles than SMs (split-K on pairs)
+// tunable: products with more tiles than SMs on the persistent kernel on CTA pairs: 1 = whole pair
+// tiles, then stream-K pieces summed by the reduce kernel; 2 = whole pair tiles, then the rest on
+// the pair split-K kernel; 0 = off (whole pair tiles, then the rest, each as a launch of the pair
+// split-K kernel: measured fastest for gate|up at 368 rows, 63.2 us against 64.8 and 74.5)
+int g_linear_pair_persistent = 0;
+int g_lmhead_pair = 1;     // tunable: 1 runs the LM head on the persistent kernel on CTA pairs
 
 struct LinPlan {
   bool gemv = false;
@@ -199,8 +205,11 @@ struct LinPlan {
   int pair_first[2] = {0, 0};   //      tiles pair_first[i] .. + pair_count[i] - 1 with pair_S[i]
   int pair_count[2] = {0, 0};   //      pairs per tile
   int pair_S[2] = {0, 0};
+  bool tc_pair = false;          // persistent kernel on CTA pairs: grid counts pairs, dp_tiles and
+                                //   sk_units count 256-row pair tiles; pair_n = 1 adds a pair
+                                //   split-K launch for the pair tiles after dp_tiles
   // token rows per TMA load: each CTA of a pair stages half of every MMA's token rows
-  int x_box_rows() const { return pair_n > 0 ? BN / 2 : BN; }
+  int x_box_rows() const { return pair_n > 0 || tc_pair ? BN / 2 : BN; }
   bool aligned = false;         // whole tiles only (no stream-K region)
   long long dp_tiles = 0, sk_units = 0;
   long long units = 0;
@@ -208,7 +217,20 @@ struct LinPlan {
   size_t counters_off = 0, partial_off = 0, bytes = 0;
 };
 
-LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
+// The smallest token-tile width >= BN with a build of the persistent pair kernel (0: none).
+int tc_pair_bn(int BN, int NSUB) {
+  static const int shapes[][2] = {
+#define X(bn, ns) {bn, ns},
+      SPEC_TC_PAIR_SHAPES(X)
+#undef X
+  };
+  int best = 0;
+  for (const auto& sh : shapes)
+    if (sh[1] == NSUB && sh[0] >= BN && (best == 0 || sh[0] < best)) best = sh[0];
+  return best;
+}
+
+LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false, size_t max_bytes = SIZE_MAX) {
   LinPlan p;
   const int sms = plan_sms();
   p.k_tiles = (K + LIN_BK - 1) / LIN_BK;
@@ -260,6 +282,50 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false) {
   // persistent stream-K: one CTA per SM, each streaming an equal share of (tile, k-step) units;
   // the LM-head epilogue needs whole tiles, so its ranges are tile-aligned
   p.aligned = lmhead || tiles > (long long)kMaxCounters;
+  // Many tiles (and the LM head): the persistent kernel on CTA pairs, 256-row pair tiles on the 2-SM
+  // MMA, each CTA staging half of the token rows (which halves the shared-memory traffic per MMA
+  // that bounds the one-SM kernels at a few hundred rows).  Whole pair tiles go round-robin to the
+  // pairs; the pair tiles left over are cut into stream-K pieces (summed by the reduce kernel) or
+  // run on the pair split-K kernel.
+  // (token tiles round up to the next shape with a pair build; the rows past M are zero-filled)
+  const int pbn = tc_pair_bn(p.BN, p.NSUB);
+  const bool want_pair = lmhead ? g_lmhead_pair != 0 : (g_linear_pair && g_linear_pair_persistent);
+  if (want_pair && g_force_grid == 0 && TN >= 64 && tiles > sms && pbn > 0) {
+    const int pairs = linear_tc_pair_capacity(pbn, p.NSUB, lmhead);
+    const long long wt = (long long)p.tiles_m * ((p.tiles_n + 1) / 2);
+    if (pairs > 0 && wt >= pairs) {
+      LinPlan q = p;
+      q.BN = pbn;
+      q.tc_pair = true;
+      q.grid = pairs;
+      q.units = wt * p.k_tiles;
+      q.aligned = lmhead || wt > (long long)kMaxCounters;
+      q.dp_tiles = q.aligned ? wt : wt / pairs * pairs;
+      q.sk_units = 0;
+      q.bytes = 0;
+      bool ok_plan = true;
+      if (lmhead) {
+        q.bytes = kCounterBytes + round_up(size_t(M) * p.tiles_n * sizeof(float2), 256);
+      } else if (q.dp_tiles < wt && g_linear_pair_persistent == 2) {
+        // the rest on the pair split-K kernel (S pairs per pair tile, on-chip sums)
+        // (the most pairs per pair tile that still fit in one wave)
+        int best = 0;
+        for (int S = std::min(4, p.k_tiles); S >= 2 && !best; --S)
+          if (linear_pair_capacity(p.BN, p.NSUB, S) >= (wt - q.dp_tiles) * 2 * S) best = S;
+        ok_plan = best > 0;
+        q.pair_n = 1;
+        q.pair_first[0] = (int)q.dp_tiles;
+        q.pair_count[0] = (int)(wt - q.dp_tiles);
+        q.pair_S[0] = best;
+      } else if (q.dp_tiles < wt) {
+        q.sk_units = (wt - q.dp_tiles) * p.k_tiles;
+        bool split = false;
+        for (int c = 1; c < pairs && !split; ++c) split = ((q.sk_units * c / pairs) % p.k_tiles) != 0;
+        q.bytes = split ? kCounterBytes + round_up(size_t(pairs) * 2 * 2 * pbn * p.NSUB * 128 * 4, 256) : 0;
+      }
+      if (ok_plan && q.bytes <= max_bytes) return q;
+    }
+  }
   // 2-SM pair tiles (256 weight rows on a CTA pair; each CTA stages half of the token rows, which
   // halves the shared-memory traffic per MMA that bounds the one-SM kernels at a few hundred rows):
   // few pair tiles -> one cluster split-K launch of S pairs per tile; more -> whole pair tiles on
@@ -430,6 +496,16 @@ int spec_set_option(const char* name, int value) {
     g_linear_pair = value;
     return ok();
   }
+  if (!strcmp(name, "lmhead_pair")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "lmhead_pair must be 0 or 1");
+    g_lmhead_pair = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_pair_persistent")) {
+    if (value < 0 || value > 2) return fail(SPEC_EINVAL, "linear_pair_persistent must be in [0, 2]");
+    g_linear_pair_persistent = value;
+    return ok();
+  }
   if (!strcmp(name, "linear_pair_few")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_pair_few must be 0 or 1");
     g_linear_pair_few = value;
@@ -551,9 +627,25 @@ static int launch_pair_plan(const LinPlan& p, const CUtensorMap& tw, const CUten
   return p.pair_n;
 }
 
-extern "C" {
-
-}  // extern "C"
+// The launches of a persistent pair plan (epilogue and args set): the persistent kernel, then
+// the pair split-K kernel for the pair tiles after dp_tiles or the reduce kernel for split pieces.
+// Returns the number of launches, or a (negative) error from fail().
+static int launch_tc_pair_plan(const LinPlan& p, const CUtensorMap& tw, const CUtensorMap& tx, LinearArgs a,
+                               cudaStream_t s) {
+  a.pair = 1;
+  cudaError_t e = launch_linear_tc_pair(p.BN, p.NSUB, a.epi, tw, tx, a, p.grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pair persistent linear launch");
+  if (p.pair_n > 0) {
+    a.dp_tiles = p.pair_first[0];
+    e = launch_linear_pair(p.BN, p.NSUB, tw, tx, a, p.pair_S[0], p.pair_count[0], s);
+    if (e != cudaSuccess) return cuda_fail(e, "pair linear launch (remainder)");
+    return 2;
+  }
+  if (p.bytes == 0) return 1;
+  e = launch_linear_reduce(a, plan_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+  return 2;
+}
 
 static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N,
                               int ldw, spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr,
@@ -561,9 +653,19 @@ static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K
 static int swiglu_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int ldx, const spec_bf16* Wgu, int ldw,
                        int I, spec_bf16* A, int lda, const spec_rownorm* norm, char* ws, DevInfo* d, cudaStream_t s);
 
-// A folded RMSNorm on a plan: the split-K epilogues (cluster and pair kernels) scale rows and sum
-// squares themselves; other plans take the normalised copy of X / a sum-of-squares pass over Y.
-static bool plan_fuses_norm(const LinPlan& p) { return !p.gemv && (p.cluster_S > 0 || p.pair_n > 0); }
+// A folded RMSNorm on a plan: every tensor-core epilogue scales rows by 1 / rms; the split-K
+// epilogues (cluster and pair kernels) also sum the squares of what they store.  Otherwise the
+// normalised copy of X / a sum-of-squares pass over Y.
+static bool plan_fuses_norm_in(const LinPlan& p) { return !p.gemv; }
+static bool plan_fuses_norm_out(const LinPlan& p) { return !p.gemv && !p.tc_pair && (p.cluster_S > 0 || p.pair_n > 0); }
+// The norm a plan is handed: in_ssq / out_ssq cleared where the caller does that part itself.
+static const spec_rownorm* plan_norm(const spec_rownorm* nm, const LinPlan& p, spec_rownorm* tmp) {
+  if (!nm) return nullptr;
+  *tmp = *nm;
+  if (!plan_fuses_norm_in(p)) tmp->in_ssq = nullptr;
+  if (!plan_fuses_norm_out(p)) tmp->out_ssq = nullptr;
+  return tmp;
+}
 static bool norm_in(const spec_rownorm* nm) { return nm && nm->in_ssq; }
 static bool norm_out(const spec_rownorm* nm) { return nm && nm->out_ssq; }
 static int check_norm(const spec_rownorm* nm) {
@@ -576,8 +678,8 @@ static int check_norm(const spec_rownorm* nm) {
 // the counter region.
 static size_t norm_copy_off(size_t plan_bytes) { return std::max(round_up(plan_bytes, 256), kCounterBytes); }
 // (out_ssq only with the plain bf16 epilogue, the one that sums the squares of what it stores)
-static void set_norm_args(LinearArgs& a, const spec_rownorm* nm, int K, bool fused) {
-  if (!fused || !nm) return;
+static void set_norm_args(LinearArgs& a, const spec_rownorm* nm, int K) {
+  if (!nm) return;
   if (nm->in_ssq) {
     a.norm_ssq = nm->in_ssq;
     a.norm_tiles = nm->in_tiles;
@@ -587,16 +689,17 @@ static void set_norm_args(LinearArgs& a, const spec_rownorm* nm, int K, bool fus
   if (a.epi == EPI_BF16) a.out_ssq = nm->out_ssq;
 }
 
+// (max_bytes: the largest scratch a plan may ask for; plans above it give way to the next choice)
 static int verify_linear_impl(const spec_bf16* X, int M, int K, int ldx, const spec_bf16* W, int N, int ldw,
                               spec_bf16* Y, int ldy, const spec_bf16* residual, int ldr, const spec_rownorm* norm,
-                              void* workspace, size_t workspace_bytes, spec_stream stream) {
+                              void* workspace, size_t workspace_bytes, spec_stream stream,
+                              size_t max_bytes = SIZE_MAX) {
   if (M < 0 || N <= 0 || K <= 0) return fail(SPEC_EINVAL, "bad sizes M=%d N=%d K=%d", M, N, K);
   if (M == 0) return ok();
   if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr)) return rc;
   if (int rc = check_norm(norm)) return rc;
-  LinPlan p = plan_linear(M, N, K, false);
-  const bool fused = plan_fuses_norm(p);
-  const bool copy_x = norm_in(norm) && !fused;
+  LinPlan p = plan_linear(M, N, K, false, false, max_bytes);
+  const bool copy_x = norm_in(norm) && !plan_fuses_norm_in(p);
   const size_t need = copy_x ? norm_copy_off(p.bytes) + round_up(size_t(M) * K * 2, 256) : p.bytes;
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SPEC_EINVAL, "workspace too small: need %zu bytes", need);
@@ -614,11 +717,12 @@ static int verify_linear_impl(const spec_bf16* X, int M, int K, int ldx, const s
     ldx = K;
     extra = 1;
   }
-  const int rc = verify_linear_plan(p, X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr,
-                                    fused ? norm : nullptr, ws, d, s);
+  spec_rownorm tmp{};
+  const int rc = verify_linear_plan(p, X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, plan_norm(norm, p, &tmp),
+                                    ws, d, s);
   if (rc) return rc;
   int n = t_launches + extra;
-  if (norm_out(norm) && !fused) {
+  if (norm_out(norm) && !plan_fuses_norm_out(p)) {
     cudaError_t e = launch_row_ssq(Y, M, N, ldy, norm->out_ssq, s);
     if (e != cudaSuccess) return cuda_fail(e, "sum-of-squares launch");
     ++n;
@@ -646,7 +750,7 @@ size_t spec_linear_norm_workspace_bytes(int M, int N, int K, int swiglu) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   const LinPlan p = plan_linear(M, swiglu ? 2 * N : N, K, false, swiglu != 0);
   const size_t own = swiglu ? spec_swiglu_linear_workspace_bytes(M, N, K) : p.bytes;
-  return plan_fuses_norm(p) ? own : norm_copy_off(own) + round_up(size_t(M) * K * 2, 256);
+  return plan_fuses_norm_in(p) ? own : norm_copy_off(own) + round_up(size_t(M) * K * 2, 256);
 }
 
 int spec_row_ssq(const spec_bf16* X, int M, int N, int ldx, float* out, spec_stream stream) {
@@ -697,7 +801,11 @@ static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_BF16;
-  set_norm_args(a, norm, K, plan_fuses_norm(p));
+  set_norm_args(a, norm, K);
+  if (p.tc_pair) {
+    const int n = launch_tc_pair_plan(p, tw, tx, a, s);
+    return n > 0 ? ok(n) : n;
+  }
   if (p.pair_n > 0) {
     cudaError_t e = cudaSuccess;
     const int n = launch_pair_plan(p, tw, tx, a, s, &e);
@@ -1032,7 +1140,7 @@ static int verify_linear_rope_impl(const spec_bf16* X, int M, int K, int ldx, co
     a.epi = EPI_ROPE;
     a.rope_cs = reinterpret_cast<const float2*>(cs);
     a.rope_tiles = rope_heads;
-    set_norm_args(a, norm, K, true);
+    set_norm_args(a, norm, K);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     int n = 1;
     if (p.pair_n > 0) {
@@ -1113,8 +1221,7 @@ static int verify_linear_swiglu_impl(const spec_bf16* X, int M, int K, int ldx, 
   if (int rc = check_norm(norm)) return rc;
   const int N = 2 * I;
   LinPlan p = plan_linear(M, N, K, false, true);
-  const bool fused = plan_fuses_norm(p);
-  const bool copy_x = norm_in(norm) && !fused;
+  const bool copy_x = norm_in(norm) && !plan_fuses_norm_in(p);
   const size_t own = spec_swiglu_linear_workspace_bytes(M, I, K);
   const size_t need = copy_x ? norm_copy_off(own) + round_up(size_t(M) * K * 2, 256) : own;
   if (need > 0 && (!workspace || workspace_bytes < need))
@@ -1132,7 +1239,10 @@ static int verify_linear_swiglu_impl(const spec_bf16* X, int M, int K, int ldx, 
     ldx = K;
     extra = 1;
   }
-  const int rc = swiglu_plan(p, X, M, K, ldx, Wgu, ldw, I, A, lda, fused ? norm : nullptr, ws, d, s);
+  spec_rownorm tmp{};
+  const spec_rownorm* pn = plan_norm(norm, p, &tmp);
+  if (pn) tmp.out_ssq = nullptr;   // (the SwiGLU epilogues do not sum squares: the pass below does)
+  const int rc = swiglu_plan(p, X, M, K, ldx, Wgu, ldw, I, A, lda, pn, ws, d, s);
   if (rc) return rc;
   int n = t_launches + extra;
   if (norm_out(norm)) {
@@ -1181,7 +1291,11 @@ static int swiglu_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int l
   a.status = d->status;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
-  set_norm_args(a, norm, K, plan_fuses_norm(p));
+  set_norm_args(a, norm, K);
+  if (p.tc_pair) {
+    const int n = launch_tc_pair_plan(p, tw, tx, a, s);
+    return n > 0 ? ok(n) : n;
+  }
   if (p.pair_n > 0) {
     cudaError_t e = cudaSuccess;
     const int n = launch_pair_plan(p, tw, tx, a, s, &e);
@@ -1260,7 +1374,13 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
     a.norm_k = (float)K;
     a.norm_eps = norm->eps;
   }
-  cudaError_t e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid), s);
+  cudaError_t e;
+  if (p.tc_pair) {
+    a.pair = 1;
+    e = launch_linear_tc_pair(p.BN, p.NSUB, greedy ? EPI_ARGMAX : EPI_LOGITS, tw, tx, a, p.grid, s);
+  } else {
+    e = launch_linear_tc_lmhead(p.BN, p.NSUB, greedy, tw, tx, a, dim3(p.grid), s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "LM-head GEMM launch");
   *stats_out = a.stats;
   return SPEC_OK;
@@ -1628,7 +1748,8 @@ extern "C" int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int 
   if (M == 0) return ok();
   // every argument check runs before anything touches the stream or the scratch
   if (int rc = check_linear_args(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr)) return rc;
-  const size_t need = spec_linear_workspace_bytes(M, N, K);
+  // (plans are chosen among those whose scratch fits in the static array)
+  const size_t need = plan_linear(M, N, K, false, false, SPEC_NOALLOC_SCRATCH_BYTES).bytes;
   if (need > SPEC_NOALLOC_SCRATCH_BYTES)
     return fail(SPEC_EUNSUPPORTED,
                 "M=%d N=%d K=%d needs %zu bytes of split-K scratch; the static scratch holds %u "
@@ -1642,6 +1763,6 @@ extern "C" int spec_verify_linear_noalloc(const spec_bf16* X, int M, int K, int 
     cudaError_t e = cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clear static scratch counters");
   }
-  return spec_verify_linear(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, scratch,
-                            SPEC_NOALLOC_SCRATCH_BYTES, stream);
+  return verify_linear_impl(X, M, K, ldx, W, N, ldw, Y, ldy, residual, ldr, nullptr, scratch,
+                            SPEC_NOALLOC_SCRATCH_BYTES, stream, SPEC_NOALLOC_SCRATCH_BYTES);
 }

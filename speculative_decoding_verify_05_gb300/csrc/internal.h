@@ -79,6 +79,17 @@ cudaError_t launch_linear_cluster(int BN, int NSUB, const CUtensorMap& tw, const
 int linear_pair_capacity(int BN, int NSUB, int S);
 cudaError_t launch_linear_pair(int BN, int NSUB, const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a,
                                int S, int pair_tiles, cudaStream_t s);
+// The persistent GEMM on CTA pairs (2-SM MMA, 256-row pair tiles; a.pair = 1, a.grid pairs): the
+// tile shapes with a build (BN token rows per MMA, NSUB MMAs per k-step), the pairs resident at
+// once (0: no build for the shape), and the launch of `pairs` clusters of 2 CTAs (epilogue epi).
+#define SPEC_TC_PAIR_SHAPES(X) \
+  X(64, 1) X(96, 1) X(128, 1) X(160, 1) X(192, 1) X(224, 1) X(256, 1) X(144, 2) X(160, 2) X(176, 2) X(192, 2)
+int linear_tc_pair_capacity(int BN, int NSUB, bool lmhead);
+int linear_tc_pair_capacity_lmhead(int BN, int NSUB);
+cudaError_t launch_linear_tc_pair(int BN, int NSUB, int epi, const CUtensorMap& tw, const CUtensorMap& tx,
+                                  const LinearArgs& a, int pairs, cudaStream_t s);
+cudaError_t launch_linear_tc_pair_lmhead(int BN, int NSUB, bool greedy, const CUtensorMap& tw, const CUtensorMap& tx,
+                                         const LinearArgs& a, int pairs, cudaStream_t s);
 // Second pass of a split GEMM: sums the fp32 pieces of every split tile (in CTA order), adds the
 // residual and writes bf16 Y.  `sms` sizes its grid.
 cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s);

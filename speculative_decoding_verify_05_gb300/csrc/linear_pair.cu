@@ -37,39 +37,6 @@ struct PairCfg {
   static constexpr int SMEM_BYTES = RMS_OFF + TN * 4 + 1024;
 };
 
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// One 2-SM MMA: D (128 lanes in each CTA of the pair) += A (128 rows per CTA) x B^T (half the
-// N rows per CTA, at the same shared-memory offset in both).
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on the mbarrier at shared::cluster address `bar` once the pair's MMAs issued so far finish.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// TMA load into this CTA's shared memory whose completion is counted on the mbarrier at
-// shared::cluster address `bar` (the pair's even CTA).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 template <int BN, int NSUB>
 __global__ void __launch_bounds__(PR_THREADS, 1)
 linear_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -169,6 +136,22 @@ linear_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
   }
   const bool ok = mbar_wait(acc_full, 0u, args.status, 0x173u);
   tc_fence_after();
+  if (S == 1 && args.epi == EPI_SWIGLU) {
+    // one pair per tile, nothing to sum: the SwiGLU epilogue straight from TMEM, each warp through
+    // a transpose block in its CTA's ring (free: the pair's MMAs, the only readers, have completed)
+    __syncthreads();   // (the row scales written by warps 2-7)
+    if (ok && n_t < args.tiles_n)
+      tmem_swiglu_epilogue<TN>(tmem, warp, lane, args, m_t, n_t,
+                               args.norm_ssq ? reinterpret_cast<const float*>(smem + Cfg::RMS_OFF) : nullptr,
+                               reinterpret_cast<float*>(smem));
+    tc_fence_before();
+    cluster_sync_all();   // both CTAs done with their TMEM before the pair frees it
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
+    }
+    return;
+  }
   // every CTA of the cluster is past its main loop: the rings are free
   cluster_sync_all();
   // the S CTAs holding the same weight rows (ranks half, half + 2, ...) exchange their pieces

@@ -67,6 +67,10 @@ struct LinearArgs {
   // the partial sums of squares of Y as stored (bf16), per row and 128-column tile: [M][tiles_n]
   // (nullptr: none)
   float* out_ssq;
+  // 1: the persistent kernel runs on CTA pairs; its work tiles are 256 weight rows (tile t covers
+  // token tile t % tiles_m and the 128-row tiles 2 (t / tiles_m) + 0, 1), grid counts pairs and
+  // the CTA of rank r in pair c leaves its split-K pieces in partial slots 2 (2c + r) + 0, 1
+  int pair;
 };
 
 // 1 / rms of row m from its partial sums of squares (t in order; the loads go out 8 at a time).
@@ -94,6 +98,68 @@ __device__ __forceinline__ void fill_row_scales(const LinearArgs& a, float* s_rm
   }
 }
 
+// SwiGLU epilogue of 32 token columns of one whole tile held by one warp (v[0..31]; columns
+// past `cols` are never stored): gate and up rows are interleaved in blocks of 16, so lane l < 16
+// holds gate row l of the warp's block and lane l + 16 the matching up row.  One register
+// exchange gives lane l < 16 the up values of columns 0-15 and lane l + 16 the gate values of
+// columns 16-31; each lane writes silu(gate) * up for its 16 columns as bf16 into the warp's
+// staging buffer ([column][16 rows], column c at slot c ^ (c >> 4) so the two half-warps hit
+// different banks), and the warp stores 16-byte runs of 8 outputs along A's rows.
+__device__ __forceinline__ void swiglu_chunk32(const float* v, int cols, float* ebuf, int lane,
+                                               const LinearArgs& args, int m_first, int n_first) {
+  const bool lo = lane < 16;
+  uint16_t* eb = reinterpret_cast<uint16_t*>(ebuf);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float send = lo ? v[k + 16] : v[k];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float g = lo ? v[k] : recv;
+    const float u = lo ? recv : v[k + 16];
+    const int col = lo ? k : k + 16;
+    eb[(col ^ (col >> 4)) * 16 + (lane & 15)] = f2bf(silu(g) * u);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int item = lane + 32 * it, col = item >> 1, h = item & 1;
+    const int m = m_first + col;
+    if (col < cols && m < args.M)
+      *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n_first + h * 8) =
+          *reinterpret_cast<const uint4*>(eb + (col ^ (col >> 4)) * 16 + h * 8);
+  }
+  __syncwarp();
+}
+
+// SwiGLU epilogue of a whole tile straight from TMEM (no pieces to sum): 8 warps, warp w reads TMEM
+// lane quarter w % 4 and half w / 4 of the TN token columns, 64 columns per wait, scales them by a
+// folded RMSNorm's row scales (s_rms[column], or nullptr) and stores silu(gate) * up through its
+// transpose block eb (16 x 33 floats per warp).
+template <int TN>
+__device__ __forceinline__ void tmem_swiglu_epilogue(uint32_t tmem, int warp, int lane, const LinearArgs& args,
+                                                     int m_t, int n_t, const float* s_rms, float* ebuf) {
+  const int q = warp & 3;
+  const uint32_t t_row = tmem + (uint32_t(q * 32) << 16);
+  constexpr int C_MID = TN / 32 * 16;
+  const int c_lo = warp < 4 ? 0 : C_MID, c_hi = warp < 4 ? C_MID : TN;
+  float* eb = ebuf + warp * (16 * 33);
+#pragma unroll 1
+  for (int c64 = c_lo; c64 < c_hi; c64 += 64) {
+    const int cols = c_hi - c64 < 64 ? c_hi - c64 : 64;
+    float v[64];
+    if (cols == 64) tmem_ld_cols<64>(t_row + c64, v);
+    else if (cols == 48) tmem_ld_cols<48>(t_row + c64, v);
+    else if (cols == 32) tmem_ld_cols<32>(t_row + c64, v);
+    else tmem_ld_cols<16>(t_row + c64, v);
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+      if (k >= cols) v[k] = 0.f;        // (never stored; defined values)
+      else if (s_rms) v[k] *= s_rms[c64 + k];
+    }
+    swiglu_chunk32(v, cols, eb, lane, args, m_t * TN + c64, n_t * 64 + q * 16);
+    if (cols > 32) swiglu_chunk32(v + 32, cols - 32, eb, lane, args, m_t * TN + c64 + 32, n_t * 64 + q * 16);
+  }
+}
+
 // k-step of the tensor-core GEMMs: LIN_BK bf16 per operand row and stage (one swizzle row of
 // LIN_ROW_BYTES): 64 with 128-byte swizzle, or 32 with 64-byte swizzle.  Half-size stages keep
 // more of the shared-memory ring in flight while the tensor core works on one of them, but each
@@ -107,15 +173,15 @@ __device__ __forceinline__ uint64_t umma_desc_lin(uint32_t smem_addr) {
 
 // A CTA tile is 128 weight rows x TN = NSUB * BN verify rows: NSUB MMAs of N = BN per
 // k-substep share one weight tile, so with up to 384 verify rows (kMaxTN) every weight byte is
-// read from HBM once.
-template <int BN, int NSUB>
+// read from HBM once.  PAIR: the tile of a CTA pair is 256 weight rows (128 per CTA) x TN, and
+// each CTA stages half (HB) of every MMA's token rows.
+template <int BN, int NSUB, bool PAIR = false>
 struct LinearCfg {
   static constexpr int TN = BN * NSUB;
+  static constexpr int HB = PAIR ? BN / 2 : BN;
   static constexpr int A_BYTES = 128 * LIN_ROW_BYTES;
-  static constexpr int B_BYTES = TN * LIN_ROW_BYTES;
+  static constexpr int B_BYTES = NSUB * HB * LIN_ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
   // accumulator buffer: power-of-two columns >= TN; two buffers when they fit in TMEM
   static constexpr int ACC_COLS = TN <= 16 ? 16 : (TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512))));
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
@@ -126,8 +192,13 @@ struct LinearCfg {
   // per epilogue warp: a 16-column x 32-row fp32 block (row stride 33) to turn TMEM rows into
   // 16-byte stores along the weight rows
   static constexpr int EPI_BUF_FLOATS = 16 * 33;
-  // ring + barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) + epilogue
-  // transpose blocks + row scales of a folded RMSNorm (TN floats) + alignment slack
+  // besides the ring: barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) +
+  // epilogue transpose blocks + row scales of a folded RMSNorm (TN floats) + alignment slack
+  static constexpr int EXTRA = 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4 + TN * 4 + 1024;
+  static constexpr int STAGES_RING = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES_SMEM = (227 * 1024 - EXTRA) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = STAGES_RING < STAGES_SMEM ? STAGES_RING : STAGES_SMEM;
+  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
   static constexpr int RMS_OFF = STAGES * STAGE_BYTES + 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4;
   static constexpr int SMEM_BYTES = RMS_OFF + TN * 4 + 1024;
 };

@@ -69,11 +69,11 @@ cudaError_t launch_linear_tc_bf16(int BN, int NSUB, const CUtensorMap& tw, const
 
 // Second pass of a split GEMM.  Every block first tabulates where each work group's stream-K
 // range starts (beg[c] = sk_units * c / grid, one 64-bit division per entry; unit u is k-step
-// u % kt of cluster tile dp_tiles + u / kt).  A cluster tile is split iff a range starts strictly
+// u % kt of work tile dp_tiles + u / kt).  A work tile is split iff a range starts strictly
 // inside it; the first such range c names it, and its pieces came from groups c - 1 .. hi (the
-// last range starting inside it): rank r of each of those clusters left the piece of weight tile
-// (t / tiles_m) cl + r.  Warp item = (c, r, 8 token columns); lane l owns weight rows
-// n0 + 4 l .. + 3 (one float4 per column of a piece).
+// last range starting inside it).  A work group is one CTA, or a CTA pair (a.pair) whose CTA of
+// rank r left the piece of 128-row weight tile 2 (t / tiles_m) + r.  Warp item = (c, r, 8 token
+// columns); lane l owns weight rows n0 + 4 l .. + 3 (one float4 per column of a piece).
 // Pieces are summed in CTA order, two contributors' loads in flight at a time, then the
 // residual is added and the sum rounded to bf16.  Launched as one wave (grid-stride over items).
 __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs a) {
@@ -98,17 +98,21 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
   }
   __syncthreads();
   const int cols8 = (TN + 7) / 8;
-  const long long items = (long long)G * cols8;
+  const int R = a.pair ? 2 : 1;
+  const long long items = (long long)G * R * cols8;
   const int lane = threadIdx.x & 31;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
-    const int c = (int)(it / cols8);
+    const int c = (int)(it / (R * cols8));
     const int hi = s_hi[c];
     if (hi < 0) continue;
-    const int j0 = (int)(it - (long long)c * cols8) * 8;
+    const int rest = (int)(it - (long long)c * R * cols8);
+    const int r = rest / cols8;
+    const int j0 = (rest - r * cols8) * 8;
     const long long t0 = s_beg[c] / kt * kt;
     const long long ctile = a.dp_tiles + t0 / kt;
-    const int n_t = (int)(ctile / a.tiles_m);
+    const int n_t = (int)(ctile / a.tiles_m) * R + r;
+    if (n_t >= a.tiles_n) continue;   // (the odd half of a pair tile past N)
     const int m0 = (int)(ctile % a.tiles_m) * TN + j0;
     const int n4 = n_t * 128 + lane * 4;
     float4 acc[8];
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(256, 2) linear_reduce_kernel(const LinearArgs 
         // slot 0 holds the piece that opens a CTA's stream-K range: the tile's iff the range starts
         // inside it; a CTA with an empty range (fewer stream-K units than CTAs) left nothing
         const float* base = (cc <= hi && s_beg[cc] < s_beg[cc + 1])
-                                ? a.partial + ((size_t)cc * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
+                                ? a.partial + (((size_t)cc * R + r) * 2 + (s_beg[cc] >= t0 ? 0 : 1)) * (TN * 128) + lane * 4
                                 : nullptr;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
@@ -189,7 +193,7 @@ cudaError_t launch_linear_reduce(const LinearArgs& a, int sms, cudaStream_t s) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   // one wave: two 256-thread blocks per SM (register budget), grid-stride over the items
-  const long long warps = (long long)a.grid * ((a.tn + 7) / 8);
+  const long long warps = (long long)a.grid * (a.pair ? 2 : 1) * ((a.tn + 7) / 8);
   long long blocks = (warps + 7) / 8;
   if (blocks > 2LL * sms) blocks = 2LL * sms;
   cudaError_t e = launch_k(linear_reduce_kernel, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), smem, s, a);

@@ -24,38 +24,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
 }
-// SwiGLU epilogue of 32 token columns of one whole tile held by one warp (v[0..31]; columns
-// past `cols` are never stored): gate and up rows are interleaved in blocks of 16, so lane l < 16
-// holds gate row l of the warp's block and lane l + 16 the matching up row.  One register
-// exchange gives lane l < 16 the up values of columns 0-15 and lane l + 16 the gate values of
-// columns 16-31; each lane writes silu(gate) * up for its 16 columns as bf16 into the warp's
-// staging buffer ([column][16 rows], column c at slot c ^ (c >> 4) so the two half-warps hit
-// different banks), and the warp stores 16-byte runs of 8 outputs along A's rows.
-__device__ __forceinline__ void swiglu_chunk32(const float* v, int cols, float* ebuf, int lane,
-                                               const LinearArgs& args, int m_first, int n_first) {
-  const bool lo = lane < 16;
-  uint16_t* eb = reinterpret_cast<uint16_t*>(ebuf);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float send = lo ? v[k + 16] : v[k];
-    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-    const float g = lo ? v[k] : recv;
-    const float u = lo ? recv : v[k + 16];
-    const int col = lo ? k : k + 16;
-    eb[(col ^ (col >> 4)) * 16 + (lane & 15)] = f2bf(silu(g) * u);
-  }
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int item = lane + 32 * it, col = item >> 1, h = item & 1;
-    const int m = m_first + col;
-    if (col < cols && m < args.M)
-      *reinterpret_cast<uint4*>(args.Y + (size_t)m * args.ldy + n_first + h * 8) =
-          *reinterpret_cast<const uint4*>(eb + (col ^ (col >> 4)) * 16 + h * 8);
-  }
-  __syncwarp();
-}
-
 // Named barrier 2 over the eight epilogue warps.
 __device__ __forceinline__ void bar_epi() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 __device__ __forceinline__ bool bar_epi_and(bool v) {
@@ -117,13 +85,19 @@ __device__ __forceinline__ Seg seg_at(const LinearArgs& a, const CtaWork& w, int
   return g;
 }
 
-template <int BN, int NSUB, int EPI>
+// PAIR: launched in clusters of 2 CTAs; the pair's even CTA issues 2-SM MMAs of 256 weight rows
+// (128 in each CTA's TMEM) over the token rows, each CTA loading its own 128 weight rows and half of
+// every MMA's token rows with completion counted on the even CTA's barriers; the MMA completions
+// are committed to both CTAs' barriers, and both CTAs' epilogues release the accumulator to the
+// even CTA.  Every CTA of a pair walks the same work list.
+template <int BN, int NSUB, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(320, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const LinearArgs args) {
-  using Cfg = LinearCfg<BN, NSUB>;
+  using Cfg = LinearCfg<BN, NSUB, PAIR>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int TN = Cfg::TN;
+  constexpr int HB = Cfg::HB;
   constexpr int NBUF = Cfg::NBUF;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,8 +115,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;                       // partial-sum slots are per CTA
-  const int wg = cta;                                // work group
+  const int wg = PAIR ? cta >> 1 : cta;             // work group: the CTA or its pair
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int half = (int)(rank & 1u);                // which 128 rows of a pair tile
+  const uint32_t leader = rank & ~1u;
   const CtaWork work = cta_work(args, wg);
+  // 128-row weight tile of work tile t (token tile t % tiles_m)
+  auto n_tile = [&](long long t) { return PAIR ? (int)(t / args.tiles_m) * 2 + half : (int)(t / args.tiles_m); };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_w);
@@ -153,13 +132,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 32 * Cfg::EPI_WARPS);
+      // (a pair: one arrival from each CTA's epilogue, on the even CTA's barrier)
+      mbar_init(&acc_empty[i], PAIR ? 2 : 32 * Cfg::EPI_WARPS);
     }
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    else tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
+  // a pair's loads complete on, and its MMAs commit to, barriers of both CTAs: all initialised first
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
@@ -169,6 +154,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 0) {
     // ---------------- TMA producer: one continuous stream over this CTA's units
     if (lane == 0) {
+      const uint32_t full_leader = PAIR ? dsmem_map(smem_u32(full), leader) : 0u;
       for (long long i = 0; i < work.n; ++i) {
         const int s = (int)(i % STAGES);
         const long long r = i / STAGES;
@@ -176,19 +162,35 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const Seg g = seg_at(args, work, wg, i);
         const int k = g.k;
         const int m_t = (int)(g.tile % args.tiles_m);
-        const int n_t = (int)(g.tile / args.tiles_m);
-        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+        const int n_t = n_tile(g.tile);
+        if constexpr (PAIR) {
+          // both CTAs' bytes count on the even CTA's barrier (which may see them before its own
+          // expect: the transaction count goes negative for a while)
+          if (half == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE_BYTES);
+          const uint32_t bar = full_leader + (uint32_t)s * 8u;
+          tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tm_w, bar, k * LIN_BK, n_t * 128);
 #pragma unroll
-        for (int sub = 0; sub < NSUB; ++sub)
-          tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_2d_pair(sB + s * Cfg::B_BYTES + sub * HB * LIN_ROW_BYTES, &tm_x, bar, k * LIN_BK,
+                             m_t * TN + sub * BN + half * HB);
+        } else {
+          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+          tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK,
+                        m_t * TN + sub * BN);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer: one TMEM accumulator per tile segment, two in flight
-    if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(128, BN);
+    // ---------------- MMA issuer (a pair's even CTA): one TMEM accumulator per tile segment, two in
+    // flight when they fit
+    if (lane == 0 && (!PAIR || half == 0)) {
+      constexpr uint32_t idesc = umma_idesc_bf16(PAIR ? 256 : 128, BN);
+      const uint32_t peer_empty = PAIR ? dsmem_map(smem_u32(empty), rank ^ 1u) : 0u;
+      const uint32_t peer_acc_full = PAIR ? dsmem_map(smem_u32(acc_full), rank ^ 1u) : 0u;
       long long i = 0;
       int seg = 0;
       bool ok = true;
@@ -208,13 +210,27 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll
           for (int kk = 0; kk < LIN_BK / 16; ++kk)
 #pragma unroll
-            for (int sub = 0; sub < NSUB; ++sub)
-              umma_bf16(d + sub * BN, umma_desc_lin(a + kk * 32), umma_desc_lin(b + sub * BN * LIN_ROW_BYTES + kk * 32),
-                        idesc, (uu > u || kk > 0) ? 1u : 0u);
-          umma_commit(&empty[s]);
+            for (int sub = 0; sub < NSUB; ++sub) {
+              const uint64_t da = umma_desc_lin(a + kk * 32);
+              const uint64_t db = umma_desc_lin(b + sub * HB * LIN_ROW_BYTES + kk * 32);
+              const uint32_t accum = (uu > u || kk > 0) ? 1u : 0u;
+              if constexpr (PAIR) umma_bf16_pair(d + sub * BN, da, db, idesc, accum);
+              else umma_bf16(d + sub * BN, da, db, idesc, accum);
+            }
+          if constexpr (PAIR) {
+            umma_commit_pair(smem_u32(&empty[s]));
+            umma_commit_pair(peer_empty + (uint32_t)s * 8u);
+          } else {
+            umma_commit(&empty[s]);
+          }
         }
         if (!ok) break;
-        umma_commit(&acc_full[acc]);
+        if constexpr (PAIR) {
+          umma_commit_pair(smem_u32(&acc_full[acc]));
+          umma_commit_pair(peer_acc_full + (uint32_t)acc * 8u);
+        } else {
+          umma_commit(&acc_full[acc]);
+        }
         u = seg_end;
       }
     }
@@ -231,6 +247,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     int seg = 0;
     bool ok = true;
     int rms_m0 = -1;       // token tile whose folded-RMSNorm scales s_rms holds
+    // hand accumulator `acc` back to the MMA issuer (a pair's: once both CTAs are done with it)
+    auto release_acc = [&](int acc) {
+      tc_fence_before();
+      if constexpr (PAIR) {
+        bar_epi();
+        if (etid == 0) {
+          if (half == 0) mbar_arrive(&acc_empty[acc]);
+          else mbar_arrive_cluster(dsmem_map(smem_u32(&acc_empty[acc]), leader));
+        }
+      } else {
+        mbar_arrive(&acc_empty[acc]);
+      }
+    };
     for (long long u = 0; u < work.n; ++seg) {
       const Seg g = seg_at(args, work, wg, u);
       const long long tile = g.tile;
@@ -238,18 +267,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       const bool whole = g.whole;
       const int acc = seg % NBUF;
       const int m0 = (int)(tile % args.tiles_m) * TN;
-      const int n_t = (int)(tile / args.tiles_m);
+      const int n_t = n_tile(tile);
+      const bool live = n_t < args.tiles_n;   // (the odd half of a pair's last tile may lie past N)
       const int n0 = n_t * 128;
       const int n = n0 + row;
-      if constexpr (EPI == EPI_LOGITS) {
-        // folded final RMSNorm: the scale of every token row of this tile, before waiting for its
-        // accumulator (so the first tile's overlaps the main loop); recomputed only when the token
-        // tile changes (the LM head has one token tile up to 384 rows)
-        if (args.norm_ssq && m0 != rms_m0) {
-          fill_row_scales(args, s_rms, m0, TN, etid, 32 * Cfg::EPI_WARPS);
-          bar_epi();
-          rms_m0 = m0;
-        }
+      // folded RMSNorm of X: the scale of every token row of this tile, before waiting for its
+      // accumulator (so the first tile's overlaps the main loop); recomputed only when the token
+      // tile changes (one token tile up to 384 rows)
+      if (args.norm_ssq && m0 != rms_m0) {
+        fill_row_scales(args, s_rms, m0, TN, etid, 32 * Cfg::EPI_WARPS);
+        bar_epi();
+        rms_m0 = m0;
       }
       ok = ok && mbar_wait(&acc_full[acc], (uint32_t)((seg / NBUF) & 1), args.status, 0x104u);
       ok = bar_epi_and(ok);
@@ -273,14 +301,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         else if (cols == 48) tmem_ld_cols<48>(t_row + c64, v64);
         else if (cols == 32) tmem_ld_cols<32>(t_row + c64, v64);
         else tmem_ld_cols<16>(t_row + c64, v64);
+        if (args.norm_ssq) {
+          // row scales of the folded RMSNorm (linear: a split tile's pieces are scaled alike)
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k < cols) v64[k] *= s_rms[c64 + k];
+        }
         if constexpr (EPI == EPI_SWIGLU) {
           if (whole) {
-            // (columns past `cols` are never stored; give them defined values)
+            if (live) {
+              // (columns past `cols` are never stored; give them defined values)
 #pragma unroll
-            for (int k = 16; k < 64; ++k)
-              if (k >= cols) v64[k] = 0.f;
-            swiglu_chunk32(v64, cols, ebuf, lane, args, m0 + c64, n_t * 64 + q * 16);
-            if (cols > 32) swiglu_chunk32(v64 + 32, cols - 32, ebuf, lane, args, m0 + c64 + 32, n_t * 64 + q * 16);
+              for (int k = 16; k < 64; ++k)
+                if (k >= cols) v64[k] = 0.f;
+              swiglu_chunk32(v64, cols, ebuf, lane, args, m0 + c64, n_t * 64 + q * 16);
+              if (cols > 32)
+                swiglu_chunk32(v64 + 32, cols - 32, ebuf, lane, args, m0 + c64 + 32, n_t * 64 + q * 16);
+            }
             continue;
           }
         }
@@ -336,66 +373,78 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           __syncwarp();
         }
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[acc]);
+        release_acc(acc);
       } else {
         // LM-head epilogues (ranges are tile-aligned, so every segment is whole): per token column
-        // reduce over the tile's 128 vocabulary rows.  Each 16-column TMEM load goes through the
-        // warp's transpose block, so lanes 2j and 2j + 1 scan column j's 32 rows (16 each) and meet
-        // in one shuffle: two shuffles per 16 columns instead of five per column per reduction
-        // (the butterfly version took 22 us per 192-column tile, 40 us per 384-column tile).
+        // reduce over the tile's 128 vocabulary rows.  Each 16-column block goes through the warp's
+        // transpose block, so lanes 2j and 2j + 1 scan column j's 32 rows (16 each) and meet in one
+        // shuffle: two shuffles per 16 columns instead of five per column per reduction (the
+        // butterfly version took 22 us per 192-column tile, 40 us per 384-column tile).
         float* eb = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
         const int jc = lane >> 1, r0 = (lane & 1) * 16;
         const int nr = n0 + q * 32 + r0;        // vocabulary row of this lane's first scanned entry
 
+        // TMEM is read 32 columns per wait (16 at the tail: the halves are multiples of 16); each
+        // lane's 16 scanned values are reduced as trees (max, then sum of exponentials), which
+        // keeps the dependent chains short
 #pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 16) {
-          float v[16];
-          tmem_ld16(t_row + c, v);
-          if constexpr (EPI == EPI_LOGITS) {
+        for (int c32 = c_begin; c32 < c_end; c32 += 32) {
+          const int cols = c_end - c32 < 32 ? c_end - c32 : 32;
+          float v[32];
+          if (cols == 32) tmem_ld_cols<32>(t_row + c32, v);
+          else tmem_ld_cols<16>(t_row + c32, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float z = v[j] * (args.norm_ssq ? args.inv_temp * s_rms[c + j] : args.inv_temp);
-              const int m = m0 + c + j;
-              if (m < args.M && n < args.N) args.P[(size_t)m * args.ldp + n] = z;
-              eb[j * 33 + lane] = z;
+          for (int h = 0; h < 32; h += 16) {
+            if (h >= cols) break;
+            const int c = c32 + h;
+            if constexpr (EPI == EPI_LOGITS) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float z = v[h + j] * (args.norm_ssq ? args.inv_temp * s_rms[c + j] : args.inv_temp);
+                const int m = m0 + c + j;
+                if (m < args.M && n < args.N) args.P[(size_t)m * args.ldp + n] = z;
+                eb[j * 33 + lane] = z;
+              }
+              __syncwarp();
+              float zz[16], t8[8];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) zz[i] = nr + i < args.N ? eb[jc * 33 + r0 + i] : -INFINITY;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t8[i] = fmaxf(zz[2 * i], zz[2 * i + 1]);
+              float mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+#pragma unroll
+              for (int i = 0; i < 16; ++i) zz[i] = nr + i < args.N ? exp_sm(zz[i] - mx) : 0.f;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t8[i] = zz[2 * i] + zz[2 * i + 1];
+              float sm = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
+              sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+              if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) eb[j * 33 + lane] = v[h + j];
+              __syncwarp();
+              float zv = -INFINITY;
+              int idx = 0x7fffffff;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {          // strict > keeps the lowest row on ties
+                const float z = eb[jc * 33 + r0 + i];
+                if (nr + i < args.N && (z > zv || idx == 0x7fffffff)) { zv = z; idx = nr + i; }
+              }
+              const float ov = __shfl_xor_sync(0xffffffffu, zv, 1);
+              const int oi = __shfl_xor_sync(0xffffffffu, idx, 1);
+              if (ov > zv || (ov == zv && oi < idx)) { zv = ov; idx = oi; }
+              if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(zv, __int_as_float(idx));
             }
-            __syncwarp();
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (nr + i < args.N) mx = fmaxf(mx, eb[jc * 33 + r0 + i]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            float sm = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (nr + i < args.N) sm += exp_sm(eb[jc * 33 + r0 + i] - mx);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-            if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) eb[j * 33 + lane] = v[j];
-            __syncwarp();
-            float zv = -INFINITY;
-            int idx = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {          // strict > keeps the lowest row on ties
-              const float z = eb[jc * 33 + r0 + i];
-              if (nr + i < args.N && (z > zv || idx == 0x7fffffff)) { zv = z; idx = nr + i; }
-            }
-            const float ov = __shfl_xor_sync(0xffffffffu, zv, 1);
-            const int oi = __shfl_xor_sync(0xffffffffu, idx, 1);
-            if (ov > zv || (ov == zv && oi < idx)) { zv = ov; idx = oi; }
-            if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(zv, __int_as_float(idx));
+            __syncwarp();                          // eb is rewritten by the next block
           }
-          __syncwarp();                          // eb is rewritten by the next block
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[acc]);
+        release_acc(acc);
         bar_epi();
         for (int j = etid; j < TN; j += 32 * Cfg::EPI_WARPS) {
           const int m = m0 + j;
-          if (m >= args.M) continue;
+          if (m >= args.M || !live) continue;
           float2 accv = red[j];
           for (int w = 1; w < 4; ++w) {
             const float2 o = red[w * TN + j];
@@ -419,18 +468,28 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  if constexpr (PAIR) {
+    // the peer may still arrive on this CTA's barriers (or this one on the peer's) until both
+    // are here
+    cluster_sync_all();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
+    }
+  } else {
+    if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
 }
 
 // Host side: one instantiation's launch.
-template <int BN, int NSUB, int EPI>
+template <int BN, int NSUB, int EPI, bool PAIR = false>
 static bool linear_tc_configure() {
   static bool configured[64] = {};   // per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && configured[dev]) return true;
-  if (cudaFuncSetAttribute(linear_tc_kernel<BN, NSUB, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           LinearCfg<BN, NSUB>::SMEM_BYTES) != cudaSuccess)
+  if (cudaFuncSetAttribute(linear_tc_kernel<BN, NSUB, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           LinearCfg<BN, NSUB, PAIR>::SMEM_BYTES) != cudaSuccess)
     return false;
   if (dev >= 0 && dev < 64) configured[dev] = true;
   return true;
@@ -445,5 +504,41 @@ static cudaError_t launch_linear_tc_one(const CUtensorMap& tw, const CUtensorMap
                            tw, tx, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+// The pair build: `pairs` clusters of 2 CTAs, and how many pairs can be resident at once.
+template <int BN, int NSUB, int EPI>
+struct LinearTcPair {
+  using Cfg = LinearCfg<BN, NSUB, true>;
+  static cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a, int pairs,
+                            cudaStream_t st) {
+    if (!linear_tc_configure<BN, NSUB, EPI, true>()) return cudaGetLastError();
+    cudaError_t e = launch_kc(linear_tc_kernel<BN, NSUB, EPI, true>, dim3(2 * pairs), dim3(Cfg::THREADS),
+                              Cfg::SMEM_BYTES, st, 2, tw, tx, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  static int capacity() {
+    if (!linear_tc_configure<BN, NSUB, EPI, true>()) {
+      cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * 64);
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)linear_tc_kernel<BN, NSUB, EPI, true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  }
+};
 
 }  // namespace spec

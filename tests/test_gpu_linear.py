@@ -249,20 +249,23 @@ def test_linear_swiglu_persistent(lib, grid):
 
 @pytest.mark.parametrize("M,N,K", [(368, 24576, 4096), (200, 20480, 136), (300, 19584, 520)])
 def test_linear_whole_tiles_then_cluster_remainder(lib, M, N, K):
-    """More weight tiles than SMs (not a multiple): whole tiles on the persistent kernel, the
-    rest on the cluster split-K kernel (two launches, no workspace); stream-K as the control."""
+    """More weight tiles than SMs (not a multiple), one-SM tiles (pairs off): whole tiles on the
+    persistent kernel, the rest on the cluster split-K kernel (two launches, no workspace);
+    stream-K as the control."""
     X = bf16_dev(synth.normal_bf16_bits(M + 1, (M, K), 1.0))
     W = bf16_dev(synth.normal_bf16_bits(M + 2, (N, K), 0.02))
     R = bf16_dev(synth.normal_bf16_bits(M + 3, (M, N), 1.0))
-    assert lib.spec_linear_workspace_bytes(M, N, K) == 0
-    lib.reset_launch_count()
-    Y = lib.spec_verify_linear(X, W, residual=R)
-    assert lib.launch_count() == 2
-    lib.spec_set_option("linear_cluster", 0)
+    lib.spec_set_option("linear_pair", 0)
     try:
+        assert lib.spec_linear_workspace_bytes(M, N, K) == 0
+        lib.reset_launch_count()
+        Y = lib.spec_verify_linear(X, W, residual=R)
+        assert lib.launch_count() == 2
+        lib.spec_set_option("linear_cluster", 0)
         Y2 = lib.spec_verify_linear(X, W, residual=R)
     finally:
         lib.spec_set_option("linear_cluster", 1)
+        lib.spec_set_option("linear_pair", 1)
     lib.spec_device_status()
     rows = np.r_[0:4, M - 4:M]
     ref = oops.linear(obf.decode(bits_of(X))[rows], obf.decode(bits_of(W)), obf.decode(bits_of(R))[rows])

@@ -13,12 +13,14 @@ from gpu_util import assert_close_chain, assert_close_rel, bf16_dev, bits_of, de
 pytestmark = pytest.mark.gpu
 
 
-# pairs for every product with 64+ token rows (split-K on pairs for few tiles), or the default:
-# pairs only for products with more 128-row tiles than SMs (whole pair tiles, then the rest split)
+# pairs for every product with 64+ token rows (split-K on pairs for few tiles), or pairs only for
+# products with more 128-row tiles than SMs (whole pair tiles, then the rest split); the persistent
+# pair kernel (an option for the latter) is off here: its own tests cover it
 @pytest.fixture(params=[1, 0], ids=["pairs-everywhere", "many-tiles"])
 def pair(lib, request):
     lib.spec_set_option("linear_pair", 1)
     lib.spec_set_option("linear_pair_few", request.param)
+    lib.spec_set_option("linear_pair_persistent", 0)
     yield lib
     lib.spec_set_option("linear_pair_few", 0)
 
