@@ -168,7 +168,12 @@ SPEC_API int spec_verify_linear(const spec_bf16* X, int M, int K, int ldx,
  * SPEC_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library
  * holds until the process exits.  Calls whose K split needs more scratch than
  * that return SPEC_EUNSUPPORTED and launch nothing (use spec_verify_linear with
- * a workspace instead; small verify passes need none or a few MiB).
+ * a workspace instead; small verify passes need none or a few MiB).  Where a
+ * shape has several plans, the first one whose scratch fits in the array is
+ * taken (the optional persistent pair plan's stream-K pieces, "linear_pair_
+ * persistent" 1, do not fit at a few hundred rows), so the plan, and the
+ * rounding of the result, can differ from spec_verify_linear's under the same
+ * options.
  * The first call in each CUDA context looks up the array's device address
  * (cudaGetSymbolAddress) and caches it for that context (a device reset gives
  * a new context, so the next call looks it up again); make that first call
