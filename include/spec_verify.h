@@ -89,12 +89,7 @@ SPEC_API int spec_version(void);
  * "attention_impl" (1 = tcgen05 kernel, default; 0 = mma.sync kernel);
  * "attention_pair_cost" (0..64, default 12): work the tcgen05 attention kernel
  * charges for starting a (sequence, kv head) pair, in quarters of a 128-key
- * tile, when it splits the key tiles evenly between CTAs; "attention_dynamic"
- * (1 default, 0 off): with a contiguous cache, at least two (sequence, kv
- * head) pairs per CTA and no pair longer than a CTA's share of the key tiles,
- * the tcgen05 kernel instead lets each CTA claim whole pairs from a counter,
- * longest first (a CTA on a slower SM claims fewer; every pair is computed by
- * one CTA, so the results do not depend on the claims);
+ * tile, when it splits the key tiles evenly between CTAs;
  * "linear_nsub" (2, default: one tensor-core tile covers up to 384 rows; 1: up
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster

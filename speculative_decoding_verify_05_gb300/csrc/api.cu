@@ -179,7 +179,6 @@ constexpr size_t kMaxCounters = kCounterBytes / 4;
 // --------------------------------------------------------------------------- linear plan
 int g_gemv_max_m = 0;    // tunable: largest M that takes the CUDA-core path (0: tensor cores for every M)
 int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
-int g_attn_dynamic = 1;  // tunable: 1 lets the tcgen05 kernel claim whole pairs dynamically, longest first
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
@@ -535,11 +534,6 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "attention_pair_cost")) {
     if (value < 0 || value > 64) return fail(SPEC_EINVAL, "attention_pair_cost must be in [0, 64]");
     g_attn_pair_cost = value;
-    return ok();
-  }
-  if (!strcmp(name, "attention_dynamic")) {
-    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "attention_dynamic must be 0 or 1");
-    g_attn_dynamic = value;
     return ok();
   }
   if (!strcmp(name, "attention_impl")) {
@@ -1547,8 +1541,6 @@ static int verify_attention_impl(const spec_bf16* Q, int ldq, const spec_bf16* K
   a.chunk = p.chunk; a.max_chunks = p.max_chunks;
   a.partial = reinterpret_cast<float*>(ws + p.partial_off);
   a.counters = reinterpret_cast<unsigned*>(ws + p.counters_off);
-  // the dynamic schedule's two counters sit at the end of the counter region (past every pair's)
-  a.claim = (p.tc && g_attn_dynamic && (size_t)B * Hkv + 2 <= kMaxCounters) ? a.counters + (kMaxCounters - 2) : nullptr;
   a.status = d->status;
   a.pair_cost = g_attn_pair_cost;
   a.block_table = block_table;

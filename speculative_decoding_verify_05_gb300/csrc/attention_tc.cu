@@ -3,20 +3,12 @@
 // Work: for every (sequence b, kv head h) the R = G * (gamma_b + 1) <= 64 query
 // rows of the group attend keys 0 .. ctx_b + gamma_b under the causal rule
 // "row j sees keys <= ctx_b + j / G".  The keys of all (b, h) pairs are cut
-// into 128-key tiles and concatenated (b-major, then h).  Two schedules:
-//  - static: one CTA per SM takes an equal contiguous range of tiles, so every
-//    SM streams the same number of K/V bytes whatever the context lengths.  A
-//    range covers whole (b, h) pairs and at most two partial ones; a partial
-//    pair's unnormalised output (O, running max, running sum) goes to the
-//    workspace and the CTA that arrives last on the pair's counter merges the
-//    pieces in CTA order (no waiting);
-//  - dynamic (many pairs, none longer than an SM's share): whole pairs are
-//    claimed one at a time from a global counter, longest first (sequences
-//    ordered by tile count, every CTA computing the same order), so an SM that
-//    streams slower simply claims fewer pairs.  Each pair is computed by one
-//    CTA in tile order, so results do not depend on which CTA took it.  The
-//    K producer claims; a small ring in shared memory hands the claimed pair
-//    ids to the other roles.
+// into 128-key tiles and concatenated (b-major, then h); one CTA per SM takes
+// an equal contiguous range of tiles, so every SM streams the same number of
+// K/V bytes whatever the context lengths.  A range covers whole (b, h) pairs
+// and at most two partial ones; a partial pair's unnormalised output (O,
+// running max, running sum) goes to the workspace and the CTA that arrives
+// last on the pair's counter merges the pieces in CTA order (no waiting).
 //
 // Per tile:
 //   S[row, key] = Q . K_tile^T     tcgen05.mma M = 64 rows, N = 128 keys, K = 128 dims
@@ -59,15 +51,7 @@ constexpr int OFF_P = OFF_Q + 2 * 2 * Q_HALF;       // [64 rows][128 keys] as tw
 constexpr int OFF_META = OFF_P + 2 * Q_HALF;        // unit prefix, ctx, cu_rows per sequence
 constexpr int OFF_BAR = OFF_META + 3 * META_N * 4;
 constexpr int OFF_FLAG = OFF_BAR + 256;
-// dynamic schedule: ring of claimed pair ids (NQ slots, full / empty barriers), the sequence order
-constexpr int NQ = 16;
-constexpr int DYN_MAX_B = 256;                      // sequences the dynamic schedule orders
-constexpr int OFF_DYN = OFF_FLAG + 16;
-constexpr int OFF_IDS = OFF_DYN + 2 * NQ * 8;
-constexpr int OFF_ORDER = OFF_IDS + NQ * 4;
-constexpr int SMEM = OFF_ORDER + DYN_MAX_B * 4 + 16 + 1024;   // + alignment slack
-// id ring consumers: the V producer, the Q warp, the MMA issuer's two cursors, the softmax warps
-constexpr int ID_CONSUMERS = 5;
+constexpr int SMEM = OFF_FLAG + 16 + 1024;          // + alignment slack
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 // Non-blocking probe of an mbarrier phase (the event-driven MMA loop polls several barriers).
@@ -198,12 +182,6 @@ __device__ __forceinline__ long long pair_first(const Meta& m, int Hkv, int p, i
   nt = (m.ctx[b] + m.cu[b + 1] - m.cu[b] + KT - 1) / KT;
   return m.pfx[b] + (long long)h * nt;
 }
-// The units [sb, se) of pair p.
-__device__ __forceinline__ void pair_units(const Meta& m, int Hkv, int p, long long& sb, long long& se) {
-  int nt;
-  sb = pair_first(m, Hkv, p, nt);
-  se = sb + nt;
-}
 // first unit owned by CTA c (U for c >= grid): the smallest u with C(u) >= T(c)
 __device__ long long range_start(const Part& q, const Meta& m, int c) {
   if (c <= 0 || q.U == 0) return 0;
@@ -332,13 +310,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* q_empty = bars + 25;       // [2]    last QK^T of a pair done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
   unsigned* last_flag = reinterpret_cast<unsigned*>(smem + OFF_FLAG);
-  unsigned* s_dyn = last_flag + 1;                                 // 1: dynamic schedule
-  int* s_cur_id = reinterpret_cast<int*>(last_flag + 2);           // [2] softmax warps' pair id
   long long* s_range = reinterpret_cast<long long*>(bars + 28);   // this CTA's [ub, ue)
-  uint64_t* id_full = reinterpret_cast<uint64_t*>(smem + OFF_DYN);  // [NQ] claimed pair id published
-  uint64_t* id_empty = id_full + NQ;                               // [NQ] every consumer has read it
-  int* s_ids = reinterpret_cast<int*>(smem + OFF_IDS);             // [NQ] pair id, -1: no pair left
-  int* s_order = reinterpret_cast<int*>(smem + OFF_ORDER);         // [B] sequences, most tiles first
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv, G = a.G;
@@ -364,10 +336,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     mbar_init(p_full, 128);
     mbar_init(pv_done, 1);
-    for (int i = 0; i < NQ; ++i) {
-      mbar_init(&id_full[i], 1);
-      mbar_init(&id_empty[i], ID_CONSUMERS);
-    }
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -382,7 +350,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   }
   __syncthreads();
   if (warp == 0) {
-    int carry = 0, nt_max = 0;
+    int carry = 0;
     bool bad = false;
     for (int base = 0; base < B; base += 32) {
       const int b = base + lane;
@@ -393,7 +361,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int cap_keys = a.block_table ? a.max_pages * KT : a.cap;
         bad |= (mb <= 0 || mb > a.max_rows || ctx < 0 || ctx + mb > cap_keys || G * mb > QR);
         units = (mb > 0 && ctx >= 0) ? (ctx + mb + KT - 1) / KT * Hkv : 0;
-        nt_max = max(nt_max, units / Hkv);
       }
       int incl = units;
 #pragma unroll
@@ -405,8 +372,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     bad = __any_sync(0xffffffffu, bad);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nt_max = max(nt_max, __shfl_xor_sync(0xffffffffu, nt_max, o));
     if (lane == 0) {
       s_pfx[B] = bad ? 0 : carry;          // nothing to do when the ragged arrays are invalid
       if (bad && blockIdx.x == 0) set_status(a.status, 0x2F1u);
@@ -417,23 +382,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const Part q{U, WT * U + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
       s_range[0] = range_start(q, meta, blockIdx.x);
       s_range[1] = range_start(q, meta, blockIdx.x + 1);
-      // dynamic schedule when allowed, for a contiguous cache, with at least two pairs per CTA and
-      // no pair longer than a CTA's share of the tiles (so the longest-first claims even out)
-      *s_dyn = (a.claim != nullptr && a.block_table == nullptr && !bad && B <= DYN_MAX_B &&
-                (long long)B * Hkv >= 2LL * gridDim.x && (long long)nt_max * gridDim.x <= U) ? 1u : 0u;
-    }
-  }
-  __syncthreads();
-  if (*s_dyn) {
-    // sequences by decreasing tile count, ties by index (the same order in every CTA)
-    for (int b = tid; b < B; b += THREADS) {
-      const int nb = (s_ctx[b] + s_cu[b + 1] - s_cu[b] + KT - 1) / KT;
-      int rank = 0;
-      for (int b2 = 0; b2 < B; ++b2) {
-        const int n2 = (s_ctx[b2] + s_cu[b2 + 1] - s_cu[b2] + KT - 1) / KT;
-        rank += (n2 > nb || (n2 == nb && b2 < b)) ? 1 : 0;
-      }
-      s_order[rank] = b;
     }
   }
   tc_fence_before();
@@ -444,40 +392,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const Part part{total, WT * total + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
   const long long ub = s_range[0], ue = s_range[1];
   const long long n_units = ue - ub;
-  const bool dyn = *s_dyn != 0u;
-  const int n_pairs = B * Hkv;
-  // Segments of units a role walks in turn: static, this CTA's range [ub, ue) (segment 0 only);
-  // dynamic, the pairs this CTA claimed, in claim order.  take_id: the pair id of claim k from the
-  // ring for one thread of a consumer role (once per role and claim): -1 none left (or a wait that
-  // ran out), -2 not published yet (poll only).
-  auto take_id = [&](int k, bool poll) -> int {
-    const int slot = k % NQ;
-    const uint32_t par = (uint32_t)((k / NQ) & 1);
-    int pid = -1;
-    if (poll) {
-      if (!mbar_test(&id_full[slot], par)) return -2;
-      pid = s_ids[slot];
-    } else if (mbar_wait(&id_full[slot], par, a.status, 0x240u)) {
-      pid = s_ids[slot];
-    }
-    mbar_arrive(&id_empty[slot]);
-    return pid;
-  };
-  auto segment = [&](int k, int pid, long long& sb, long long& se) -> bool {
-    if (!dyn) {
-      sb = ub;
-      se = ue;
-      return k == 0 && n_units > 0;
-    }
-    if (pid < 0) return false;
-    pair_units(meta, Hkv, pid, sb, se);
-    return true;
-  };
 
   if (warp == 4 || warp == 6) {
-    // ------------------------------------------------------------ TMA producers: K and V (the K
-    // producer also claims the pairs of the dynamic schedule and publishes them on the id ring)
-    if (lane == 0 && (dyn || n_units > 0)) {
+    // ------------------------------------------------------------ TMA producers: K and V
+    if (lane == 0 && n_units > 0) {
       const bool is_k = warp == 4;
       const int nst = is_k ? ST_K : ST_V;
       const CUtensorMap* tm = is_k ? &tmK : &tmV;
@@ -485,72 +403,42 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint64_t* land = is_k ? k_land : v_land;
       uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
-      const bool paged = a.block_table != nullptr;   // (static schedule only)
-      long long i = 0;                               // units issued: the ring position
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        int pid = -1;
-        if (dyn && is_k) {
-          // claim the next pair, longest first; the CTA that finds none left last resets the counters
-          const unsigned pos = atomicAdd(&a.claim[0], 1u);
-          if (pos < (unsigned)n_pairs) {
-            pid = s_order[pos / Hkv] * Hkv + (int)(pos % Hkv);
-          } else {
-            __threadfence();
-            if (atomicAdd(&a.claim[1], 1u) == gridDim.x - 1) {
-              a.claim[0] = 0u;
-              a.claim[1] = 0u;
-            }
+      Cursor c = cur_at(meta, B, ub);
+      // paged cache: the block-table entries are read PF units ahead of the loads that use them
+      // (a second cursor), so a page lookup's latency never sits in front of a TMA issue
+      constexpr int PF = 4;
+      int pq[PF] = {0, 0, 0, 0};
+      Cursor ca = c;
+      const bool paged = a.block_table != nullptr;
+      if (paged) {
+#pragma unroll
+        for (int j = 0; j < PF; ++j)
+          if (j < n_units) {
+            if (j > 0) cur_next(ca, meta, B, Hkv);
+            pq[j] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
           }
-          const int slot = k % NQ;
-          if (k >= NQ && !mbar_wait(&id_empty[slot], (uint32_t)(((k / NQ) - 1) & 1), a.status, 0x241u))
-            pid = -1;
-          s_ids[slot] = pid;
-          mbar_arrive(&id_full[slot]);
-        } else if (dyn) {
-          pid = take_id(k, false);
-        }
-        long long sb, se;
-        if (!segment(k, pid, sb, se)) break;
-        const long long n_seg = se - sb;
-        Cursor c = cur_at(meta, B, sb);
-        // paged cache: the block-table entries are read PF units ahead of the loads that use them
-        // (a second cursor), so a page lookup's latency never sits in front of a TMA issue
-        constexpr int PF = 4;
-        int pq[PF] = {0, 0, 0, 0};
-        Cursor ca = c;
+      }
+      for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
+        const int s = (int)(i % nst);
+        const int key0 = c.t * KT;
+        const int page = pq[0];
         if (paged) {
 #pragma unroll
-          for (int j = 0; j < PF; ++j)
-            if (j < n_seg) {
-              if (j > 0) cur_next(ca, meta, B, Hkv);
-              pq[j] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
-            }
-        }
-        for (long long j = 0; j < n_seg; ++j, ++i, cur_next(c, meta, B, Hkv)) {
-          const int s = (int)(i % nst);
-          const int key0 = c.t * KT;
-          const int page = pq[0];
-          if (paged) {
-#pragma unroll
-            for (int jj = 0; jj + 1 < PF; ++jj) pq[jj] = pq[jj + 1];
-            if (j + PF < n_seg) {
-              cur_next(ca, meta, B, Hkv);
-              pq[PF - 1] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
-            }
+          for (int j = 0; j + 1 < PF; ++j) pq[j] = pq[j + 1];
+          if (i + PF < n_units) {
+            cur_next(ca, meta, B, Hkv);
+            pq[PF - 1] = a.block_table[(size_t)ca.b * a.max_pages + ca.t];
           }
-          if (i >= nst &&
-              !mbar_wait(&empty[s], (uint32_t)(((i / nst) - 1) & 1), a.status, is_k ? 0x211u : 0x212u)) {
-            ok = false;
-            break;
-          }
-          uint64_t* bar = (key0 + KT > c.ctx) ? &land[s] : &full[s];
-          uint8_t* st = ring + s * KV_TILE;
-          const KvTile kt = paged ? kv_tile_page(a, page, c.h) : kv_tile(a, c.b, c.h, c.t);
-          mbar_arrive_expect_tx(bar, KV_TILE);
-          tma_load_3d(st, tm, bar, 0, kt.y, kt.z);
-          tma_load_3d(st + KV_HALF, tm, bar, 64, kt.y, kt.z);
         }
+        if (i >= nst &&
+            !mbar_wait(&empty[s], (uint32_t)(((i / nst) - 1) & 1), a.status, is_k ? 0x211u : 0x212u))
+          break;
+        uint64_t* bar = (key0 + KT > c.ctx) ? &land[s] : &full[s];
+        uint8_t* st = ring + s * KV_TILE;
+        const KvTile kt = paged ? kv_tile_page(a, page, c.h) : kv_tile(a, c.b, c.h, c.t);
+        mbar_arrive_expect_tx(bar, KV_TILE);
+        tma_load_3d(st, tm, bar, 0, kt.y, kt.z);
+        tma_load_3d(st + KV_HALF, tm, bar, 64, kt.y, kt.z);
       }
     }
     __syncwarp();
@@ -559,18 +447,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     bool ok = true;
     int piece = -1;
     int n_land_k[ST_K] = {0, 0};
-    long long i = 0;                          // units walked: the K ring position
-    for (int kq = 0; ok; ++kq) {
-      int pid = -1;
-      if (dyn) {
-        if (lane == 0) pid = take_id(kq, false);
-        pid = __shfl_sync(0xffffffffu, pid, 0);
-      }
-      long long sb, se;
-      if (!segment(kq, pid, sb, se)) break;
-      Cursor c = cur_at(meta, B, sb);
-    for (long long u = sb; u < se && ok; ++u, ++i, cur_next(c, meta, B, Hkv)) {
-      if (c.u == sb || c.t == 0) {
+    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
+    for (long long i = 0; i < n_units && ok; ++i, cur_next(c, meta, B, Hkv)) {
+      if (c.u == ub || c.t == 0) {
         // a new pair: its Q rows (row j = token row j / G, head j % G), zero-padded to 64,
         // loaded into registers first, stored once QK^T of the pair two back is done
         ++piece;
@@ -613,45 +492,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (lane == 0) mbar_arrive(&k_full[sk]);
       }
     }
-    }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer (event driven)
-    if (lane == 0 && (dyn || n_units > 0)) {
+    if (lane == 0 && n_units > 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(QR, KT);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(QR, D) | (1u << 16);   // B (V) MN-major
-      // the QK^T cursor cs walks segment [s_sb, s_se), the PV cursor cp segment [p_sb, p_se); each
-      // takes its segments in turn, polling the id ring in the dynamic schedule (never blocking)
-      Cursor cs{}, cp{};
-      long long s_sb = 0, s_se = 0, p_sb = 0, p_se = 0;
-      int ks = 0, kp = 0;                // segments taken by each cursor
-      bool s_have = false, p_have = false, s_end = false, p_end = false;
-      // 1: segment taken, 0: not published yet, -1: none left
-      auto take = [&](int& kk, long long& sb, long long& se) -> int {
-        int pid = -1;
-        if (dyn) {
-          pid = take_id(kk, true);
-          if (pid == -2) return 0;
-        }
-        const bool got = segment(kk, pid, sb, se);
-        ++kk;
-        return got ? 1 : -1;
-      };
+      Cursor cs = cur_at(meta, B, ub), cp = cs;
       long long ns = 0, np = 0;          // next QK^T, next PV
       int piece_s = -1, piece_p = -1;
       uint32_t spin = 0;
       uint64_t t0 = 0;
-      while (!p_end) {
+      while (np < n_units) {
         bool did = false;
-        if (!s_have && !s_end) {
-          const int r = take(ks, s_sb, s_se);
-          if (r > 0) cs = cur_at(meta, B, s_sb);
-          s_have = r > 0;
-          s_end = r < 0;
-          did = r != 0;
-        }
-        if (s_have) {
-          const bool first = (cs.u == s_sb || cs.t == 0);
-          const bool last = (cs.u + 1 == s_se) || (cs.t + 1 == cs.nt);
+        if (ns < n_units) {
+          const bool first = (cs.u == ub || cs.t == 0);
+          const bool last = (cs.u + 1 == ue) || (cs.t + 1 == cs.nt);
           const int pc = first ? piece_s + 1 : piece_s;
           const int qb = pc & 1, s = (int)(ns % ST_K);
           if ((!first || mbar_test(&q_full[qb], (uint32_t)((pc >> 1) & 1))) &&
@@ -673,19 +528,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (last) umma_commit(&q_empty[qb]);
             ++ns;
             cur_next(cs, meta, B, Hkv);
-            if (cs.u == s_se) s_have = false;
             did = true;
           }
         }
-        if (!p_have && !p_end) {
-          const int r = take(kp, p_sb, p_se);
-          if (r > 0) cp = cur_at(meta, B, p_sb);
-          p_have = r > 0;
-          p_end = r < 0;
-          did = did || r != 0;
-        }
-        if (p_have && np < ns) {
-          const bool first = (cp.u == p_sb || cp.t == 0);
+        if (np < ns) {
+          const bool first = (cp.u == ub || cp.t == 0);
           const int pc = first ? piece_p + 1 : piece_p;
           const int ob = pc & 1, s = (int)(np % ST_V);
           if (mbar_test(p_full, (uint32_t)(np & 1)) &&
@@ -707,7 +554,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             umma_commit(pv_done);
             ++np;
             cur_next(cp, meta, B, Hkv);
-            if (cp.u == p_se) p_have = false;
             did = true;
           }
         }
@@ -737,25 +583,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     bool ok = true;
     int piece = -1;
     int n_land_v[ST_V] = {0, 0, 0};
-    long long i = 0;                          // units walked: the S / V ring position
-    for (int kw = 0;; ++kw) {
-      int pid = -1;
-      if (dyn) {
-        // one reader for the four warps (the named barriers below stay matched): thread 0 takes the
-        // id, the others read it after the barrier (two slots: the next write follows a barrier
-        // that every reader of this one has passed)
-        if (tid == 0) s_cur_id[kw & 1] = take_id(kw, false);
-        bar_compute();
-        pid = s_cur_id[kw & 1];
-      }
-      long long sb, se;
-      if (!segment(kw, pid, sb, se)) break;
-      Cursor c = cur_at(meta, B, sb);
-    for (long long uu = sb; uu < se; ++uu, ++i, cur_next(c, meta, B, Hkv)) {
+    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
+    for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
       const long long u = c.u;
       const int R = G * c.Mb;
-      const bool first = (u == sb || c.t == 0);
-      const bool last = (u + 1 == se) || (c.t + 1 == c.nt);
+      const bool first = (u == ub || c.t == 0);
+      const bool last = (u + 1 == ue) || (c.t + 1 == c.nt);
       if (first) {
         ++piece;
         m_run = -INFINITY;
@@ -860,14 +693,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const int bh = c.b * Hkv + c.h;
       const long long pair0 = u - c.t;
       const long long pair_last = pair0 + c.nt - 1;
-      const bool complete = (pair0 >= sb) && (u == pair_last);
+      const bool complete = (pair0 >= ub) && (u == pair_last);
       if (row < R) {
         if (complete) {
           const int tr = row / G, g = row - tr * G;
           store_half_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D + half * 64, ov, 1.f / l_run);
         } else {
           // slot 0: the piece that opens this CTA's range; slot 1: the piece that closes it
-          const int slot = (pair0 < sb) ? 0 : 1;
+          const int slot = (pair0 < ub) ? 0 : 1;
           float* pb = a.partial + ((size_t)blockIdx.x * 2 + slot) * (QR * (D + 2));
 #pragma unroll
           for (int d = 0; d < 64; d += 4)
@@ -881,7 +714,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       __threadfence();
       bar_compute();
       if (tid == 0) {
-        const long long piece_first = pair0 > sb ? pair0 : sb;
+        const long long piece_first = pair0 > ub ? pair0 : ub;
         const unsigned add = (unsigned)(u - piece_first + 1);
         const unsigned prev = atomicAdd(&a.counters[bh], add);
         *last_flag = (prev + add == (unsigned)c.nt) ? 1u : 0u;
@@ -933,7 +766,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         store_half_bf16(a.O + (size_t)(c.r0 + tr) * a.ldo + (size_t)(c.h * G + g) * D + half * 64, acc, 1.f / L);
       }
       if (tid == 0) a.counters[bh] = 0u;
-    }
     }
   }
   tc_fence_before();

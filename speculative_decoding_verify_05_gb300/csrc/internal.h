@@ -168,8 +168,6 @@ struct AttnArgs {
   int max_chunks;
   float* partial;       // [B*Hkv][max_chunks][64][128 + 2]
   unsigned* counters;   // [B*Hkv]
-  unsigned* claim;      // tcgen05 kernel: [2] claim position, CTAs done (both returned to 0); nullptr:
-                        // the static schedule only
   unsigned* status;
   int pair_cost;        // tcgen05 kernel: work charged per (sequence, kv head) pair, quarter tiles
   // paged cache (tcgen05 kernel only; nullptr: the contiguous [B][Hkv][cap][D] layout): Kc / Vc are

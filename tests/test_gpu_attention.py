@@ -15,17 +15,12 @@ pytestmark = pytest.mark.gpu
 D = 128
 
 
-@pytest.fixture(params=[(1, 1), (1, 0), (0, 1)], ids=["tcgen05", "tcgen05-static", "mma_sync"])
+@pytest.fixture(params=[1, 0], ids=["tcgen05", "mma_sync"])
 def impl(request, lib):
-    """Run each case on both attention kernels (tcgen05 is the default), the tcgen05 one with its
-    dynamic schedule allowed (the default; it applies to batches of many pairs) and with the static
-    split only."""
-    kernel, dynamic = request.param
-    lib.spec_set_option("attention_impl", kernel)
-    lib.spec_set_option("attention_dynamic", dynamic)
-    yield kernel
+    """Run each case on both attention kernels (tcgen05 is the default)."""
+    lib.spec_set_option("attention_impl", request.param)
+    yield request.param
     lib.spec_set_option("attention_impl", 1)
-    lib.spec_set_option("attention_dynamic", 1)
 
 
 def run_case(lib, gammas, ctx, Hq, Hkv, seed, cap=None, fused_qkv=True):
@@ -165,18 +160,12 @@ def test_attention_pair_cost_partitions(lib, pair_cost, grid):
         lib.spec_set_option("persistent_grid", 0)
 
 
-# ------------------------------------------------------------------ dynamic schedule (whole pairs,
-# claimed longest first): batches with at least two (sequence, kv head) pairs per CTA
-def _many_pairs(seed, B):
-    rng = np.random.default_rng(seed)
-    return list(rng.integers(0, 6, size=B)), list(rng.integers(0, 700, size=B))
-
-
 @pytest.mark.parametrize("grid,B", [(0, 48), (5, 48), (37, 48), (300, 96)])
-def test_attention_dynamic_schedule(lib, grid, B):
-    """Many short pairs (48 or 96 sequences x 8 kv heads): the dynamic schedule against the
-    oracle on several grids, including more CTAs than fit on the GPU at once."""
-    gammas, ctx = _many_pairs(grid + B, B)
+def test_attention_many_short_pairs(lib, grid, B):
+    """48 or 96 sequences x 8 kv heads of short contexts (0-700 keys, 1-6 rows): many pairs per
+    CTA, on several grids including more CTAs than fit on the GPU at once."""
+    rng = np.random.default_rng(grid + B)
+    gammas, ctx = list(rng.integers(0, 6, size=B)), list(rng.integers(0, 700, size=B))
     lib.spec_set_option("persistent_grid", grid)
     try:
         run_case(lib, gammas, ctx, 32, 8, seed=90 + grid)
@@ -184,42 +173,7 @@ def test_attention_dynamic_schedule(lib, grid, B):
         lib.spec_set_option("persistent_grid", 0)
 
 
-def test_attention_dynamic_results_do_not_depend_on_the_claims(lib):
-    """Each pair is computed whole by one CTA in tile order: the same bits on every call and on
-    every grid (different CTAs claim different pairs), and the counters are back at zero after each
-    launch (the next one claims from the start again)."""
-    gammas, ctx = _many_pairs(7, 80)            # 640 pairs: the dynamic schedule on every grid below
-    batch = synth.RaggedBatch(gammas, ctx)
-    Hq, Hkv = 32, 8
-    qkv = bf16_dev(synth.normal_bf16_bits(70, (batch.M, (Hq + 2 * Hkv) * D), 1.0))
-    kc0 = bf16_dev(synth.normal_bf16_bits(71, (batch.B, Hkv, batch.cap, D), 1.0))
-    vc0 = bf16_dev(synth.normal_bf16_bits(72, (batch.B, Hkv, batch.cap, D), 1.0))
-    hq, hk = Hq * D, Hkv * D
-    outs = []
-    for grid in (0, 0, 37, 300, 0):
-        lib.spec_set_option("persistent_grid", grid)
-        try:
-            kc, vc = kc0.clone(), vc0.clone()
-            outs.append(bits_of(lib.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:],
-                                                          dev(batch.cu_rows), dev(batch.ctx_len), kc, vc,
-                                                          batch.max_rows)))
-        finally:
-            lib.spec_set_option("persistent_grid", 0)
-    lib.spec_device_status()
-    for o in outs[1:]:
-        assert np.array_equal(o, outs[0])
-
-
-@pytest.mark.parametrize("dynamic", [1, 0], ids=["dynamic", "static"])
-def test_attention_full_ragged_round_sampled(lib, dynamic):
-    lib.spec_set_option("attention_dynamic", dynamic)
-    try:
-        _full_ragged_round_sampled(lib)
-    finally:
-        lib.spec_set_option("attention_dynamic", 1)
-
-
-def _full_ragged_round_sampled(lib):
+def test_attention_full_ragged_round_sampled(lib):
     """The benchmark's attention launch at full size: B = 64, gamma_b ~ U{1..10}, ctx_b ~ U[128, 8192],
     GQA 32/8, D = 128, the default persistent grid and pair cost.  Outputs and the cache append are
     checked against the oracle on a sample of sequences (the shortest and longest contexts, the
