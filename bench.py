@@ -1201,6 +1201,20 @@ def run_profile_case(args):
         for _ in range(args.reps):
             S.spec_verify_attention(qkv[:, :hq], qkv[:, hq:hq + hk], qkv[:, hq + hk:], cu, ctx, kc, vc,
                                     batch.max_rows, ws=ws)
+    elif args.profile == "sampler":
+        # the round's fused LM head -> sampler on synthetic inputs: the benchmark batch (368 rows), the
+        # full vocabulary, draft rows q = softmax of random logits, drafts sampled from q
+        batch = make_batch()
+        M, K, V = batch.M, dims.d, dims.V
+        W = torch.empty((V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.02, generator=g)
+        X = torch.empty((M, K), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=g)
+        nq = batch.n_drafts
+        q = torch.softmax(torch.empty((nq, V), device=dev).normal_(0, 1, generator=g), dim=1).contiguous()
+        drafts = torch.multinomial(q, 1, generator=g).view(-1).to(torch.int32)
+        U = torch.from_numpy(synth.uniforms_f32(SEED, M)).to(dev)
+        cu = torch.from_numpy(batch.cu_rows).to(dev)
+        for _ in range(args.reps):
+            S.spec_lmhead_reject_sample(X, W, TEMP, q, drafts, U, cu, ws=ws)
     else:
         M = args.rows
         if args.nsub:
@@ -1232,7 +1246,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-draft", action="store_true", help="skip the draft-phase measurement")
     ap.add_argument("--no-extra", action="store_true", help="skip the sweep points and configuration 3")
-    ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead", "chain"], default=None,
+    ap.add_argument("--profile", choices=["round", "attention", "linear", "swiglu", "lmhead", "chain", "sampler"],
+                    default=None,
                     help="run a small case of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--rows", type=int, default=368, help="rows for --profile linear/lmhead/chain")
     ap.add_argument("--layers", type=int, default=4, help="stack layers for --profile chain")

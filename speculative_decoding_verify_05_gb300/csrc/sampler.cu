@@ -235,9 +235,28 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
   const RowP prow{P + (size_t)(r0 + n) * ldp, s_mx[ri], s_inv[ri], s_am[ri]};
   const float* qrow = resid ? Q + (size_t)(q0 + n) * V : prow.v;
 
-  // ---- 2. per-tile totals of the residual and of p (coalesced 16-byte loads, four tiles' loads in
-  // flight per thread, no block barrier per tile), kept in fp64
+  // ---- 2. per-tile totals of the residual and of p, kept in fp64: each thread reads its 8 tokens of
+  // the final row (and of q at a rejection) once per tile, the 16-byte loads of four tiles issued
+  // before any of them is used (no block barrier per tile)
   for (int t0 = 0; t0 < n_tiles; t0 += 4) {
+    float4 zr[4][2], qr[4][2];
+    bool full[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int x0 = (t0 + k) * TILE + tid * PER_THREAD;
+      full[k] = vec && t0 + k < n_tiles && x0 + PER_THREAD <= V;
+      zr[k][0] = zr[k][1] = qr[k][0] = qr[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (full[k]) {
+        if constexpr (MODE != P_ARGMAX) {
+          zr[k][0] = __ldcg(reinterpret_cast<const float4*>(prow.v + x0));
+          zr[k][1] = __ldcg(reinterpret_cast<const float4*>(prow.v + x0 + 4));
+        }
+        if (resid) {
+          qr[k][0] = __ldcg(reinterpret_cast<const float4*>(qrow + x0));
+          qr[k][1] = __ldcg(reinterpret_cast<const float4*>(qrow + x0 + 4));
+        }
+      }
+    }
     float sr[4], sp[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -246,15 +265,33 @@ reject_sample_kernel(const float* __restrict__ P, const float2* __restrict__ sta
       const int t = t0 + k;
       if (t >= n_tiles) continue;
       const int x0 = t * TILE + tid * PER_THREAD;
-      float pw[PER_THREAD];
-      load_weights<MODE>(prow, qrow, x0, V, true, vec, pw);
+      // p and the residual weights max(0, p - q) of this thread's tokens (tokens past V weigh 0)
+      float pv[PER_THREAD], qv[PER_THREAD];
+      if (full[k]) {
+        const float zz[PER_THREAD] = {zr[k][0].x, zr[k][0].y, zr[k][0].z, zr[k][0].w,
+                                      zr[k][1].x, zr[k][1].y, zr[k][1].z, zr[k][1].w};
+        const float qq[PER_THREAD] = {qr[k][0].x, qr[k][0].y, qr[k][0].z, qr[k][0].w,
+                                      qr[k][1].x, qr[k][1].y, qr[k][1].z, qr[k][1].w};
 #pragma unroll
-      for (int e = 0; e < PER_THREAD; ++e) sp[k] += pw[e];
+        for (int e = 0; e < PER_THREAD; ++e) {
+          if constexpr (MODE == P_ARGMAX) pv[e] = (x0 + e == prow.am) ? 1.f : 0.f;
+          else if constexpr (MODE == P_LOGITS) pv[e] = exp_sm(zz[e] - prow.mx) * prow.inv;
+          else pv[e] = zz[e];
+          qv[e] = qq[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < PER_THREAD; ++e) {
+          const int x = x0 + e;
+          pv[e] = x < V ? p_at<MODE>(prow, x) : 0.f;
+          qv[e] = (resid && x < V) ? qrow[x] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < PER_THREAD; ++e) sp[k] += pv[e];
       if (resid) {
-        float w[PER_THREAD];
-        load_weights<MODE>(prow, qrow, x0, V, false, vec, w);
 #pragma unroll
-        for (int e = 0; e < PER_THREAD; ++e) sr[k] += w[e];
+        for (int e = 0; e < PER_THREAD; ++e) sr[k] += fmaxf(pv[e] - qv[e], 0.f);
       }
     }
 #pragma unroll
