@@ -175,7 +175,7 @@ __device__ __forceinline__ uint64_t umma_desc_lin(uint32_t smem_addr) {
 // k-substep share one weight tile, so with up to 384 verify rows (kMaxTN) every weight byte is
 // read from HBM once.  PAIR: the tile of a CTA pair is 256 weight rows (128 per CTA) x TN, and
 // each CTA stages half (HB) of every MMA's token rows.
-template <int BN, int NSUB, bool PAIR = false>
+template <int BN, int NSUB, bool PAIR = false, bool STATS = false>
 struct LinearCfg {
   static constexpr int TN = BN * NSUB;
   static constexpr int HB = PAIR ? BN / 2 : BN;
@@ -189,9 +189,11 @@ struct LinearCfg {
   // producer warp, MMA warp, 8 epilogue warps (two per TMEM lane quarter, each half of the columns)
   static constexpr int THREADS = 320;
   static constexpr int EPI_WARPS = 8;
-  // per epilogue warp: a 16-column x 32-row fp32 block (row stride 33) to turn TMEM rows into
-  // 16-byte stores along the weight rows
-  static constexpr int EPI_BUF_FLOATS = 16 * 33;
+  // per epilogue warp: a column block x 32 rows of fp32 (row stride 33) to turn TMEM rows into
+  // 16-byte stores along the weight rows (16 columns), or to scan the LM head's columns (STATS:
+  // 8 columns, which leaves a 2-SM LM head room for a fifth ring stage)
+  static constexpr int EPI_COLS = STATS ? 8 : 16;
+  static constexpr int EPI_BUF_FLOATS = EPI_COLS * 33;
   // besides the ring: barriers/flags (1 KB) + LM-head reduction scratch (4 warps x TN x float2) +
   // epilogue transpose blocks + row scales of a folded RMSNorm (TN floats) + alignment slack
   static constexpr int EXTRA = 1024 + 4 * TN * 8 + EPI_WARPS * EPI_BUF_FLOATS * 4 + TN * 4 + 1024;

@@ -94,7 +94,7 @@ template <int BN, int NSUB, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(320, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const LinearArgs args) {
-  using Cfg = LinearCfg<BN, NSUB, PAIR>;
+  using Cfg = LinearCfg<BN, NSUB, PAIR, EPI == EPI_LOGITS || EPI == EPI_ARGMAX>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int TN = Cfg::TN;
   constexpr int HB = Cfg::HB;
@@ -376,17 +376,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         release_acc(acc);
       } else {
         // LM-head epilogues (ranges are tile-aligned, so every segment is whole): per token column
-        // reduce over the tile's 128 vocabulary rows.  Each 16-column block goes through the warp's
-        // transpose block, so lanes 2j and 2j + 1 scan column j's 32 rows (16 each) and meet in one
-        // shuffle: two shuffles per 16 columns instead of five per column per reduction (the
-        // butterfly version took 22 us per 192-column tile, 40 us per 384-column tile).
+        // reduce over the tile's 128 vocabulary rows.  Each 8-column block goes through the warp's
+        // transpose block, so lanes 4j .. 4j + 3 scan column j's 32 rows (8 each, reduced as trees)
+        // and meet in two shuffles, instead of five shuffles per column per reduction (the butterfly
+        // version took 22 us per 192-column tile, 40 us per 384-column tile).
         float* eb = ebuf_all + ewarp * Cfg::EPI_BUF_FLOATS;
-        const int jc = lane >> 1, r0 = (lane & 1) * 16;
+        const int jc = lane >> 2, r0 = (lane & 3) * 8;
         const int nr = n0 + q * 32 + r0;        // vocabulary row of this lane's first scanned entry
 
-        // TMEM is read 32 columns per wait (16 at the tail: the halves are multiples of 16); each
-        // lane's 16 scanned values are reduced as trees (max, then sum of exponentials), which
-        // keeps the dependent chains short
+        // TMEM is read 32 columns per wait (16 at the tail: the halves are multiples of 16)
 #pragma unroll 1
         for (int c32 = c_begin; c32 < c_end; c32 += 32) {
           const int cols = c_end - c32 < 32 ? c_end - c32 : 32;
@@ -394,48 +392,49 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           if (cols == 32) tmem_ld_cols<32>(t_row + c32, v);
           else tmem_ld_cols<16>(t_row + c32, v);
 #pragma unroll
-          for (int h = 0; h < 32; h += 16) {
+          for (int h = 0; h < 32; h += 8) {
             if (h >= cols) break;
             const int c = c32 + h;
             if constexpr (EPI == EPI_LOGITS) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < 8; ++j) {
                 const float z = v[h + j] * (args.norm_ssq ? args.inv_temp * s_rms[c + j] : args.inv_temp);
                 const int m = m0 + c + j;
                 if (m < args.M && n < args.N) args.P[(size_t)m * args.ldp + n] = z;
                 eb[j * 33 + lane] = z;
               }
               __syncwarp();
-              float zz[16], t8[8];
+              float zz[8];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) zz[i] = nr + i < args.N ? eb[jc * 33 + r0 + i] : -INFINITY;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) t8[i] = fmaxf(zz[2 * i], zz[2 * i + 1]);
-              float mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
-                               fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+              for (int i = 0; i < 8; ++i) zz[i] = nr + i < args.N ? eb[jc * 33 + r0 + i] : -INFINITY;
+              float mx = fmaxf(fmaxf(fmaxf(zz[0], zz[1]), fmaxf(zz[2], zz[3])),
+                               fmaxf(fmaxf(zz[4], zz[5]), fmaxf(zz[6], zz[7])));
               mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
 #pragma unroll
-              for (int i = 0; i < 16; ++i) zz[i] = nr + i < args.N ? exp_sm(zz[i] - mx) : 0.f;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) t8[i] = zz[2 * i] + zz[2 * i + 1];
-              float sm = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
+              for (int i = 0; i < 8; ++i) zz[i] = nr + i < args.N ? exp_sm(zz[i] - mx) : 0.f;
+              float sm = ((zz[0] + zz[1]) + (zz[2] + zz[3])) + ((zz[4] + zz[5]) + (zz[6] + zz[7]));
               sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-              if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
+              sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+              if ((lane & 3) == 0) red[q * TN + c + jc] = make_float2(mx, sm);
             } else {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) eb[j * 33 + lane] = v[h + j];
+              for (int j = 0; j < 8; ++j) eb[j * 33 + lane] = v[h + j];
               __syncwarp();
               float zv = -INFINITY;
               int idx = 0x7fffffff;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {          // strict > keeps the lowest row on ties
+              for (int i = 0; i < 8; ++i) {           // strict > keeps the lowest row on ties
                 const float z = eb[jc * 33 + r0 + i];
                 if (nr + i < args.N && (z > zv || idx == 0x7fffffff)) { zv = z; idx = nr + i; }
               }
-              const float ov = __shfl_xor_sync(0xffffffffu, zv, 1);
-              const int oi = __shfl_xor_sync(0xffffffffu, idx, 1);
-              if (ov > zv || (ov == zv && oi < idx)) { zv = ov; idx = oi; }
-              if ((lane & 1) == 0) red[q * TN + c + jc] = make_float2(zv, __int_as_float(idx));
+#pragma unroll
+              for (int o = 1; o <= 2; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, zv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+                if (ov > zv || (ov == zv && oi < idx)) { zv = ov; idx = oi; }
+              }
+              if ((lane & 3) == 0) red[q * TN + c + jc] = make_float2(zv, __int_as_float(idx));
             }
             __syncwarp();                          // eb is rewritten by the next block
           }
@@ -489,7 +488,8 @@ static bool linear_tc_configure() {
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && configured[dev]) return true;
   if (cudaFuncSetAttribute(linear_tc_kernel<BN, NSUB, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           LinearCfg<BN, NSUB, PAIR>::SMEM_BYTES) != cudaSuccess)
+                           LinearCfg<BN, NSUB, PAIR, EPI == EPI_LOGITS || EPI == EPI_ARGMAX>::SMEM_BYTES) !=
+      cudaSuccess)
     return false;
   if (dev >= 0 && dev < 64) configured[dev] = true;
   return true;
@@ -498,7 +498,7 @@ static bool linear_tc_configure() {
 template <int BN, int NSUB, int EPI>
 static cudaError_t launch_linear_tc_one(const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a,
                                         dim3 grid, cudaStream_t st) {
-  using Cfg = LinearCfg<BN, NSUB>;
+  using Cfg = LinearCfg<BN, NSUB, false, EPI == EPI_LOGITS || EPI == EPI_ARGMAX>;
   if (!linear_tc_configure<BN, NSUB, EPI>()) return cudaGetLastError();
   cudaError_t e = launch_k(linear_tc_kernel<BN, NSUB, EPI>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, st,
                            tw, tx, a);
@@ -508,7 +508,7 @@ static cudaError_t launch_linear_tc_one(const CUtensorMap& tw, const CUtensorMap
 // The pair build: `pairs` clusters of 2 CTAs, and how many pairs can be resident at once.
 template <int BN, int NSUB, int EPI>
 struct LinearTcPair {
-  using Cfg = LinearCfg<BN, NSUB, true>;
+  using Cfg = LinearCfg<BN, NSUB, true, EPI == EPI_LOGITS || EPI == EPI_ARGMAX>;
   static cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const LinearArgs& a, int pairs,
                             cudaStream_t st) {
     if (!linear_tc_configure<BN, NSUB, EPI, true>()) return cudaGetLastError();
