@@ -108,6 +108,9 @@ SPEC_API int spec_version(void);
  * between the pairs of a cluster; "linear_pair_few" (0
  * default, 1): the pair kernel also for products with fewer tiles (split-K
  * on pairs; measured slower than the one-SM cluster kernel at 368 rows);
+ * "weight_l2_promotion" / "kv_l2_promotion" (0..3: none, 64, 128, 256 bytes;
+ * defaults 2 and 3): the L2 promotion of the TMA loads of weight tiles and of
+ * the attention kernels' K/V tiles;
  * "pdl" (1 default, 0 off):
  * kernels are launched with programmatic dependent launch, so each one's
  * launch and on-chip setup overlap the end of the kernel before it on the

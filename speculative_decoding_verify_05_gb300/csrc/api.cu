@@ -151,6 +151,7 @@ int get_encoder() {
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, rank-1 entries)
 constexpr CUtensorMapSwizzle kLinSwizzle = LIN_BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 int g_w_promotion = 2;    // tunable: L2 promotion of weight-tile loads (0 none, 1 64 B, 2 128 B, 3 256 B)
+int g_kv_promotion = 3;   // tunable: L2 promotion of the attention kernels' K/V tile loads (same scale)
 
 int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                 const cuuint64_t* strides, const cuuint32_t* box, const char* what,
@@ -514,6 +515,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "pdl must be 0 or 1");
     g_pdl = value;
+    return ok();
+  }
+  if (!strcmp(name, "kv_l2_promotion")) {
+    if (value < 0 || value > 3) return fail(SPEC_EINVAL, "kv_l2_promotion must be in [0, 3]");
+    g_kv_promotion = value;
     return ok();
   }
   if (!strcmp(name, "weight_l2_promotion")) {
@@ -1529,8 +1535,8 @@ static int verify_attention_impl(const spec_bf16* Q, int ldq, const spec_bf16* K
   cuuint64_t dims[3] = {(cuuint64_t)D, rows, zs};
   cuuint64_t str[2] = {(cuuint64_t)D * 2, rows * D * 2};
   cuuint32_t box[3] = {64, p.tc ? (cuuint32_t)kt : 64u, 1};
-  if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache")) return rc;
-  if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache")) return rc;
+  if (int rc = encode_bf16(&tk, Kcache, 3, dims, str, box, "Kcache", g_kv_promotion)) return rc;
+  if (int rc = encode_bf16(&tv, Vcache, 3, dims, str, box, "Vcache", g_kv_promotion)) return rc;
   char* ws = static_cast<char*>(workspace);
   AttnArgs a{};
   a.Q = Q; a.ldq = ldq; a.Knew = Knew; a.Vnew = Vnew; a.ldkv = ldkv;

@@ -106,16 +106,18 @@ def test_in_ssq_linear_rope(lib, M):
     assert_close_chain(f64_of_bf16(Y), ref, 1, f"normed linear + rope M={M}")
 
 
-@pytest.mark.parametrize("T", [0.7, 0.0])
-def test_in_ssq_lmhead_sampler(lib, T):
+@pytest.mark.parametrize("M,V,T", [(40, 8192, 0.7), (40, 8192, 0.0), (368, 20480, 0.7), (368, 20480, 0.0)])
+def test_in_ssq_lmhead_sampler(lib, M, V, T):
     """The LM head -> sampler on the residual stream x with the final norm folded: the same
     decisions as the oracle wherever they are not near ties of either side.  This checks the op
     against its own definition (the product's rows scaled by 1 / rms: the normed rows are not
     rounded), on rows peaked by a W of std 0.25 (logits of std ~5.7), where a bf16 rounding of the
     normed rows alone would move p by a few percent; the layer-level reading, which rounds them, is
-    held to the chain bar by the stack tests."""
-    M, K, V = 40, 512, 8192
-    batch = synth.RaggedBatch([4] * 8, [100] * 8)
+    held to the chain bar by the stack tests.  At 368 rows and 160 vocabulary tiles the LM head runs
+    on CTA pairs."""
+    K = 512
+    batch = synth.RaggedBatch([4] * 8, [100] * 8) if M == 40 else synth.RaggedBatch([4] * 73 + [2], [100] * 74)
+    assert batch.M == M
     X, ssq = _x_and_ssq(lib, 5, M, K)
     W = synth.normal_bf16_bits(6, (V, K), 0.25)
     h = oops.rmsnorm(f64_of_bf16(X), np.ones(K), EPS)

@@ -124,6 +124,8 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"linear_pair_persistent", 0) == 0
     assert L.spec_set_option(b"lmhead_pair", 2) == E
     assert L.spec_set_option(b"lmhead_pair", 1) == 0
+    assert L.spec_set_option(b"kv_l2_promotion", 4) == E
+    assert L.spec_set_option(b"kv_l2_promotion", 3) == 0
     # the bounded-wait probe checks its limit before touching the device
     assert L.spec_probe_bounded_wait(0, 0, None) == E
     assert L.spec_probe_bounded_wait(2000001, 0, None) == E
