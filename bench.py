@@ -735,7 +735,9 @@ class SweepRig:
         import synth
         M = nb * (gm + 1)
         x, h, qkv, o, a, ws = self.x, self.h, self.qkv, self.o, self.a, self.ws
-        # the small-M path (M <= 32): the weight-streaming chain; above it, one call per product
+        # the small-M path (M <= 32): the weight-streaming chain; above it, one call per product (the
+        # chain takes up to 64 rows, but at 40 rows its 64-column pieces made it slower: 3.51 ms
+        # against 3.33 ms)
         chain = M <= 32
         if chain:
             ops = stack_chain_ops(S, None, M, bufs=(self.sw.layers, h, o, qkv, x, a))

@@ -252,7 +252,7 @@ typedef struct {
   int swiglu;
 } spec_linear_op;
 
-/* Runs n_ops products over the same M (1..32) verify rows, in order: the
+/* Runs n_ops products over the same M (1..64) verify rows, in order: the
  * result is that of calling spec_verify_linear / spec_verify_linear_swiglu
  * for each in turn.  At small M the verify pass is a weight stream ([P1] "The
  * speedup is borrowed, and there is a lender": one weight read serves all

@@ -100,7 +100,7 @@ cudaError_t launch_linear_tc_lmhead(int BN, int NSUB, bool greedy, const CUtenso
 // ---- weight-streaming chain of small-M GEMMs (one persistent launch for a list of products)
 constexpr int CH_MAX_OPS = 48;     // products per launch (kernel parameter space)
 constexpr int CH_MAX_DEPS = 6;
-constexpr int CH_MAX_M = 32;
+constexpr int CH_MAX_M = 64;
 enum ChainDepKind : int {
   CH_DEP_X = 0,       // X of the product reads Y of `op`: token loads wait (per tile when shift >= 0)
   CH_DEP_RES = 1,     // the residual reads Y of `op`: the epilogue waits (per tile when shift >= 0)

@@ -1,4 +1,4 @@
-// Weight-streaming chain of verify GEMMs for a handful of rows (M <= 32): one persistent launch
+// Weight-streaming chain of verify GEMMs for a handful of rows (M <= 64): one persistent launch
 // runs a list of products Y_j = X_j W_j^T (+ residual, or the SwiGLU activation) in order.
 //
 // At small M the verify pass is a weight stream ("Speculative Decoding Spends Arithmetic You May
@@ -19,16 +19,18 @@
 // done) waits for the pieces and adds them to its own accumulator in CTA order (deterministic),
 // then runs the epilogue and marks the tile stored.
 //
-// Roles (8 warps): warp 0 streams weight tiles, warp 1 issues tcgen05.mma into a ring of TMEM
-// accumulators, warp 2 streams token tiles once their flags allow, warps 4-7 drain the
-// accumulators (TMEM lane quarter = warp % 4, one weight row per thread).  Every wait is bounded.
+// Roles (12 warps): warp 0 streams weight tiles, warp 1 issues tcgen05.mma into a ring of TMEM
+// accumulators, warp 2 streams token tiles once their flags allow, warps 4-11 drain the
+// accumulators (TMEM lane quarter = warp % 4, one weight row and half of the token columns per
+// thread).  Every wait is bounded.
 #include "internal.h"
 #include "linear_tc.cuh"
 
 namespace spec {
 namespace {
 
-constexpr int CH_THREADS = 256;
+constexpr int CH_THREADS = 384;
+constexpr int CH_EPI_THREADS = 256;   // warps 4-11: 4 lane quarters x 2 column halves
 constexpr int CH_W_BYTES = 128 * LIN_ROW_BYTES;   // one 128 x 64 weight tile
 
 template <int BN>
@@ -68,18 +70,38 @@ __device__ __forceinline__ bool spin_geq(const unsigned* p, unsigned target, uns
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-__device__ __forceinline__ void bar_chain_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bar_chain_epi() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier, returning whether `v` held on every epilogue thread (keeps the epilogue's
 // control flow uniform after a wait that one thread took and that may have run out).
 __device__ __forceinline__ bool bar_chain_epi_and(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      " bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
       : "r"((uint32_t)v)
       : "memory");
   return r != 0;
+}
+
+// N consecutive TMEM columns of this thread's lane (N = 8, 16 or 32: half of a 16-, 32- or
+// 64-column accumulator), loaded and waited for.
+template <int N>
+__device__ __forceinline__ void chain_tmem_ld(uint32_t taddr, float* v) {
+  if constexpr (N == 16 || N == 32) {
+    tmem_ld_cols<N>(taddr, v);
+  } else {
+    static_assert(N == 8, "column count");
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8+0];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  }
 }
 
 // ------------------------------------------------------------------ work of one CTA
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
     }
     for (int i = 0; i < Cfg::NACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], CH_EPI_THREADS);
     }
     fence_barrier_init();
   }
@@ -296,10 +318,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ---------------- epilogue: thread r = weight row r of the tile (TMEM lane r)
+    // ---------------- epilogue: thread r = weight row r of the tile (TMEM lane r), token columns
+    // col0 .. col0 + HB - 1 of the accumulator
+    constexpr int HB = BN / 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const uint32_t t_lane = uint32_t(q * 32) << 16;
+    const int col0 = ((warp - 4) >> 2) * HB;
+    const uint32_t t_lane = (uint32_t(q * 32) << 16) + (uint32_t)col0;
     SegWalker w;
     w.begin(p, c);
     int seg = 0;
@@ -312,12 +337,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
       ok = ok && mbar_wait(&acc_full[acc], (uint32_t)((seg / Cfg::NACC) & 1), p.status, 0x154u);
       ok = bar_chain_epi_and(ok);
       tc_fence_after();
-      float v[BN];
+      float v[HB];
       if (ok) {
-        tmem_ld_cols<BN>(tmem + acc * Cfg::ACC_COLS + t_lane, v);
+        chain_tmem_ld<HB>(tmem + acc * Cfg::ACC_COLS + t_lane, v);
       } else {
 #pragma unroll
-        for (int j = 0; j < BN; ++j) v[j] = 0.f;
+        for (int j = 0; j < HB; ++j) v[j] = 0.f;
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
       if (g.kind == 2) {
         // publisher: the fp32 piece, [column][128 rows] (one 128-byte line per column per warp)
 #pragma unroll
-        for (int j = 0; j < BN; ++j) __stcg(my_piece + j * 128 + r, v[j]);
+        for (int j = 0; j < HB; ++j) __stcg(my_piece + (col0 + j) * 128 + r, v[j]);
         bar_chain_epi();
         if (threadIdx.x == 128) {
           __threadfence();
@@ -344,26 +369,26 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
         if (threadIdx.x == 128) ok = ok && spin_geq(p.arrive + o.flag_base + g.tile, n_other, p.status, 0x155u);
         ok = bar_chain_epi_and(ok);
         // the contributors' pieces, PB CTAs' loads in flight at a time, added in CTA order
-        constexpr int PB = BN <= 16 ? 4 : 1;
+        constexpr int PB = HB <= 8 ? 4 : HB <= 16 ? 1 : 2;   // (no register spills at 384 threads)
         int c2 = c + 1;
         while (c2 < p.grid && range_start(o.units, c2, p.grid) < t_end) {
           int cs[PB];
           int nc = 0;
           for (; nc < PB && c2 < p.grid && range_start(o.units, c2, p.grid) < t_end; ++c2)
             if (range_start(o.units, c2, p.grid) < range_start(o.units, c2 + 1, p.grid)) cs[nc++] = c2;
-          float pv[PB][BN];
+          float pv[PB][HB];
 #pragma unroll
           for (int b = 0; b < PB; ++b) {
             if (b >= nc) break;
             const float* pc = p.pieces + ((size_t)g.op * p.grid + cs[b]) * (BN * 128);
 #pragma unroll
-            for (int j = 0; j < BN; ++j) pv[b][j] = __ldcg(pc + j * 128 + r);
+            for (int j = 0; j < HB; ++j) pv[b][j] = __ldcg(pc + (col0 + j) * 128 + r);
           }
 #pragma unroll
           for (int b = 0; b < PB; ++b) {
             if (b >= nc) break;
 #pragma unroll
-            for (int j = 0; j < BN; ++j) v[j] += pv[b][j];
+            for (int j = 0; j < HB; ++j) v[j] += pv[b][j];
           }
         }
       }
@@ -377,17 +402,19 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
         // the matching up row; output column tile * 64 + q * 16 + l
         const int col = g.tile * 64 + q * 16 + (lane & 15);
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
+        for (int j = 0; j < HB; ++j) {
           const float up = __shfl_xor_sync(0xffffffffu, v[j], 16);
-          if (lane < 16 && j < p.M) o.Y[(size_t)j * o.ldy + col] = f2bf(silu(v[j]) * up);
+          const int m = col0 + j;
+          if (lane < 16 && m < p.M) o.Y[(size_t)m * o.ldy + col] = f2bf(silu(v[j]) * up);
         }
       } else if (n < o.N) {
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          if (j >= p.M) break;
+        for (int j = 0; j < HB; ++j) {
+          const int m = col0 + j;
+          if (m >= p.M) break;
           float y = v[j];
-          if (o.residual) y += bf16f(o.residual[(size_t)j * o.ldr + n]);
-          o.Y[(size_t)j * o.ldy + n] = f2bf(y);
+          if (o.residual) y += bf16f(o.residual[(size_t)m * o.ldr + n]);
+          o.Y[(size_t)m * o.ldy + n] = f2bf(y);
         }
       }
       bar_chain_epi();
@@ -421,12 +448,13 @@ cudaError_t launch_chain_bn(const ChainParams& p, cudaStream_t s) {
 
 }  // namespace
 
-int chain_bn(int M) { return M <= 16 ? 16 : M <= CH_MAX_M ? 32 : -1; }
+int chain_bn(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= CH_MAX_M ? 64 : -1; }
 
 cudaError_t launch_linear_chain(const ChainParams& p, cudaStream_t s) {
   switch (chain_bn(p.M)) {
     case 16: return launch_chain_bn<16>(p, s);
     case 32: return launch_chain_bn<32>(p, s);
+    case 64: return launch_chain_bn<64>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }

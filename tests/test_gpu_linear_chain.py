@@ -42,7 +42,7 @@ def ref_swiglu(X, Wgu, lib):
     return oops.silu_mul(g, u)
 
 
-@pytest.mark.parametrize("M", [1, 3, 5, 16, 17, 32])
+@pytest.mark.parametrize("M", [1, 3, 5, 16, 17, 32, 33, 40, 64])
 def test_independent_products(lib, M):
     """Products with no shared buffers: ragged N, K not a multiple of 64, a SwiGLU product."""
     shapes = [(4096, 4096), (1000, 520), (6144, 4096), (136, 72), (384, 1000)]
@@ -76,7 +76,7 @@ def _layer_buffers(M, d, I, L, seed):
     return dev, Wq, Wo, Wgu, Wd, h, o, x0
 
 
-@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("M", [1, 5, 16, 40])
 @pytest.mark.parametrize("interleaved", [False, True])
 def test_layer_chain_with_distinct_buffers(lib, M, interleaved):
     """QKV, O (+ residual), gate|up (SwiGLU), down (+ residual) per layer, every output in its own
@@ -114,7 +114,7 @@ def test_layer_chain_with_distinct_buffers(lib, M, interleaved):
         assert_close_rel(f64_of_bf16(xd[l]), ref_linear(a[l], Wd[l], xo[l]), f"down {l}")
 
 
-@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("M", [1, 5, 16, 64])
 def test_layer_chain_in_place_matches_product_by_product(lib, M):
     """The residual stream updated in place (x = x + ...) and one activation buffer reused by every
     layer (gate|up of layer l+1 overwrites what down of layer l read): the chain equals the same
