@@ -448,7 +448,7 @@ struct AttnPlan {
   bool tc = false;               // persistent tcgen05 kernel
   int grid = 1;
   int chunk = 256, max_chunks = 1;
-  size_t counters_off = 0, partial_off = 0, bytes = 0;
+  size_t counters_off = 0, partial_off = 0, pfx_off = 0, bytes = 0;
 };
 
 AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
@@ -460,7 +460,8 @@ AttnPlan plan_attention(int B, int max_rows, int Hq, int Hkv, int cap) {
   p.partial_off = kCounterBytes;
   if (p.tc) {
     p.grid = g_force_grid > 0 ? g_force_grid : sms;
-    p.bytes = kCounterBytes + round_up(size_t(p.grid) * 2 * 64 * (128 + 2) * 4, 256);
+    p.pfx_off = kCounterBytes + round_up(size_t(p.grid) * 2 * 64 * (128 + 2) * 4, 256);
+    p.bytes = p.pfx_off + round_up(size_t(p.grid) * (B + 1) * 4, 256);
     return p;
   }
   const double keys = double(B) * Hkv * cap;
@@ -1552,6 +1553,7 @@ static int verify_attention_impl(const spec_bf16* Q, int ldq, const spec_bf16* K
   a.block_table = block_table;
   a.max_pages = max_pages;
   a.num_pages = num_pages;
+  a.pfx = reinterpret_cast<int*>(ws + p.pfx_off);
   cudaError_t e = p.tc ? launch_attention_tc(tk, tv, a, p.grid, static_cast<cudaStream_t>(stream))
                        : launch_attention(tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

@@ -19,12 +19,15 @@
 //            goes straight to shared memory
 //   O[row, d] += P . V_tile        tcgen05.mma M = 64, N = 128 dims (V read MN-major), K = 128 keys
 // Roles (8 warps): 0-3 softmax + epilogue; 4 and 6 only issue the TMA loads of K
-// (2-stage ring) and V (3-stage ring: a V tile waits for the softmax, a K tile only for
+// (2-stage ring) and V (4-stage ring: a V tile waits for the softmax, a K tile only for
 // QK^T); 5 issues the MMAs (lane 0, event driven: whichever of QK^T or PV has its inputs
 // ready goes first); 7 stages each pair's Q rows and patches the newest gamma_b + 1 keys
 // (from Knew) into the K tiles holding keys >= ctx once their loads land; the softmax
 // warps do the same for V (zeroing the rows past the block) just before that tile's PV.
-// Both write the new rows into the cache too.  Q, S and O are double buffered, P single.
+// Both write the new rows into the cache too.  S and O are double buffered, Q and P single:
+// shared memory goes to the K/V rings instead, whose depth sets the bytes each SM keeps in
+// flight (for the same reason the per-sequence metadata sits in the V ring during the setup
+// only, and in global memory afterwards).
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,24 +37,30 @@ namespace {
 constexpr int D = 128;
 constexpr int KT = 128;                  // keys per tile = MMA N of QK^T, MMA K of PV
 constexpr int QR = 64;                   // query rows per (b, h) pair = MMA M
+// Ring depths and Q buffers, measured on the 64-sequence verify launch (K/V stages, Q buffers:
+// time): 2/3/2 203 us with the metadata resident in shared memory; 2/4/1 191 us, 3/3/1 197 us,
+// 2/3/1 194 us with it in the V ring during the setup only.
 constexpr int ST_K = 2;                  // K ring stages
-constexpr int ST_V = 3;                  // V ring stages
+constexpr int ST_V = 4;                  // V ring stages
+constexpr int QB = 1;                    // Q buffers
 constexpr int KV_HALF = KT * 128;        // 128 keys x 64 dims (128 B rows), 16 KB
 constexpr int KV_TILE = 2 * KV_HALF;     // 32 KB
 constexpr int Q_HALF = QR * 128;         // 64 rows x 64 bf16, 8 KB
 constexpr int THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;      // S x2 then O x2, 128 columns each
 constexpr int MAX_B = 1024;              // sequences per call handled by this kernel
-constexpr int META_N = MAX_B + 8;        // entries per metadata array
 
 constexpr int OFF_K = 0;
 constexpr int OFF_V = ST_K * KV_TILE;
-constexpr int OFF_Q = OFF_V + ST_V * KV_TILE;       // 2 buffers x two 64-dim halves
-constexpr int OFF_P = OFF_Q + 2 * 2 * Q_HALF;       // [64 rows][128 keys] as two 64-key halves
-constexpr int OFF_META = OFF_P + 2 * Q_HALF;        // unit prefix, ctx, cu_rows per sequence
-constexpr int OFF_BAR = OFF_META + 3 * META_N * 4;
-constexpr int OFF_FLAG = OFF_BAR + 256;
-constexpr int SMEM = OFF_FLAG + 16 + 1024;          // + alignment slack
+constexpr int OFF_Q = OFF_V + ST_V * KV_TILE;       // QB buffers x two 64-dim halves
+constexpr int OFF_P = OFF_Q + QB * 2 * Q_HALF;      // [64 rows][128 keys] as two 64-key halves
+constexpr int OFF_BAR = OFF_P + 2 * Q_HALF;
+constexpr int N_BARS = 3 * (ST_K + ST_V) + 8 + 2 * QB;
+static_assert((N_BARS + 4) * 8 <= 256, "barrier block");
+constexpr int OFF_FLAG = OFF_BAR + 256;             // merge flag, then the first cursor
+constexpr int SMEM = OFF_FLAG + 64 + 1024;          // + alignment slack
+// the setup keeps ctx, cu_rows and the unit prefix (3 B + 2 ints) in the V ring before its first load
+static_assert(3 * MAX_B + 2 <= ST_V * KV_TILE / 4, "setup metadata");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 // Non-blocking probe of an mbarrier phase (the event-driven MMA loop polls several barriers).
@@ -113,7 +122,8 @@ __device__ __forceinline__ void tmem_st_split16(uint32_t taddr, const float* v) 
       : "memory");
 }
 
-// Per-sequence metadata in shared memory.
+// Per-sequence metadata: during the setup a copy in shared memory (the V ring, idle until the
+// first load), afterwards the caller's arrays and the CTA's own prefix slice of the workspace.
 struct Meta {
   const int* pfx;   // [B + 1] first unit of sequence b (pfx[B] = total units)
   const int* ctx;   // [B] cached context length
@@ -290,27 +300,30 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* s_pfx = reinterpret_cast<int*>(smem + OFF_META);
-  int* s_ctx = s_pfx + META_N;
-  int* s_cu = s_ctx + META_N;
-  const Meta meta{s_pfx, s_ctx, s_cu};
+  int* g_pfx = a.pfx + (size_t)blockIdx.x * (a.B + 1);
+  const Meta meta{g_pfx, a.ctx_len, a.cu_rows};
+  int* s_pfx = reinterpret_cast<int*>(smem + OFF_V);
+  int* s_ctx = s_pfx + (a.B + 1);
+  int* s_cu = s_ctx + a.B;
+  const Meta smeta{s_pfx, s_ctx, s_cu};
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* k_full = bars;             // [ST_K] K tile ready (tiles with new keys: after the patch)
-  uint64_t* k_empty = bars + 2;        // [ST_K] QK^T done with the K stage
-  uint64_t* k_land = bars + 4;         // [ST_K] load landed of a tile that gets new keys
-  uint64_t* v_full = bars + 6;         // [ST_V]
-  uint64_t* v_empty = bars + 9;        // [ST_V] PV done with the V stage
-  uint64_t* v_land = bars + 12;        // [ST_V]
-  uint64_t* s_full = bars + 15;        // [2]    S in TMEM
-  uint64_t* s_empty = bars + 17;       // [2]    softmax has read S
-  uint64_t* p_full = bars + 19;        //        P in smem, O rescaled
-  uint64_t* pv_done = bars + 20;       //        PV finished (P free, O current)
-  uint64_t* o_empty = bars + 21;       // [2]    epilogue has read the O buffer
-  uint64_t* q_full = bars + 23;        // [2]    Q of a pair staged
-  uint64_t* q_empty = bars + 25;       // [2]    last QK^T of a pair done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
+  uint64_t* k_full = bars;                 // [ST_K] K tile ready (tiles with new keys: after the patch)
+  uint64_t* k_empty = k_full + ST_K;       // [ST_K] QK^T done with the K stage
+  uint64_t* k_land = k_empty + ST_K;       // [ST_K] load landed of a tile that gets new keys
+  uint64_t* v_full = k_land + ST_K;        // [ST_V]
+  uint64_t* v_empty = v_full + ST_V;       // [ST_V] PV done with the V stage
+  uint64_t* v_land = v_empty + ST_V;       // [ST_V]
+  uint64_t* s_full = v_land + ST_V;        // [2]    S in TMEM
+  uint64_t* s_empty = s_full + 2;          // [2]    softmax has read S
+  uint64_t* p_full = s_empty + 2;          //        P in smem, O rescaled
+  uint64_t* pv_done = p_full + 1;          //        PV finished (P free, O current)
+  uint64_t* o_empty = pv_done + 1;         // [2]    epilogue has read the O buffer
+  uint64_t* q_full = o_empty + 2;          // [QB]   Q of a pair staged
+  uint64_t* q_empty = q_full + QB;         // [QB]   last QK^T of a pair done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
   unsigned* last_flag = reinterpret_cast<unsigned*>(smem + OFF_FLAG);
-  long long* s_range = reinterpret_cast<long long*>(bars + 28);   // this CTA's [ub, ue)
+  long long* s_range = reinterpret_cast<long long*>(bars + N_BARS + 1);   // this CTA's [ub, ue), units
+  Cursor* s_cur = reinterpret_cast<Cursor*>(smem + OFF_FLAG + 8);         // the cursor at ub
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv, G = a.G;
@@ -331,6 +344,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 128);
       mbar_init(&o_empty[i], 128);
+    }
+    for (int i = 0; i < QB; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
@@ -343,7 +358,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   pdl_wait();
   pdl_trigger();
 
-  // ---- per-sequence metadata: one parallel load, then a warp-0 scan of the tile counts
+  // ---- per-sequence metadata: one parallel load, then a warp-0 scan of the tile counts (kept
+  // in shared memory for the searches below and copied to this CTA's prefix slice for merges)
   for (int b = tid; b <= B; b += THREADS) {
     s_cu[b] = a.cu_rows[b];
     if (b < B) s_ctx[b] = a.ctx_len[b];
@@ -368,27 +384,31 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      if (b < B) s_pfx[b] = carry + incl - units;
+      if (b < B) s_pfx[b] = g_pfx[b] = carry + incl - units;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      s_pfx[B] = bad ? 0 : carry;          // nothing to do when the ragged arrays are invalid
+      s_pfx[B] = g_pfx[B] = bad ? 0 : carry;   // nothing to do when the ragged arrays are invalid
       if (bad && blockIdx.x == 0) set_status(a.status, 0x2F1u);
     }
     __syncwarp();
     if (lane == 0) {
       const long long U = s_pfx[B];
       const Part q{U, WT * U + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
-      s_range[0] = range_start(q, meta, blockIdx.x);
-      s_range[1] = range_start(q, meta, blockIdx.x + 1);
+      s_range[0] = range_start(q, smeta, blockIdx.x);
+      s_range[1] = range_start(q, smeta, blockIdx.x + 1);
+      s_range[2] = U;
+      if (s_range[1] > s_range[0]) *s_cur = cur_at(smeta, B, s_range[0]);
     }
   }
+  // the V ring's metadata copy is dead from here: order its generic accesses before the TMA writes
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const long long total = s_pfx[B];
+  const long long total = s_range[2];
   const Part part{total, WT * total + (long long)a.pair_cost * B * Hkv, B * Hkv, (int)gridDim.x, Hkv, a.pair_cost};
   const long long ub = s_range[0], ue = s_range[1];
   const long long n_units = ue - ub;
@@ -403,7 +423,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint64_t* land = is_k ? k_land : v_land;
       uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
-      Cursor c = cur_at(meta, B, ub);
+      Cursor c = *s_cur;
       // paged cache: the block-table entries are read PF units ahead of the loads that use them
       // (a second cursor), so a page lookup's latency never sits in front of a TMA issue
       constexpr int PF = 4;
@@ -446,14 +466,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     // ------------------------------------------------------------ Q staging + new K rows
     bool ok = true;
     int piece = -1;
-    int n_land_k[ST_K] = {0, 0};
-    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
+    int n_land_k[ST_K] = {};
+    Cursor c = n_units > 0 ? *s_cur : Cursor{};
     for (long long i = 0; i < n_units && ok; ++i, cur_next(c, meta, B, Hkv)) {
       if (c.u == ub || c.t == 0) {
         // a new pair: its Q rows (row j = token row j / G, head j % G), zero-padded to 64,
-        // loaded into registers first, stored once QK^T of the pair two back is done
+        // loaded into registers first, stored once the last QK^T of the pair QB back is done
         ++piece;
-        const int qb = piece & 1;
+        const int qb = piece % QB;
         const int R = G * c.Mb, ch = lane & 15;
         uint4 v[32];
 #pragma unroll
@@ -465,7 +485,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             v[k] = *reinterpret_cast<const uint4*>(a.Q + (size_t)(c.r0 + tr) * a.ldq + (size_t)(c.h * G + g) * D + ch * 8);
           }
         }
-        if (piece >= 2) ok = mbar_wait(&q_empty[qb], (uint32_t)(((piece >> 1) - 1) & 1), a.status, 0x210u);
+        if (piece >= QB) ok = mbar_wait(&q_empty[qb], (uint32_t)((piece / QB - 1) & 1), a.status, 0x210u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         uint8_t* qd = smem + OFF_Q + qb * 2 * Q_HALF;
@@ -497,7 +517,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     if (lane == 0 && n_units > 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(QR, KT);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(QR, D) | (1u << 16);   // B (V) MN-major
-      Cursor cs = cur_at(meta, B, ub), cp = cs;
+      Cursor cs = *s_cur, cp = cs;
       long long ns = 0, np = 0;          // next QK^T, next PV
       int piece_s = -1, piece_p = -1;
       uint32_t spin = 0;
@@ -508,8 +528,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           const bool first = (cs.u == ub || cs.t == 0);
           const bool last = (cs.u + 1 == ue) || (cs.t + 1 == cs.nt);
           const int pc = first ? piece_s + 1 : piece_s;
-          const int qb = pc & 1, s = (int)(ns % ST_K);
-          if ((!first || mbar_test(&q_full[qb], (uint32_t)((pc >> 1) & 1))) &&
+          const int qb = pc % QB, s = (int)(ns % ST_K);
+          if ((!first || mbar_test(&q_full[qb], (uint32_t)((pc / QB) & 1))) &&
               mbar_test(&k_full[s], (uint32_t)((ns / ST_K) & 1)) &&
               (ns < 2 || mbar_test(&s_empty[ns & 1], (uint32_t)(((ns >> 1) - 1) & 1)))) {
             piece_s = pc;
@@ -582,8 +602,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     int piece = -1;
-    int n_land_v[ST_V] = {0, 0, 0};
-    Cursor c = n_units > 0 ? cur_at(meta, B, ub) : Cursor{};
+    int n_land_v[ST_V] = {};
+    Cursor c = n_units > 0 ? *s_cur : Cursor{};
     for (long long i = 0; i < n_units; ++i, cur_next(c, meta, B, Hkv)) {
       const long long u = c.u;
       const int R = G * c.Mb;

@@ -174,11 +174,13 @@ struct AttnArgs {
   // pools [Hkv][num_pages][128][D] and key tile t of sequence b is page block_table[b * max_pages + t]
   const int32_t* block_table;
   int max_pages, num_pages;
+  int* pfx;             // tcgen05 kernel: [grid][B + 1] each CTA's copy of the per-sequence unit prefix
 };
 cudaError_t launch_attention(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
                              cudaStream_t s);
 // tcgen05 variant (persistent, stream-K over 128-key tiles): K/V tensor maps with
-// 128-key boxes; `grid` persistent CTAs, partial slots [grid][2][64][128 + 2]
+// 128-key boxes; `grid` persistent CTAs, partial slots [grid][2][64][128 + 2], prefix slices
+// [grid][B + 1]
 int attention_tc_key_tile();
 int attention_tc_max_batch();
 int attention_tc_rows(int G, int max_rows);   // padded query rows per kv head, -1 if unsupported
