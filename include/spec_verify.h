@@ -93,7 +93,10 @@ SPEC_API int spec_version(void);
  * "linear_nsub" (2, default: one tensor-core tile covers up to 384 rows; 1: up
  * to 256); "linear_cluster" (1 default, 0 off): layers with few weight
  * tiles split each tile's k-steps between the CTAs of a thread-block cluster
- * and sum the pieces on chip; "lmhead_nsub" (2 default, or 1): the LM head's
+ * and sum the pieces on chip; "linear_split_rows" (1 default, 0 off): such a
+ * product at 257..384 rows may take two tiles of half the rows on clusters of
+ * half the size when a cost model says the smaller on-chip exchange pays
+ * (the O projection at 368 rows); "lmhead_nsub" (2 default, or 1): the LM head's
  * tensor-core tiles cover up to 384 or 256 rows; "lmhead_pair" (1 default,
  * 0 off): the LM head (64+ rows) runs 256-row vocabulary tiles on CTA pairs
  * (the tcgen05 2-SM MMA: each CTA of a pair stages half of the token rows),

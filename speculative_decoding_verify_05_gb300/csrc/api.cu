@@ -183,6 +183,7 @@ int g_attn_impl = 1;     // tunable: 0 = mma.sync kernel, 1 = tcgen05 kernel
 int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair start, quarter tiles
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
+int g_linear_split_rows = 1;  // tunable: 1 lets few-tile products at 257..384 rows take two half-row tiles
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 384 verify rows
 int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 384 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
@@ -229,6 +230,37 @@ int tc_pair_bn(int BN, int NSUB) {
   for (const auto& sh : shapes)
     if (sh[1] == NSUB && sh[0] >= BN && (best == 0 || sh[0] < best)) best = sh[0];
   return best;
+}
+
+// A cluster split-K plan on one two-MMA tile of 257..384 rows, or two one-MMA tiles of half the
+// rows?  After the main loop each CTA of an S-way cluster moves (S - 1) / S of its 128 x TN fp32
+// accumulator through distributed shared memory, which is slow (tens of GB/s per SM); half-row
+// tiles fill the same SMs with half the split ways, so each CTA moves about a third of the bytes,
+// while a k-step keeps its whole 128-row weight tile for half the MMA work.  Model in k-steps of
+// the 384-row tile: a k-step of TN rows 0.1 + 0.9 TN / 384, exchange and epilogue 11 (S - 1) / S
+// TN / 384 (fitted to the O projection at 368 rows: 21.3 us on 4-way clusters of 384-row tiles,
+// 17.9 us on 2-way clusters of 192-row tiles).
+void cluster_split_rows(LinPlan& p, int M) {
+  auto model = [&](int TN, int S) {
+    return double((p.k_tiles + S - 1) / S) * (0.1 + 0.9 * TN / 384.0) + 11.0 * (S - 1) / S * TN / 384.0;
+  };
+  const int bn1 = std::max(16, ((M + 1) / 2 + 15) / 16 * 16);
+  const long long tiles1 = 2LL * p.tiles_n;
+  int best = 0;
+  double best_cost = model(p.BN * p.NSUB, p.cluster_S);
+  for (int S = 2; S <= 8 && S <= p.k_tiles; ++S) {
+    const int cap = linear_cluster_capacity(bn1, 1, S);
+    if (cap <= 0 || tiles1 * S > cap) continue;
+    const double c = model(bn1, S);
+    if (c < best_cost) { best = S; best_cost = c; }
+  }
+  if (best == 0) return;
+  p.BN = bn1;
+  p.NSUB = 1;
+  p.tiles_m = 2;
+  p.units = tiles1 * p.k_tiles;
+  p.cluster_S = best;
+  p.grid = (int)(tiles1 * best);
 }
 
 LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false, size_t max_bytes = SIZE_MAX) {
@@ -391,6 +423,7 @@ LinPlan plan_linear(int M, int N, int K, bool lmhead, bool swiglu = false, size_
       p.cluster_S = best;
       p.grid = (int)(tiles * best);
       p.bytes = 0;
+      if (g_linear_split_rows && p.NSUB == 2 && p.tiles_m == 1) cluster_split_rows(p, M);
       return p;
     }
   }
@@ -536,6 +569,11 @@ int spec_set_option(const char* name, int value) {
   if (!strcmp(name, "linear_cluster")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_cluster must be 0 or 1");
     g_linear_cluster = value;
+    return ok();
+  }
+  if (!strcmp(name, "linear_split_rows")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_split_rows must be 0 or 1");
+    g_linear_split_rows = value;
     return ok();
   }
   if (!strcmp(name, "attention_pair_cost")) {

@@ -129,6 +129,22 @@ def test_linear_cluster_split_k(lib, M, N, K):
             lib.spec_set_option("linear_cluster", 1)
 
 
+@pytest.mark.parametrize("M,N,K", [(368, 4096, 4096), (368, 4096, 12288), (300, 4096, 1000), (260, 2048, 520)])
+def test_linear_cluster_half_row_tiles(lib, M, N, K):
+    """Few weight tiles at 257..384 rows: the cluster plan on two half-row tiles (the planner's
+    choice where its exchange model says it pays) and on one two-MMA tile both match the oracle,
+    each in one launch without workspace."""
+    for split in (1, 0):
+        lib.spec_set_option("linear_split_rows", split)
+        try:
+            assert lib.spec_linear_workspace_bytes(M, N, K) == 0
+            lib.reset_launch_count()
+            run_case(lib, M, N, K, True, seed=M + N + K + split, gemv_max_m=0)
+            assert lib.launch_count() == 1
+        finally:
+            lib.spec_set_option("linear_split_rows", 1)
+
+
 # --------------------------------------------------------------------------- fused gate/up + SwiGLU
 def run_swiglu(lib, M, I, K, seed, gemv_max_m=4, grid=0, std=0.05):
     """A = silu(X Wg^T) * (X Wu^T) through spec_verify_linear_swiglu vs the oracle in fp64

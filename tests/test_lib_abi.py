@@ -121,6 +121,9 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"attention_pair_cost", 8) == 0
     assert L.spec_set_option(b"linear_multicast", 1) == E      # removed knob
     assert L.spec_set_option(b"linear_pair_persistent", 3) == E
+    assert L.spec_set_option(b"linear_split_rows", 2) == E
+    assert L.spec_set_option(b"linear_split_rows", 0) == 0
+    assert L.spec_set_option(b"linear_split_rows", 1) == 0
     assert L.spec_set_option(b"linear_pair_persistent", 0) == 0
     assert L.spec_set_option(b"lmhead_pair", 2) == E
     assert L.spec_set_option(b"lmhead_pair", 1) == 0
