@@ -114,6 +114,11 @@ SPEC_API int spec_version(void);
  * "weight_l2_promotion" / "kv_l2_promotion" (0..3: none, 64, 128, 256 bytes;
  * defaults 2 and 3): the L2 promotion of the TMA loads of weight tiles and of
  * the attention kernels' K/V tiles;
+ * "weight_prefetch" (1 default, 0 off): the cluster split-K kernel issues its
+ * first ring stages' weight-tile loads before waiting for the kernel ahead of
+ * it on the stream; the library never writes a weight matrix, and a caller
+ * whose own kernel, launched just before with programmatic dependent launch,
+ * writes W must set 0;
  * "pdl" (1 default, 0 off):
  * kernels are launched with programmatic dependent launch, so each one's
  * launch and on-chip setup overlap the end of the kernel before it on the

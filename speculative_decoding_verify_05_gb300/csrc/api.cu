@@ -184,6 +184,7 @@ int g_attn_pair_cost = 12;  // tunable: tcgen05 attention work charged per pair 
 int g_force_grid = 0;    // tunable: CTAs of the persistent kernels, 0 = one per SM
 int g_linear_cluster = 1;  // tunable: 0 disables the cluster split-K GEMM
 int g_linear_split_rows = 1;  // tunable: 1 lets few-tile products at 257..384 rows take two half-row tiles
+int g_weight_prefetch = 1;  // tunable: 1 loads the first weight tiles before the dependency wait
 int g_nsub_max = 2;      // tunable: 2 lets one CTA tile cover up to 384 verify rows
 int g_lmhead_nsub = 2;   // tunable: the LM head's tiles cover up to 256 (1) or 384 (2) rows
 int g_pdl = 1;           // tunable: programmatic dependent launch between the library's kernels
@@ -573,6 +574,11 @@ int spec_set_option(const char* name, int value) {
     g_linear_cluster = value;
     return ok();
   }
+  if (!strcmp(name, "weight_prefetch")) {
+    if (value < 0 || value > 1) return fail(SPEC_EINVAL, "weight_prefetch must be 0 or 1");
+    g_weight_prefetch = value;
+    return ok();
+  }
   if (!strcmp(name, "linear_split_rows")) {
     if (value < 0 || value > 1) return fail(SPEC_EINVAL, "linear_split_rows must be 0 or 1");
     g_linear_split_rows = value;
@@ -846,6 +852,7 @@ static int verify_linear_plan(const LinPlan& p, const spec_bf16* X, int M, int K
   a.Y = Y; a.ldy = ldy; a.residual = residual; a.ldr = ldr;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
+  a.w_early = g_weight_prefetch;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_BF16;
   set_norm_args(a, norm, K);
@@ -1183,6 +1190,7 @@ static int verify_linear_rope_impl(const spec_bf16* X, int M, int K, int ldx, co
     a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
     a.Y = Y; a.ldy = ldy; a.residual = nullptr; a.ldr = 0;
     a.status = d->status;
+    a.w_early = g_weight_prefetch;
     a.tn = p.BN * p.NSUB;
     a.epi = EPI_ROPE;
     a.rope_cs = reinterpret_cast<const float2*>(cs);
@@ -1336,6 +1344,7 @@ static int swiglu_plan(const LinPlan& p, const spec_bf16* X, int M, int K, int l
   a.Y = A; a.ldy = lda; a.residual = nullptr; a.ldr = 0;
   a.partial = p.bytes > 0 ? reinterpret_cast<float*>(ws + p.partial_off) : nullptr;
   a.status = d->status;
+  a.w_early = g_weight_prefetch;
   a.tn = p.BN * p.NSUB;
   a.epi = EPI_SWIGLU;
   set_norm_args(a, norm, K);
@@ -1410,6 +1419,7 @@ static int launch_lmhead_gemm(const spec_bf16* H, int M, int K, const spec_bf16*
   a.M = M; a.N = V; a.K = K; a.k_tiles = p.k_tiles; a.tiles_m = p.tiles_m; a.tiles_n = p.tiles_n;
   a.units = p.units; a.grid = p.grid; a.dp_tiles = p.dp_tiles; a.sk_units = p.sk_units;
   a.status = d->status;
+  a.w_early = g_weight_prefetch;
   a.inv_temp = greedy ? 1.f : 1.f / temperature;
   a.P = Z;
   a.ldp = ldz;

@@ -68,7 +68,14 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // shared-memory and TMEM setup above overlaps the previous kernel; global memory only below
+  // shared-memory and TMEM setup above overlaps the previous kernel, and so do the first stages'
+  // weight loads when W is not that kernel's output; everything else in global memory only below
+  const int n_early = args.w_early ? min(STAGES, k1 - k0) : 0;
+  if (warp == 0 && lane == 0)
+    for (int i = 0; i < n_early; ++i) {
+      mbar_arrive_expect_tx(&full[i], Cfg::STAGE_BYTES);
+      tma_load_2d(sA + i * Cfg::A_BYTES, &tm_w, &full[i], (k0 + i) * LIN_BK, n_t * 128);
+    }
   pdl_wait();
   pdl_trigger();
 
@@ -78,8 +85,10 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
       for (int k = k0; k < k1; ++k) {
         const int i = k - k0, s = i % STAGES;
         if (i >= STAGES && !mbar_wait(&empty[s], (uint32_t)((i / STAGES - 1) & 1), args.status, 0x141u)) break;
-        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+        if (i >= n_early) {
+          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+          tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+        }
 #pragma unroll
         for (int sub = 0; sub < NSUB; ++sub)
           tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK, m_t * TN + sub * BN);

@@ -71,6 +71,9 @@ struct LinearArgs {
   // token tile t % tiles_m and the 128-row tiles 2 (t / tiles_m) + 0, 1), grid counts pairs and
   // the CTA of rank r in pair c leaves its split-K pieces in partial slots 2 (2c + r) + 0, 1
   int pair;
+  // 1: W is not written by the kernel ahead on the stream, so the first ring stages' weight tiles
+  // may be loaded before the programmatic-dependent-launch wait
+  int w_early;
 };
 
 // 1 / rms of row m from its partial sums of squares (t in order; the loads go out 8 at a time).

@@ -124,6 +124,9 @@ def test_host_side_validation(built):
     assert L.spec_set_option(b"linear_split_rows", 2) == E
     assert L.spec_set_option(b"linear_split_rows", 0) == 0
     assert L.spec_set_option(b"linear_split_rows", 1) == 0
+    assert L.spec_set_option(b"weight_prefetch", 2) == E
+    assert L.spec_set_option(b"weight_prefetch", 0) == 0
+    assert L.spec_set_option(b"weight_prefetch", 1) == 0
     assert L.spec_set_option(b"linear_pair_persistent", 0) == 0
     assert L.spec_set_option(b"lmhead_pair", 2) == E
     assert L.spec_set_option(b"lmhead_pair", 1) == 0
