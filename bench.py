@@ -122,8 +122,8 @@ def algorithmic_bytes(batch, dims):
 # sources whose SHA-256 prefix is ATTN_TRAFFIC_SOURCES.  Traffic grows with the keys streamed, so the
 # bench scales the ratio to its own launch; once either source file changes the ratio no longer
 # describes the kernel and the bench reports traffic as null.
-ATTN_DRAM_PER_ALG_BYTE = 1.038
-ATTN_TRAFFIC_SOURCES = "cf93694c5112aba3"
+ATTN_DRAM_PER_ALG_BYTE = 1.032
+ATTN_TRAFFIC_SOURCES = "b8241e892ef4c034"
 ATTN_SOURCE_FILES = ("speculative_decoding_verify_05_gb300/csrc/attention_tc.cu",
                      "speculative_decoding_verify_05_gb300/csrc/common.cuh")
 

@@ -423,6 +423,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint64_t* land = is_k ? k_land : v_land;
       uint8_t* ring = smem + (is_k ? OFF_K : OFF_V);
+      const uint64_t pol = l2_policy_evict_first();
       Cursor c = *s_cur;
       // paged cache: the block-table entries are read PF units ahead of the loads that use them
       // (a second cursor), so a page lookup's latency never sits in front of a TMA issue
@@ -457,8 +458,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         uint8_t* st = ring + s * KV_TILE;
         const KvTile kt = paged ? kv_tile_page(a, page, c.h) : kv_tile(a, c.b, c.h, c.t);
         mbar_arrive_expect_tx(bar, KV_TILE);
-        tma_load_3d(st, tm, bar, 0, kt.y, kt.z);
-        tma_load_3d(st + KV_HALF, tm, bar, 64, kt.y, kt.z);
+        tma_load_3d_hint(st, tm, bar, 0, kt.y, kt.z, pol);
+        tma_load_3d_hint(st + KV_HALF, tm, bar, 64, kt.y, kt.z, pol);
       }
     }
     __syncwarp();

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) linear_chain_kernel(const __gri
             tma_load_2d(sX + s * Cfg::X_BYTES, tm, &full[s], k * LIN_BK, 0);
           } else {
             mbar_arrive_expect_tx(&full[s], CH_W_BYTES);
-            tma_load_2d(sW + s * CH_W_BYTES, tm, &full[s], k * LIN_BK, g.tile * 128);
+            tma_load_2d_hint(sW + s * CH_W_BYTES, tm, &full[s], k * LIN_BK, g.tile * 128, l2_policy_evict_first());
           }
         }
       }

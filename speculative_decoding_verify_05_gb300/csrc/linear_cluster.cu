@@ -71,10 +71,11 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
   // shared-memory and TMEM setup above overlaps the previous kernel, and so do the first stages'
   // weight loads when W is not that kernel's output; everything else in global memory only below
   const int n_early = args.w_early ? min(STAGES, k1 - k0) : 0;
+  const uint64_t pol = l2_policy_evict_first();
   if (warp == 0 && lane == 0)
     for (int i = 0; i < n_early; ++i) {
       mbar_arrive_expect_tx(&full[i], Cfg::STAGE_BYTES);
-      tma_load_2d(sA + i * Cfg::A_BYTES, &tm_w, &full[i], (k0 + i) * LIN_BK, n_t * 128);
+      tma_load_2d_hint(sA + i * Cfg::A_BYTES, &tm_w, &full[i], (k0 + i) * LIN_BK, n_t * 128, pol);
     }
   pdl_wait();
   pdl_trigger();
@@ -87,7 +88,7 @@ linear_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_con
         if (i >= STAGES && !mbar_wait(&empty[s], (uint32_t)((i / STAGES - 1) & 1), args.status, 0x141u)) break;
         if (i >= n_early) {
           mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-          tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+          tma_load_2d_hint(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128, pol);
         }
 #pragma unroll
         for (int sub = 0; sub < NSUB; ++sub)

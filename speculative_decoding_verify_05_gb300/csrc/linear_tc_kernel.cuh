@@ -168,14 +168,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           // expect: the transaction count goes negative for a while)
           if (half == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE_BYTES);
           const uint32_t bar = full_leader + (uint32_t)s * 8u;
-          tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tm_w, bar, k * LIN_BK, n_t * 128);
+          tma_load_2d_pair_hint(sA + s * Cfg::A_BYTES, &tm_w, bar, k * LIN_BK, n_t * 128, l2_policy_evict_first());
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
             tma_load_2d_pair(sB + s * Cfg::B_BYTES + sub * HB * LIN_ROW_BYTES, &tm_x, bar, k * LIN_BK,
                              m_t * TN + sub * BN + half * HB);
         } else {
           mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-          tma_load_2d(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128);
+          tma_load_2d_hint(sA + s * Cfg::A_BYTES, &tm_w, &full[s], k * LIN_BK, n_t * 128, l2_policy_evict_first());
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
             tma_load_2d(sB + s * Cfg::B_BYTES + sub * BN * LIN_ROW_BYTES, &tm_x, &full[s], k * LIN_BK,
