@@ -140,6 +140,20 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
     const int ritems = (n_chunks > 0 ? n_chunks : 0) * 8;
     for (int it = threadIdx.x; it < ritems; it += NT) {
       const int kk = it >> 3, r8 = (it & 7) * 8;
+      const int mb = m_t * TN + (me * cpr + kk) * 4;
+      // this item's table entries first: their global loads overlap the slot sums below
+      float2 csr[4][8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = min(mb + e, args.M - 1);
+        const float4* cs4 = reinterpret_cast<const float4*>(args.rope_cs + (size_t)m * 64 + r8);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = __ldg(cs4 + q);
+          csr[e][2 * q] = make_float2(v.x, v.y);
+          csr[e][2 * q + 1] = make_float2(v.z, v.w);
+        }
+      }
       float a[8][4], b[8][4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -158,7 +172,6 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
         }
       }
       const int n = n_t * 128 + r8;
-      const int mb = m_t * TN + (me * cpr + kk) * 4;
       if (scale) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -171,11 +184,10 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
       for (int e = 0; e < 4; ++e) {
         const int m = mb + e;
         if (m >= args.M) break;
-        const float2* cs = args.rope_cs + (size_t)m * 64 + r8;
         uint32_t x4[4], y4[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float2 c0 = cs[2 * h], c1 = cs[2 * h + 1];
+          const float2 c0 = csr[e][2 * h], c1 = csr[e][2 * h + 1];
           const float a0 = a[2 * h][e], a1 = a[2 * h + 1][e], b0 = b[2 * h][e], b1 = b[2 * h + 1][e];
           x4[h] = pack_bf16x2(a0 * c0.x - b0 * c0.y, a1 * c1.x - b1 * c1.y);
           y4[h] = pack_bf16x2(b0 * c0.x + a0 * c0.y, b1 * c1.x + a1 * c1.y);
