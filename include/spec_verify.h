@@ -112,7 +112,7 @@ SPEC_API int spec_version(void);
  * default, 1): the pair kernel also for products with fewer tiles (split-K
  * on pairs; measured slower than the one-SM cluster kernel at 368 rows);
  * "weight_l2_promotion" / "kv_l2_promotion" (0..3: none, 64, 128, 256 bytes;
- * defaults 2 and 3): the L2 promotion of the TMA loads of weight tiles and of
+ * default 3 for both): the L2 promotion of the TMA loads of weight tiles and of
  * the attention kernels' K/V tiles;
  * "weight_prefetch" (1 default, 0 off): the cluster split-K kernel issues its
  * first ring stages' weight-tile loads before waiting for the kernel ahead of

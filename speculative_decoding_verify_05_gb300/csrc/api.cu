@@ -150,7 +150,7 @@ int get_encoder() {
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes, rank-1 entries)
 constexpr CUtensorMapSwizzle kLinSwizzle = LIN_BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-int g_w_promotion = 2;    // tunable: L2 promotion of weight-tile loads (0 none, 1 64 B, 2 128 B, 3 256 B)
+int g_w_promotion = 3;    // tunable: L2 promotion of weight-tile loads (0 none, 1 64 B, 2 128 B, 3 256 B)
 int g_kv_promotion = 3;   // tunable: L2 promotion of the attention kernels' K/V tile loads (same scale)
 
 int encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
