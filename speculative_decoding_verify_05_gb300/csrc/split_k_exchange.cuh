@@ -204,6 +204,16 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
   for (int it = threadIdx.x; it < items_w; it += NT) {
     const bool act = it < items;
     const int kk = act ? it >> 4 : 0, r8 = (it & 15) * 8;
+    const int n0 = n_t * 128 + r8;
+    const int mb = m_t * TN + (me * cpr + kk) * 4;
+    const bool whole = act && n0 + 8 <= args.N;
+    // the residual rows first: their global loads overlap the slot sums below
+    uint4 res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      res[e] = (whole && args.residual && mb + e < args.M)
+                   ? *reinterpret_cast<const uint4*>(args.residual + (size_t)(mb + e) * args.ldr + n0)
+                   : make_uint4(0, 0, 0, 0);
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -225,16 +235,8 @@ __device__ __forceinline__ void split_sum_epilogue(const float4* slots, const Li
         for (int i = 0; i < 8; ++i) acc[i][e] *= rs;
       }
     }
-    const int n0 = n_t * 128 + r8;
-    const int mb = m_t * TN + (me * cpr + kk) * 4;
     float sq[4] = {0.f, 0.f, 0.f, 0.f};
-    if (act && n0 + 8 <= args.N) {
-      uint4 res[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        res[e] = (args.residual && mb + e < args.M)
-                     ? *reinterpret_cast<const uint4*>(args.residual + (size_t)(mb + e) * args.ldr + n0)
-                     : make_uint4(0, 0, 0, 0);
+    if (whole) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (mb + e >= args.M) break;
