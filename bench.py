@@ -735,10 +735,10 @@ class SweepRig:
         import synth
         M = nb * (gm + 1)
         x, h, qkv, o, a, ws = self.x, self.h, self.qkv, self.o, self.a, self.ws
-        # the small-M path (M <= 32): the weight-streaming chain; above it, one call per product (the
-        # chain takes up to 64 rows, but at 40 rows its 64-column pieces made it slower: 3.51 ms
-        # against 3.33 ms)
-        chain = M <= 32
+        # the small-M path (up to the chain's 64 rows): the weight-streaming chain; above it, one call
+        # per product (with the weight streams marked evict-first the chain is the faster stack at every
+        # M it takes: 2.94 against 3.32 ms at 40 rows, 2.97 against 3.14 ms at 64)
+        chain = M <= 64
         if chain:
             ops = stack_chain_ops(S, None, M, bufs=(self.sw.layers, h, o, qkv, x, a))
             cws = S.Workspace(dev, S.spec_linear_chain_workspace_bytes(ops, M))
