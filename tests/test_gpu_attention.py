@@ -173,6 +173,16 @@ def test_attention_many_short_pairs(lib, grid, B):
         lib.spec_set_option("persistent_grid", 0)
 
 
+def test_attention_at_the_batch_limit(lib):
+    """1024 sequences, the most the tcgen05 kernel takes, of short contexts (0-199 keys, 1-4 rows):
+    the per-sequence metadata its set-up stages in the V ring (3 x 1024 + 2 ints) and each CTA's
+    1025-entry prefix slice in the workspace are at their largest, and most CTAs start many pairs."""
+    rng = np.random.default_rng(7)
+    B = 1024
+    gammas, ctx = list(rng.integers(0, 4, size=B)), list(rng.integers(0, 200, size=B))
+    run_case(lib, gammas, ctx, 8, 2, seed=1024)
+
+
 def test_attention_full_ragged_round_sampled(lib):
     """The benchmark's attention launch at full size: B = 64, gamma_b ~ U{1..10}, ctx_b ~ U[128, 8192],
     GQA 32/8, D = 128, the default persistent grid and pair cost.  Outputs and the cache append are
